@@ -1,0 +1,21 @@
+"""GB300-native greedy speculative decoding.
+
+One speculative round -- K draft guesses (a small draft model decoding
+greedily, or prompt lookup), one causal verify pass of the target over the
+pending token and the guesses, acceptance of the longest agreeing prefix plus
+the target's bonus token, in-place rollback of both KV caches -- runs as
+hand-written sm_103a CUDA kernels behind the C ABI in include/sf.h, replayed
+as one CUDA graph per round.
+
+``SpecEngine`` wraps that ABI; PyTorch only provides device memory and the
+stream. The library is loaded on first use and its absence raises
+ImportError (build it with ``python -m greedy_speculative_decoding_gb300.build``);
+there is no fallback path.
+"""
+
+from . import _lib
+from ._lib import (SF_DRAFT_NEURAL, SF_DRAFT_NGRAM, SF_MAX_ROWS, SFError, load)
+from .engine import SpecEngine, linear, model_cfg, nf4_quantize, weight_order
+
+__all__ = ["SpecEngine", "SFError", "linear", "model_cfg", "weight_order", "nf4_quantize", "SF_DRAFT_NEURAL",
+           "SF_DRAFT_NGRAM", "SF_MAX_ROWS"]

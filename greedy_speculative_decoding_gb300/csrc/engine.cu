@@ -1,0 +1,967 @@
+// Host side of the engine: the C ABI declared in include/sf.h.
+//
+// The engine binds caller-owned device buffers, plans every GEMM once (row
+// blocks, K split) from the matrix shape and the SM count, and enqueues the
+// forward passes of the draft and target models. All lengths, positions and
+// tokens of the speculative round live on the device, so one round is a
+// fixed sequence of launches: it is captured once into a CUDA graph per
+// drafter and replayed with no host writes in between ("CUDA Graphs: What
+// They Are and Why They Helped" and "Why It Kept Breaking (and How I Fixed
+// It)", I Got 28 TPS Out of Free Kaggle GPUs: static cache, in-place
+// buffers, positions updated on the device, in-place rewind).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "sf_kernels.h"
+
+using namespace sf;
+
+namespace {
+
+thread_local std::string g_err;
+
+sf_status fail(sf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define CK(x)                                                                                   \
+  do {                                                                                          \
+    cudaError_t e_ = (x);                                                                       \
+    if (e_ != cudaSuccess)                                                                      \
+      return fail(SF_ERR_CUDA, "%s failed: %s (%s:%d)", #x, cudaGetErrorString(e_), __FILE__, \
+                  __LINE__);                                                                    \
+  } while (0)
+
+struct Plan {
+  int nblocks = 0, nsplit = 1, cps = 1;
+};
+
+// Split K only when the row blocks alone cannot fill the GPU; the split
+// depends on the matrix shape and the SM count, never on the number of
+// token rows, so every row is computed the same way in every launch.
+Plan make_plan(int nblocks, int K, int slots) {
+  Plan p;
+  p.nblocks = nblocks;
+  const int nch = (K + kChunk - 1) / kChunk;
+  int ns = 1;
+  if (nblocks * 10 < slots * 9) ns = std::max(1, slots / nblocks);
+  ns = std::min(ns, nch);
+  p.cps = (nch + ns - 1) / ns;
+  p.nsplit = (nch + p.cps - 1) / p.cps;
+  return p;
+}
+
+enum { W_Q = 0, W_K, W_V, W_O, W_G, W_U, W_D };
+
+struct LayerW {
+  const void* w[7] = {};
+  const __half* sc[7] = {};
+  const bf16 *ln1 = nullptr, *ln2 = nullptr, *bq = nullptr, *bk = nullptr, *bv = nullptr;
+};
+
+struct Model {
+  sf_model_cfg c{};
+  const bf16* embed = nullptr;
+  int embed_ld = 0;
+  std::vector<LayerW> L;
+  const bf16* norm = nullptr;
+  const bf16* lm = nullptr;
+  int lm_ld = 0;
+  bf16* kv = nullptr;
+  float2* rope = nullptr;
+  Plan p_qkv, p_o, p_gu, p_d, p_lm;
+  int q_dim() const { return c.n_heads * c.head_dim; }
+  int kv_dim() const { return c.n_kv_heads * c.head_dim; }
+};
+
+constexpr int kMaxPlanTiles = 1024;   // split-K partial tiles the scratch holds
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool cfg_ok(const sf_model_cfg* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return false;
+  };
+  if (!c) return bad("null model config");
+  if (c->layers < 1 || c->hidden < 128 || c->n_heads < 1 || c->n_kv_heads < 1 || c->ffn < 8 ||
+      c->vocab < 1)
+    return bad("non-positive dimension");
+  if (c->hidden % 128) return bad("hidden must be a multiple of 128");
+  if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+  if ((c->n_heads * c->head_dim) % 128 || (c->n_kv_heads * c->head_dim) % 128)
+    return bad("n_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
+  if (c->ffn % 8) return bad("ffn must be a multiple of 8");
+  if (c->wdtype != SF_WDTYPE_BF16 && c->wdtype != SF_WDTYPE_NF4) return bad("unknown wdtype");
+  if (c->wdtype == SF_WDTYPE_NF4) return bad("NF4 weights are not supported by this build yet");
+  const int eld = c->embed_ld ? c->embed_ld : c->hidden;
+  if (eld < c->hidden || eld % 8) return bad("embed_ld must be >= hidden and a multiple of 8");
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps or rope_theta");
+  return true;
+}
+
+struct Layout {
+  size_t x, ssq, q, attn_o, act, apart, gpart, counters, keys, done, zeros, rope_t, rope_d, state, total;
+  int n_kv_chunks, max_blocks;
+};
+
+int nblocks_of(const sf_model_cfg* c, int which) {
+  switch (which) {
+    case 0: return (c->n_heads * c->head_dim + 2 * c->n_kv_heads * c->head_dim + 127) / 128;
+    case 1: return (c->hidden + 127) / 128;
+    case 2: return (c->ffn + 63) / 64;
+    default: return (c->vocab + 127) / 128;
+  }
+}
+
+// State ints: len_t, len_d, vtok, ttok, dtok0, nprop, hist, prompt_len,
+// acc_hist, then the report block (ncommit, nacc, commit, total, err) that
+// one copy brings back to the host.
+struct StateOff {
+  size_t len_t, len_d, vtok, ttok, dtok0, nprop, hist, prompt_len, acc_hist, report, ncommit, nacc, commit,
+      total, err, n_ints, report_ints;
+};
+
+StateOff state_offsets(int B, int K, int s_max) {
+  StateOff o{};
+  size_t p = 0;
+  auto take = [&](size_t n) {
+    size_t r = p;
+    p += (n + 63) & ~size_t(63);
+    return r;
+  };
+  const int K1 = K + 1;
+  o.len_t = take(B);
+  o.len_d = take(B);
+  o.vtok = take(B * K1);
+  o.ttok = take(B * K1);
+  o.dtok0 = take(2 * B);
+  o.nprop = take(B);
+  o.hist = take((size_t)B * s_max);
+  o.prompt_len = take(B);
+  o.acc_hist = take(B * K1);
+  o.report = p;
+  o.ncommit = p;
+  p += B;
+  o.nacc = p;
+  p += B;
+  o.commit = p;
+  p += B * K1;
+  o.total = p;
+  p += B;
+  o.err = p;
+  p += 1;
+  o.report_ints = p - o.report;
+  o.n_ints = p;
+  return o;
+}
+
+Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, int s_max) {
+  Layout L{};
+  auto mx = [&](auto f) { return d ? std::max(f(t), f(d)) : f(t); };
+  const int H = mx([](const sf_model_cfg* c) { return c->hidden; });
+  const int QD = mx([](const sf_model_cfg* c) { return c->n_heads * c->head_dim; });
+  const int NQ = mx([](const sf_model_cfg* c) { return c->n_heads; });
+  const int HD = mx([](const sf_model_cfg* c) { return c->head_dim; });
+  const int F = mx([](const sf_model_cfg* c) { return c->ffn; });
+  L.n_kv_chunks = s_max / kKvChunk;
+  L.max_blocks = 0;
+  for (int w = 0; w < 4; ++w) L.max_blocks = std::max(L.max_blocks, mx([w](const sf_model_cfg* c) { return nblocks_of(c, w); }));
+  size_t p = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = p;
+    p = align256(p + bytes);
+    return r;
+  };
+  L.x = take((size_t)kRows * H * 4);
+  L.ssq = take((size_t)(H / 128) * kRows * 4);
+  L.q = take((size_t)kRows * QD * 4);
+  L.attn_o = take((size_t)kRows * QD * 4);
+  L.act = take((size_t)kRows * ((F + 3) / 4 * 4) * 4);
+  L.apart = take((size_t)kRows * NQ * L.n_kv_chunks * (HD + 2) * 4);
+  L.gpart = take((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
+  L.counters = take((size_t)L.max_blocks * 4);
+  L.keys = take((size_t)kRows * 8);
+  L.done = take(4);
+  L.zeros = take((size_t)B * 4);
+  L.rope_t = take((size_t)s_max * (t->head_dim / 2) * 8);
+  L.rope_d = d ? take((size_t)s_max * (d->head_dim / 2) * 8) : p;
+  L.state = take(state_offsets(B, K, s_max).n_ints * 4);
+  L.total = p;
+  return L;
+}
+
+}  // namespace
+
+struct sf_engine {
+  Model tgt, dft;
+  bool has_dft = false;
+  int B = 0, K = 0, s_max = 0, num_sms = 0, slots = 0;
+  cudaStream_t user = nullptr, cap = nullptr;
+  unsigned char* ws = nullptr;
+  Layout lay{};
+  StateOff so{};
+  float *x = nullptr, *ssq = nullptr, *q = nullptr, *attn_o = nullptr, *act = nullptr, *apart = nullptr,
+        *gpart = nullptr;
+  int *counters = nullptr, *done = nullptr, *zeros = nullptr;
+  unsigned long long* keys = nullptr;
+  SpecState st{};
+  int* pin = nullptr;   // pinned host copy of the report block
+  cudaGraphExec_t graph[2] = {nullptr, nullptr};   // whole round, per drafter
+  cudaGraphExec_t g_draft = nullptr, g_verify = nullptr;
+  int drafter = SF_DRAFT_NEURAL, ng_min = 2, ng_max = 4;
+  std::vector<int> C;   // committed tokens per sequence (host mirror)
+  int P = 0;            // prompt length
+  int phase = 0;        // 0: no prompt, 1: ready, 2: drafted, 3: verified
+  int drafted_mode = SF_DRAFT_NEURAL;
+  bool draft_stale = false;
+};
+
+namespace {
+
+sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void* const* w, bf16* kv) {
+  md.c = *c;
+  // Null is allowed only for biases of a bias-free config; every pointer must
+  // be 16-byte aligned (the kernels read rows with 128-bit loads).
+  auto check = [](const void* p, const char*, bool allow_null) -> bool {
+    if (!p) return allow_null;
+    return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+  };
+  int i = 0;
+  md.embed = static_cast<const bf16*>(w[i++]);
+  if (!check(md.embed, "embed", false)) return fail(SF_ERR_ARG, "embed pointer null or not 16-byte aligned");
+  md.embed_ld = c->embed_ld ? c->embed_ld : c->hidden;
+  md.L.resize(c->layers);
+  for (int l = 0; l < c->layers; ++l) {
+    LayerW& lw = md.L[l];
+    lw.ln1 = static_cast<const bf16*>(w[i++]);
+    lw.w[W_Q] = w[i++];
+    lw.w[W_K] = w[i++];
+    lw.w[W_V] = w[i++];
+    lw.bq = static_cast<const bf16*>(w[i++]);
+    lw.bk = static_cast<const bf16*>(w[i++]);
+    lw.bv = static_cast<const bf16*>(w[i++]);
+    lw.w[W_O] = w[i++];
+    lw.ln2 = static_cast<const bf16*>(w[i++]);
+    lw.w[W_G] = w[i++];
+    lw.w[W_U] = w[i++];
+    lw.w[W_D] = w[i++];
+    if (!c->qkv_bias) lw.bq = lw.bk = lw.bv = nullptr;
+    bool ok = check(lw.ln1, "ln1", false) && check(lw.ln2, "ln2", false);
+    for (int k = 0; k < 7; ++k) ok = ok && check(lw.w[k], "w", false);
+    if (c->qkv_bias) ok = ok && check(lw.bq, "bq", false) && check(lw.bk, "bk", false) && check(lw.bv, "bv", false);
+    if (!ok) return fail(SF_ERR_ARG, "layer %d: a weight pointer is null or not 16-byte aligned", l);
+  }
+  md.norm = static_cast<const bf16*>(w[i++]);
+  if (!check(md.norm, "norm", false)) return fail(SF_ERR_ARG, "final norm pointer null or misaligned");
+  if (c->tied) {
+    md.lm = md.embed;
+    md.lm_ld = md.embed_ld;
+  } else {
+    md.lm = static_cast<const bf16*>(w[i++]);
+    md.lm_ld = c->hidden;
+    if (!check(md.lm, "lm_head", false)) return fail(SF_ERR_ARG, "lm_head pointer null or misaligned");
+  }
+  md.kv = kv;
+  const int H = c->hidden;
+  md.p_qkv = make_plan(nblocks_of(c, 0), H, e->slots);
+  md.p_o = make_plan(nblocks_of(c, 1), c->n_heads * c->head_dim, e->slots);
+  md.p_gu = make_plan(nblocks_of(c, 2), H, e->slots);
+  md.p_d = make_plan(nblocks_of(c, 1), c->ffn, e->slots);
+  md.p_lm = make_plan(nblocks_of(c, 3), H, e->slots);
+  for (const Plan* p : {&md.p_qkv, &md.p_o, &md.p_gu, &md.p_d, &md.p_lm})
+    if (p->nsplit > 1 && p->nblocks * p->nsplit > kMaxPlanTiles)
+      return fail(SF_ERR_UNSUPPORTED, "split-K plan exceeds the scratch tiles");
+  return SF_OK;
+}
+
+GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& rs) {
+  GemmArgs a{};
+  a.nblocks = p.nblocks;
+  a.nsplit = p.nsplit;
+  a.cps = p.cps;
+  a.part = e->gpart;
+  a.counter = e->counters;
+  a.err = e->st.err;
+  a.rs = rs;
+  a.eps = md.c.rms_eps;
+  return a;
+}
+
+struct TokOut {
+  int* tok = nullptr;
+  int stride = 0, skip = 0, off = 0;
+  float* logits = nullptr;
+  int lg_stride = 0, lg_off = 0;
+};
+
+// Enqueue one forward pass of `md` over the rows `rs`. With `lm` the final
+// norm + LM head + argmax run too and write tokens (and optional logits).
+sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokOut& to, cudaStream_t s) {
+  const sf_model_cfg& c = md.c;
+  const int H = c.hidden, QD = md.q_dim(), KVD = md.kv_dim();
+  EmbedArgs ea{};
+  ea.E = md.embed;
+  ea.ld = md.embed_ld;
+  ea.H = H;
+  ea.vocab = c.vocab;
+  ea.err = e->st.err;
+  ea.x = e->x;
+  ea.ssq = e->ssq;
+  ea.rs = rs;
+  CK(launch_embed(ea, s, true));
+  const size_t layer_elems = (size_t)2 * e->B * c.n_kv_heads * e->s_max * c.head_dim;
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerW& lw = md.L[l];
+    bf16* kc = md.kv + (size_t)l * layer_elems;
+    bf16* vc = kc + layer_elems / 2;
+    // q, k, v (+ bias, RoPE, cache append)
+    GemmArgs a = base_args(e, md, md.p_qkv, rs);
+    a.w[0] = lw.w[W_Q];
+    a.w[1] = lw.w[W_K];
+    a.w[2] = lw.w[W_V];
+    a.bias[0] = lw.bq;
+    a.bias[1] = lw.bk;
+    a.bias[2] = lw.bv;
+    a.seg_end[0] = QD;
+    a.seg_end[1] = QD + KVD;
+    a.seg_end[2] = QD + 2 * KVD;
+    a.ld[0] = a.ld[1] = a.ld[2] = H;
+    a.nseg = 3;
+    a.N = QD + 2 * KVD;
+    a.K = H;
+    a.in = e->x;
+    a.in_ld = H;
+    a.ssq = e->ssq;
+    a.nssq = H / 128;
+    a.gain = lw.ln1;
+    a.inv_k = 1.0f / H;
+    a.out = e->q;
+    a.out_ld = QD;
+    a.q_dim = QD;
+    a.kv_dim = KVD;
+    a.hd = c.head_dim;
+    a.nkv = c.n_kv_heads;
+    a.s_max = e->s_max;
+    a.kc = kc;
+    a.vc = vc;
+    a.rope = md.rope;
+    CK(launch_gemm(a, EPI_QKV, s, true));
+    // attention
+    AttnArgs t{};
+    t.q = e->q;
+    t.kc = kc;
+    t.vc = vc;
+    t.part = e->apart;
+    t.out = e->attn_o;
+    t.nq = c.n_heads;
+    t.nkv = c.n_kv_heads;
+    t.hd = c.head_dim;
+    t.s_max = e->s_max;
+    t.B = e->B;
+    t.n_kv_chunks = e->lay.n_kv_chunks;
+    t.scale = 1.0f / sqrtf((float)c.head_dim);
+    t.err = e->st.err;
+    t.rs = rs;
+    CK(launch_attention(t, e->num_sms, s, true));
+    // o-projection + residual
+    a = base_args(e, md, md.p_o, rs);
+    a.w[0] = lw.w[W_O];
+    a.seg_end[0] = H;
+    a.ld[0] = QD;
+    a.nseg = 1;
+    a.N = H;
+    a.K = QD;
+    a.in = e->attn_o;
+    a.in_ld = QD;
+    a.out = e->x;
+    a.out_ld = H;
+    a.ssq_out = e->ssq;
+    CK(launch_gemm(a, EPI_RESID, s, true));
+    // gate/up + SwiGLU
+    a = base_args(e, md, md.p_gu, rs);
+    a.w[0] = lw.w[W_G];
+    a.w[1] = lw.w[W_U];
+    a.ld[0] = a.ld[1] = H;
+    a.nseg = 2;
+    a.N = c.ffn;
+    a.K = H;
+    a.in = e->x;
+    a.in_ld = H;
+    a.ssq = e->ssq;
+    a.nssq = H / 128;
+    a.gain = lw.ln2;
+    a.inv_k = 1.0f / H;
+    a.out = e->act;
+    a.out_ld = (c.ffn + 3) / 4 * 4;
+    CK(launch_gemm(a, EPI_SWIGLU, s, true));
+    // down + residual
+    a = base_args(e, md, md.p_d, rs);
+    a.w[0] = lw.w[W_D];
+    a.seg_end[0] = H;
+    a.ld[0] = c.ffn;
+    a.nseg = 1;
+    a.N = H;
+    a.K = c.ffn;
+    a.in = e->act;
+    a.in_ld = (c.ffn + 3) / 4 * 4;
+    a.out = e->x;
+    a.out_ld = H;
+    a.ssq_out = e->ssq;
+    CK(launch_gemm(a, EPI_RESID, s, true));
+  }
+  if (!lm) return SF_OK;
+  GemmArgs a = base_args(e, md, md.p_lm, rs);
+  a.w[0] = md.lm;
+  a.seg_end[0] = c.vocab;
+  a.ld[0] = md.lm_ld;
+  a.nseg = 1;
+  a.N = c.vocab;
+  a.K = H;
+  a.in = e->x;
+  a.in_ld = H;
+  a.ssq = e->ssq;
+  a.nssq = H / 128;
+  a.gain = md.norm;
+  a.inv_k = 1.0f / H;
+  a.keys = e->keys;
+  a.done = e->done;
+  a.tok_out = to.tok;
+  a.tok_stride = to.stride;
+  a.tok_skip = to.skip;
+  a.tok_off = to.off;
+  a.logits = to.logits;
+  a.lg_stride = to.lg_stride;
+  a.lg_off = to.lg_off;
+  CK(launch_gemm(a, EPI_ARGMAX, s, true));
+  return SF_OK;
+}
+
+sf_status enqueue_draft(sf_engine* e, float* logits, cudaStream_t s) {
+  const int K1 = e->K + 1;
+  // Step 0: rows (committed[C-2], committed[C-1]) at positions C-2, C-1.
+  RowSet rs{e->st.dtok0, 2, 0, 2, 2 * e->B, e->st.len_d, 0};
+  TokOut to;
+  to.tok = e->st.vtok;
+  to.stride = K1;
+  to.skip = 1;
+  to.off = 1;
+  to.logits = logits;
+  to.lg_stride = e->K;
+  to.lg_off = 0;
+  sf_status r = forward(e, e->dft, rs, true, to, s);
+  if (r != SF_OK) return r;
+  for (int i = 1; i < e->K; ++i) {
+    // Step i: d_i at position C - 1 + i.
+    RowSet ri{e->st.vtok, K1, i, 1, e->B, e->st.len_d, 1 + i};
+    TokOut ti;
+    ti.tok = e->st.vtok;
+    ti.stride = K1;
+    ti.skip = 0;
+    ti.off = i + 1;
+    ti.logits = logits;
+    ti.lg_stride = e->K;
+    ti.lg_off = i;
+    if ((r = forward(e, e->dft, ri, true, ti, s)) != SF_OK) return r;
+  }
+  return SF_OK;
+}
+
+sf_status enqueue_verify(sf_engine* e, float* logits, cudaStream_t s) {
+  const int K1 = e->K + 1;
+  RowSet rs{e->st.vtok, K1, 0, K1, e->B * K1, e->st.len_t, 0};
+  TokOut to;
+  to.tok = e->st.ttok;
+  to.stride = K1;
+  to.skip = 0;
+  to.off = 0;
+  to.logits = logits;
+  to.lg_stride = K1;
+  to.lg_off = 0;
+  return forward(e, e->tgt, rs, true, to, s);
+}
+
+sf_status enqueue_round(sf_engine* e, int mode, cudaStream_t s) {
+  sf_status r;
+  if (mode == SF_DRAFT_NEURAL) {
+    if ((r = enqueue_draft(e, nullptr, s)) != SF_OK) return r;
+  } else {
+    CK(launch_ngram(e->st, e->K, e->ng_min, e->ng_max, nullptr, nullptr, s, true));
+  }
+  if ((r = enqueue_verify(e, nullptr, s)) != SF_OK) return r;
+  CK(launch_accept(e->st, mode, s, true));
+  return SF_OK;
+}
+
+enum { CAP_ROUND_NEURAL = 0, CAP_ROUND_NGRAM = 1, CAP_DRAFT = 2, CAP_VERIFY = 3 };
+
+cudaGraphExec_t* graph_slot(sf_engine* e, int what) {
+  if (what == CAP_DRAFT) return &e->g_draft;
+  if (what == CAP_VERIFY) return &e->g_verify;
+  return &e->graph[what];
+}
+
+// Capture (once) the launches of `what` on the private stream and keep the
+// instantiated graph; replays then cost one launch.
+sf_status build_graph(sf_engine* e, int what) {
+  cudaGraphExec_t* slot = graph_slot(e, what);
+  if (*slot) return SF_OK;
+  CK(cudaStreamBeginCapture(e->cap, cudaStreamCaptureModeThreadLocal));
+  sf_status r;
+  if (what == CAP_DRAFT) r = enqueue_draft(e, nullptr, e->cap);
+  else if (what == CAP_VERIFY) r = enqueue_verify(e, nullptr, e->cap);
+  else r = enqueue_round(e, what, e->cap);
+  cudaGraph_t g = nullptr;
+  cudaError_t ce = cudaStreamEndCapture(e->cap, &g);
+  if (r != SF_OK) {
+    if (g) cudaGraphDestroy(g);
+    return r;
+  }
+  if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(ce));
+  ce = cudaGraphInstantiate(slot, g, 0);
+  cudaGraphDestroy(g);
+  if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(ce));
+  return SF_OK;
+}
+
+// Copy the report block to pinned memory, wait, and turn device error bits
+// into a status (clearing them).
+sf_status sync_report(sf_engine* e) {
+  CK(cudaMemcpyAsync(e->pin, e->st.ncommit, e->so.report_ints * sizeof(int), cudaMemcpyDeviceToHost, e->user));
+  CK(cudaStreamSynchronize(e->user));
+  const int err = e->pin[e->so.err - e->so.report];
+  if (err) {
+    CK(cudaMemsetAsync(e->st.err, 0, sizeof(int), e->user));
+    CK(cudaStreamSynchronize(e->user));
+    if (err & kErrWait) return fail(SF_ERR_DEVICE, "a kernel's bounded wait expired (device flag %d)", err);
+    if (err & kErrNonfinite) return fail(SF_ERR_NONFINITE, "non-finite logits (device flag %d)", err);
+    return fail(SF_ERR_CAPACITY, "cache capacity or token range exceeded on the device (flag %d)", err);
+  }
+  const int* tot = e->pin + (e->so.total - e->so.report);
+  for (int b = 0; b < e->B; ++b) e->C[b] = e->P + tot[b];
+  return SF_OK;
+}
+
+int max_committed(const sf_engine* e) {
+  int m = 0;
+  for (int v : e->C) m = std::max(m, v);
+  return m;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+int32_t sf_weight_count(const sf_model_cfg* cfg) {
+  if (!cfg || cfg->layers < 1) return -1;
+  const int per_layer = cfg->wdtype == SF_WDTYPE_NF4 ? 12 + 7 : 12;
+  return 1 + cfg->layers * per_layer + 1 + (cfg->tied ? 0 : 1);
+}
+
+size_t sf_kv_bytes(const sf_model_cfg* cfg, int32_t batch, int32_t s_max) {
+  if (!cfg || batch < 1 || s_max < 1) return 0;
+  return (size_t)cfg->layers * 2 * batch * cfg->n_kv_heads * (size_t)s_max * cfg->head_dim * 2;
+}
+
+size_t sf_workspace_bytes(const sf_model_cfg* tgt, const sf_model_cfg* dft, int32_t batch, int32_t K,
+                          int32_t s_max) {
+  std::string why;
+  if (!cfg_ok(tgt, &why) || (dft && !cfg_ok(dft, &why)) || batch < 1 || K < 1 || s_max < 64 ||
+      s_max % kKvChunk)
+    return 0;
+  return make_layout(tgt, dft, batch, K, s_max).total;
+}
+
+const char* sf_status_str(sf_status s) {
+  switch (s) {
+    case SF_OK: return "ok";
+    case SF_ERR_ARG: return "invalid argument";
+    case SF_ERR_CAPACITY: return "cache capacity exceeded";
+    case SF_ERR_CUDA: return "CUDA error";
+    case SF_ERR_NONFINITE: return "non-finite logits";
+    case SF_ERR_STATE: return "call out of order";
+    case SF_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case SF_ERR_DEVICE: return "device-side wait expired";
+    default: return "unknown status";
+  }
+}
+
+const char* sf_last_error(void) { return g_err.c_str(); }
+
+sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_model_cfg* dft,
+                    const void* const* dft_w, int32_t batch, int32_t K, int32_t s_max, void* kv_t, void* kv_d,
+                    void* workspace, void* cuda_stream, sf_handle* out) {
+  if (!out) return fail(SF_ERR_ARG, "out is null");
+  *out = nullptr;
+  std::string why;
+  if (!cfg_ok(tgt, &why)) return fail(tgt && tgt->wdtype == SF_WDTYPE_NF4 ? SF_ERR_UNSUPPORTED : SF_ERR_ARG, "target: %s", why.c_str());
+  if (dft && !cfg_ok(dft, &why)) return fail(dft->wdtype == SF_WDTYPE_NF4 ? SF_ERR_UNSUPPORTED : SF_ERR_ARG, "draft: %s", why.c_str());
+  if (!tgt_w || (dft && !dft_w)) return fail(SF_ERR_ARG, "weight pointer array is null");
+  if (batch < 1 || K < 1 || K > 15) return fail(SF_ERR_ARG, "batch must be >= 1 and K in 1..15");
+  if (batch * (K + 1) > SF_MAX_ROWS || batch * 2 > SF_MAX_ROWS)
+    return fail(SF_ERR_UNSUPPORTED, "batch*(K+1) = %d exceeds %d rows", batch * (K + 1), SF_MAX_ROWS);
+  if (s_max < 64 || s_max % kKvChunk) return fail(SF_ERR_ARG, "s_max must be a positive multiple of 64");
+  if (!kv_t || (dft && !kv_d) || !workspace) return fail(SF_ERR_ARG, "null cache or workspace pointer");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(kv_t) & 255) ||
+      (kv_d && (reinterpret_cast<uintptr_t>(kv_d) & 255)))
+    return fail(SF_ERR_ARG, "workspace and caches must be 256-byte aligned");
+  if (dft && dft->vocab != tgt->vocab)
+    return fail(SF_ERR_ARG, "draft and target vocabularies differ (%d vs %d)", dft->vocab, tgt->vocab);
+
+  sf_engine* e = new sf_engine();
+  e->B = batch;
+  e->K = K;
+  e->s_max = s_max;
+  e->user = static_cast<cudaStream_t>(cuda_stream);
+  e->has_dft = dft != nullptr;
+  e->drafter = dft ? SF_DRAFT_NEURAL : SF_DRAFT_NGRAM;
+  auto bail = [&](sf_status s) {
+    sf_destroy(e);
+    return s;
+  };
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return bail(fail(SF_ERR_CUDA, "no CUDA device"));
+  e->slots = 2 * e->num_sms;
+  sf_status r = bind_model(e, e->tgt, tgt, tgt_w, static_cast<bf16*>(kv_t));
+  if (r != SF_OK) return bail(r);
+  if (dft && (r = bind_model(e, e->dft, dft, dft_w, static_cast<bf16*>(kv_d))) != SF_OK) return bail(r);
+
+  e->lay = make_layout(tgt, dft, batch, K, s_max);
+  e->so = state_offsets(batch, K, s_max);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  e->ws = ws;
+  e->x = reinterpret_cast<float*>(ws + e->lay.x);
+  e->ssq = reinterpret_cast<float*>(ws + e->lay.ssq);
+  e->q = reinterpret_cast<float*>(ws + e->lay.q);
+  e->attn_o = reinterpret_cast<float*>(ws + e->lay.attn_o);
+  e->act = reinterpret_cast<float*>(ws + e->lay.act);
+  e->apart = reinterpret_cast<float*>(ws + e->lay.apart);
+  e->gpart = reinterpret_cast<float*>(ws + e->lay.gpart);
+  e->counters = reinterpret_cast<int*>(ws + e->lay.counters);
+  e->keys = reinterpret_cast<unsigned long long*>(ws + e->lay.keys);
+  e->done = reinterpret_cast<int*>(ws + e->lay.done);
+  e->zeros = reinterpret_cast<int*>(ws + e->lay.zeros);
+  e->tgt.rope = reinterpret_cast<float2*>(ws + e->lay.rope_t);
+  if (dft) e->dft.rope = reinterpret_cast<float2*>(ws + e->lay.rope_d);
+  int* S = reinterpret_cast<int*>(ws + e->lay.state);
+  SpecState& st = e->st;
+  st.len_t = S + e->so.len_t;
+  st.len_d = S + e->so.len_d;
+  st.vtok = S + e->so.vtok;
+  st.ttok = S + e->so.ttok;
+  st.dtok0 = S + e->so.dtok0;
+  st.nprop = S + e->so.nprop;
+  st.hist = S + e->so.hist;
+  st.prompt_len = S + e->so.prompt_len;
+  st.acc_hist = S + e->so.acc_hist;
+  st.ncommit = S + e->so.ncommit;
+  st.nacc = S + e->so.nacc;
+  st.commit = S + e->so.commit;
+  st.total = S + e->so.total;
+  st.err = S + e->so.err;
+  st.B = batch;
+  st.K = K;
+  st.s_max = s_max;
+  e->C.assign(batch, 0);
+
+  cudaError_t ce;
+  if ((ce = gemm_init()) != cudaSuccess) return bail(fail(SF_ERR_CUDA, "gemm_init: %s", cudaGetErrorString(ce)));
+  // Zero everything that must start at zero: counters, keys, state.
+  if ((ce = cudaMemsetAsync(ws + e->lay.counters, 0, e->lay.rope_t - e->lay.counters, e->user)) ||
+      (ce = cudaMemsetAsync(ws + e->lay.state, 0, e->so.n_ints * 4, e->user)) ||
+      (ce = launch_rope_table(e->tgt.rope, s_max, tgt->head_dim, tgt->rope_theta, e->user)) ||
+      (dft && (ce = launch_rope_table(e->dft.rope, s_max, dft->head_dim, dft->rope_theta, e->user))) ||
+      (ce = cudaStreamCreateWithFlags(&e->cap, cudaStreamNonBlocking)) ||
+      (ce = cudaHostAlloc(reinterpret_cast<void**>(&e->pin), e->so.report_ints * sizeof(int) + 64,
+                          cudaHostAllocDefault)) ||
+      (ce = cudaStreamSynchronize(e->user)))
+    return bail(fail(SF_ERR_CUDA, "sf_create set-up: %s", cudaGetErrorString(ce)));
+  *out = e;
+  return SF_OK;
+}
+
+void sf_destroy(sf_handle h) {
+  if (!h) return;
+  for (auto& g : h->graph)
+    if (g) cudaGraphExecDestroy(g);
+  if (h->g_draft) cudaGraphExecDestroy(h->g_draft);
+  if (h->g_verify) cudaGraphExecDestroy(h->g_verify);
+  if (h->cap) cudaStreamDestroy(h->cap);
+  if (h->pin) cudaFreeHost(h->pin);
+  delete h;
+}
+
+sf_status sf_prefill(sf_handle h, const int32_t* h_tokens, const int32_t* h_lens, int32_t stride) {
+  if (!h || !h_tokens || !h_lens) return fail(SF_ERR_ARG, "null argument");
+  const int P = h_lens[0];
+  for (int b = 0; b < h->B; ++b)
+    if (h_lens[b] != P) return fail(SF_ERR_UNSUPPORTED, "prompts of different lengths are not supported yet");
+  if (P < 2 || stride < P) return fail(SF_ERR_ARG, "prompt length must be >= 2 and <= stride");
+  if (P + h->K + 1 > h->s_max) return fail(SF_ERR_CAPACITY, "prompt of %d tokens leaves no room for a round", P);
+  for (int b = 0; b < h->B; ++b)
+    for (int i = 0; i < P; ++i) {
+      const int t = h_tokens[(size_t)b * stride + i];
+      if (t < 0 || t >= h->tgt.c.vocab) return fail(SF_ERR_ARG, "token %d out of range at [%d][%d]", t, b, i);
+    }
+  for (int b = 0; b < h->B; ++b)
+    CK(cudaMemcpyAsync(h->st.hist + (size_t)b * h->s_max, h_tokens + (size_t)b * stride, P * sizeof(int),
+                       cudaMemcpyHostToDevice, h->user));
+  std::vector<int> lens(h->B, P);
+  CK(cudaMemcpyAsync(h->st.prompt_len, lens.data(), h->B * sizeof(int), cudaMemcpyHostToDevice, h->user));
+  CK(launch_reset(h->st, h->user));
+  // Fill the caches with prompt[0..P-1) in chunks of SF_MAX_ROWS rows.
+  const int cl = SF_MAX_ROWS / h->B;
+  for (Model* md : {&h->tgt, &h->dft}) {
+    if (md == &h->dft && !h->has_dft) continue;
+    for (int start = 0; start < P - 1; start += cl) {
+      const int n = std::min(cl, P - 1 - start);
+      RowSet rs{h->st.hist, h->s_max, start, n, h->B * n, h->zeros, start};
+      sf_status r = forward(h, *md, rs, false, TokOut(), h->user);
+      if (r != SF_OK) return r;
+    }
+  }
+  CK(cudaStreamSynchronize(h->user));
+  h->P = P;
+  h->C.assign(h->B, P);
+  h->phase = 1;
+  h->draft_stale = false;
+  return SF_OK;
+}
+
+sf_status sf_reset(sf_handle h) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase == 0) return fail(SF_ERR_STATE, "no prompt loaded");
+  CK(launch_reset(h->st, h->user));
+  CK(cudaStreamSynchronize(h->user));
+  h->C.assign(h->B, h->P);
+  h->phase = 1;
+  h->draft_stale = false;
+  return SF_OK;
+}
+
+sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (mode != SF_DRAFT_NEURAL && mode != SF_DRAFT_NGRAM) return fail(SF_ERR_ARG, "unknown drafter");
+  if (mode == SF_DRAFT_NEURAL && !h->has_dft) return fail(SF_ERR_STATE, "no draft model");
+  if (mode == SF_DRAFT_NGRAM && (min_n < 1 || max_n < min_n || max_n > 64))
+    return fail(SF_ERR_ARG, "need 1 <= min_n <= max_n <= 64");
+  if (mode == SF_DRAFT_NGRAM && (min_n != h->ng_min || max_n != h->ng_max)) {
+    if (h->graph[SF_DRAFT_NGRAM]) {
+      cudaGraphExecDestroy(h->graph[SF_DRAFT_NGRAM]);
+      h->graph[SF_DRAFT_NGRAM] = nullptr;
+    }
+    h->ng_min = min_n;
+    h->ng_max = max_n;
+  }
+  h->drafter = mode;
+  return SF_OK;
+}
+
+sf_status sf_draft(sf_handle h, int32_t* d_draft, float* d_logits) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (!h->has_dft) return fail(SF_ERR_STATE, "no draft model");
+  if (h->phase != 1) return fail(SF_ERR_STATE, "sf_draft needs a prefilled engine between rounds");
+  if (h->draft_stale) return fail(SF_ERR_STATE, "draft cache is behind after n-gram rounds; call sf_reset or sf_prefill");
+  if (max_committed(h) + h->K + 1 > h->s_max) return fail(SF_ERR_CAPACITY, "round would exceed s_max");
+  sf_status r;
+  if (!d_draft && !d_logits) {
+    if ((r = build_graph(h, CAP_DRAFT)) != SF_OK) return r;
+    CK(cudaGraphLaunch(h->g_draft, h->user));
+  } else if ((r = enqueue_draft(h, d_logits, h->user)) != SF_OK) {
+    return r;
+  }
+  if (d_draft) CK(launch_copy_draft(h->st, d_draft, h->user));
+  h->phase = 2;
+  h->drafted_mode = SF_DRAFT_NEURAL;
+  return SF_OK;
+}
+
+sf_status sf_ngram_draft(sf_handle h, int32_t max_guess, int32_t min_n, int32_t max_n, int32_t* d_prop,
+                         int32_t* d_count) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase != 1) return fail(SF_ERR_STATE, "sf_ngram_draft needs a prefilled engine between rounds");
+  if (max_guess < 1 || max_guess > h->K || min_n < 1 || max_n < min_n || max_n > 64)
+    return fail(SF_ERR_ARG, "need 1 <= max_guess <= K and 1 <= min_n <= max_n <= 64");
+  if (max_committed(h) + h->K + 1 > h->s_max) return fail(SF_ERR_CAPACITY, "round would exceed s_max");
+  CK(launch_ngram(h->st, max_guess, min_n, max_n, d_prop, d_count, h->user, false));
+  h->phase = 2;
+  h->drafted_mode = SF_DRAFT_NGRAM;
+  return SF_OK;
+}
+
+sf_status sf_verify(sf_handle h, int32_t* d_tgt_argmax, float* d_logits) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase != 2) return fail(SF_ERR_STATE, "sf_verify needs a draft first");
+  sf_status r;
+  if (!d_tgt_argmax && !d_logits) {
+    if ((r = build_graph(h, CAP_VERIFY)) != SF_OK) return r;
+    CK(cudaGraphLaunch(h->g_verify, h->user));
+  } else if ((r = enqueue_verify(h, d_logits, h->user)) != SF_OK) {
+    return r;
+  }
+  if (d_tgt_argmax)
+    CK(cudaMemcpyAsync(d_tgt_argmax, h->st.ttok, h->B * (h->K + 1) * sizeof(int), cudaMemcpyDeviceToDevice,
+                       h->user));
+  h->phase = 3;
+  return SF_OK;
+}
+
+static void copy_out(sf_handle h, int32_t* h_n_accepted, int32_t* h_committed, int32_t* h_n_committed) {
+  const int* rep = h->pin;
+  const int K1 = h->K + 1;
+  for (int b = 0; b < h->B; ++b) {
+    if (h_n_committed) h_n_committed[b] = rep[h->so.ncommit - h->so.report + b];
+    if (h_n_accepted) h_n_accepted[b] = rep[h->so.nacc - h->so.report + b];
+    if (h_committed)
+      for (int j = 0; j < K1; ++j) h_committed[b * K1 + j] = rep[h->so.commit - h->so.report + b * K1 + j];
+  }
+}
+
+sf_status sf_accept_rollback(sf_handle h, int32_t* h_n_accepted, int32_t* h_committed, int32_t* h_n_committed) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase != 3) return fail(SF_ERR_STATE, "sf_accept_rollback needs a verify first");
+  CK(launch_accept(h->st, h->drafted_mode, h->user, false));
+  h->phase = 1;
+  if (h->drafted_mode == SF_DRAFT_NGRAM && h->has_dft) h->draft_stale = true;
+  sf_status r = sync_report(h);
+  if (r != SF_OK) return r;
+  copy_out(h, h_n_accepted, h_committed, h_n_committed);
+  return SF_OK;
+}
+
+sf_status sf_step(sf_handle h, int32_t* h_n_committed, int32_t* h_committed) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase != 1) return fail(SF_ERR_STATE, "sf_step needs a prefilled engine between rounds");
+  const int mode = h->drafter;
+  if (mode == SF_DRAFT_NEURAL && h->draft_stale)
+    return fail(SF_ERR_STATE, "draft cache is behind after n-gram rounds; call sf_reset or sf_prefill");
+  if (max_committed(h) + h->K + 1 > h->s_max) return fail(SF_ERR_CAPACITY, "round would exceed s_max");
+  sf_status r = build_graph(h, mode);
+  if (r != SF_OK) return r;
+  CK(cudaGraphLaunch(h->graph[mode], h->user));
+  if (mode == SF_DRAFT_NGRAM && h->has_dft) h->draft_stale = true;
+  if ((r = sync_report(h)) != SF_OK) return r;
+  copy_out(h, nullptr, h_committed, h_n_committed);
+  return SF_OK;
+}
+
+sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rounds) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase != 1) return fail(SF_ERR_STATE, "sf_generate needs a prefilled engine between rounds");
+  if (n_new < 1) return fail(SF_ERR_ARG, "n_new must be >= 1");
+  const int mode = h->drafter;
+  if (mode == SF_DRAFT_NEURAL && h->draft_stale)
+    return fail(SF_ERR_STATE, "draft cache is behind after n-gram rounds; call sf_reset or sf_prefill");
+  sf_status r = build_graph(h, mode);
+  if (r != SF_OK) return r;
+  const int K1 = h->K + 1;
+  int rounds = 0;
+  for (;;) {
+    int gen_min = 1 << 30;
+    for (int b = 0; b < h->B; ++b) gen_min = std::min(gen_min, h->C[b] - h->P);
+    const int remaining = n_new - gen_min;
+    if (remaining <= 0) break;
+    // Each round commits at most K+1 tokens, so this many rounds never
+    // overshoots the target by more than one round's worth.
+    int R = (remaining + K1 - 1) / K1;
+    const int room = (h->s_max - h->K - 1 - max_committed(h)) / K1;
+    R = std::min(R, room);
+    if (R < 1) return fail(SF_ERR_CAPACITY, "s_max reached after %d new tokens", gen_min);
+    for (int i = 0; i < R; ++i) CK(cudaGraphLaunch(h->graph[mode], h->user));
+    rounds += R;
+    if (mode == SF_DRAFT_NGRAM && h->has_dft) h->draft_stale = true;
+    if ((r = sync_report(h)) != SF_OK) return r;
+  }
+  if (h_out)
+    for (int b = 0; b < h->B; ++b)
+      CK(cudaMemcpyAsync(h_out + (size_t)b * n_new, h->st.hist + (size_t)b * h->s_max + h->P, n_new * sizeof(int),
+                         cudaMemcpyDeviceToHost, h->user));
+  CK(cudaStreamSynchronize(h->user));
+  if (h_rounds) *h_rounds = rounds;
+  return SF_OK;
+}
+
+sf_status sf_get_lengths(sf_handle h, int32_t* h_len_t, int32_t* h_len_d) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h_len_t) CK(cudaMemcpyAsync(h_len_t, h->st.len_t, h->B * sizeof(int), cudaMemcpyDeviceToHost, h->user));
+  if (h_len_d) CK(cudaMemcpyAsync(h_len_d, h->st.len_d, h->B * sizeof(int), cudaMemcpyDeviceToHost, h->user));
+  CK(cudaStreamSynchronize(h->user));
+  return SF_OK;
+}
+
+sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist) {
+  if (!h || !h_hist) return fail(SF_ERR_ARG, "null argument");
+  CK(cudaMemcpyAsync(h_hist, h->st.acc_hist, h->B * (h->K + 1) * sizeof(int), cudaMemcpyDeviceToHost, h->user));
+  CK(cudaStreamSynchronize(h->user));
+  return SF_OK;
+}
+
+size_t sf_linear_workspace_bytes(int32_t N, int32_t K) {
+  if (N < 1 || K < 8 || K % 8) return 0;
+  return align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4) + align256((size_t)((N + 127) / 128) * 4);
+}
+
+sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M, float* d_y,
+                    void* d_workspace, void* cuda_stream) {
+  if (!d_w || !d_x || !d_y || !d_workspace) return fail(SF_ERR_ARG, "null pointer");
+  if (N < 1 || K < 8 || K % 8 || ld < K || ld % 8 || M < 1 || M > SF_MAX_ROWS)
+    return fail(SF_ERR_ARG, "need N >= 1, K and ld multiples of 8 with ld >= K, 1 <= M <= %d", SF_MAX_ROWS);
+  if ((reinterpret_cast<uintptr_t>(d_w) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
+      (reinterpret_cast<uintptr_t>(d_workspace) & 255))
+    return fail(SF_ERR_ARG, "W and x must be 16-byte aligned, the workspace 256-byte aligned");
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const Plan p = make_plan((N + 127) / 128, K, 2 * sms);
+  if (p.nsplit > 1 && p.nblocks * p.nsplit > kMaxPlanTiles) return fail(SF_ERR_UNSUPPORTED, "plan too large");
+  CK(gemm_init());
+  unsigned char* ws = static_cast<unsigned char*>(d_workspace);
+  const size_t part_bytes = align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * 4, st));
+  GemmArgs a{};
+  a.w[0] = d_w;
+  a.seg_end[0] = N;
+  a.ld[0] = ld;
+  a.nseg = 1;
+  a.N = N;
+  a.K = K;
+  a.nblocks = p.nblocks;
+  a.nsplit = p.nsplit;
+  a.cps = p.cps;
+  a.in = d_x;
+  a.in_ld = K;
+  a.part = reinterpret_cast<float*>(ws);
+  a.counter = reinterpret_cast<int*>(ws + part_bytes);
+  a.out = d_y;
+  a.out_ld = N;
+  a.rs.M = M;
+  a.rs.rps = M;
+  CK(launch_gemm(a, EPI_STORE, st, false));
+  return SF_OK;
+}
+
+sf_status sf_nf4_quantize(const void* d_w, int32_t rows, int32_t cols, int32_t ld, void* d_packed, void* d_scales,
+                          void* cuda_stream) {
+  if (!d_w || !d_packed || !d_scales) return fail(SF_ERR_ARG, "null pointer");
+  if (rows < 1 || cols < 64 || cols % 64 || ld < cols) return fail(SF_ERR_ARG, "need cols a multiple of 64 and ld >= cols");
+  CK(launch_nf4_quantize(static_cast<const bf16*>(d_w), rows, cols, ld, static_cast<uint8_t*>(d_packed),
+                         static_cast<__half*>(d_scales), static_cast<cudaStream_t>(cuda_stream)));
+  return SF_OK;
+}
+
+}  // extern "C"

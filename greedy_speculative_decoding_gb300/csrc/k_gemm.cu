@@ -1,0 +1,403 @@
+// Skinny bf16 GEMM for decode (1-2 rows) and verify (K+1 rows) on sm_103a.
+//
+// The work is weight streaming: y[m][n] = sum_k a[m][k] W[n][k] with at most
+// SF_MAX_ROWS token rows m, so every weight byte is read once and used by all
+// rows. Each CTA owns 128 output rows (8 warps x 16) and one slice of K; each
+// warp streams its 16 weight rows straight from HBM into registers with
+// 128-bit non-allocating loads (a whole 128-byte line per row per step) and
+// feeds them to mma.sync m16n8k16 as the A operand ("swap AB": weights are
+// the M side, tokens the N side). The token activations are staged in
+// shared memory, converted to a bf16 pair (hi + lo) so that the product keeps
+// about 16 mantissa bits of the fp32 activation; hi and lo of one token sit
+// in adjacent columns of the n8 tile and are summed in the epilogue.
+//
+// Inside an MMA the order of k does not matter as long as A and B agree, so
+// each thread takes 16 consecutive k of its rows and the activation tile is
+// laid out in the matching "fragment order" (conflict-free 128-bit reads).
+//
+// Every row's arithmetic is independent of how many rows are present (same
+// K split, same MMA sequence, same reduction order), so a verify row equals
+// the decode of the same token at the same position bit for bit.
+//
+// Split-K partial tiles go to a global scratch area; the last CTA of a row
+// block (arrival counter) adds them in fixed slice order and runs the
+// epilogue, so results are deterministic without float atomics.
+#include "sf_kernels.h"
+
+namespace sf {
+
+namespace {
+
+constexpr int kPf = 2;   // chunks of weights in flight per thread
+
+template <int EPI>
+__device__ __forceinline__ const bf16* weight_row(const GemmArgs& a, int rb, int r) {
+  if (EPI == EPI_SWIGLU) {
+    const int f = rb * 64 + (r & 63);
+    if (f >= a.N) return nullptr;
+    return static_cast<const bf16*>(a.w[r >> 6]) + (size_t)f * a.ld[0];
+  } else {
+    const int n = rb * kBlockRows + r;
+    if (n >= a.N) return nullptr;
+    int s = 0;
+    while (s < a.nseg - 1 && n >= a.seg_end[s]) ++s;
+    const int base = s ? a.seg_end[s - 1] : 0;
+    return static_cast<const bf16*>(a.w[s]) + (size_t)(n - base) * a.ld[s];
+  }
+}
+
+__device__ __forceinline__ void load_chunk(uint4 (&w)[4], const bf16* p0, const bf16* p1, int k, int K) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  w[0] = (p0 && k < K) ? ldg_stream(p0 + k) : z;
+  w[1] = (p0 && k + 8 < K) ? ldg_stream(p0 + k + 8) : z;
+  w[2] = (p1 && k < K) ? ldg_stream(p1 + k) : z;
+  w[3] = (p1 && k + 8 < K) ? ldg_stream(p1 + k + 8) : z;
+}
+
+// Stage activation chunks [wc0, wc0 + nwc) of this CTA (absolute chunk index
+// c0 + wc) into fragment order: [wc][t][h][lane][8] bf16, lane = 4*col + c
+// with col = 2*(m%4) + {0: hi, 1: lo}, and k = 64*chunk + 16*c + 8*h + e.
+template <int T>
+__device__ __forceinline__ void stage_acts(const GemmArgs& a, uint2* act, const float* rinv, int cabs0,
+                                           int nwc, int M) {
+  const int per_m = nwc * 16;  // groups of 4 k per token row
+  for (int idx = threadIdx.x; idx < 4 * T * per_m; idx += kGemmThreads) {
+    const int m = idx / per_m;
+    const int q4 = idx - m * per_m;
+    const int k = cabs0 * kChunk + q4 * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < M && k < a.K) {
+      v = *reinterpret_cast<const float4*>(a.in + (size_t)m * a.in_ld + k);
+      if (a.gain) {
+        const float r = rinv[m];
+        const uint2 gg = *reinterpret_cast<const uint2*>(a.gain + k);
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg.x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg.y));
+        v.x = (v.x * r) * g01.x;
+        v.y = (v.y * r) * g01.y;
+        v.z = (v.z * r) * g23.x;
+        v.w = (v.w * r) * g23.y;
+      }
+    }
+    const bf16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
+    const bf16 h2 = __float2bfloat16_rn(v.z), h3 = __float2bfloat16_rn(v.w);
+    const bf16 l0 = __float2bfloat16_rn(v.x - __bfloat162float(h0));
+    const bf16 l1 = __float2bfloat16_rn(v.y - __bfloat162float(h1));
+    const bf16 l2 = __float2bfloat16_rn(v.z - __bfloat162float(h2));
+    const bf16 l3 = __float2bfloat16_rn(v.w - __bfloat162float(h3));
+    const int wc = q4 >> 4;
+    const int kk = (q4 & 15) * 4;
+    const int c = kk >> 4, h = (kk >> 3) & 1, e = kk & 7;
+    const int t = m >> 2, col = 2 * (m & 3);
+    const int base = ((wc * T + t) * 2 + h) * 32;     // in 16-byte units
+    // uint2 index: 16-byte unit * 2 + (e / 4)
+    act[(base + 4 * col + c) * 2 + (e >> 2)] = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+    act[(base + 4 * (col + 1) + c) * 2 + (e >> 2)] = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+  }
+}
+
+template <int T>
+__device__ __forceinline__ void mma_chunk(float (&acc)[T][4], const uint4 (&w)[4], const uint4* act, int wc,
+                                          int lane) {
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const uint4 b0 = act[((wc * T + t) * 2 + 0) * 32 + lane];
+    const uint4 b1 = act[((wc * T + t) * 2 + 1) * 32 + lane];
+    mma_bf16_16816(acc[t], w[0].x, w[2].x, w[0].y, w[2].y, b0.x, b0.y);
+    mma_bf16_16816(acc[t], w[0].z, w[2].z, w[0].w, w[2].w, b0.z, b0.w);
+    mma_bf16_16816(acc[t], w[1].x, w[3].x, w[1].y, w[3].y, b1.x, b1.y);
+    mma_bf16_16816(acc[t], w[1].z, w[3].z, w[1].w, w[3].w, b1.z, b1.w);
+  }
+}
+
+__device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------- epilogues
+__device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M) {
+  for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
+    const int m = i / kBlockRows, r = i - m * kBlockRows;
+    const int n = rb * kBlockRows + r;
+    float v = 0.f;
+    if (n < a.N) {
+      float* px = a.out + (size_t)m * a.out_ld + n;
+      v = *px + ys[i];
+      *px = v;
+    }
+    ys[i] = v;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int m = warp; m < M; m += kGemmThreads / 32) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = ys[m * kBlockRows + lane + 32 * j];
+      s = fmaf(v, v, s);
+    }
+    s = warp_sum(s);
+    if (lane == 0) a.ssq_out[rb * kRows + m] = s;
+  }
+}
+
+__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M) {
+  const int half = a.hd >> 1;
+  for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
+    const int m = i / kBlockRows, r = i - m * kBlockRows;
+    const int n = rb * kBlockRows + r;
+    if (n >= a.N) continue;
+    const int s = n < a.seg_end[0] ? 0 : (n < a.seg_end[1] ? 1 : 2);
+    const int local = n - (s ? a.seg_end[s - 1] : 0);
+    const bf16* bias = a.bias[s];
+    const int b = m / a.rs.rps;
+    const int pos = row_pos(a.rs, m);
+    const int d = local % a.hd;
+    if (s == 2) {
+      const float v = ys[i] + (bias ? __bfloat162float(bias[local]) : 0.f);
+      const int kvh = local / a.hd;
+      a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(v);
+      continue;
+    }
+    if (d >= half) continue;
+    const float x1 = ys[i] + (bias ? __bfloat162float(bias[local]) : 0.f);
+    const float x2 = ys[i + half] + (bias ? __bfloat162float(bias[local + half]) : 0.f);
+    const float2 cs = a.rope[(size_t)pos * half + d];
+    const float y1 = x1 * cs.x - x2 * cs.y;
+    const float y2 = x2 * cs.x + x1 * cs.y;
+    if (s == 0) {
+      float* q = a.out + (size_t)m * a.out_ld + local;
+      q[0] = y1;
+      q[half] = y2;
+    } else {
+      const int kvh = local / a.hd;
+      bf16* kp = a.kc + (((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d;
+      kp[0] = __float2bfloat16_rn(y1);
+      kp[half] = __float2bfloat16_rn(y2);
+    }
+  }
+}
+
+__device__ void epi_swiglu(const GemmArgs& a, const float* ys, int rb, int M) {
+  for (int i = threadIdx.x; i < M * 64; i += kGemmThreads) {
+    const int m = i >> 6, j = i & 63;
+    const int f = rb * 64 + j;
+    if (f >= a.N) continue;
+    const float gte = ys[m * kBlockRows + j];
+    const float up = ys[m * kBlockRows + 64 + j];
+    a.out[(size_t)m * a.out_ld + f] = gte / (1.0f + expf(-gte)) * up;
+  }
+}
+
+__device__ void epi_store(const GemmArgs& a, const float* ys, int rb, int M) {
+  for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
+    const int m = i / kBlockRows, r = i - m * kBlockRows;
+    const int n = rb * kBlockRows + r;
+    if (n < a.N) a.out[(size_t)m * a.out_ld + n] = ys[i];
+  }
+}
+
+__device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, int* s_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int m = warp; m < M; m += kGemmThreads / 32) {
+    unsigned long long best = 0ull;
+    bool bad = false;
+    const int mb = m / a.rs.rps, mj = m - mb * a.rs.rps;
+    const int lg_row = mj >= a.tok_skip ? mb * a.lg_stride + a.lg_off + mj - a.tok_skip : -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = lane + 32 * j;
+      const int n = rb * kBlockRows + r;
+      if (n < a.N) {
+        const float v = ys[m * kBlockRows + r];
+        if (a.logits && lg_row >= 0) a.logits[(size_t)lg_row * a.N + n] = v;
+        bad |= !isfinite(v);
+        const unsigned long long k = argmax_key(v, n);
+        best = k > best ? k : best;
+      }
+    }
+    best = shfl_max_u64(best);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, kErrNonfinite);
+    if (lane == 0) atomicMax(a.keys + m, best);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.done, 1) == a.nblocks - 1);
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  if (threadIdx.x < M) {
+    const int m = threadIdx.x;
+    const unsigned long long k = atomicExch(a.keys + m, 0ull);
+    const int b = m / a.rs.rps, j = m - b * a.rs.rps;
+    if (j >= a.tok_skip) a.tok_out[b * a.tok_stride + a.tok_off + j - a.tok_skip] = key_index(k);
+  }
+  if (threadIdx.x == 0) *a.done = 0;
+}
+
+}  // namespace
+
+template <int T, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant__ GemmArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint4* act = reinterpret_cast<uint4*>(smem);
+  float* ys = reinterpret_cast<float*>(smem + kWinChunks * T * 1024);
+  float* rinv = ys + 4 * T * kBlockRows;
+  __shared__ int s_flag;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int rb = blockIdx.x / a.nsplit, sp = blockIdx.x - rb * a.nsplit;
+  const int nch_total = (a.K + kChunk - 1) / kChunk;
+  const int c0 = sp * a.cps;
+  const int nch = min(a.cps, nch_total - c0);
+
+  const int r0 = warp * 16 + g;
+  const bf16* p0 = weight_row<EPI>(a, rb, r0);
+  const bf16* p1 = weight_row<EPI>(a, rb, r0 + 8);
+  const int koff = c0 * kChunk + 16 * c;
+
+  // Weights are never written by the preceding kernels: start streaming them
+  // before waiting on the producer of the activations.
+  uint4 ring[kPf][4];
+#pragma unroll
+  for (int i = 0; i < kPf; ++i)
+    if (i < nch) load_chunk(ring[i], p0, p1, koff + i * kChunk, a.K);
+
+  pdl_wait();
+  pdl_launch_next();
+  const int M = a.rs.M;
+  if (a.gain && tid < M) {
+    float s = 0.f;
+    for (int i = 0; i < a.nssq; ++i) s += a.ssq[i * kRows + tid];
+    rinv[tid] = 1.0f / sqrtf(s * a.inv_k + a.eps);
+  }
+  __syncthreads();
+  stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0, min(nch, kWinChunks), M);
+  __syncthreads();
+
+  float acc[T][4];
+#pragma unroll
+  for (int t = 0; t < T; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+
+  for (int base = 0; base < nch; base += kPf) {
+#pragma unroll
+    for (int i = 0; i < kPf; ++i) {
+      const int ch = base + i;
+      if (ch < nch) {
+        if (ch > 0 && (ch % kWinChunks) == 0) {
+          __syncthreads();
+          stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
+          __syncthreads();
+        }
+        uint4 w[4] = {ring[i][0], ring[i][1], ring[i][2], ring[i][3]};
+        if (ch + kPf < nch) load_chunk(ring[i], p0, p1, koff + (ch + kPf) * kChunk, a.K);
+        mma_chunk<T>(acc, w, act, ch % kWinChunks, lane);
+      }
+    }
+  }
+
+  // Token m = 4t + c: hi in column 2c, lo in column 2c + 1.
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const int m = 4 * t + c;
+    ys[m * kBlockRows + r0] = acc[t][0] + acc[t][1];
+    ys[m * kBlockRows + r0 + 8] = acc[t][2] + acc[t][3];
+  }
+  __syncthreads();
+
+  if (a.nsplit > 1) {
+    float* mine = a.part + ((size_t)rb * a.nsplit + sp) * (kRows * kBlockRows);
+    for (int i = tid; i < M * kBlockRows; i += kGemmThreads) __stcg(mine + i, ys[i]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_flag = (atomicAdd(a.counter + rb, 1) == a.nsplit - 1);
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    const float* src = a.part + (size_t)rb * a.nsplit * (kRows * kBlockRows);
+    for (int i = tid; i < M * kBlockRows; i += kGemmThreads) {
+      float s = __ldcg(src + i);
+      for (int p = 1; p < a.nsplit; ++p) s += __ldcg(src + (size_t)p * (kRows * kBlockRows) + i);
+      ys[i] = s;
+    }
+    if (tid == 0) a.counter[rb] = 0;
+    __syncthreads();
+  }
+
+  if (EPI == EPI_RESID) epi_resid(a, ys, rb, M);
+  else if (EPI == EPI_QKV) epi_qkv(a, ys, rb, M);
+  else if (EPI == EPI_SWIGLU) epi_swiglu(a, ys, rb, M);
+  else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
+  else epi_argmax(a, ys, rb, M, &s_flag);
+}
+
+int gemm_smem_bytes(int M) {
+  const int T = (M + 3) / 4;
+  return kWinChunks * T * 1024 + 4 * T * kBlockRows * 4 + 4 * T * 4;
+}
+
+template <int T, int EPI>
+static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nblocks * a.nsplit);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_gemm<T, EPI>, a);
+}
+
+template <int T>
+static cudaError_t init_t() {
+  const int smem = gemm_smem_bytes(4 * T);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+  return cudaFuncSetAttribute(k_gemm<T, EPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+// Raise the dynamic shared-memory limit of every instantiation (current device).
+cudaError_t gemm_init() {
+  cudaError_t e;
+  if ((e = init_t<1>())) return e;
+  if ((e = init_t<2>())) return e;
+  if ((e = init_t<3>())) return e;
+  return init_t<4>();
+}
+
+template <int EPI>
+static cudaError_t launch_e(const GemmArgs& a, cudaStream_t st, bool pdl) {
+  switch ((a.rs.M + 3) / 4) {
+    case 1: return launch_t<1, EPI>(a, st, pdl);
+    case 2: return launch_t<2, EPI>(a, st, pdl);
+    case 3: return launch_t<3, EPI>(a, st, pdl);
+    case 4: return launch_t<4, EPI>(a, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
+  if (a.rs.M < 1 || a.rs.M > kRows) return cudaErrorInvalidValue;
+  switch (epi) {
+    case EPI_QKV: return launch_e<EPI_QKV>(a, st, pdl);
+    case EPI_RESID: return launch_e<EPI_RESID>(a, st, pdl);
+    case EPI_SWIGLU: return launch_e<EPI_SWIGLU>(a, st, pdl);
+    case EPI_ARGMAX: return launch_e<EPI_ARGMAX>(a, st, pdl);
+    case EPI_STORE: return launch_e<EPI_STORE>(a, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sf

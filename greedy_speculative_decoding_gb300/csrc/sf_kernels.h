@@ -1,0 +1,109 @@
+// Internal launch interface between the engine (host) and the kernels.
+#pragma once
+
+#include "sf_common.cuh"
+
+namespace sf {
+
+enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_STORE = 4 };
+
+// Skinny GEMM y[m][n] = sum_k a[m][k] * W[n][k] over up to SF_MAX_ROWS token
+// rows, with a fused prologue (optional RMSNorm of the fp32 input) and one of
+// five epilogues. Weights are bf16 row-major, or NF4 (packed codes + fp16
+// block scales) when nf4 != 0.
+struct GemmArgs {
+  const void* w[3];           // row segments (QKV: q, k, v; SWIGLU: gate, up)
+  const __half* scales[3];    // NF4 block scales per segment
+  const bf16* bias[3];
+  int seg_end[3];             // cumulative row ends of the segments
+  int ld[3];                  // row stride in elements (bf16) / codes (NF4)
+  int nseg;
+  int nf4;
+  int N, K;                   // output rows (SWIGLU: ffn features), reduction length
+  int nblocks, nsplit, cps;   // row blocks, K splits, chunks per split
+  // input activations fp32 [M][in_ld]; RMSNorm applied when gain != nullptr
+  const float* in;
+  int in_ld;
+  const float* ssq;           // [nssq][kRows] partial sums of squares of `in`
+  int nssq;
+  const bf16* gain;
+  float eps, inv_k;
+  // split-K scratch: partial tiles and per-row-block arrival counters
+  float* part;
+  int* counter;
+  // epilogue outputs
+  float* out;                 // QKV: q [M][q_dim]; RESID: x [M][H]; SWIGLU: act [M][F]; STORE: y [M][N]
+  int out_ld;
+  float* ssq_out;             // RESID: [nblocks][kRows]
+  int q_dim, kv_dim, hd, nkv, s_max;
+  bf16* kc;                   // this layer's key cache [B][nkv][s_max][hd]
+  bf16* vc;
+  const float2* rope;         // [s_max][hd/2] (cos, sin)
+  unsigned long long* keys;   // ARGMAX: [kRows] packed (value, index)
+  int* done;                  // ARGMAX: finished-block counter
+  int* tok_out;               // ARGMAX: token of row m -> tok_out[b*tok_stride + tok_off + j - tok_skip]
+  int tok_stride, tok_skip, tok_off;   // rows with j < tok_skip produce nothing
+  float* logits;              // ARGMAX: optional fp32 rows, row (b*lg_stride + lg_off + j - tok_skip)
+  int lg_stride, lg_off;
+  int* err;
+  RowSet rs;
+};
+
+int gemm_smem_bytes(int M);
+cudaError_t gemm_init();
+cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
+
+struct EmbedArgs {
+  const bf16* E;
+  int ld, H, vocab;
+  int* err;
+  float* x;      // [M][H]
+  float* ssq;    // [H/128][kRows]
+  RowSet rs;
+};
+cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl);
+
+struct AttnArgs {
+  const float* q;          // [M][nq*hd], RoPE applied
+  const bf16* kc;          // layer key cache [B][nkv][s_max][hd]
+  const bf16* vc;
+  float* part;             // [M*nq][n_kv_chunks][hd + 2]
+  float* out;              // [M][nq*hd]
+  int nq, nkv, hd, s_max, B, n_kv_chunks;
+  float scale;
+  int* err;
+  RowSet rs;
+};
+cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl);
+
+cudaError_t launch_rope_table(float2* table, int s_max, int hd, float theta, cudaStream_t st);
+
+// Engine state on the device (one sequence per b).
+struct SpecState {
+  int* len_t;       // [B] target cache length = committed - 1
+  int* len_d;       // [B] draft cache slots known valid (committed - 2)
+  int* vtok;        // [B][K+1] verify rows: pending, d_1..d_K
+  int* ttok;        // [B][K+1] target argmax per verify row
+  int* dtok0;       // [B][2] first draft step rows: the last two committed tokens
+  int* nprop;       // [B] real guesses this round
+  int* hist;        // [B][s_max] committed tokens
+  int* ncommit;     // [B] tokens committed by the last round
+  int* nacc;        // [B] accepted guesses of the last round
+  int* commit;      // [B][K+1] tokens committed by the last round
+  int* total;       // [B] tokens generated since prefill
+  int* acc_hist;    // [B][K+1] accept-length histogram
+  int* prompt_len;  // [B]
+  int* err;
+  int B, K, s_max;
+};
+
+cudaError_t launch_accept(const SpecState& s, int mode, cudaStream_t st, bool pdl);
+cudaError_t launch_ngram(const SpecState& s, int max_guess, int min_n, int max_n, int* d_prop,
+                         int* d_count, cudaStream_t st, bool pdl);
+cudaError_t launch_reset(const SpecState& s, cudaStream_t st);
+cudaError_t launch_copy_draft(const SpecState& s, int* d_draft, cudaStream_t st);
+void nf4_levels(double out[16]);
+cudaError_t launch_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8_t* packed,
+                                __half* scales, cudaStream_t st);
+
+}  // namespace sf

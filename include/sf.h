@@ -1,0 +1,232 @@
+/*
+ * sf.h — C ABI of the GB300 greedy speculative-decoding engine.
+ *
+ * One speculative round (the hot path) has four parts:
+ *   draft    — a small draft model decodes K tokens greedily over its own
+ *              static KV cache (sf_draft), or prompt lookup proposes up to K
+ *              tokens (sf_ngram_draft);
+ *   verify   — the target model runs one causal pass over the pending token
+ *              and the K guesses and returns its own greedy choice at every
+ *              position (sf_verify);
+ *   accept   — the longest prefix of guesses that agrees with the target's
+ *              choices is accepted, and the target's choice after it (the
+ *              bonus token) is committed as well;
+ *   rollback — both KV caches are cut back, in place, to the last committed
+ *              position (sf_accept_rollback).
+ * sf_step runs all four as one CUDA graph replay.
+ *
+ * Sources (page title, then section):
+ *   "I Got 28 TPS Out of Free Kaggle GPUs. Here's What It Took." —
+ *     "Speculative Decoding: The Idea" (draft guesses K tokens, the target
+ *     checks them in one pass, agreed tokens are committed);
+ *     "CUDA Graphs: What They Are and Why They Helped" (the whole draft
+ *     forward, LM head and argmax replayed as one driver call);
+ *     "Why It Kept Breaking (and How I Fixed It)" (static preallocated KV
+ *     cache, in-place intermediates, explicit position updates, in-place KV
+ *     rewind on rejection).
+ *   "Qwen3.5-397B on 20 GPUs, through a relay" (Sangama results) —
+ *     "Speculative decoding: correct, but slower (for now)" (look-back
+ *     guesses of up to 4 tokens from the last 2-4 tokens; the verifier returns
+ *     its own choice at every position; output equals normal decoding).
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller allocates and owns every device buffer (weights,
+ *     both KV caches, the workspace). They must stay valid until sf_destroy.
+ *     The library never allocates device memory; it allocates a little
+ *     pinned host memory and one CUDA stream in sf_create.
+ *   - Streams: all device work is enqueued on the stream given to sf_create.
+ *     Calls that return host results synchronise that stream.
+ *   - Errors: every call returns an sf_status and never aborts. On
+ *     SF_ERR_ARG, SF_ERR_CAPACITY or SF_ERR_STATE nothing was enqueued and
+ *     the engine state is unchanged. sf_last_error() gives a message for the
+ *     calling thread's last failure.
+ *   - Batch: sequences are independent; per-sequence lengths and accept
+ *     lengths are kept on the device.
+ *   - Rows per forward (batch * (K + 1)) are limited to SF_MAX_ROWS.
+ */
+#ifndef SF_H_
+#define SF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SF_API __attribute__((visibility("default")))
+#else
+#define SF_API
+#endif
+
+#define SF_MAX_ROWS 16
+
+typedef struct sf_engine* sf_handle;
+
+typedef enum {
+  SF_OK = 0,
+  SF_ERR_ARG = 1,          /* invalid argument, null or misaligned pointer */
+  SF_ERR_CAPACITY = 2,     /* a round would write past s_max cache slots */
+  SF_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  SF_ERR_NONFINITE = 4,    /* a non-finite logit was produced */
+  SF_ERR_STATE = 5,        /* call out of order (e.g. verify before draft) */
+  SF_ERR_UNSUPPORTED = 6,  /* shape or mode not supported by this build */
+  SF_ERR_DEVICE = 7        /* a kernel reported a bounded wait that expired */
+} sf_status;
+
+enum { SF_WDTYPE_BF16 = 0, SF_WDTYPE_NF4 = 1 };
+enum { SF_DRAFT_NEURAL = 0, SF_DRAFT_NGRAM = 1 };
+
+/* Decoder shape (Qwen2-style: GQA attention with RoPE, RMSNorm, SwiGLU MLP). */
+typedef struct {
+  int32_t layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int32_t tied;       /* 1: the LM head is the embedding matrix */
+  int32_t qkv_bias;   /* 1: q, k, v projections carry biases */
+  int32_t embed_ld;   /* row stride of the embedding in elements; 0 = hidden */
+  float rope_theta;   /* RoPE base */
+  float rms_eps;      /* RMSNorm epsilon */
+  int32_t wdtype;     /* SF_WDTYPE_BF16, or SF_WDTYPE_NF4 for the 7 linear
+                         maps of every layer (embedding, norms, LM head stay bf16) */
+} sf_model_cfg;
+
+/*
+ * Weight pointers (device, row-major [out, in], bf16 unless stated), in this
+ * order: embed [vocab, hidden] (row stride embed_ld); per layer: ln1 [hidden],
+ * wq [n_heads*head_dim, hidden], wk, wv [n_kv_heads*head_dim, hidden],
+ * bq, bk, bv (NULL when qkv_bias == 0), wo [hidden, n_heads*head_dim],
+ * ln2 [hidden], wg, wu [ffn, hidden], wd [hidden, ffn]; final norm [hidden];
+ * lm_head [vocab, hidden] (omitted when tied).
+ * With SF_WDTYPE_NF4 each of wq, wk, wv, wo, wg, wu, wd takes two consecutive
+ * slots: packed codes (uint8 [out, in/2], element 2i in the low nibble) then
+ * block scales (fp16 [out, in/64]).
+ * Every row must start on a 16-byte boundary.
+ * Returns the number of slots, or -1 for an invalid cfg.
+ */
+SF_API int32_t sf_weight_count(const sf_model_cfg* cfg);
+
+/* Bytes of one KV cache: layout [layers][2 (k, v)][batch][n_kv_heads][s_max][head_dim] bf16. */
+SF_API size_t sf_kv_bytes(const sf_model_cfg* cfg, int32_t batch, int32_t s_max);
+
+/* Bytes of device workspace sf_create needs (dft may be NULL: n-gram only). */
+SF_API size_t sf_workspace_bytes(const sf_model_cfg* tgt, const sf_model_cfg* dft, int32_t batch,
+                          int32_t K, int32_t s_max);
+
+/*
+ * Bind caller-owned buffers and build the engine. kv_d may be NULL when dft
+ * is NULL. workspace must hold sf_workspace_bytes(...) bytes, 256-byte
+ * aligned. K: guesses per round (1..15, batch*(K+1) <= SF_MAX_ROWS).
+ * s_max: cache slots per sequence, a multiple of 64.
+ * cuda_stream: a cudaStream_t (NULL = legacy default stream).
+ * The engine starts with SF_DRAFT_NEURAL when dft is given, else
+ * SF_DRAFT_NGRAM (max guess K, n from 4 down to 2).
+ */
+SF_API sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w,
+                    const sf_model_cfg* dft, const void* const* dft_w,
+                    int32_t batch, int32_t K, int32_t s_max,
+                    void* kv_t, void* kv_d, void* workspace, void* cuda_stream,
+                    sf_handle* out);
+
+/*
+ * Load prompts and fill both caches. h_tokens: host [batch][stride] int32,
+ * h_lens: host [batch] prompt lengths (>= 2, all equal in this build). After
+ * it, each cache holds the prompt except its last token, which is pending.
+ */
+SF_API sf_status sf_prefill(sf_handle h, const int32_t* h_tokens, const int32_t* h_lens, int32_t stride);
+
+/*
+ * Neural draft: K greedy decode steps of the draft model. Writes the guesses
+ * to the engine's device state and, when not NULL, to d_draft (device
+ * [batch][K] int32) and their logits to d_logits (device [batch][K][vocab]
+ * fp32). The first step runs two rows (the last two committed tokens) so the
+ * draft cache always catches up with the committed sequence. With both
+ * outputs NULL the K steps replay as one captured CUDA graph.
+ */
+SF_API sf_status sf_draft(sf_handle h, int32_t* d_draft, float* d_logits);
+
+/*
+ * Prompt-lookup draft: for n = max_n down to min_n, the rightmost earlier
+ * occurrence of the last n committed tokens; up to max_guess tokens that
+ * followed it are proposed (cut at the end of the context). Optional device
+ * outputs: d_prop [batch][max_guess] (unused slots 0), d_count [batch].
+ * max_guess must be <= K.
+ */
+SF_API sf_status sf_ngram_draft(sf_handle h, int32_t max_guess, int32_t min_n, int32_t max_n,
+                         int32_t* d_prop, int32_t* d_count);
+
+/*
+ * Target verify: one causal pass over [pending, d_1..d_K] per sequence,
+ * appending K+1 entries to the target cache. Optional device outputs: the
+ * target's argmax at every row (d_tgt_argmax [batch][K+1] int32) and the
+ * logits (d_logits [batch][K+1][vocab] fp32). Ties go to the lowest index.
+ * With both outputs NULL the pass replays as one captured CUDA graph.
+ */
+SF_API sf_status sf_verify(sf_handle h, int32_t* d_tgt_argmax, float* d_logits);
+
+/*
+ * Accept and roll back, per sequence: n = longest prefix of guesses equal to
+ * the target's choices (capped at the number of real guesses); d_1..d_n and
+ * the target's choice t_n are committed; both caches are cut back in place
+ * to the committed length minus one. Host outputs (may be NULL):
+ * h_n_accepted [batch], h_committed [batch][K+1], h_n_committed [batch].
+ */
+SF_API sf_status sf_accept_rollback(sf_handle h, int32_t* h_n_accepted, int32_t* h_committed,
+                             int32_t* h_n_committed);
+
+/* draft (neural or n-gram, per sf_set_drafter) + verify + accept/rollback as
+ * one CUDA graph replay. Host outputs as in sf_accept_rollback (may be NULL). */
+SF_API sf_status sf_step(sf_handle h, int32_t* h_n_committed, int32_t* h_committed);
+
+/*
+ * Run rounds until every sequence has at least n_new new tokens, replaying
+ * the step graph back to back and synchronising only to count. h_out: host
+ * [batch][n_new] (the first n_new generated tokens). h_rounds: rounds run
+ * (may be NULL).
+ */
+SF_API sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rounds);
+
+/* Rewind every sequence to its prompt (prefix already in the caches). */
+SF_API sf_status sf_reset(sf_handle h);
+
+/* Select the drafter used by sf_step / sf_generate. */
+SF_API sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n);
+
+/* Current cache lengths per sequence (host [batch] each, may be NULL). */
+SF_API sf_status sf_get_lengths(sf_handle h, int32_t* h_len_t, int32_t* h_len_d);
+
+/* Accept-length histogram since prefill: host [batch][K+1]. */
+SF_API sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist);
+
+SF_API const char* sf_status_str(sf_status s);
+SF_API const char* sf_last_error(void);
+SF_API void sf_destroy(sf_handle h);
+
+/*
+ * One skinny linear map on its own: y[m][n] = sum_k x[m][k] * W[n][k] for
+ * m < M (1..SF_MAX_ROWS), the weight-streaming GEMM every projection of the
+ * forward pass uses. W: device bf16 [N, ld] row-major (ld >= K, K and ld
+ * multiples of 8, 16-byte aligned rows); x: device fp32 [M, K]; y: device
+ * fp32 [M, N]. d_workspace: device scratch of
+ * sf_linear_workspace_bytes(N, K) bytes, 256-byte aligned, for split-K
+ * partial tiles and arrival counters (zeroed by the call). Enqueued on
+ * cuda_stream; returns without synchronising.
+ */
+SF_API size_t sf_linear_workspace_bytes(int32_t N, int32_t K);
+SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M,
+                           float* d_y, void* d_workspace, void* cuda_stream);
+
+/*
+ * Blockwise NF4 quantisation of a bf16 matrix on the device (a preparation
+ * step for SF_WDTYPE_NF4 weights): w [rows, cols] with row stride ld
+ * elements, cols a multiple of 64; writes packed codes [rows, cols/2] and fp16
+ * block scales [rows, cols/64]. Codebook: the NormalFloat construction of
+ * Dettmers et al., "QLoRA" (2023), section 3 (format named in "The Numbers").
+ */
+SF_API sf_status sf_nf4_quantize(const void* d_w, int32_t rows, int32_t cols, int32_t ld,
+                          void* d_packed, void* d_scales, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SF_H_ */

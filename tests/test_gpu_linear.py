@@ -1,0 +1,65 @@
+"""GPU parity of the weight-streaming GEMM (sf_linear) against a float64
+matrix product, over shapes that span several 128-row blocks and 64-wide K
+chunks with ragged tails, every row count 1..16, and K splits across CTAs.
+
+Error bound: the activation is carried as a bf16 pair (hi + lo, about 16
+mantissa bits) and products are summed in fp32, so |y - y_ref| stays within
+a small multiple of 2^-16 * sum_k |x_k w_nk|; the test allows 1e-4 of that sum.
+"""
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as p
+    return p
+
+
+def _check(pkg, N, K, M, ld=None, seed=0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    ld = ld or K
+    wfull = (torch.randn(N, ld, generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    w = wfull[:, :K]
+    x = torch.randn(M, K, generator=g, device="cuda")
+    y = pkg.linear(w, x)
+    torch.cuda.synchronize()
+    wd, xd = w.double(), x.double()
+    ref = xd @ wd.t()
+    bound = xd.abs() @ wd.abs().t()
+    err = (y.double() - ref).abs()
+    assert bool((err <= 1e-4 * bound + 1e-30).all()), float((err / bound).max())
+    return float((err / bound).max())
+
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_rows_1_to_16(pkg, M):
+    _check(pkg, N=1000, K=904, M=M, seed=M)
+
+
+@pytest.mark.parametrize("N,K", [(128, 64), (129, 72), (4608, 3584), (3584, 18944), (896, 4864),
+                                 (1024, 256), (688 * 2, 256), (256, 688), (5, 8)])
+def test_shapes(pkg, N, K):
+    _check(pkg, N=N, K=K, M=9)
+
+
+def test_strided_rows(pkg):
+    # rows of a wider matrix: a column slice, as the shared-embedding draft uses
+    _check(pkg, N=700, K=896, M=2, ld=3584)
+
+
+def test_deterministic_and_row_independent(pkg):
+    g = torch.Generator(device="cuda").manual_seed(7)
+    w = (torch.randn(3584, 18944, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    x = torch.randn(9, 18944, generator=g, device="cuda")
+    y1 = pkg.linear(w, x)
+    y2 = pkg.linear(w, x)
+    assert torch.equal(y1, y2)
+    for m in range(9):
+        ym = pkg.linear(w, x[m:m + 1].contiguous())
+        assert torch.equal(ym[0], y1[m]), m

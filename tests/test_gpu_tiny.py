@@ -1,0 +1,295 @@
+"""GPU parity on the tiny workload (2-layer target, 1-layer draft, vocab 1024).
+
+Every check runs the CUDA path through the C ABI and compares it with the
+CPU oracle on the same seeded inputs:
+  * logits of the draft steps and of the verify rows within 3e-2 of each
+    row's logit range (bf16 weights), with the actual error reported;
+  * token streams equal to the oracle's greedy stream (near ties allowed);
+  * accept lengths, committed tokens, cache lengths, n-gram proposals:
+    bit-exact integer work;
+  * the cache after in-place rollback equals a fresh prefill of the
+    committed prefix (bit for bit);
+  * batch invariance: a row's logits do not depend on how many rows share
+    the launch (draft decode rows == verify rows, bit for bit).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as od
+from oracle import model as om
+from synth import (TINY_DRAFT, TINY_TARGET, draft_from_target_layer0, make_weights, ngram_prompt,
+                   uniform_prompt)
+
+from gpu_helpers import (LOGIT_TOL_BF16, accept_brute, check_token_against_oracle, logit_err,
+                          teacher_forced_stream_check, to_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as p
+    return p
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    tw = make_weights(TINY_TARGET, seed=0)
+    dw = draft_from_target_layer0(tw, TINY_DRAFT, 0.005, seed=1)
+    gt = to_cuda(tw)
+    gd = to_cuda(dw)
+    gd["embed"], gd["norm"] = gt["embed"], gt["norm"]
+    return tw, dw, gt, gd
+
+
+def make_engine(pkg, tiny, K=4, s_max=256, draft=True, batch=1):
+    tw, dw, gt, gd = tiny
+    if draft:
+        return pkg.SpecEngine(TINY_TARGET, gt, TINY_DRAFT, gd, batch=batch, K=K, s_max=s_max)
+    return pkg.SpecEngine(TINY_TARGET, gt, batch=batch, K=K, s_max=s_max)
+
+
+def test_draft_and_verify_logits_match_oracle(pkg, tiny):
+    tw, dw, _, _ = tiny
+    K = 4
+    V = TINY_TARGET.vocab
+    prompt = uniform_prompt(32, 1024, seed=100).tolist()
+    eng = make_engine(pkg, tiny, K=K)
+    eng.prefill([prompt])
+    d_out = torch.zeros(K, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros(K, V, dtype=torch.float32, device="cuda")
+    eng.draft(d_out, d_log)
+    t_out = torch.zeros(K + 1, dtype=torch.int32, device="cuda")
+    t_log = torch.zeros(K + 1, V, dtype=torch.float32, device="cuda")
+    eng.verify(t_out, t_log)
+    torch.cuda.synchronize()
+    d = d_out.cpu().tolist()
+    # draft oracle, teacher-forced on the GPU's guesses
+    dm = om.Model(TINY_DRAFT, dw)
+    dc = dm.new_cache()
+    dm.forward(prompt[:-1], dc, logit_rows=[])
+    feed = [prompt[-1]]
+    worst = 0.0
+    for i in range(K):
+        ref = dm.forward(feed, dc)[0]
+        worst = max(worst, logit_err(d_log[i], ref))
+        check_token_against_oracle(d[i], ref)
+        feed = [d[i]]
+    # target oracle on [pending, d_1..d_K]
+    tm = om.Model(TINY_TARGET, tw)
+    tc = tm.new_cache()
+    tm.forward(prompt[:-1], tc, logit_rows=[])
+    ref = tm.forward([prompt[-1]] + d, tc)
+    for j in range(K + 1):
+        worst = max(worst, logit_err(t_log[j], ref[j]))
+    print(f"tiny: max logit error / range = {worst:.3e}")
+    assert worst < LOGIT_TOL_BF16
+    # the argmax kernel picks the first maximum of the logits it produced
+    assert t_out.cpu().tolist() == [int(torch.argmax(t_log[j])) for j in range(K + 1)]
+    assert d == [int(torch.argmax(d_log[i])) for i in range(K)]
+    n_acc, committed = eng.accept_rollback()
+    t = t_out.cpu().tolist()
+    n = accept_brute(d, t, K)
+    assert int(n_acc[0]) == n and committed[0] == d[:n] + [t[n]]
+    eng.close()
+
+
+def test_batch_invariance_target_as_its_own_draft(pkg, tiny):
+    """Draft = the target itself: decode rows (1-2 per launch) and verify rows
+    (K+1 per launch) must agree bit for bit, so every guess is accepted."""
+    _, _, gt, _ = tiny
+    K = 4
+    V = TINY_TARGET.vocab
+    eng = pkg.SpecEngine(TINY_TARGET, gt, TINY_TARGET, gt, batch=1, K=K, s_max=256)
+    eng.prefill([uniform_prompt(20, 1024, seed=5).tolist()])
+    d_log = torch.zeros(K, V, dtype=torch.float32, device="cuda")
+    t_log = torch.zeros(K + 1, V, dtype=torch.float32, device="cuda")
+    for _ in range(5):
+        eng.draft(None, d_log)
+        eng.verify(None, t_log)
+        torch.cuda.synchronize()
+        assert torch.equal(d_log, t_log[:K])
+        n_acc, committed = eng.accept_rollback()
+        assert int(n_acc[0]) == K and len(committed[0]) == K + 1
+    eng.close()
+
+
+@pytest.mark.parametrize("K", [1, 4, 7])
+def test_generate_matches_oracle_greedy(pkg, tiny, K):
+    tw = tiny[0]
+    prompt = uniform_prompt(32, 1024, seed=100).tolist()
+    eng = make_engine(pkg, tiny, K=K)
+    eng.prefill([prompt])
+    out, rounds = eng.generate(64)
+    hist = eng.accept_hist()
+    eng.close()
+    stream = out[0].tolist()
+    ref = od.greedy(om.Model(TINY_TARGET, tw), prompt, 64)
+    if stream != ref:
+        near = teacher_forced_stream_check(om.Model(TINY_TARGET, tw), prompt, stream)
+        print(f"K={K}: {near} near-tie positions")
+    assert rounds >= 64 // (K + 1)
+    assert int((hist[0] * (np.arange(K + 1) + 1)).sum()) >= 64
+
+
+def test_spec_streams_identical_across_drafters(pkg, tiny):
+    """Speculation never changes the output: neural K=1, K=4, K=7 and n-gram
+    drafting all give the same tokens bit for bit on the GPU."""
+    prompt = uniform_prompt(32, 1024, seed=101).tolist()
+    streams = []
+    for K in (1, 4, 7):
+        eng = make_engine(pkg, tiny, K=K)
+        eng.prefill([prompt])
+        streams.append(eng.generate(48)[0][0].tolist())
+        eng.close()
+    eng = make_engine(pkg, tiny, K=4, draft=False)
+    eng.prefill([prompt])
+    streams.append(eng.generate(48)[0][0].tolist())
+    eng.close()
+    assert all(s == streams[0] for s in streams)
+
+
+def test_rounds_integer_state_and_rollback(pkg, tiny):
+    K = 4
+    prompt = uniform_prompt(24, 1024, seed=102).tolist()
+    eng = make_engine(pkg, tiny, K=K)
+    eng.prefill([prompt])
+    seq = list(prompt)
+    d_out = torch.zeros(K, dtype=torch.int32, device="cuda")
+    t_out = torch.zeros(K + 1, dtype=torch.int32, device="cuda")
+    for _ in range(8):
+        eng.draft(d_out)
+        eng.verify(t_out)
+        n_acc, committed = eng.accept_rollback()
+        d, t = d_out.cpu().tolist(), t_out.cpu().tolist()
+        n = accept_brute(d, t, K)
+        assert int(n_acc[0]) == n
+        assert committed[0] == d[:n] + [t[n]]
+        seq += committed[0]
+        lt, ld = eng.lengths()
+        assert int(lt[0]) == len(seq) - 1 and int(ld[0]) == len(seq) - 2
+    # The caches below the lengths equal a fresh prefill of the committed prefix.
+    kv_t = eng.kv_view("target").clone()
+    kv_d = eng.kv_view("draft").clone()
+    C = len(seq)
+    fresh = make_engine(pkg, tiny, K=K)
+    fresh.prefill([seq])
+    ft, fd = fresh.kv_view("target"), fresh.kv_view("draft")
+    assert torch.equal(kv_t[..., : C - 1, :], ft[..., : C - 1, :])
+    assert torch.equal(kv_d[..., : C - 2, :], fd[..., : C - 2, :])
+    fresh.close()
+    eng.close()
+
+
+def test_ngram_drafting_matches_oracle(pkg, tiny):
+    tw = tiny[0]
+    K = 4
+    prompt, _ = ngram_prompt(96, 0.8, 1024, seed=200, base_len=48, seg_lo=8, seg_hi=16)
+    prompt = prompt.tolist()
+    eng = make_engine(pkg, tiny, K=K, draft=False)
+    eng.prefill([prompt])
+    seq = list(prompt)
+    prop = torch.zeros(K, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t_out = torch.zeros(K + 1, dtype=torch.int32, device="cuda")
+    proposed = 0
+    for _ in range(12):
+        eng.ngram_draft(K, 2, 4, prop, cnt)
+        eng.verify(t_out)
+        torch.cuda.synchronize()
+        ref = od.ngram_propose(seq, K, 2, 4)
+        c = int(cnt.item())
+        assert c == len(ref) and prop.cpu().tolist()[:c] == ref
+        assert all(v == 0 for v in prop.cpu().tolist()[c:])
+        proposed += c
+        n_acc, committed = eng.accept_rollback()
+        t = t_out.cpu().tolist()
+        n = accept_brute(ref + [0] * (K - c), t, c)
+        assert int(n_acc[0]) == n and committed[0] == ref[:n] + [t[n]]
+        seq += committed[0]
+    assert proposed > 0
+    # and the generated stream is greedy
+    teacher_forced_stream_check(om.Model(TINY_TARGET, tw), prompt, seq[len(prompt):])
+    eng.close()
+
+
+@pytest.mark.parametrize("ctx", [[5, 9], [1, 2, 3, 1, 2], [7] * 9])
+def test_ngram_edge_cases(pkg, tiny, ctx):
+    K = 4
+    eng = make_engine(pkg, tiny, K=K, draft=False)
+    eng.prefill([ctx])
+    prop = torch.zeros(K, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for mg in (1, 4):
+        eng.ngram_draft(mg, 2, 4, prop, cnt)
+        ref = od.ngram_propose(ctx, mg, 2, 4)
+        assert int(cnt.item()) == len(ref) and prop.cpu().tolist()[:len(ref)] == ref
+        eng.verify()
+        eng.accept_rollback()
+        eng.reset()
+    eng.close()
+
+
+def test_long_context_attention(pkg, tiny):
+    """Prompt of 1500 tokens: attention spans 24 cache chunks of 64 slots."""
+    tw = tiny[0]
+    K = 4
+    prompt = uniform_prompt(1500, 1024, seed=103).tolist()
+    eng = make_engine(pkg, tiny, K=K, s_max=2048)
+    eng.prefill([prompt])
+    d_out = torch.zeros(K, dtype=torch.int32, device="cuda")
+    t_log = torch.zeros(K + 1, TINY_TARGET.vocab, dtype=torch.float32, device="cuda")
+    eng.draft(d_out)
+    eng.verify(None, t_log)
+    torch.cuda.synchronize()
+    d = d_out.cpu().tolist()
+    tm = om.Model(TINY_TARGET, tw)
+    tc = tm.new_cache()
+    tm.forward(prompt[:-1], tc, logit_rows=[])
+    ref = tm.forward([prompt[-1]] + d, tc)
+    worst = max(logit_err(t_log[j], ref[j]) for j in range(K + 1))
+    print(f"tiny ctx 1500: max logit error / range = {worst:.3e}")
+    assert worst < LOGIT_TOL_BF16
+    eng.close()
+
+
+def test_state_and_capacity_errors(pkg, tiny):
+    from greedy_speculative_decoding_gb300 import SFError
+    from greedy_speculative_decoding_gb300 import _lib as L
+    eng = make_engine(pkg, tiny, K=4, s_max=128)
+    with pytest.raises(SFError) as e:
+        eng.verify()
+    assert e.value.status == L.SF_ERR_STATE
+    with pytest.raises(SFError) as e:
+        eng.prefill([list(range(125))])          # no room for a round
+    assert e.value.status == L.SF_ERR_CAPACITY
+    eng.prefill([list(range(100))])
+    with pytest.raises(SFError) as e:
+        eng.accept_rollback()
+    assert e.value.status == L.SF_ERR_STATE
+    with pytest.raises(SFError) as e:
+        eng.generate(64)                          # s_max 128 runs out
+    assert e.value.status == L.SF_ERR_CAPACITY
+    with pytest.raises(SFError) as e:
+        eng.prefill([[3, 2000]])                  # token out of range
+    assert e.value.status == L.SF_ERR_ARG
+    eng.close()
+
+
+def test_nonfinite_logits_are_reported(pkg, tiny):
+    from greedy_speculative_decoding_gb300 import SFError
+    from greedy_speculative_decoding_gb300 import _lib as L
+    tw, dw, gt, gd = tiny
+    bad = dict(gt)
+    bad["norm"] = gt["norm"].clone()
+    bad["norm"][3] = float("nan")
+    eng = pkg.SpecEngine(TINY_TARGET, bad, batch=1, K=2, s_max=128)
+    eng.prefill([[1, 2, 3]])
+    with pytest.raises(SFError) as e:
+        eng.step()
+    assert e.value.status == L.SF_ERR_NONFINITE
+    eng.close()
