@@ -156,6 +156,27 @@ def launches_per_round(t_shape, d_shape, K) -> int:
 
 
 # ---------------------------------------------------------------------------- ours
+def run_gemm_only(args):
+    """Small case for kernel profiling: the 7B gate+up matrix (271 MB, above
+    L2) streamed by sf_linear with 9 rows, a few launches."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as pkg
+    t_shape, _ = _shapes()
+    N, K, M = 2 * t_shape.ffn, t_shape.hidden, K_GUESS + 1
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    w = (torch.randn(N, K, generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+    x = torch.randn(M, K, generator=gen, device="cuda")
+    y = torch.empty(M, N, device="cuda")
+    ws = torch.empty(pkg.load().sf_linear_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    for _ in range(6):
+        pkg.linear(w, x, y, ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"gemm_only": True, "N": N, "K": K, "M": M}))
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -184,6 +205,7 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
         e0.record(stream)
         for _ in range(args.steps):
             eng.reset()
@@ -191,6 +213,7 @@ def run_ours(args):
             rounds_total += r
         e1.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     _barrier(dist)
     ms = e0.elapsed_time(e1)
     ms_max = _max_over_ranks(dist, ms)
@@ -255,7 +278,10 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del eng
-        cpu = cpu_baseline(tw, dw)
+        try:
+            cpu = cpu_baseline(tw, dw)
+        except Exception as ex:  # report, keep the GPU line
+            cpu = {"value": None, "unit": "tokens/s", "kind": "oracle", "error": repr(ex)[:300]}
 
     if rank == 0:
         mean_commit = float((hist * (np.arange(K_GUESS + 1) + 1)).sum() / max(1, hist.sum()))
@@ -377,7 +403,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=N_NEW, help="new tokens per step (profiling runs use fewer)")
+    ap.add_argument("--gemm-only", action="store_true", help="small case for kernel profiling")
     args = ap.parse_args()
+    globals()["N_NEW"] = args.tokens
+    if args.gemm_only:
+        run_gemm_only(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

@@ -133,6 +133,8 @@ class Model:
 
     def lin(self, W: torch.Tensor, rows: list) -> list:
         """W @ r for every row r (W is [out, in])."""
+        if not rows:
+            return []
         if self.rowwise or len(rows) == 1:
             return [torch.mv(W, r) for r in rows]
         y = torch.mm(torch.stack(rows), W.t())
