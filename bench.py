@@ -34,6 +34,23 @@ K_GUESS = 8
 S_MAX = 4096
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# the roofline kernel from one ncu capture, valid only for the k_gemm.cu
+# source it was taken on (sha256 prefix); reported as null otherwise.
+GEMM_TRAFFIC = {"sha": None, "bytes": None}
+
+
+def _gemm_traffic():
+    import hashlib
+    src = os.path.join(ROOT, "greedy_speculative_decoding_gb300", "csrc", "k_gemm.cu")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return GEMM_TRAFFIC["bytes"] if sha == GEMM_TRAFFIC["sha"] else None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -299,7 +316,7 @@ def run_ours(args):
             "gpu_launches": rounds_total * launches_per_round(t_shape, d_shape, K_GUESS),
             "roofline": {"kernel": "k_gemm (weight-streaming GEMM), 7B gate+up [37888 x 3584] bf16, 9 rows",
                          "bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gemm_gbs / peak, 4), "traffic": None, "peak_source": peak_src,
+                         "frac": round(gemm_gbs / peak, 4), "traffic": _gemm_traffic(), "peak_source": peak_src,
                          "algorithmic_bytes": gemm_bytes, "ms_per_launch": round(gemm_ms, 4)},
             "verify_step": {"ms": round(verify_ms, 4), "bytes": v_bytes, "ctx": VERIFY_CTX,
                             "gbs": round(v_bytes / (verify_ms / 1e3) / 1e9, 1),
