@@ -21,7 +21,7 @@ EXPORTS = (
     "sf_weight_count", "sf_kv_bytes", "sf_workspace_bytes", "sf_create", "sf_prefill", "sf_draft",
     "sf_ngram_draft", "sf_verify", "sf_accept_rollback", "sf_step", "sf_generate", "sf_reset",
     "sf_set_drafter", "sf_get_lengths", "sf_get_accept_hist", "sf_status_str", "sf_last_error",
-    "sf_destroy", "sf_nf4_quantize", "sf_linear_workspace_bytes", "sf_linear",
+    "sf_destroy", "sf_nf4_quantize", "sf_linear_workspace_bytes", "sf_linear", "sf_linear_noalloc",
 )
 
 
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sf_nf4_quantize": (ST, [P, I32, I32, I32, P, P, P]),
         "sf_linear_workspace_bytes": (SZ, [I32, I32]),
         "sf_linear": (ST, [P, I32, I32, I32, P, I32, P, P, P]),
+        "sf_linear_noalloc": (ST, [P, I32, I32, I32, P, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

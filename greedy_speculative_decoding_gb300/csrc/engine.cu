@@ -204,6 +204,16 @@ Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, i
 
 }  // namespace
 
+sf_status sf::set_error(sf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
 struct sf_engine {
   Model tgt, dft;
   bool has_dft = false;

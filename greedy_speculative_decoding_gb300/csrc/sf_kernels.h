@@ -97,6 +97,9 @@ struct SpecState {
   int B, K, s_max;
 };
 
+// Record a message for sf_last_error() and return `s`.
+sf_status set_error(sf_status s, const char* fmt, ...);
+
 cudaError_t launch_accept(const SpecState& s, int mode, cudaStream_t st, bool pdl);
 cudaError_t launch_ngram(const SpecState& s, int max_guess, int min_n, int max_n, int* d_prop,
                          int* d_count, cudaStream_t st, bool pdl);

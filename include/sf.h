@@ -216,6 +216,28 @@ SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, co
                            float* d_y, void* d_workspace, void* cuda_stream);
 
 /*
+ * sf_linear without any caller-provided scratch, for callers that cannot
+ * allocate device memory where they need the projection: code running while
+ * a stream is captured into a CUDA graph, plug-ins whose host framework owns
+ * all device allocations, and latency-critical loops that cannot afford
+ * cudaMalloc's implicit synchronisation. Same arguments and result as
+ * sf_linear minus d_workspace. (The pages describe no such call; it has no
+ * counterpart there.)
+ *
+ * The split-K scratch is a file-scope device array of about 8 MB inside the
+ * library (enough for N up to 1,048,576 rows); every GPU that loads the
+ * library keeps it until the process exits. The call allocates nothing: the
+ * first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make that first call
+ * before any stream capture. All calls share the array: it keeps the last
+ * call's contents, the counters that must start at zero are cleared by each
+ * call, and calls that overlap on the GPU race with each other. N beyond the
+ * limit returns SF_ERR_ARG with a message in sf_last_error().
+ */
+SF_API sf_status sf_linear_noalloc(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x,
+                                   int32_t M, float* d_y, void* cuda_stream);
+
+/*
  * Blockwise NF4 quantisation of a bf16 matrix on the device (a preparation
  * step for SF_WDTYPE_NF4 weights): w [rows, cols] with row stride ld
  * elements, cols a multiple of 64; writes packed codes [rows, cols/2] and fp16
