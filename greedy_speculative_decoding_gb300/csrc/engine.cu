@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -64,6 +65,7 @@ Plan make_plan(int nblocks, int K, int slots) {
 enum { W_Q = 0, W_K, W_V, W_O, W_G, W_U, W_D };
 
 struct LayerW {
+  CUtensorMap tm[7];
   const void* w[7] = {};
   const __half* sc[7] = {};
   const bf16 *ln1 = nullptr, *ln2 = nullptr, *bq = nullptr, *bk = nullptr, *bv = nullptr;
@@ -77,6 +79,7 @@ struct Model {
   const bf16* norm = nullptr;
   const bf16* lm = nullptr;
   int lm_ld = 0;
+  CUtensorMap lm_tm;
   bf16* kv = nullptr;
   float2* rope = nullptr;
   Plan p_qkv, p_o, p_gu, p_d, p_lm;
@@ -217,6 +220,7 @@ sf_status sf::set_error(sf_status s, const char* fmt, ...) {
 struct sf_engine {
   Model tgt, dft;
   bool has_dft = false;
+  bool pdl = true;      // programmatic dependent launch between the round's kernels
   int B = 0, K = 0, s_max = 0, num_sms = 0, slots = 0;
   cudaStream_t user = nullptr, cap = nullptr;
   unsigned char* ws = nullptr;
@@ -285,6 +289,21 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   }
   md.kv = kv;
   const int H = c->hidden;
+  const int QD = c->n_heads * c->head_dim, KVD = c->n_kv_heads * c->head_dim, F = c->ffn;
+  for (int l = 0; l < c->layers; ++l) {
+    LayerW& lw = md.L[l];
+    const int rows[7] = {QD, KVD, KVD, H, F, F, H};
+    const int ks[7] = {H, H, H, QD, H, H, F};
+    for (int k = 0; k < 7; ++k) {
+      const cudaError_t ce = make_weight_map(&lw.tm[k], lw.w[k], rows[k], ks[k], ks[k]);
+      if (ce != cudaSuccess)
+        return fail(SF_ERR_CUDA, "layer %d weight %d: tensor map: %s", l, k, cudaGetErrorString(ce));
+    }
+  }
+  {
+    const cudaError_t ce = make_weight_map(&md.lm_tm, md.lm, c->vocab, H, md.lm_ld);
+    if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "LM head tensor map: %s", cudaGetErrorString(ce));
+  }
   md.p_qkv = make_plan(nblocks_of(c, 0), H, e->slots);
   md.p_o = make_plan(nblocks_of(c, 1), c->n_heads * c->head_dim, e->slots);
   md.p_gu = make_plan(nblocks_of(c, 2), H, e->slots);
@@ -330,7 +349,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.x = e->x;
   ea.ssq = e->ssq;
   ea.rs = rs;
-  CK(launch_embed(ea, s, true));
+  CK(launch_embed(ea, s, e->pdl));
   const size_t layer_elems = (size_t)2 * e->B * c.n_kv_heads * e->s_max * c.head_dim;
   for (int l = 0; l < c.layers; ++l) {
     const LayerW& lw = md.L[l];
@@ -341,6 +360,9 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.w[0] = lw.w[W_Q];
     a.w[1] = lw.w[W_K];
     a.w[2] = lw.w[W_V];
+    a.tm[0] = lw.tm[W_Q];
+    a.tm[1] = lw.tm[W_K];
+    a.tm[2] = lw.tm[W_V];
     a.bias[0] = lw.bq;
     a.bias[1] = lw.bk;
     a.bias[2] = lw.bv;
@@ -367,7 +389,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.kc = kc;
     a.vc = vc;
     a.rope = md.rope;
-    CK(launch_gemm(a, EPI_QKV, s, true));
+    CK(launch_gemm(a, EPI_QKV, s, e->pdl));
     // attention
     AttnArgs t{};
     t.q = e->q;
@@ -384,10 +406,11 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     t.scale = 1.0f / sqrtf((float)c.head_dim);
     t.err = e->st.err;
     t.rs = rs;
-    CK(launch_attention(t, e->num_sms, s, true));
+    CK(launch_attention(t, e->num_sms, s, e->pdl));
     // o-projection + residual
     a = base_args(e, md, md.p_o, rs);
     a.w[0] = lw.w[W_O];
+    a.tm[0] = lw.tm[W_O];
     a.seg_end[0] = H;
     a.ld[0] = QD;
     a.nseg = 1;
@@ -398,11 +421,13 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.out = e->x;
     a.out_ld = H;
     a.ssq_out = e->ssq;
-    CK(launch_gemm(a, EPI_RESID, s, true));
+    CK(launch_gemm(a, EPI_RESID, s, e->pdl));
     // gate/up + SwiGLU
     a = base_args(e, md, md.p_gu, rs);
     a.w[0] = lw.w[W_G];
     a.w[1] = lw.w[W_U];
+    a.tm[0] = lw.tm[W_G];
+    a.tm[1] = lw.tm[W_U];
     a.ld[0] = a.ld[1] = H;
     a.nseg = 2;
     a.N = c.ffn;
@@ -415,10 +440,11 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.inv_k = 1.0f / H;
     a.out = e->act;
     a.out_ld = (c.ffn + 3) / 4 * 4;
-    CK(launch_gemm(a, EPI_SWIGLU, s, true));
+    CK(launch_gemm(a, EPI_SWIGLU, s, e->pdl));
     // down + residual
     a = base_args(e, md, md.p_d, rs);
     a.w[0] = lw.w[W_D];
+    a.tm[0] = lw.tm[W_D];
     a.seg_end[0] = H;
     a.ld[0] = c.ffn;
     a.nseg = 1;
@@ -429,11 +455,12 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.out = e->x;
     a.out_ld = H;
     a.ssq_out = e->ssq;
-    CK(launch_gemm(a, EPI_RESID, s, true));
+    CK(launch_gemm(a, EPI_RESID, s, e->pdl));
   }
   if (!lm) return SF_OK;
   GemmArgs a = base_args(e, md, md.p_lm, rs);
   a.w[0] = md.lm;
+  a.tm[0] = md.lm_tm;
   a.seg_end[0] = c.vocab;
   a.ld[0] = md.lm_ld;
   a.nseg = 1;
@@ -454,7 +481,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   a.logits = to.logits;
   a.lg_stride = to.lg_stride;
   a.lg_off = to.lg_off;
-  CK(launch_gemm(a, EPI_ARGMAX, s, true));
+  CK(launch_gemm(a, EPI_ARGMAX, s, e->pdl));
   return SF_OK;
 }
 
@@ -507,10 +534,10 @@ sf_status enqueue_round(sf_engine* e, int mode, cudaStream_t s) {
   if (mode == SF_DRAFT_NEURAL) {
     if ((r = enqueue_draft(e, nullptr, s)) != SF_OK) return r;
   } else {
-    CK(launch_ngram(e->st, e->K, e->ng_min, e->ng_max, nullptr, nullptr, s, true));
+    CK(launch_ngram(e->st, e->K, e->ng_min, e->ng_max, nullptr, nullptr, s, e->pdl));
   }
   if ((r = enqueue_verify(e, nullptr, s)) != SF_OK) return r;
-  CK(launch_accept(e->st, mode, s, true));
+  CK(launch_accept(e->st, mode, s, e->pdl));
   return SF_OK;
 }
 
@@ -637,6 +664,9 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->user = static_cast<cudaStream_t>(cuda_stream);
   e->has_dft = dft != nullptr;
   e->drafter = dft ? SF_DRAFT_NEURAL : SF_DRAFT_NGRAM;
+  // SF_PDL=0 in the environment launches the kernels without programmatic
+  // dependent launch (for comparing the two; results are identical).
+  if (const char* v = getenv("SF_PDL")) e->pdl = v[0] != '0';
   auto bail = [&](sf_status s) {
     sf_destroy(e);
     return s;
@@ -944,6 +974,7 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * 4, st));
   GemmArgs a{};
+  CK(make_weight_map(&a.tm[0], d_w, N, K, ld));
   a.w[0] = d_w;
   a.seg_end[0] = N;
   a.ld[0] = ld;

@@ -2,14 +2,13 @@
 //
 // Attention is split over the cache ("flash decoding"): one work item is
 // (sequence, KV head, 64-slot chunk). Its keys and values are contiguous in
-// the cache, so one CTA brings them into shared memory with two bulk
-// (TMA) copies completing on an mbarrier, and then serves every query that
-// reads this KV head: all rows of the sequence times the query heads of the
-// group. A query's scores come from one warp (two keys per lane, head
-// dimension walked in a per-lane rotated order so the 16-byte shared reads
-// never collide), with warp-shuffle max/sum; the chunk's partial result
-// (max, sum of exponentials, unnormalised output) goes to scratch. A second
-// kernel merges the chunks of every (row, head) in fixed chunk order.
+// the cache; one warp brings them into padded shared-memory rows with bulk
+// (TMA) copies completing on an mbarrier, and the CTA then serves every
+// query that reads this KV head (all rows of the sequence times the query
+// heads of the group) on the tensor cores, 16 queries per warp. The chunk's
+// partial result (row max, sum of exponentials, unnormalised output) goes to
+// scratch; a second kernel merges the chunks of every (row, head) in fixed
+// chunk order.
 //
 // Chunk boundaries are fixed multiples of 64 slots and a row at position p
 // reads slots 0..p, so a row's result does not depend on the other rows.
@@ -56,27 +55,49 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl) {
 // ------------------------------------------------------------------ attention
 constexpr uint32_t kWaitIters = 1u << 24;
 
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const bf16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
+  hi = pack_bf16x2(hx, hy);
+  lo = pack_bf16x2(__float2bfloat16_rn(x - __bfloat162float(hx)), __float2bfloat16_rn(y - __bfloat162float(hy)));
+}
+
+// One work item = (sequence b, KV head, 64-slot chunk c). Each warp takes a
+// tile of 16 queries (rows of the sequence x query heads of the group):
+//   S = Q K^T with mma.sync m16n8k16 (Q as an fp32-accurate bf16 hi+lo pair,
+//   the head dimension walked in an order that makes each thread's key
+//   fragment one 8-byte shared load), masked to the slots each row may see,
+//   row max / exp / row sum on the accumulators (quad shuffles), then
+//   O = P V with P (hi+lo) taken straight from the S accumulators and V
+//   fragments from ldmatrix.trans.
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads) k_attn_chunks(const __grid_constant__ AttnArgs a) {
-  constexpr int kUnits = HD / 8;            // 16-byte units per key row
-  constexpr int kDims = HD / 32;            // output dims per lane
-  __shared__ __align__(128) bf16 ks[kKvChunk * HD];
-  __shared__ __align__(128) bf16 vs[kKvChunk * HD];
-  __shared__ __align__(16) float qs[kAttnThreads / 32][HD];
+__global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_constant__ AttnArgs a) {
+  constexpr int KP = HD * 2 + 32;   // key row pitch: 8-bank shift per row for the 8-byte fragment loads
+  constexpr int VP = HD * 2 + 16;   // value row pitch: 4-bank shift per row for ldmatrix
+  constexpr int KS = HD / 16;       // k-steps over the head dimension
+  constexpr int NT = HD / 8;        // n-tiles of the output
+  __shared__ __align__(128) unsigned char ks[kKvChunk * KP];
+  __shared__ __align__(128) unsigned char vs[kKvChunk * VP];
   __shared__ __align__(8) uint64_t bar;
 
   pdl_wait();
   pdl_launch_next();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c4 = lane & 3;
   const int group = a.nq / a.nkv;
   const int rps = a.rs.rps;
+  const int Mq = rps * group;
   if (tid == 0) {
     mbar_init(&bar, 1);
-    fence_proxy_async();
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // Work items: for each sequence b, nkv heads x chunks covering slots 0..p_last.
   int total = 0;
   for (int b = 0; b < a.B; ++b) {
     const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
@@ -93,14 +114,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_chunks(const __grid_const
     }
     const int kvh = rest / nch, c = rest - kvh * nch;
     const size_t off = (((size_t)b * a.nkv + kvh) * a.s_max + (size_t)c * kKvChunk) * HD;
-    if (tid == 0) {
+    if (warp == 0) {
+      if (lane == 0) mbar_expect_tx(&bar, 2u * kKvChunk * HD * sizeof(bf16));
+      __syncwarp();
       fence_proxy_async();   // earlier generic reads of ks/vs before the async writes
-      mbar_expect_tx(&bar, 2u * kKvChunk * HD * sizeof(bf16));
-      bulk_g2s(ks, a.kc + off, kKvChunk * HD * sizeof(bf16), &bar);
-      bulk_g2s(vs, a.vc + off, kKvChunk * HD * sizeof(bf16), &bar);
+      for (int r = lane; r < kKvChunk; r += 32) {
+        bulk_g2s(ks + r * KP, a.kc + off + (size_t)r * HD, HD * sizeof(bf16), &bar);
+        bulk_g2s(vs + r * VP, a.vc + off + (size_t)r * HD, HD * sizeof(bf16), &bar);
+      }
     }
     if (!mbar_wait(&bar, phase, kWaitIters)) {
-      // The copy did not land: report, give it one more bounded chance, stop.
       if (tid == 0) atomicOr(a.err, kErrWait);
       mbar_wait(&bar, phase, kWaitIters);
       return;
@@ -108,75 +131,115 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_chunks(const __grid_const
     phase ^= 1u;
 
     const int p0 = a.rs.pos_base[b] + a.rs.pos_off;
-    for (int qi = warp; qi < rps * group; qi += kAttnThreads / 32) {
-      const int j = qi / group, hh = qi - j * group;
-      const int p = p0 + j;
-      const int nk = min(kKvChunk, p - c * kKvChunk + 1);
-      if (nk <= 0) continue;
-      const int m = b * rps + j, h = kvh * group + hh;
-      const float* qg = a.q + (size_t)m * a.nq * HD + (size_t)h * HD;
-#pragma unroll
-      for (int d = 0; d < kDims; ++d) qs[warp][lane + 32 * d] = qg[lane + 32 * d];
-      __syncwarp();
-      float s[2];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int kk = lane + 32 * half;
-        float acc = 0.f;
-        const uint4* krow = reinterpret_cast<const uint4*>(ks + kk * HD);
-#pragma unroll
-        for (int u0 = 0; u0 < kUnits; ++u0) {
-          const int u = (u0 + lane) % kUnits;
-          const uint4 kv = krow[u];
-          const float4 qa = *reinterpret_cast<const float4*>(&qs[warp][8 * u]);
-          const float4 qb = *reinterpret_cast<const float4*>(&qs[warp][8 * u + 4]);
-          const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
-          const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
-          const float2 k45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.z));
-          const float2 k67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.w));
-          acc = fmaf(qa.x, k01.x, acc);
-          acc = fmaf(qa.y, k01.y, acc);
-          acc = fmaf(qa.z, k23.x, acc);
-          acc = fmaf(qa.w, k23.y, acc);
-          acc = fmaf(qb.x, k45.x, acc);
-          acc = fmaf(qb.y, k45.y, acc);
-          acc = fmaf(qb.z, k67.x, acc);
-          acc = fmaf(qb.w, k67.y, acc);
-        }
-        s[half] = kk < nk ? acc * a.scale : -INFINITY;
+    // Slots past the last row's position hold stale or never-written cache
+    // entries; a zero probability times a NaN there would still be NaN in
+    // the P V product, so clear those rows of the tile.
+    const int nvalid = min(kKvChunk, p0 + rps - c * kKvChunk);
+    if (nvalid < kKvChunk) {
+      for (int i = tid; i < (kKvChunk - nvalid) * (HD / 8); i += kAttnThreads) {
+        const int r = nvalid + i / (HD / 8), u = i % (HD / 8);
+        *reinterpret_cast<uint4*>(ks + r * KP + 16 * u) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vs + r * VP + 16 * u) = make_uint4(0, 0, 0, 0);
       }
-      const float mx = warp_max(fmaxf(s[0], s[1]));
-      const float e0 = lane < nk ? expf(s[0] - mx) : 0.f;
-      const float e1 = lane + 32 < nk ? expf(s[1] - mx) : 0.f;
-      const float l = warp_sum(e0 + e1);
-      float o[kDims];
+      __syncthreads();
+    }
+    for (int qt = warp; qt * 16 < Mq; qt += kAttnThreads / 32) {
+      // Rows g and g+8 of the tile.
+      int nk[2];
+      const float* qrow[2];
+      int mrow[2], hrow[2];
 #pragma unroll
-      for (int d = 0; d < kDims; ++d) o[d] = 0.f;
-      for (int kk = 0; kk < nk; ++kk) {
-        const float pk = __shfl_sync(0xffffffffu, kk < 32 ? e0 : e1, kk & 31);
-        const bf16* vrow = vs + kk * HD + lane * kDims;
-        if (kDims == 4) {
-          const uint2 vv = *reinterpret_cast<const uint2*>(vrow);
-          const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv.x));
-          const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv.y));
-          o[0] = fmaf(pk, v01.x, o[0]);
-          o[1] = fmaf(pk, v01.y, o[1]);
-          o[2 % kDims] = fmaf(pk, v23.x, o[2 % kDims]);
-          o[3 % kDims] = fmaf(pk, v23.y, o[3 % kDims]);
-        } else {
-          const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vrow));
-          o[0] = fmaf(pk, v01.x, o[0]);
-          o[1 % kDims] = fmaf(pk, v01.y, o[1 % kDims]);
+      for (int r = 0; r < 2; ++r) {
+        const int qi = qt * 16 + g + 8 * r;
+        const int j = qi / group, hh = qi - j * group;
+        mrow[r] = b * rps + j;
+        hrow[r] = kvh * group + hh;
+        nk[r] = qi < Mq ? min(kKvChunk, p0 + j - c * kKvChunk + 1) : 0;
+        qrow[r] = a.q + ((size_t)mrow[r] * a.nq + hrow[r]) * HD;
+      }
+      // S = Q K^T
+      float sacc[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        uint32_t qh[4], ql[4];
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 q0 = nk[0] > 0 ? *reinterpret_cast<const float4*>(qrow[0] + 16 * k + 4 * c4) : z;
+        const float4 q1 = nk[1] > 0 ? *reinterpret_cast<const float4*>(qrow[1] + 16 * k + 4 * c4) : z;
+        split_bf16x2(q0.x, q0.y, qh[0], ql[0]);
+        split_bf16x2(q1.x, q1.y, qh[1], ql[1]);
+        split_bf16x2(q0.z, q0.w, qh[2], ql[2]);
+        split_bf16x2(q1.z, q1.w, qh[3], ql[3]);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const uint2 kb = *reinterpret_cast<const uint2*>(ks + (8 * nt + g) * KP + 32 * k + 8 * c4);
+          mma_bf16_16816(sacc[nt], qh[0], qh[1], qh[2], qh[3], kb.x, kb.y);
+          mma_bf16_16816(sacc[nt], ql[0], ql[1], ql[2], ql[3], kb.x, kb.y);
         }
       }
-      float* dst = a.part + (((size_t)m * a.nq + h) * a.n_kv_chunks + c) * (HD + 2);
+      // Softmax pieces per row: max, exp, sum (rows g: e = 0,1; g+8: e = 2,3).
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int d = 0; d < kDims; ++d) dst[lane * kDims + d] = o[d];
-      if (lane == 0) {
-        dst[HD] = mx;
-        dst[HD + 1] = l;
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = e >> 1, key = 8 * nt + 2 * c4 + (e & 1);
+          sacc[nt][e] = key < nk[r] ? sacc[nt][e] * a.scale : -INFINITY;
+          mx[r] = fmaxf(mx[r], sacc[nt][e]);
+        }
+      float l[2] = {0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
       }
-      __syncwarp();
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = e >> 1, key = 8 * nt + 2 * c4 + (e & 1);
+          const float pe = key < nk[r] ? expf(sacc[nt][e] - mx[r]) : 0.f;
+          sacc[nt][e] = pe;
+          l[r] += pe;
+        }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+      }
+      // O = P V
+      float oacc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < kKvChunk / 16; ++kk) {
+        uint32_t ph[4], pl[4];
+        split_bf16x2(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
+        split_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
+        split_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
+        split_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
+        const unsigned char* vrow = vs + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * VP;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          uint32_t b0, b1;
+          ldsm_x2_trans(b0, b1, vrow + 16 * nt);
+          mma_bf16_16816(oacc[nt], ph[0], ph[1], ph[2], ph[3], b0, b1);
+          mma_bf16_16816(oacc[nt], pl[0], pl[1], pl[2], pl[3], b0, b1);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        if (nk[r] <= 0) continue;
+        float* dst = a.part + (((size_t)mrow[r] * a.nq + hrow[r]) * a.n_kv_chunks + c) * (HD + 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<float2*>(dst + 8 * nt + 2 * c4) = make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
+        if (c4 == 0) {
+          dst[HD] = mx[r];
+          dst[HD + 1] = l[r];
+        }
+      }
     }
     __syncthreads();   // everyone is done with ks/vs before the next copy
   }

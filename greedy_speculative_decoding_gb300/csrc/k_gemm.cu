@@ -2,11 +2,13 @@
 //
 // The work is weight streaming: y[m][n] = sum_k a[m][k] W[n][k] with at most
 // SF_MAX_ROWS token rows m, so every weight byte is read once and used by all
-// rows. Each CTA owns 128 output rows (8 warps x 16) and one slice of K; each
-// warp streams its 16 weight rows straight from HBM into registers with
-// 128-bit non-allocating loads (a whole 128-byte line per row per step) and
-// feeds them to mma.sync m16n8k16 as the A operand ("swap AB": weights are
-// the M side, tokens the N side). The token activations are staged in
+// rows. Each CTA owns 128 output rows (8 warps x 16) and one slice of K.
+// Every warp runs its own TMA pipeline: a ring of kStages shared-memory
+// tiles (16 weight rows x 64 k, 128-byte swizzle) filled by
+// cp.async.bulk.tensor loads that complete on per-stage mbarriers, so about
+// 80 KB of weights per CTA are in flight without holding registers. The tiles
+// feed mma.sync m16n8k16 as the A operand ("swap AB": weights are the M
+// side, tokens the N side). The token activations are staged in
 // shared memory, converted to a bf16 pair (hi + lo) so that the product keeps
 // about 16 mantissa bits of the fp32 activation; hi and lo of one token sit
 // in adjacent columns of the n8 tile and are summed in the epilogue.
@@ -28,30 +30,20 @@ namespace sf {
 
 namespace {
 
-constexpr int kPf = 2;   // chunks of weights in flight per thread
+constexpr uint32_t kWaitIters = 1u << 24;
 
+// Tensor map and row coordinate of warp w's 16 rows in row block rb.
 template <int EPI>
-__device__ __forceinline__ const bf16* weight_row(const GemmArgs& a, int rb, int r) {
-  if (EPI == EPI_SWIGLU) {
-    const int f = rb * 64 + (r & 63);
-    if (f >= a.N) return nullptr;
-    return static_cast<const bf16*>(a.w[r >> 6]) + (size_t)f * a.ld[0];
-  } else {
-    const int n = rb * kBlockRows + r;
-    if (n >= a.N) return nullptr;
-    int s = 0;
-    while (s < a.nseg - 1 && n >= a.seg_end[s]) ++s;
-    const int base = s ? a.seg_end[s - 1] : 0;
-    return static_cast<const bf16*>(a.w[s]) + (size_t)(n - base) * a.ld[s];
+__device__ __forceinline__ int warp_tile_row(const GemmArgs& a, int rb, int w, int* seg) {
+  if (EPI == EPI_SWIGLU) {           // warps 0-3: gate rows, 4-7: up rows of the same 64 features
+    *seg = w >> 2;
+    return rb * 64 + 16 * (w & 3);
   }
-}
-
-__device__ __forceinline__ void load_chunk(uint4 (&w)[4], const bf16* p0, const bf16* p1, int k, int K) {
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  w[0] = (p0 && k < K) ? ldg_stream(p0 + k) : z;
-  w[1] = (p0 && k + 8 < K) ? ldg_stream(p0 + k + 8) : z;
-  w[2] = (p1 && k < K) ? ldg_stream(p1 + k) : z;
-  w[3] = (p1 && k + 8 < K) ? ldg_stream(p1 + k + 8) : z;
+  const int n = rb * kBlockRows;     // segment boundaries are multiples of 128
+  int s = 0;
+  while (s < a.nseg - 1 && n >= a.seg_end[s]) ++s;
+  *seg = s;
+  return n - (s ? a.seg_end[s - 1] : 0) + 16 * w;
 }
 
 // Stage activation chunks [wc0, wc0 + nwc) of this CTA (absolute chunk index
@@ -244,10 +236,14 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, in
 
 template <int T, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant__ GemmArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint4* act = reinterpret_cast<uint4*>(smem);
-  float* ys = reinterpret_cast<float*>(smem + kWinChunks * T * 1024);
+  extern __shared__ unsigned char smem_raw[];
+  // The swizzled TMA tiles need a 1024-byte aligned base.
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  unsigned char* ring = smem;                                            // [8][kStages][kTileBytes]
+  uint4* act = reinterpret_cast<uint4*>(smem + 8 * kStages * kTileBytes);
+  float* ys = reinterpret_cast<float*>(smem + 8 * kStages * kTileBytes + kWinChunks * T * 1024);
   float* rinv = ys + 4 * T * kBlockRows;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);           // [8][kStages]
   __shared__ int s_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -257,17 +253,24 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
   const int c0 = sp * a.cps;
   const int nch = min(a.cps, nch_total - c0);
 
-  const int r0 = warp * 16 + g;
-  const bf16* p0 = weight_row<EPI>(a, rb, r0);
-  const bf16* p1 = weight_row<EPI>(a, rb, r0 + 8);
-  const int koff = c0 * kChunk + 16 * c;
-
-  // Weights are never written by the preceding kernels: start streaming them
-  // before waiting on the producer of the activations.
-  uint4 ring[kPf][4];
-#pragma unroll
-  for (int i = 0; i < kPf; ++i)
-    if (i < nch) load_chunk(ring[i], p0, p1, koff + i * kChunk, a.K);
+  int seg = 0;
+  const int trow = warp_tile_row<EPI>(a, rb, warp, &seg);
+  const CUtensorMap* map = &a.tm[seg];
+  unsigned char* my_ring = ring + warp * kStages * kTileBytes;
+  uint64_t* my_bar = bars + warp * kStages;
+  uint64_t policy = 0;
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&my_bar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    policy = policy_evict_first();
+    // Weights are never written by the preceding kernels: start streaming
+    // them before waiting on the producer of the activations.
+    for (int s = 0; s < kStages && s < nch; ++s) {
+      mbar_expect_tx(&my_bar[s], kTileBytes);
+      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + s) * kChunk, trow, &my_bar[s], policy);
+    }
+  }
+  __syncwarp();
 
   pdl_wait();
   pdl_launch_next();
@@ -285,24 +288,44 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
 #pragma unroll
   for (int t = 0; t < T; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
-  for (int base = 0; base < nch; base += kPf) {
-#pragma unroll
-    for (int i = 0; i < kPf; ++i) {
-      const int ch = base + i;
-      if (ch < nch) {
-        if (ch > 0 && (ch % kWinChunks) == 0) {
-          __syncthreads();
-          stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
-          __syncthreads();
-        }
-        uint4 w[4] = {ring[i][0], ring[i][1], ring[i][2], ring[i][3]};
-        if (ch + kPf < nch) load_chunk(ring[i], p0, p1, koff + (ch + kPf) * kChunk, a.K);
-        mma_chunk<T>(acc, w, act, ch % kWinChunks, lane);
-      }
+  // Row g / g+8 of the tile, 16-byte units 2c and 2c+1 (k = 16c .. 16c+15),
+  // at their 128-byte-swizzled positions.
+  const int sw = g & 7;
+  const int off_lo = g * 128 + (((2 * c) ^ sw) << 4);
+  const int off_hi = g * 128 + (((2 * c + 1) ^ sw) << 4);
+  bool timed_out = false;
+  for (int ch = 0; ch < nch; ++ch) {
+    if (ch > 0 && (ch % kWinChunks) == 0) {
+      __syncthreads();
+      stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
+      __syncthreads();
     }
+    const int s = ch % kStages;
+    if (!mbar_wait(&my_bar[s], (ch / kStages) & 1, kWaitIters)) timed_out = true;
+    const unsigned char* tile = my_ring + s * kTileBytes;
+    uint4 w[4];
+    w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
+    w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
+    w[2] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_lo);
+    w[3] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_hi);
+    __syncwarp();
+    if (lane == 0 && ch + kStages < nch) {
+      fence_proxy_async();   // the warp's reads of this stage before the async refill
+      mbar_expect_tx(&my_bar[s], kTileBytes);
+      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + ch + kStages) * kChunk, trow, &my_bar[s], policy);
+    }
+    mma_chunk<T>(acc, w, act, ch % kWinChunks, lane);
+  }
+  if (timed_out) {
+    // A tile never arrived: report, and give every copy of this warp one more
+    // bounded chance to land before the CTA's shared memory is released.
+    if (lane == 0) atomicOr(a.err, kErrWait);
+    for (int ch = max(0, nch - kStages); ch < nch; ++ch)
+      mbar_wait(&my_bar[ch % kStages], (ch / kStages) & 1, kWaitIters);
   }
 
   // Token m = 4t + c: hi in column 2c, lo in column 2c + 1.
+  const int r0 = warp * 16 + g;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     const int m = 4 * t + c;
@@ -339,7 +362,31 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
 
 int gemm_smem_bytes(int M) {
   const int T = (M + 3) / 4;
-  return kWinChunks * T * 1024 + 4 * T * kBlockRows * 4 + 4 * T * 4;
+  return 1024 /* alignment slack */ + 8 * kStages * kTileBytes + kWinChunks * T * 1024 + 4 * T * kBlockRows * 4 +
+         4 * T * 4 + 8 * kStages * 8;
+}
+
+cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld) {
+  typedef CUresult (*encode_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static encode_fn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    encode = reinterpret_cast<encode_fn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kChunk, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int T, int EPI>

@@ -1,6 +1,7 @@
 // Shared device helpers and kernel parameter blocks of the engine.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -15,8 +16,10 @@ typedef __nv_bfloat16 bf16;
 constexpr int kRows = SF_MAX_ROWS;     // tokens per forward, at most
 constexpr int kBlockRows = 128;        // output rows (features) per GEMM CTA
 constexpr int kGemmThreads = 256;      // 8 warps x 16 rows
-constexpr int kChunk = 64;             // k per pipeline step
-constexpr int kWinChunks = 16;         // chunks of activations staged at once
+constexpr int kChunk = 64;             // k per pipeline step (one 128-byte line per weight row)
+constexpr int kWinChunks = 8;          // chunks of activations staged at once
+constexpr int kStages = 5;             // weight tiles in flight per warp (TMA ring)
+constexpr int kTileBytes = 16 * kChunk * 2;   // one warp's 16 rows x 64 k of bf16
 constexpr int kKvChunk = 64;           // cache slots per attention work item
 constexpr int kAttnThreads = 256;
 
@@ -86,6 +89,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     if (done) return true;
   }
   return false;
+}
+
+// Two-dimensional tensor tile global -> shared (TMA) at coordinates (x, y),
+// completion on an mbarrier, with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // One-dimensional bulk copy global -> shared (TMA), completion on an mbarrier.

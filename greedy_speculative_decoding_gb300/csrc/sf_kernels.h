@@ -12,6 +12,7 @@ enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_STORE
 // five epilogues. Weights are bf16 row-major, or NF4 (packed codes + fp16
 // block scales) when nf4 != 0.
 struct GemmArgs {
+  CUtensorMap tm[3];          // per segment: 2-D map {K, rows}, box {64, 16}, 128-byte swizzle
   const void* w[3];           // row segments (QKV: q, k, v; SWIGLU: gate, up)
   const __half* scales[3];    // NF4 block scales per segment
   const bf16* bias[3];
@@ -48,6 +49,10 @@ struct GemmArgs {
   int* err;
   RowSet rs;
 };
+
+// Tensor map of a bf16 weight matrix [rows, K] with row stride ld elements,
+// in the layout the GEMM's TMA ring expects.
+cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld);
 
 int gemm_smem_bytes(int M);
 cudaError_t gemm_init();

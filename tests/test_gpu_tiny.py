@@ -293,3 +293,43 @@ def test_nonfinite_logits_are_reported(pkg, tiny):
         eng.step()
     assert e.value.status == L.SF_ERR_NONFINITE
     eng.close()
+
+
+SHAPES = {
+    "hd128_g2": TINY_TARGET.with_(n_heads=2, n_kv_heads=1, head_dim=128),
+    "hd64_g7": TINY_TARGET.with_(n_heads=14, n_kv_heads=2, head_dim=64),
+    "hd128_g7": TINY_TARGET.with_(hidden=384, n_heads=14, n_kv_heads=2, head_dim=128),
+}
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_head_shapes_with_poisoned_caches(pkg, name):
+    """Other head sizes and GQA group widths, with both caches filled with
+    NaN bytes before prefill: every slot the kernels may read is one they
+    wrote, and stale slots never leak into a result."""
+    shape = SHAPES[name]
+    K = 4
+    w = make_weights(shape, seed=21)
+    g = to_cuda(w)
+    eng = pkg.SpecEngine(shape, g, shape, g, batch=1, K=K, s_max=256)
+    eng.kv_t.fill_(0xFF)
+    eng.kv_d.fill_(0xFF)
+    prompt = uniform_prompt(70, shape.vocab, seed=22).tolist()
+    eng.prefill([prompt])
+    d_out = torch.zeros(K, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros(K, shape.vocab, dtype=torch.float32, device="cuda")
+    t_log = torch.zeros(K + 1, shape.vocab, dtype=torch.float32, device="cuda")
+    eng.draft(d_out, d_log)
+    eng.verify(None, t_log)
+    torch.cuda.synchronize()
+    assert torch.equal(d_log, t_log[:K])            # the draft is the target: bitwise equal rows
+    d = d_out.cpu().tolist()
+    m = om.Model(shape, w)
+    c = m.new_cache()
+    m.forward(prompt[:-1], c, logit_rows=[])
+    ref = m.forward([prompt[-1]] + d, c)
+    worst = max(logit_err(t_log[j], ref[j]) for j in range(K + 1))
+    print(f"{name}: max logit error / range = {worst:.3e}")
+    assert worst < LOGIT_TOL_BF16
+    eng.accept_rollback()
+    eng.close()
