@@ -649,7 +649,8 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   if (batch < 1 || K < 1 || K > 15) return fail(SF_ERR_ARG, "batch must be >= 1 and K in 1..15");
   if (batch * (K + 1) > SF_MAX_ROWS || batch * 2 > SF_MAX_ROWS)
     return fail(SF_ERR_UNSUPPORTED, "batch*(K+1) = %d exceeds %d rows", batch * (K + 1), SF_MAX_ROWS);
-  if (s_max < 64 || s_max % kKvChunk) return fail(SF_ERR_ARG, "s_max must be a positive multiple of 64");
+  if (s_max < 64 || s_max % kKvChunk || s_max > 16384)
+    return fail(SF_ERR_ARG, "s_max must be a multiple of 64 in 64..16384");
   if (!kv_t || (dft && !kv_d) || !workspace) return fail(SF_ERR_ARG, "null cache or workspace pointer");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(kv_t) & 255) ||
       (kv_d && (reinterpret_cast<uintptr_t>(kv_d) & 255)))

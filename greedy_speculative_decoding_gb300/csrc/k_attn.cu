@@ -245,25 +245,66 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   }
 }
 
-// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), chunks in order.
+// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), chunks in
+// order. One CTA per (row, head), one thread per output dimension; every
+// chunk's (max, sum) pair is loaded at once, and the output sums load eight
+// chunks at a time so the global loads overlap.
+constexpr int kMaxKvChunks = 256;
+
 __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
+  __shared__ float wgt[kMaxKvChunks];
+  __shared__ float lw[kMaxKvChunks];
+  __shared__ float red[4];
+  __shared__ float s_mx, s_l;
   pdl_wait();
   pdl_launch_next();
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
-  const int d = threadIdx.x;
-  const int p = row_pos(a.rs, m);
-  const int nch = p / kKvChunk + 1;
-  const float* src = a.part + ((size_t)m * a.nq + h) * a.n_kv_chunks * (a.hd + 2);
-  float mx = -INFINITY;
-  for (int c = 0; c < nch; ++c) mx = fmaxf(mx, src[(size_t)c * (a.hd + 2) + a.hd]);
-  float l = 0.f, o = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float* pc = src + (size_t)c * (a.hd + 2);
-    const float w = expf(pc[a.hd] - mx);
-    l = fmaf(pc[a.hd + 1], w, l);
-    o = fmaf(pc[d], w, o);
+  const int d = threadIdx.x, lane = d & 31, warp = d >> 5, nwarps = blockDim.x >> 5;
+  const int nch = row_pos(a.rs, m) / kKvChunk + 1;
+  const int stride = a.hd + 2;
+  const float* src = a.part + ((size_t)m * a.nq + h) * a.n_kv_chunks * stride;
+  float mc[2], lc[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int c = d + r * blockDim.x;
+    mc[r] = c < nch ? src[(size_t)c * stride + a.hd] : -INFINITY;
+    lc[r] = c < nch ? src[(size_t)c * stride + a.hd + 1] : 0.f;
   }
-  a.out[(size_t)m * a.nq * a.hd + (size_t)h * a.hd + d] = o / l;
+  const float wm = warp_max(fmaxf(mc[0], mc[1]));
+  if (lane == 0) red[warp] = wm;
+  __syncthreads();
+  if (d == 0) {
+    float v = red[0];
+    for (int w = 1; w < nwarps; ++w) v = fmaxf(v, red[w]);
+    s_mx = v;
+  }
+  __syncthreads();
+  const float mx = s_mx;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int c = d + r * blockDim.x;
+    if (c < nch) {
+      wgt[c] = expf(mc[r] - mx);
+      lw[c] = lc[r];
+    }
+  }
+  __syncthreads();
+  if (d == 0) {
+    float l = 0.f;
+    for (int c = 0; c < nch; ++c) l = fmaf(lw[c], wgt[c], l);
+    s_l = l;
+  }
+  float o = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = c0 + q < nch ? src[(size_t)(c0 + q) * stride + d] : 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (c0 + q < nch) o = fmaf(v[q], wgt[c0 + q], o);
+  }
+  __syncthreads();
+  a.out[(size_t)m * a.nq * a.hd + (size_t)h * a.hd + d] = o / s_l;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl) {

@@ -52,31 +52,46 @@ __device__ __forceinline__ int warp_tile_row(const GemmArgs& a, int rb, int w, i
 template <int T>
 __device__ __forceinline__ void stage_acts(const GemmArgs& a, uint2* act, const float* rinv, int cabs0,
                                            int nwc, int M) {
+  constexpr int kItems = (4 * T * kWinChunks * 16 + kGemmThreads - 1) / kGemmThreads;
   const int per_m = nwc * 16;  // groups of 4 k per token row
-  for (int idx = threadIdx.x; idx < 4 * T * per_m; idx += kGemmThreads) {
+  const int total = 4 * T * per_m;
+  // All global loads of this thread first, so their latencies overlap.
+  float4 v[kItems];
+  uint2 gg[kItems];
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int idx = threadIdx.x + it * kGemmThreads;
+    const int m = idx / per_m;
+    const int k = cabs0 * kChunk + (idx - m * per_m) * 4;
+    v[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    gg[it] = make_uint2(0, 0);
+    if (idx < total && m < M && k < a.K) {
+      v[it] = *reinterpret_cast<const float4*>(a.in + (size_t)m * a.in_ld + k);
+      if (a.gain) gg[it] = *reinterpret_cast<const uint2*>(a.gain + k);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int idx = threadIdx.x + it * kGemmThreads;
+    if (idx >= total) continue;
     const int m = idx / per_m;
     const int q4 = idx - m * per_m;
-    const int k = cabs0 * kChunk + q4 * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m < M && k < a.K) {
-      v = *reinterpret_cast<const float4*>(a.in + (size_t)m * a.in_ld + k);
-      if (a.gain) {
-        const float r = rinv[m];
-        const uint2 gg = *reinterpret_cast<const uint2*>(a.gain + k);
-        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg.x));
-        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg.y));
-        v.x = (v.x * r) * g01.x;
-        v.y = (v.y * r) * g01.y;
-        v.z = (v.z * r) * g23.x;
-        v.w = (v.w * r) * g23.y;
-      }
+    float4 x = v[it];
+    if (a.gain && m < M) {
+      const float r = rinv[m];
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg[it].x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg[it].y));
+      x.x = (x.x * r) * g01.x;
+      x.y = (x.y * r) * g01.y;
+      x.z = (x.z * r) * g23.x;
+      x.w = (x.w * r) * g23.y;
     }
-    const bf16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
-    const bf16 h2 = __float2bfloat16_rn(v.z), h3 = __float2bfloat16_rn(v.w);
-    const bf16 l0 = __float2bfloat16_rn(v.x - __bfloat162float(h0));
-    const bf16 l1 = __float2bfloat16_rn(v.y - __bfloat162float(h1));
-    const bf16 l2 = __float2bfloat16_rn(v.z - __bfloat162float(h2));
-    const bf16 l3 = __float2bfloat16_rn(v.w - __bfloat162float(h3));
+    const bf16 h0 = __float2bfloat16_rn(x.x), h1 = __float2bfloat16_rn(x.y);
+    const bf16 h2 = __float2bfloat16_rn(x.z), h3 = __float2bfloat16_rn(x.w);
+    const bf16 l0 = __float2bfloat16_rn(x.x - __bfloat162float(h0));
+    const bf16 l1 = __float2bfloat16_rn(x.y - __bfloat162float(h1));
+    const bf16 l2 = __float2bfloat16_rn(x.z - __bfloat162float(h2));
+    const bf16 l3 = __float2bfloat16_rn(x.w - __bfloat162float(h3));
     const int wc = q4 >> 4;
     const int kk = (q4 & 15) * 4;
     const int c = kk >> 4, h = (kk >> 3) & 1, e = kk & 7;
@@ -112,15 +127,25 @@ __device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v)
 }
 
 // ---------------------------------------------------------------- epilogues
+template <int T>
 __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M) {
-  for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
-    const int m = i / kBlockRows, r = i - m * kBlockRows;
-    const int n = rb * kBlockRows + r;
+  constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
+  float old[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const int i = threadIdx.x + e * kGemmThreads;
+    const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
+    old[e] = (m < M && n < a.N) ? a.out[(size_t)m * a.out_ld + n] : 0.f;
+  }
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const int i = threadIdx.x + e * kGemmThreads;
+    if (i >= M * kBlockRows) continue;
+    const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
     float v = 0.f;
     if (n < a.N) {
-      float* px = a.out + (size_t)m * a.out_ld + n;
-      v = *px + ys[i];
-      *px = v;
+      v = old[e] + ys[i];
+      a.out[(size_t)m * a.out_ld + n] = v;
     }
     ys[i] = v;
   }
@@ -138,30 +163,52 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M) {
   }
 }
 
+template <int T>
 __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M) {
+  constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
   const int half = a.hd >> 1;
-  for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
+  const int n0 = rb * kBlockRows;
+  const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);   // one segment per block
+  const int seg0 = s ? a.seg_end[s - 1] : 0;
+  const bf16* bias = a.bias[s];
+  // Gather every global operand first (bias pairs, rotation factors, positions).
+  float b1[kE], b2[kE];
+  float2 cs[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const int i = threadIdx.x + e * kGemmThreads;
     const int m = i / kBlockRows, r = i - m * kBlockRows;
-    const int n = rb * kBlockRows + r;
-    if (n >= a.N) continue;
-    const int s = n < a.seg_end[0] ? 0 : (n < a.seg_end[1] ? 1 : 2);
-    const int local = n - (s ? a.seg_end[s - 1] : 0);
-    const bf16* bias = a.bias[s];
+    const int local = n0 + r - seg0;
+    const int d = local % a.hd;
+    b1[e] = b2[e] = 0.f;
+    cs[e] = make_float2(1.f, 0.f);
+    if (m < M && n0 + r < a.N) {
+      if (bias) b1[e] = __bfloat162float(bias[local]);
+      if (s < 2 && d < half) {
+        if (bias) b2[e] = __bfloat162float(bias[local + half]);
+        cs[e] = a.rope[(size_t)row_pos(a.rs, m) * half + d];
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const int i = threadIdx.x + e * kGemmThreads;
+    const int m = i / kBlockRows, r = i - m * kBlockRows;
+    if (m >= M || n0 + r >= a.N) continue;
+    const int local = n0 + r - seg0;
+    const int d = local % a.hd;
     const int b = m / a.rs.rps;
     const int pos = row_pos(a.rs, m);
-    const int d = local % a.hd;
     if (s == 2) {
-      const float v = ys[i] + (bias ? __bfloat162float(bias[local]) : 0.f);
       const int kvh = local / a.hd;
-      a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(v);
+      a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(ys[i] + b1[e]);
       continue;
     }
     if (d >= half) continue;
-    const float x1 = ys[i] + (bias ? __bfloat162float(bias[local]) : 0.f);
-    const float x2 = ys[i + half] + (bias ? __bfloat162float(bias[local + half]) : 0.f);
-    const float2 cs = a.rope[(size_t)pos * half + d];
-    const float y1 = x1 * cs.x - x2 * cs.y;
-    const float y2 = x2 * cs.x + x1 * cs.y;
+    const float x1 = ys[i] + b1[e];
+    const float x2 = ys[i + half] + b2[e];
+    const float y1 = x1 * cs[e].x - x2 * cs[e].y;
+    const float y2 = x2 * cs[e].x + x1 * cs[e].y;
     if (s == 0) {
       float* q = a.out + (size_t)m * a.out_ld + local;
       q[0] = y1;
@@ -275,10 +322,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
   pdl_wait();
   pdl_launch_next();
   const int M = a.rs.M;
-  if (a.gain && tid < M) {
-    float s = 0.f;
-    for (int i = 0; i < a.nssq; ++i) s += a.ssq[i * kRows + tid];
-    rinv[tid] = 1.0f / sqrtf(s * a.inv_k + a.eps);
+  if (a.gain) {
+    // 1 / rms of each token row from the per-128-feature sums of squares:
+    // one warp per row, one load per lane (at most 64 partial sums).
+    for (int m = warp; m < M; m += kGemmThreads / 32) {
+      float s0 = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
+      float s1 = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
+      const float s = warp_sum(s0 + s1);
+      if (lane == 0) rinv[m] = 1.0f / sqrtf(s * a.inv_k + a.eps);
+    }
   }
   __syncthreads();
   stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0, min(nch, kWinChunks), M);
@@ -343,18 +395,40 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
     __syncthreads();
     if (!s_flag) return;
     __threadfence();
+    // Sum the slices in fixed order 0, 1, ..., loading four slices' worth of
+    // this thread's elements at a time so the loads overlap.
     const float* src = a.part + (size_t)rb * a.nsplit * (kRows * kBlockRows);
-    for (int i = tid; i < M * kBlockRows; i += kGemmThreads) {
-      float s = __ldcg(src + i);
-      for (int p = 1; p < a.nsplit; ++p) s += __ldcg(src + (size_t)p * (kRows * kBlockRows) + i);
-      ys[i] = s;
+    constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
+    float sum[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) sum[e] = 0.f;
+    for (int p0 = 0; p0 < a.nsplit; p0 += 4) {
+      float v[4][kE];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int e = 0; e < kE; ++e) {
+          const int i = tid + e * kGemmThreads;
+          v[q][e] = (p0 + q < a.nsplit && i < M * kBlockRows)
+                        ? __ldcg(src + (size_t)(p0 + q) * (kRows * kBlockRows) + i)
+                        : 0.f;
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int e = 0; e < kE; ++e) sum[e] += v[q][e];
+    }
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      const int i = tid + e * kGemmThreads;
+      if (i < M * kBlockRows) ys[i] = sum[e];
     }
     if (tid == 0) a.counter[rb] = 0;
     __syncthreads();
   }
 
-  if (EPI == EPI_RESID) epi_resid(a, ys, rb, M);
-  else if (EPI == EPI_QKV) epi_qkv(a, ys, rb, M);
+  if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, M);
+  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M);
   else if (EPI == EPI_SWIGLU) epi_swiglu(a, ys, rb, M);
   else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
   else epi_argmax(a, ys, rb, M, &s_flag);

@@ -17,8 +17,14 @@ constexpr int kRows = SF_MAX_ROWS;     // tokens per forward, at most
 constexpr int kBlockRows = 128;        // output rows (features) per GEMM CTA
 constexpr int kGemmThreads = 256;      // 8 warps x 16 rows
 constexpr int kChunk = 64;             // k per pipeline step (one 128-byte line per weight row)
-constexpr int kWinChunks = 8;          // chunks of activations staged at once
-constexpr int kStages = 5;             // weight tiles in flight per warp (TMA ring)
+#ifndef SF_WIN_CHUNKS
+#define SF_WIN_CHUNKS 8
+#endif
+#ifndef SF_STAGES
+#define SF_STAGES 4
+#endif
+constexpr int kWinChunks = SF_WIN_CHUNKS;   // chunks of activations staged at once
+constexpr int kStages = SF_STAGES;          // weight tiles in flight per warp (TMA ring)
 constexpr int kTileBytes = 16 * kChunk * 2;   // one warp's 16 rows x 64 k of bf16
 constexpr int kKvChunk = 64;           // cache slots per attention work item
 constexpr int kAttnThreads = 256;
