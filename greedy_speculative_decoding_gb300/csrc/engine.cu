@@ -50,14 +50,15 @@ struct Plan {
 // Split K only when the row blocks alone cannot fill the GPU; the split
 // depends on the matrix shape and the SM count, never on the number of
 // token rows, so every row is computed the same way in every launch.
-Plan make_plan(int nblocks, int K, int slots) {
+Plan make_plan(int nblocks, int K, int slots, int max_split, int cps_align = 1) {
   Plan p;
   p.nblocks = nblocks;
   const int nch = (K + kChunk - 1) / kChunk;
   int ns = 1;
   if (nblocks * 10 < slots * 9) ns = std::max(1, slots / nblocks);
-  ns = std::min(ns, nch);
+  ns = std::min(std::min(ns, nch), max_split);
   p.cps = (nch + ns - 1) / ns;
+  p.cps = (p.cps + cps_align - 1) / cps_align * cps_align;   // NF4 slices start on 4-chunk groups
   p.nsplit = (nch + p.cps - 1) / p.cps;
   return p;
 }
@@ -66,8 +67,9 @@ enum { W_Q = 0, W_K, W_V, W_O, W_G, W_U, W_D };
 
 struct LayerW {
   CUtensorMap tm[7];
+  CUtensorMap tms[7];      // NF4 block scales
   const void* w[7] = {};
-  const __half* sc[7] = {};
+  const void* sc[7] = {};  // NF4 block scales
   const bf16 *ln1 = nullptr, *ln2 = nullptr, *bq = nullptr, *bk = nullptr, *bv = nullptr;
 };
 
@@ -107,7 +109,7 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
     return bad("n_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
   if (c->ffn % 8) return bad("ffn must be a multiple of 8");
   if (c->wdtype != SF_WDTYPE_BF16 && c->wdtype != SF_WDTYPE_NF4) return bad("unknown wdtype");
-  if (c->wdtype == SF_WDTYPE_NF4) return bad("NF4 weights are not supported by this build yet");
+  if (c->wdtype == SF_WDTYPE_NF4 && c->ffn % 64) return bad("NF4 weights need ffn to be a multiple of 64");
   const int eld = c->embed_ld ? c->embed_ld : c->hidden;
   if (eld < c->hidden || eld % 8) return bad("embed_ld must be >= hidden and a multiple of 8");
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("bad rms_eps or rope_theta");
@@ -115,7 +117,7 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
 }
 
 struct Layout {
-  size_t x, ssq, q, attn_o, act, apart, gpart, counters, keys, done, zeros, rope_t, rope_d, state, total;
+  size_t x, ssq, q, attn_o, act, apart, gpart, counters, keys, done, zeros, rope_t, rope_d, state, trace, total;
   int n_kv_chunks, max_blocks;
 };
 
@@ -201,6 +203,7 @@ Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, i
   L.rope_t = take((size_t)s_max * (t->head_dim / 2) * 8);
   L.rope_d = d ? take((size_t)s_max * (d->head_dim / 2) * 8) : p;
   L.state = take(state_offsets(B, K, s_max).n_ints * 4);
+  L.trace = take((size_t)2 * 8192 * 8);
   L.total = p;
   return L;
 }
@@ -221,6 +224,9 @@ struct sf_engine {
   Model tgt, dft;
   bool has_dft = false;
   bool pdl = true;      // programmatic dependent launch between the round's kernels
+  unsigned long long* trace = nullptr;     // launch timeline (SF_TRACE=1), kTraceSlots entries
+  int trace_next = 0;
+  std::vector<std::string> trace_labels;
   int B = 0, K = 0, s_max = 0, num_sms = 0, slots = 0;
   cudaStream_t user = nullptr, cap = nullptr;
   unsigned char* ws = nullptr;
@@ -257,23 +263,29 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   if (!check(md.embed, "embed", false)) return fail(SF_ERR_ARG, "embed pointer null or not 16-byte aligned");
   md.embed_ld = c->embed_ld ? c->embed_ld : c->hidden;
   md.L.resize(c->layers);
+  const bool nf4 = c->wdtype == SF_WDTYPE_NF4;
   for (int l = 0; l < c->layers; ++l) {
     LayerW& lw = md.L[l];
+    // NF4: every linear map is two slots, packed codes then block scales.
+    auto lin = [&](int k) {
+      lw.w[k] = w[i++];
+      if (nf4) lw.sc[k] = w[i++];
+    };
     lw.ln1 = static_cast<const bf16*>(w[i++]);
-    lw.w[W_Q] = w[i++];
-    lw.w[W_K] = w[i++];
-    lw.w[W_V] = w[i++];
+    lin(W_Q);
+    lin(W_K);
+    lin(W_V);
     lw.bq = static_cast<const bf16*>(w[i++]);
     lw.bk = static_cast<const bf16*>(w[i++]);
     lw.bv = static_cast<const bf16*>(w[i++]);
-    lw.w[W_O] = w[i++];
+    lin(W_O);
     lw.ln2 = static_cast<const bf16*>(w[i++]);
-    lw.w[W_G] = w[i++];
-    lw.w[W_U] = w[i++];
-    lw.w[W_D] = w[i++];
+    lin(W_G);
+    lin(W_U);
+    lin(W_D);
     if (!c->qkv_bias) lw.bq = lw.bk = lw.bv = nullptr;
     bool ok = check(lw.ln1, "ln1", false) && check(lw.ln2, "ln2", false);
-    for (int k = 0; k < 7; ++k) ok = ok && check(lw.w[k], "w", false);
+    for (int k = 0; k < 7; ++k) ok = ok && check(lw.w[k], "w", false) && (!nf4 || check(lw.sc[k], "scales", false));
     if (c->qkv_bias) ok = ok && check(lw.bq, "bq", false) && check(lw.bk, "bk", false) && check(lw.bv, "bv", false);
     if (!ok) return fail(SF_ERR_ARG, "layer %d: a weight pointer is null or not 16-byte aligned", l);
   }
@@ -295,7 +307,8 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     const int rows[7] = {QD, KVD, KVD, H, F, F, H};
     const int ks[7] = {H, H, H, QD, H, H, F};
     for (int k = 0; k < 7; ++k) {
-      const cudaError_t ce = make_weight_map(&lw.tm[k], lw.w[k], rows[k], ks[k], ks[k]);
+      const cudaError_t ce = nf4 ? make_nf4_maps(&lw.tm[k], &lw.tms[k], lw.w[k], lw.sc[k], rows[k], ks[k])
+                                 : make_weight_map(&lw.tm[k], lw.w[k], rows[k], ks[k], ks[k]);
       if (ce != cudaSuccess)
         return fail(SF_ERR_CUDA, "layer %d weight %d: tensor map: %s", l, k, cudaGetErrorString(ce));
     }
@@ -304,11 +317,13 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     const cudaError_t ce = make_weight_map(&md.lm_tm, md.lm, c->vocab, H, md.lm_ld);
     if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "LM head tensor map: %s", cudaGetErrorString(ce));
   }
-  md.p_qkv = make_plan(nblocks_of(c, 0), H, e->slots);
-  md.p_o = make_plan(nblocks_of(c, 1), c->n_heads * c->head_dim, e->slots);
-  md.p_gu = make_plan(nblocks_of(c, 2), H, e->slots);
-  md.p_d = make_plan(nblocks_of(c, 1), c->ffn, e->slots);
-  md.p_lm = make_plan(nblocks_of(c, 3), H, e->slots);
+  // The K splits of a row block run as one thread-block cluster.
+  const int al = nf4 ? 4 : 1;
+  md.p_qkv = make_plan(nblocks_of(c, 0), H, e->slots, kMaxClusterSplit, al);
+  md.p_o = make_plan(nblocks_of(c, 1), c->n_heads * c->head_dim, e->slots, kMaxClusterSplit, al);
+  md.p_gu = make_plan(nblocks_of(c, 2), H, e->slots, kMaxClusterSplit, al);
+  md.p_d = make_plan(nblocks_of(c, 1), c->ffn, e->slots, kMaxClusterSplit, al);
+  md.p_lm = make_plan(nblocks_of(c, 3), H, e->slots, kMaxClusterSplit);
   for (const Plan* p : {&md.p_qkv, &md.p_o, &md.p_gu, &md.p_d, &md.p_lm})
     if (p->nsplit > 1 && p->nblocks * p->nsplit > kMaxPlanTiles)
       return fail(SF_ERR_UNSUPPORTED, "split-K plan exceeds the scratch tiles");
@@ -320,12 +335,28 @@ GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& r
   a.nblocks = p.nblocks;
   a.nsplit = p.nsplit;
   a.cps = p.cps;
+  a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, e->num_sms);
   a.part = e->gpart;
   a.counter = e->counters;
+  a.cluster = 1;
   a.err = e->st.err;
   a.rs = rs;
   a.eps = md.c.rms_eps;
   return a;
+}
+
+constexpr int kTraceSlots = 8192;
+
+// Give the next launch a timeline slot (when tracing) and remember its name.
+RowSet traced(sf_engine* e, RowSet rs, const char* what) {
+  rs.trace = e->trace;
+  if (e->trace) {
+    rs.trace_id = e->trace_next % kTraceSlots;
+    if ((int)e->trace_labels.size() <= rs.trace_id) e->trace_labels.resize(rs.trace_id + 1);
+    e->trace_labels[rs.trace_id] = what;
+    ++e->trace_next;
+  }
+  return rs;
 }
 
 struct TokOut {
@@ -339,6 +370,7 @@ struct TokOut {
 // norm + LM head + argmax run too and write tokens (and optional logits).
 sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokOut& to, cudaStream_t s) {
   const sf_model_cfg& c = md.c;
+  const int nf4 = c.wdtype == SF_WDTYPE_NF4 ? 1 : 0;
   const int H = c.hidden, QD = md.q_dim(), KVD = md.kv_dim();
   EmbedArgs ea{};
   ea.E = md.embed;
@@ -348,7 +380,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.err = e->st.err;
   ea.x = e->x;
   ea.ssq = e->ssq;
-  ea.rs = rs;
+  ea.rs = traced(e, rs, "embed");
   CK(launch_embed(ea, s, e->pdl));
   const size_t layer_elems = (size_t)2 * e->B * c.n_kv_heads * e->s_max * c.head_dim;
   for (int l = 0; l < c.layers; ++l) {
@@ -363,6 +395,11 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.tm[0] = lw.tm[W_Q];
     a.tm[1] = lw.tm[W_K];
     a.tm[2] = lw.tm[W_V];
+    a.tms[0] = lw.tms[W_Q];
+    a.tms[1] = lw.tms[W_K];
+    a.tms[2] = lw.tms[W_V];
+    a.nf4 = nf4;
+    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
     a.bias[0] = lw.bq;
     a.bias[1] = lw.bk;
     a.bias[2] = lw.bv;
@@ -389,6 +426,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.kc = kc;
     a.vc = vc;
     a.rope = md.rope;
+    a.rs = traced(e, rs, "qkv");
     CK(launch_gemm(a, EPI_QKV, s, e->pdl));
     // attention
     AttnArgs t{};
@@ -405,12 +443,16 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     t.n_kv_chunks = e->lay.n_kv_chunks;
     t.scale = 1.0f / sqrtf((float)c.head_dim);
     t.err = e->st.err;
-    t.rs = rs;
+    t.rs = traced(e, rs, "attention");
+    t.merge_trace_id = traced(e, rs, "merge").trace_id;
     CK(launch_attention(t, e->num_sms, s, e->pdl));
     // o-projection + residual
     a = base_args(e, md, md.p_o, rs);
     a.w[0] = lw.w[W_O];
     a.tm[0] = lw.tm[W_O];
+    a.tms[0] = lw.tms[W_O];
+    a.nf4 = nf4;
+    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
     a.seg_end[0] = H;
     a.ld[0] = QD;
     a.nseg = 1;
@@ -421,6 +463,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.out = e->x;
     a.out_ld = H;
     a.ssq_out = e->ssq;
+    a.rs = traced(e, rs, "o_proj");
     CK(launch_gemm(a, EPI_RESID, s, e->pdl));
     // gate/up + SwiGLU
     a = base_args(e, md, md.p_gu, rs);
@@ -428,6 +471,10 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.w[1] = lw.w[W_U];
     a.tm[0] = lw.tm[W_G];
     a.tm[1] = lw.tm[W_U];
+    a.tms[0] = lw.tms[W_G];
+    a.tms[1] = lw.tms[W_U];
+    a.nf4 = nf4;
+    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
     a.ld[0] = a.ld[1] = H;
     a.nseg = 2;
     a.N = c.ffn;
@@ -440,11 +487,15 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.inv_k = 1.0f / H;
     a.out = e->act;
     a.out_ld = (c.ffn + 3) / 4 * 4;
+    a.rs = traced(e, rs, "gate_up");
     CK(launch_gemm(a, EPI_SWIGLU, s, e->pdl));
     // down + residual
     a = base_args(e, md, md.p_d, rs);
     a.w[0] = lw.w[W_D];
     a.tm[0] = lw.tm[W_D];
+    a.tms[0] = lw.tms[W_D];
+    a.nf4 = nf4;
+    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
     a.seg_end[0] = H;
     a.ld[0] = c.ffn;
     a.nseg = 1;
@@ -455,6 +506,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.out = e->x;
     a.out_ld = H;
     a.ssq_out = e->ssq;
+    a.rs = traced(e, rs, "down");
     CK(launch_gemm(a, EPI_RESID, s, e->pdl));
   }
   if (!lm) return SF_OK;
@@ -481,6 +533,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   a.logits = to.logits;
   a.lg_stride = to.lg_stride;
   a.lg_off = to.lg_off;
+  a.rs = traced(e, rs, "lm_head");
   CK(launch_gemm(a, EPI_ARGMAX, s, e->pdl));
   return SF_OK;
 }
@@ -643,8 +696,8 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   if (!out) return fail(SF_ERR_ARG, "out is null");
   *out = nullptr;
   std::string why;
-  if (!cfg_ok(tgt, &why)) return fail(tgt && tgt->wdtype == SF_WDTYPE_NF4 ? SF_ERR_UNSUPPORTED : SF_ERR_ARG, "target: %s", why.c_str());
-  if (dft && !cfg_ok(dft, &why)) return fail(dft->wdtype == SF_WDTYPE_NF4 ? SF_ERR_UNSUPPORTED : SF_ERR_ARG, "draft: %s", why.c_str());
+  if (!cfg_ok(tgt, &why)) return fail(SF_ERR_ARG, "target: %s", why.c_str());
+  if (dft && !cfg_ok(dft, &why)) return fail(SF_ERR_ARG, "draft: %s", why.c_str());
   if (!tgt_w || (dft && !dft_w)) return fail(SF_ERR_ARG, "weight pointer array is null");
   if (batch < 1 || K < 1 || K > 15) return fail(SF_ERR_ARG, "batch must be >= 1 and K in 1..15");
   if (batch * (K + 1) > SF_MAX_ROWS || batch * 2 > SF_MAX_ROWS)
@@ -668,6 +721,9 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   // SF_PDL=0 in the environment launches the kernels without programmatic
   // dependent launch (for comparing the two; results are identical).
   if (const char* v = getenv("SF_PDL")) e->pdl = v[0] != '0';
+  // SF_TRACE=1: kernels stamp a launch timeline (see sf_trace).
+  const char* tr = getenv("SF_TRACE");
+  const bool trace_on = tr && tr[0] == '1';
   auto bail = [&](sf_status s) {
     sf_destroy(e);
     return s;
@@ -697,6 +753,7 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->done = reinterpret_cast<int*>(ws + e->lay.done);
   e->zeros = reinterpret_cast<int*>(ws + e->lay.zeros);
   e->tgt.rope = reinterpret_cast<float2*>(ws + e->lay.rope_t);
+  if (trace_on) e->trace = reinterpret_cast<unsigned long long*>(ws + e->lay.trace);
   if (dft) e->dft.rope = reinterpret_cast<float2*>(ws + e->lay.rope_d);
   int* S = reinterpret_cast<int*>(ws + e->lay.state);
   SpecState& st = e->st;
@@ -721,6 +778,14 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
 
   cudaError_t ce;
   if ((ce = gemm_init()) != cudaSuccess) return bail(fail(SF_ERR_CUDA, "gemm_init: %s", cudaGetErrorString(ce)));
+  if (tgt->wdtype == SF_WDTYPE_NF4 || (dft && dft->wdtype == SF_WDTYPE_NF4)) {
+    double lv[16];
+    float lf[16];
+    nf4_levels(lv);
+    for (int k = 0; k < 16; ++k) lf[k] = (float)lv[k];
+    if ((ce = set_nf4_levels(lf)) != cudaSuccess)
+      return bail(fail(SF_ERR_CUDA, "NF4 levels: %s", cudaGetErrorString(ce)));
+  }
   // Zero everything that must start at zero: counters, keys, state.
   if ((ce = cudaMemsetAsync(ws + e->lay.counters, 0, e->lay.rope_t - e->lay.counters, e->user)) ||
       (ce = cudaMemsetAsync(ws + e->lay.state, 0, e->so.n_ints * 4, e->user)) ||
@@ -967,7 +1032,7 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   int dev = 0, sms = 0;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const Plan p = make_plan((N + 127) / 128, K, 2 * sms);
+  const Plan p = make_plan((N + 127) / 128, K, 2 * sms, 1 << 30);
   if (p.nsplit > 1 && p.nblocks * p.nsplit > kMaxPlanTiles) return fail(SF_ERR_UNSUPPORTED, "plan too large");
   CK(gemm_init());
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
@@ -985,6 +1050,7 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   a.nblocks = p.nblocks;
   a.nsplit = p.nsplit;
   a.cps = p.cps;
+  a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, sms);
   a.in = d_x;
   a.in_ld = K;
   a.part = reinterpret_cast<float*>(ws);
@@ -997,12 +1063,29 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   return SF_OK;
 }
 
+int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches) {
+  if (!h || !h->trace) return 0;
+  if (!h_out) return h->trace_next;
+  const int n = std::min(std::min(h->trace_next, kTraceSlots), max_launches);
+  if (h_out && n > 0) {
+    if (cudaMemcpyAsync(h_out, h->trace, (size_t)2 * n * 8, cudaMemcpyDeviceToHost, h->user) != cudaSuccess ||
+        cudaStreamSynchronize(h->user) != cudaSuccess)
+      return 0;
+  }
+  return n;
+}
+
+const char* sf_trace_label(sf_handle h, int32_t i) {
+  if (!h || i < 0 || i >= (int)h->trace_labels.size()) return "";
+  return h->trace_labels[i].c_str();
+}
+
 sf_status sf_nf4_quantize(const void* d_w, int32_t rows, int32_t cols, int32_t ld, void* d_packed, void* d_scales,
                           void* cuda_stream) {
   if (!d_w || !d_packed || !d_scales) return fail(SF_ERR_ARG, "null pointer");
   if (rows < 1 || cols < 64 || cols % 64 || ld < cols) return fail(SF_ERR_ARG, "need cols a multiple of 64 and ld >= cols");
   CK(launch_nf4_quantize(static_cast<const bf16*>(d_w), rows, cols, ld, static_cast<uint8_t*>(d_packed),
-                         static_cast<__half*>(d_scales), static_cast<cudaStream_t>(cuda_stream)));
+                         static_cast<__half*>(d_scales), nf4_scale_ld(cols), static_cast<cudaStream_t>(cuda_stream)));
   return SF_OK;
 }
 

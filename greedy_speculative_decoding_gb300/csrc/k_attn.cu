@@ -20,7 +20,9 @@ namespace sf {
 // x[m][:] = E[tok_m][:] in fp32, plus the per-128-feature sums of squares the
 // next RMSNorm needs.
 __global__ void __launch_bounds__(128) k_embed(const __grid_constant__ EmbedArgs a) {
+  trace_mark(a.rs, 0);
   pdl_wait();
+  trace_mark(a.rs, 1);
   pdl_launch_next();
   __shared__ float part[4];
   const int m = blockIdx.x, blk = blockIdx.y, i = threadIdx.x;
@@ -85,8 +87,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   __shared__ __align__(128) unsigned char vs[kKvChunk * VP];
   __shared__ __align__(8) uint64_t bar;
 
-  pdl_wait();
-  pdl_launch_next();
+  trace_mark(a.rs, 0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c4 = lane & 3;
   const int group = a.nq / a.nkv;
@@ -98,31 +99,56 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   }
   __syncthreads();
 
+  // The lengths were written by kernels that finished before the preceding
+  // one started, so they (and the cache slots below this pass's first
+  // position) can be read before waiting on the preceding kernel.
   int total = 0;
   for (int b = 0; b < a.B; ++b) {
     const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
     total += a.nkv * (p_last / kKvChunk + 1);
   }
-  uint32_t phase = 0;
-  for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    int b = 0, rest = item, nch = 0;
-    for (; b < a.B; ++b) {
+  auto locate = [&](int item, int& b, int& kvh, int& c) {
+    int rest = item, nch = 0;
+    for (b = 0; b < a.B; ++b) {
       const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
       nch = p_last / kKvChunk + 1;
       if (rest < a.nkv * nch) break;
       rest -= a.nkv * nch;
     }
-    const int kvh = rest / nch, c = rest - kvh * nch;
+    kvh = rest / nch;
+    c = rest - kvh * nch;
+  };
+  auto issue = [&](int b, int kvh, int c) {
     const size_t off = (((size_t)b * a.nkv + kvh) * a.s_max + (size_t)c * kKvChunk) * HD;
     if (warp == 0) {
       if (lane == 0) mbar_expect_tx(&bar, 2u * kKvChunk * HD * sizeof(bf16));
       __syncwarp();
-      fence_proxy_async();   // earlier generic reads of ks/vs before the async writes
+      fence_proxy_async();   // earlier generic accesses of ks/vs before the async writes
       for (int r = lane; r < kKvChunk; r += 32) {
         bulk_g2s(ks + r * KP, a.kc + off + (size_t)r * HD, HD * sizeof(bf16), &bar);
         bulk_g2s(vs + r * VP, a.vc + off + (size_t)r * HD, HD * sizeof(bf16), &bar);
       }
     }
+  };
+  bool issued = false;
+  if ((int)blockIdx.x < total) {
+    int b, kvh, c;
+    locate(blockIdx.x, b, kvh, c);
+    if ((c + 1) * kKvChunk <= a.rs.pos_base[b] + a.rs.pos_off) {   // no slot of this pass in the chunk
+      issue(b, kvh, c);
+      issued = true;
+    }
+  }
+  pdl_wait();
+  trace_mark(a.rs, 1);
+  pdl_launch_next();
+
+  uint32_t phase = 0;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    int b, kvh, c;
+    locate(item, b, kvh, c);
+    if (!issued) issue(b, kvh, c);
+    issued = false;
     if (!mbar_wait(&bar, phase, kWaitIters)) {
       if (tid == 0) atomicOr(a.err, kErrWait);
       mbar_wait(&bar, phase, kWaitIters);
@@ -256,7 +282,11 @@ __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
   __shared__ float lw[kMaxKvChunks];
   __shared__ float red[4];
   __shared__ float s_mx, s_l;
+  RowSet rs1 = a.rs;
+  rs1.trace_id = a.merge_trace_id;
+  trace_mark(rs1, 0);
   pdl_wait();
+  trace_mark(rs1, 1);
   pdl_launch_next();
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
   const int d = threadIdx.x, lane = d & 31, warp = d >> 5, nwarps = blockDim.x >> 5;

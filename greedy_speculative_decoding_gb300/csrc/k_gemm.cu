@@ -31,6 +31,9 @@ namespace sf {
 namespace {
 
 constexpr uint32_t kWaitIters = 1u << 24;
+constexpr int kScaleTileBytes = 16 * 8 * 2;   // NF4: 16 rows x 8 block scales (fp16)
+
+__constant__ float c_nf4_levels[16];
 
 // Tensor map and row coordinate of warp w's 16 rows in row block rb.
 template <int EPI>
@@ -50,41 +53,55 @@ __device__ __forceinline__ int warp_tile_row(const GemmArgs& a, int rb, int w, i
 // c0 + wc) into fragment order: [wc][t][h][lane][8] bf16, lane = 4*col + c
 // with col = 2*(m%4) + {0: hi, 1: lo}, and k = 64*chunk + 16*c + 8*h + e.
 template <int T>
-__device__ __forceinline__ void stage_acts(const GemmArgs& a, uint2* act, const float* rinv, int cabs0,
-                                           int nwc, int M) {
-  constexpr int kItems = (4 * T * kWinChunks * 16 + kGemmThreads - 1) / kGemmThreads;
-  const int per_m = nwc * 16;  // groups of 4 k per token row
-  const int total = 4 * T * per_m;
-  // All global loads of this thread first, so their latencies overlap.
+struct StageRegs {
+  static constexpr int kItems = (4 * T * kWinChunks * 16 + kGemmThreads - 1) / kGemmThreads;
   float4 v[kItems];
   uint2 gg[kItems];
+};
+
+// Load this thread's share of activation chunks [cabs0, cabs0 + nwc) (and
+// the RMSNorm gains) into registers: all loads issued before any is used.
+template <int T>
+__device__ __forceinline__ void stage_load(const GemmArgs& a, StageRegs<T>& r, int cabs0, int nwc, int M) {
+  const int per_m = nwc * 16;  // groups of 4 k per token row
+  const int total = 4 * T * per_m;
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
+  for (int it = 0; it < StageRegs<T>::kItems; ++it) {
     const int idx = threadIdx.x + it * kGemmThreads;
     const int m = idx / per_m;
     const int k = cabs0 * kChunk + (idx - m * per_m) * 4;
-    v[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-    gg[it] = make_uint2(0, 0);
+    r.v[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    r.gg[it] = make_uint2(0, 0);
     if (idx < total && m < M && k < a.K) {
-      v[it] = *reinterpret_cast<const float4*>(a.in + (size_t)m * a.in_ld + k);
-      if (a.gain) gg[it] = *reinterpret_cast<const uint2*>(a.gain + k);
+      r.v[it] = *reinterpret_cast<const float4*>(a.in + (size_t)m * a.in_ld + k);
+      if (a.gain) r.gg[it] = *reinterpret_cast<const uint2*>(a.gain + k);
     }
   }
+}
+
+// Apply the RMSNorm (when a.gain), split into bf16 hi + lo and store in
+// fragment order: [wc][t][h][lane][8] bf16, lane = 4*col + c with
+// col = 2*(m%4) + {0: hi, 1: lo}, and k = 64*chunk + 16*c + 8*h + e.
+template <int T>
+__device__ __forceinline__ void stage_convert(const GemmArgs& a, const StageRegs<T>& r, uint2* act,
+                                              const float* rinv, int nwc, int M) {
+  const int per_m = nwc * 16;
+  const int total = 4 * T * per_m;
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
+  for (int it = 0; it < StageRegs<T>::kItems; ++it) {
     const int idx = threadIdx.x + it * kGemmThreads;
     if (idx >= total) continue;
     const int m = idx / per_m;
     const int q4 = idx - m * per_m;
-    float4 x = v[it];
+    float4 x = r.v[it];
     if (a.gain && m < M) {
-      const float r = rinv[m];
-      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg[it].x));
-      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg[it].y));
-      x.x = (x.x * r) * g01.x;
-      x.y = (x.y * r) * g01.y;
-      x.z = (x.z * r) * g23.x;
-      x.w = (x.w * r) * g23.y;
+      const float rr = rinv[m];
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.gg[it].x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.gg[it].y));
+      x.x = (x.x * rr) * g01.x;
+      x.y = (x.y * rr) * g01.y;
+      x.z = (x.z * rr) * g23.x;
+      x.w = (x.w * rr) * g23.y;
     }
     const bf16 h0 = __float2bfloat16_rn(x.x), h1 = __float2bfloat16_rn(x.y);
     const bf16 h2 = __float2bfloat16_rn(x.z), h3 = __float2bfloat16_rn(x.w);
@@ -101,6 +118,14 @@ __device__ __forceinline__ void stage_acts(const GemmArgs& a, uint2* act, const 
     act[(base + 4 * col + c) * 2 + (e >> 2)] = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
     act[(base + 4 * (col + 1) + c) * 2 + (e >> 2)] = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
   }
+}
+
+template <int T>
+__device__ __forceinline__ void stage_acts(const GemmArgs& a, uint2* act, const float* rinv, int cabs0,
+                                           int nwc, int M) {
+  StageRegs<T> r;
+  stage_load<T>(a, r, cabs0, nwc, M);
+  stage_convert<T>(a, r, act, rinv, nwc, M);
 }
 
 template <int T>
@@ -127,16 +152,53 @@ __device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v)
 }
 
 // ---------------------------------------------------------------- epilogues
+// Global operands of the epilogue, loaded right after the kernel waits on
+// its producer so their latency overlaps the weight stream.
 template <int T>
-__device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M) {
-  constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
-  float old[kE];
+struct EpiPre {
+  static constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
+  float v0[kE], v1[kE];
+  float2 cs[kE];
+};
+
+template <int T, int EPI>
+__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, EpiPre<T>& pre) {
+  constexpr int kE = EpiPre<T>::kE;
+  if (EPI == EPI_RESID) {
 #pragma unroll
-  for (int e = 0; e < kE; ++e) {
-    const int i = threadIdx.x + e * kGemmThreads;
-    const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
-    old[e] = (m < M && n < a.N) ? a.out[(size_t)m * a.out_ld + n] : 0.f;
+    for (int e = 0; e < kE; ++e) {
+      const int i = threadIdx.x + e * kGemmThreads;
+      const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
+      pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)m * a.out_ld + n] : 0.f;
+    }
+  } else if (EPI == EPI_QKV) {
+    const int half = a.hd >> 1;
+    const int n0 = rb * kBlockRows;
+    const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);   // one segment per block
+    const int seg0 = s ? a.seg_end[s - 1] : 0;
+    const bf16* bias = a.bias[s];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      const int i = threadIdx.x + e * kGemmThreads;
+      const int m = i / kBlockRows, r = i - m * kBlockRows;
+      const int local = n0 + r - seg0;
+      const int d = local % a.hd;
+      pre.v0[e] = pre.v1[e] = 0.f;
+      pre.cs[e] = make_float2(1.f, 0.f);
+      if (m < M && n0 + r < a.N) {
+        if (bias) pre.v0[e] = __bfloat162float(bias[local]);
+        if (s < 2 && d < half) {
+          if (bias) pre.v1[e] = __bfloat162float(bias[local + half]);
+          pre.cs[e] = a.rope[(size_t)row_pos(a.rs, m) * half + d];
+        }
+      }
+    }
   }
+}
+
+template <int T>
+__device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M, const EpiPre<T>& pre) {
+  constexpr int kE = EpiPre<T>::kE;
 #pragma unroll
   for (int e = 0; e < kE; ++e) {
     const int i = threadIdx.x + e * kGemmThreads;
@@ -144,7 +206,7 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M) {
     const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
     float v = 0.f;
     if (n < a.N) {
-      v = old[e] + ys[i];
+      v = pre.v0[e] + ys[i];
       a.out[(size_t)m * a.out_ld + n] = v;
     }
     ys[i] = v;
@@ -164,32 +226,12 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M) {
 }
 
 template <int T>
-__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M) {
-  constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
+__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const EpiPre<T>& pre) {
+  constexpr int kE = EpiPre<T>::kE;
   const int half = a.hd >> 1;
   const int n0 = rb * kBlockRows;
-  const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);   // one segment per block
+  const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);
   const int seg0 = s ? a.seg_end[s - 1] : 0;
-  const bf16* bias = a.bias[s];
-  // Gather every global operand first (bias pairs, rotation factors, positions).
-  float b1[kE], b2[kE];
-  float2 cs[kE];
-#pragma unroll
-  for (int e = 0; e < kE; ++e) {
-    const int i = threadIdx.x + e * kGemmThreads;
-    const int m = i / kBlockRows, r = i - m * kBlockRows;
-    const int local = n0 + r - seg0;
-    const int d = local % a.hd;
-    b1[e] = b2[e] = 0.f;
-    cs[e] = make_float2(1.f, 0.f);
-    if (m < M && n0 + r < a.N) {
-      if (bias) b1[e] = __bfloat162float(bias[local]);
-      if (s < 2 && d < half) {
-        if (bias) b2[e] = __bfloat162float(bias[local + half]);
-        cs[e] = a.rope[(size_t)row_pos(a.rs, m) * half + d];
-      }
-    }
-  }
 #pragma unroll
   for (int e = 0; e < kE; ++e) {
     const int i = threadIdx.x + e * kGemmThreads;
@@ -201,14 +243,15 @@ __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M) {
     const int pos = row_pos(a.rs, m);
     if (s == 2) {
       const int kvh = local / a.hd;
-      a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(ys[i] + b1[e]);
+      a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(ys[i] + pre.v0[e]);
       continue;
     }
     if (d >= half) continue;
-    const float x1 = ys[i] + b1[e];
-    const float x2 = ys[i + half] + b2[e];
-    const float y1 = x1 * cs[e].x - x2 * cs[e].y;
-    const float y2 = x2 * cs[e].x + x1 * cs[e].y;
+    const float x1 = ys[i] + pre.v0[e];
+    const float x2 = ys[i + half] + pre.v1[e];
+    const float2 cs = pre.cs[e];
+    const float y1 = x1 * cs.x - x2 * cs.y;
+    const float y2 = x2 * cs.x + x1 * cs.y;
     if (s == 0) {
       float* q = a.out + (size_t)m * a.out_ld + local;
       q[0] = y1;
@@ -281,17 +324,23 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, in
 
 }  // namespace
 
-template <int T, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant__ GemmArgs a) {
+template <int T, int EPI, bool NF4>
+__global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const __grid_constant__ GemmArgs a) {
   extern __shared__ unsigned char smem_raw[];
   // The swizzled TMA tiles need a 1024-byte aligned base.
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   unsigned char* ring = smem;                                            // [8][kStages][kTileBytes]
-  uint4* act = reinterpret_cast<uint4*>(smem + 8 * kStages * kTileBytes);
-  float* ys = reinterpret_cast<float*>(smem + 8 * kStages * kTileBytes + kWinChunks * T * 1024);
+  const int kStages = a.stages;
+  // NF4: each stage also carries the block scales of its rows ([16][8] fp16).
+  unsigned char* sring = smem + 8 * kStages * kTileBytes;                // [8][kStages][kScaleTileBytes]
+  unsigned char* after_ring = sring + (NF4 ? 8 * kStages * kScaleTileBytes : 0);
+  uint4* act = reinterpret_cast<uint4*>(after_ring);
+  float* ys = reinterpret_cast<float*>(after_ring + kWinChunks * T * 1024);
   float* rinv = ys + 4 * T * kBlockRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);           // [8][kStages]
   __shared__ int s_flag;
+  __shared__ uint32_t lut[NF4 ? 256 : 1];   // NF4: byte (two codes) -> bf16 pair of levels
+  trace_mark(a.rs, 0);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -303,37 +352,61 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
   int seg = 0;
   const int trow = warp_tile_row<EPI>(a, rb, warp, &seg);
   const CUtensorMap* map = &a.tm[seg];
+  const CUtensorMap* smap = &a.tms[seg];
   unsigned char* my_ring = ring + warp * kStages * kTileBytes;
+  unsigned char* my_sring = sring + warp * kStages * kScaleTileBytes;
   uint64_t* my_bar = bars + warp * kStages;
-  uint64_t policy = 0;
+  // bf16: one stage = one 64-k chunk; NF4: one stage = four chunks (16 rows x
+  // 128 bytes of codes) plus the 8-block scale group that holds them.
+  const int per_stage = NF4 ? 4 : 1;
+  const int nst = (nch + per_stage - 1) / per_stage;
+  auto issue = [&](int s, int st) {
+    if (NF4) {
+      const int cabs = c0 + 4 * st;
+      mbar_expect_tx(&my_bar[s], kTileBytes + kScaleTileBytes);
+      tma_load_2d(my_ring + s * kTileBytes, map, cabs * (kChunk / 2), trow, &my_bar[s], policy_evict_first());
+      tma_load_2d(my_sring + s * kScaleTileBytes, smap, (cabs / 8) * 8, trow, &my_bar[s], policy_evict_first());
+    } else {
+      mbar_expect_tx(&my_bar[s], kTileBytes);
+      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + st) * kChunk, trow, &my_bar[s], policy_evict_first());
+    }
+  };
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&my_bar[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    policy = policy_evict_first();
     // Weights are never written by the preceding kernels: start streaming
     // them before waiting on the producer of the activations.
-    for (int s = 0; s < kStages && s < nch; ++s) {
-      mbar_expect_tx(&my_bar[s], kTileBytes);
-      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + s) * kChunk, trow, &my_bar[s], policy);
-    }
+    for (int s = 0; s < kStages && s < nst; ++s) issue(s, s);
+  }
+  if (NF4) {
+    const uint32_t i = tid;   // 256 threads, 256 byte values
+    lut[i] = pack_bf16x2(__float2bfloat16_rn(c_nf4_levels[i & 15]), __float2bfloat16_rn(c_nf4_levels[i >> 4]));
   }
   __syncwarp();
 
   pdl_wait();
+  trace_mark(a.rs, 1);
   pdl_launch_next();
   const int M = a.rs.M;
-  if (a.gain) {
-    // 1 / rms of each token row from the per-128-feature sums of squares:
-    // one warp per row, one load per lane (at most 64 partial sums).
-    for (int m = warp; m < M; m += kGemmThreads / 32) {
-      float s0 = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
-      float s1 = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
-      const float s = warp_sum(s0 + s1);
-      if (lane == 0) rinv[m] = 1.0f / sqrtf(s * a.inv_k + a.eps);
+  EpiPre<T> pre;
+  if (!(a.cluster && a.nsplit > 1) || cluster_rank() == 0) epi_prefetch<T, EPI>(a, rb, M, pre);
+  {
+    // The first activation window and the RMSNorm sums are loaded together.
+    StageRegs<T> r;
+    stage_load<T>(a, r, c0, min(nch, kWinChunks), M);
+    if (a.gain) {
+      // 1 / rms of each token row from the per-128-feature sums of squares:
+      // one warp per row, one load per lane (at most 64 partial sums).
+      for (int m = warp; m < M; m += kGemmThreads / 32) {
+        float s0 = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
+        float s1 = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
+        const float s = warp_sum(s0 + s1);
+        if (lane == 0) rinv[m] = 1.0f / sqrtf(s * a.inv_k + a.eps);
+      }
     }
+    __syncthreads();
+    stage_convert<T>(a, r, reinterpret_cast<uint2*>(act), rinv, min(nch, kWinChunks), M);
   }
-  __syncthreads();
-  stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0, min(nch, kWinChunks), M);
   __syncthreads();
 
   float acc[T][4];
@@ -346,34 +419,79 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
   const int off_lo = g * 128 + (((2 * c) ^ sw) << 4);
   const int off_hi = g * 128 + (((2 * c + 1) ^ sw) << 4);
   bool timed_out = false;
-  for (int ch = 0; ch < nch; ++ch) {
-    if (ch > 0 && (ch % kWinChunks) == 0) {
-      __syncthreads();
-      stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
-      __syncthreads();
-    }
-    const int s = ch % kStages;
-    if (!mbar_wait(&my_bar[s], (ch / kStages) & 1, kWaitIters)) timed_out = true;
+  for (int st = 0; st < nst; ++st) {
+    const int s = st % kStages;
+    if (!mbar_wait(&my_bar[s], (st / kStages) & 1, kWaitIters)) timed_out = true;
     const unsigned char* tile = my_ring + s * kTileBytes;
-    uint4 w[4];
-    w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
-    w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
-    w[2] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_lo);
-    w[3] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_hi);
-    __syncwarp();
-    if (lane == 0 && ch + kStages < nch) {
-      fence_proxy_async();   // the warp's reads of this stage before the async refill
-      mbar_expect_tx(&my_bar[s], kTileBytes);
-      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + ch + kStages) * kChunk, trow, &my_bar[s], policy);
+    if (!NF4) {
+      const int ch = st;
+      if (ch > 0 && (ch % kWinChunks) == 0) {
+        __syncthreads();
+        stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
+        __syncthreads();
+      }
+      uint4 w[4];
+      w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
+      w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
+      w[2] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_lo);
+      w[3] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_hi);
+      __syncwarp();
+      if (lane == 0 && st + kStages < nst) {
+        fence_proxy_async();   // the warp's reads of this stage before the async refill
+        issue(s, st + kStages);
+      }
+      mma_chunk<T>(acc, w, act, ch % kWinChunks, lane);
+    } else {
+      const __half* sct = reinterpret_cast<const __half*>(my_sring + s * kScaleTileBytes);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ch = 4 * st + q;
+        if (ch >= nch) break;
+        if (ch > 0 && (ch % kWinChunks) == 0) {
+          __syncthreads();
+          stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
+          __syncthreads();
+        }
+        // 8 code bytes (k = 16c .. 16c+15 of this chunk) of rows g and g+8,
+        // at their 128-byte-swizzled positions; the scale of each row.
+        const int cofs = ((((2 * q + (c >> 1)) ^ sw) << 4) + 8 * (c & 1));
+        const uint2 b0 = *reinterpret_cast<const uint2*>(tile + g * 128 + cofs);
+        const uint2 b1 = *reinterpret_cast<const uint2*>(tile + (g + 8) * 128 + cofs);
+        const int scol = (c0 + ch) & 7;
+        const float s_lo = __half2float(sct[g * 8 + scol]);
+        const float s_hi = __half2float(sct[(g + 8) * 8 + scol]);
+        uint4 w[4];
+        w[0] = make_uint4(lut[b0.x & 255], lut[(b0.x >> 8) & 255], lut[(b0.x >> 16) & 255], lut[b0.x >> 24]);
+        w[1] = make_uint4(lut[b0.y & 255], lut[(b0.y >> 8) & 255], lut[(b0.y >> 16) & 255], lut[b0.y >> 24]);
+        w[2] = make_uint4(lut[b1.x & 255], lut[(b1.x >> 8) & 255], lut[(b1.x >> 16) & 255], lut[b1.x >> 24]);
+        w[3] = make_uint4(lut[b1.y & 255], lut[(b1.y >> 8) & 255], lut[(b1.y >> 16) & 255], lut[b1.y >> 24]);
+        // Levels are unscaled; one chunk shares one scale per row, applied
+        // to the chunk's product before it joins the running sum.
+        float part[T][4];
+#pragma unroll
+        for (int t = 0; t < T; ++t) part[t][0] = part[t][1] = part[t][2] = part[t][3] = 0.f;
+        mma_chunk<T>(part, w, act, ch % kWinChunks, lane);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          acc[t][0] = fmaf(s_lo, part[t][0], acc[t][0]);
+          acc[t][1] = fmaf(s_lo, part[t][1], acc[t][1]);
+          acc[t][2] = fmaf(s_hi, part[t][2], acc[t][2]);
+          acc[t][3] = fmaf(s_hi, part[t][3], acc[t][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && st + kStages < nst) {
+        fence_proxy_async();
+        issue(s, st + kStages);
+      }
     }
-    mma_chunk<T>(acc, w, act, ch % kWinChunks, lane);
   }
   if (timed_out) {
     // A tile never arrived: report, and give every copy of this warp one more
     // bounded chance to land before the CTA's shared memory is released.
     if (lane == 0) atomicOr(a.err, kErrWait);
-    for (int ch = max(0, nch - kStages); ch < nch; ++ch)
-      mbar_wait(&my_bar[ch % kStages], (ch / kStages) & 1, kWaitIters);
+    for (int st = max(0, nst - kStages); st < nst; ++st)
+      mbar_wait(&my_bar[st % kStages], (st / kStages) & 1, kWaitIters);
   }
 
   // Token m = 4t + c: hi in column 2c, lo in column 2c + 1.
@@ -386,7 +504,42 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
   }
   __syncthreads();
 
-  if (a.nsplit > 1) {
+  if (a.nsplit > 1 && a.cluster) {
+    // The K slices of this row block are the CTAs of one cluster: after the
+    // barrier every partial tile sits in its CTA's shared memory; rank 0 adds
+    // them in rank order and runs the epilogue; the second barrier keeps the
+    // other CTAs' shared memory alive until it has read them.
+    cluster_sync();
+    const uint32_t rank = cluster_rank();
+    if (rank == 0) {
+      constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
+      const uint32_t ys_s = smem_u32(ys);
+      float sum[kE];
+#pragma unroll
+      for (int e = 0; e < kE; ++e) sum[e] = 0.f;
+      for (int p0 = 0; p0 < a.nsplit; p0 += 4) {
+        float v[4][kE];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < kE; ++e) {
+            const int i = tid + e * kGemmThreads;
+            v[q][e] = (p0 + q < a.nsplit && i < M * kBlockRows) ? ld_dsmem(dsmem_addr(ys_s + 4 * i, p0 + q)) : 0.f;
+          }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < kE; ++e) sum[e] += v[q][e];
+      }
+#pragma unroll
+      for (int e = 0; e < kE; ++e) {
+        const int i = tid + e * kGemmThreads;
+        if (i < M * kBlockRows) ys[i] = sum[e];
+      }
+    }
+    cluster_sync();
+    if (rank != 0) return;
+  } else if (a.nsplit > 1) {
     float* mine = a.part + ((size_t)rb * a.nsplit + sp) * (kRows * kBlockRows);
     for (int i = tid; i < M * kBlockRows; i += kGemmThreads) __stcg(mine + i, ys[i]);
     __threadfence();
@@ -427,20 +580,26 @@ __global__ void __launch_bounds__(kGemmThreads, 2) k_gemm(const __grid_constant_
     __syncthreads();
   }
 
-  if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, M);
-  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M);
+  if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, M, pre);
+  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M, pre);
   else if (EPI == EPI_SWIGLU) epi_swiglu(a, ys, rb, M);
   else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
   else epi_argmax(a, ys, rb, M, &s_flag);
 }
 
-int gemm_smem_bytes(int M) {
+int gemm_smem_bytes(int M, int stages, bool nf4) {
   const int T = (M + 3) / 4;
-  return 1024 /* alignment slack */ + 8 * kStages * kTileBytes + kWinChunks * T * 1024 + 4 * T * kBlockRows * 4 +
-         4 * T * 4 + 8 * kStages * 8;
+  return 1024 /* alignment slack */ + 8 * stages * (kTileBytes + (nf4 ? kScaleTileBytes : 0)) +
+         kWinChunks * T * 1024 + 4 * T * kBlockRows * 4 + 4 * T * 4 + 8 * stages * 8;
 }
 
-cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld) {
+cudaError_t set_nf4_levels(const float levels[16]) {
+  return cudaMemcpyToSymbol(c_nf4_levels, levels, 16 * sizeof(float));
+}
+
+static cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                             uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                             CUtensorMapSwizzle sw) {
   typedef CUresult (*encode_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -453,72 +612,108 @@ cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, in
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
     encode = reinterpret_cast<encode_fn>(fn);
   }
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kChunk, 16};
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int T, int EPI>
+cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, rows, (uint64_t)ld * 2, kChunk, 16,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int nf4_scale_ld(int K) { return ((K / 64 + 7) / 8) * 8; }
+
+cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const void* codes, const void* scales,
+                          int rows, int K) {
+  cudaError_t e = encode_2d(codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, rows, K / 2, 128, 16,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  return encode_2d(scale_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, K / 64, rows, (uint64_t)nf4_scale_ld(K) * 2,
+                   8, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <int T, int EPI, bool NF4>
 static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nblocks * a.nsplit);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (a.cluster && a.nsplit > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = a.nsplit;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_gemm<T, EPI>, a);
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k_gemm<T, EPI, NF4>, a);
 }
 
-template <int T>
+template <int T, bool NF4>
 static cudaError_t init_t() {
-  const int smem = gemm_smem_bytes(4 * T);
+  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4);
+  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
-  return cudaFuncSetAttribute(k_gemm<T, EPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_QKV, NF4>, A, smem))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_RESID, NF4>, A, smem))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_SWIGLU, NF4>, A, smem))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_STORE, NF4>, A, smem))) return e;
+  return cudaFuncSetAttribute(k_gemm<T, EPI_ARGMAX, NF4>, A, smem);
 }
 
 // Raise the dynamic shared-memory limit of every instantiation (current device).
 cudaError_t gemm_init() {
   cudaError_t e;
-  if ((e = init_t<1>())) return e;
-  if ((e = init_t<2>())) return e;
-  if ((e = init_t<3>())) return e;
-  return init_t<4>();
+  if ((e = init_t<1, false>()) || (e = init_t<2, false>()) || (e = init_t<3, false>()) ||
+      (e = init_t<4, false>()) || (e = init_t<1, true>()) || (e = init_t<2, true>()) ||
+      (e = init_t<3, true>()) || (e = init_t<4, true>()))
+    return e;
+  return cudaSuccess;
 }
 
-template <int EPI>
+template <int EPI, bool NF4>
 static cudaError_t launch_e(const GemmArgs& a, cudaStream_t st, bool pdl) {
   switch ((a.rs.M + 3) / 4) {
-    case 1: return launch_t<1, EPI>(a, st, pdl);
-    case 2: return launch_t<2, EPI>(a, st, pdl);
-    case 3: return launch_t<3, EPI>(a, st, pdl);
-    case 4: return launch_t<4, EPI>(a, st, pdl);
+    case 1: return launch_t<1, EPI, NF4>(a, st, pdl);
+    case 2: return launch_t<2, EPI, NF4>(a, st, pdl);
+    case 3: return launch_t<3, EPI, NF4>(a, st, pdl);
+    case 4: return launch_t<4, EPI, NF4>(a, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool NF4>
+static cudaError_t launch_f(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
+  switch (epi) {
+    case EPI_QKV: return launch_e<EPI_QKV, NF4>(a, st, pdl);
+    case EPI_RESID: return launch_e<EPI_RESID, NF4>(a, st, pdl);
+    case EPI_SWIGLU: return launch_e<EPI_SWIGLU, NF4>(a, st, pdl);
+    case EPI_ARGMAX: return launch_e<EPI_ARGMAX, NF4>(a, st, pdl);
+    case EPI_STORE: return launch_e<EPI_STORE, NF4>(a, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
   if (a.rs.M < 1 || a.rs.M > kRows) return cudaErrorInvalidValue;
-  switch (epi) {
-    case EPI_QKV: return launch_e<EPI_QKV>(a, st, pdl);
-    case EPI_RESID: return launch_e<EPI_RESID>(a, st, pdl);
-    case EPI_SWIGLU: return launch_e<EPI_SWIGLU>(a, st, pdl);
-    case EPI_ARGMAX: return launch_e<EPI_ARGMAX>(a, st, pdl);
-    case EPI_STORE: return launch_e<EPI_STORE>(a, st, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.cluster && a.nsplit > kMaxClusterSplit) return cudaErrorInvalidValue;
+  if (a.stages < 2 || a.stages > (a.nf4 ? kMaxStagesNF4 : kMaxStages)) return cudaErrorInvalidValue;
+  if (a.nf4 && (a.K % 64 || (a.cps * a.nsplit > 1 && a.cps % 4))) return cudaErrorInvalidValue;
+  return a.nf4 ? launch_f<true>(a, epi, st, pdl) : launch_f<false>(a, epi, st, pdl);
 }
 
 }  // namespace sf

@@ -206,7 +206,7 @@ void nf4_levels(double out[16]) {
 __constant__ float c_nf4_mid[15];
 
 __global__ void k_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8_t* packed,
-                               __half* scales) {
+                               __half* scales, int scale_ld) {
   const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int nblk = cols / 64;
@@ -229,11 +229,11 @@ __global__ void k_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8_
     }
   }
   packed[(size_t)r * (cols / 2) + blk * 32 + lane] = (uint8_t)(ca | (cb << 4));
-  if (lane == 0) scales[(size_t)r * nblk + blk] = sh;
+  if (lane == 0) scales[(size_t)r * scale_ld + blk] = sh;
 }
 
 cudaError_t launch_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8_t* packed,
-                                __half* scales, cudaStream_t st) {
+                                __half* scales, int scale_ld, cudaStream_t st) {
   double lv[16];
   nf4_levels(lv);
   float mids[15];
@@ -243,7 +243,7 @@ cudaError_t launch_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8
   const long warps = (long)rows * (cols / 64);
   const int threads = 256;
   const long blocks = (warps * 32 + threads - 1) / threads;
-  k_nf4_quantize<<<(unsigned)blocks, threads, 0, st>>>(w, rows, cols, ld, packed, scales);
+  k_nf4_quantize<<<(unsigned)blocks, threads, 0, st>>>(w, rows, cols, ld, packed, scales, scale_ld);
   return cudaGetLastError();
 }
 

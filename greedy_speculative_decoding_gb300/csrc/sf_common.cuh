@@ -43,7 +43,20 @@ struct RowSet {
   int M;               // rows in total
   const int* pos_base;
   int pos_off;
+  unsigned long long* trace;   // optional launch timeline: [2 * trace_id + {0: entry, 1: producer done}]
+  int trace_id;
 };
+
+// Launch timeline for profiling: CTA 0 stamps the global timer when the
+// kernel starts and when its wait on the preceding kernel returns (that is,
+// when the preceding kernel has finished).
+__device__ __forceinline__ void trace_mark(const RowSet& rs, int k) {
+  if (rs.trace && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    rs.trace[2 * rs.trace_id + k] = t;
+  }
+}
 
 __device__ __forceinline__ int row_pos(const RowSet& rs, int m) {
   return rs.pos_base[m / rs.rps] + rs.pos_off + m % rs.rps;
@@ -125,6 +138,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Thread-block clusters: full-cluster barrier (release/acquire), this CTA's
+// rank, and loads from another CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // Programmatic dependent launch: wait for the preceding grid's results /

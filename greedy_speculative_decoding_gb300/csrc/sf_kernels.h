@@ -13,8 +13,9 @@ enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_STORE
 // block scales) when nf4 != 0.
 struct GemmArgs {
   CUtensorMap tm[3];          // per segment: 2-D map {K, rows}, box {64, 16}, 128-byte swizzle
+                              // (NF4: codes {K/2 bytes, rows}, box {128, 16}, 128-byte swizzle)
+  CUtensorMap tms[3];         // NF4 block scales per segment: {K/64, rows}, box {8, 16}
   const void* w[3];           // row segments (QKV: q, k, v; SWIGLU: gate, up)
-  const __half* scales[3];    // NF4 block scales per segment
   const bf16* bias[3];
   int seg_end[3];             // cumulative row ends of the segments
   int ld[3];                  // row stride in elements (bf16) / codes (NF4)
@@ -22,6 +23,10 @@ struct GemmArgs {
   int nf4;
   int N, K;                   // output rows (SWIGLU: ffn features), reduction length
   int nblocks, nsplit, cps;   // row blocks, K splits, chunks per split
+  int stages;                 // weight tiles in flight per warp (2..kMaxStages)
+  int cluster;                // 1: the splits of a row block form one thread-block
+                              // cluster and are summed through distributed shared
+                              // memory; 0: through `part` in global memory
   // input activations fp32 [M][in_ld]; RMSNorm applied when gain != nullptr
   const float* in;
   int in_ld;
@@ -53,8 +58,28 @@ struct GemmArgs {
 // Tensor map of a bf16 weight matrix [rows, K] with row stride ld elements,
 // in the layout the GEMM's TMA ring expects.
 cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld);
+// NF4: codes [rows, K/2] bytes and fp16 block scales [rows, nf4_scale_ld(K)].
+int nf4_scale_ld(int K);
+cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const void* codes, const void* scales,
+                          int rows, int K);
+cudaError_t set_nf4_levels(const float levels[16]);
 
-int gemm_smem_bytes(int M);
+constexpr int kMaxClusterSplit = 8;   // portable cluster size
+constexpr int kMaxStages = 11;        // deepest bf16 weight ring that fits next to 16 token rows
+constexpr int kMaxStagesNF4 = 10;     // NF4 stages also carry their block scales
+
+// Ring depth for a plan: when the whole grid fits on the GPU at one CTA per
+// SM, every weight tile of a CTA is requested up front (before the kernel
+// waits on its producer); otherwise four tiles per warp keep two CTAs per SM.
+// An NF4 stage holds four 64-k chunks.
+inline int pick_stages(int ctas, int cps, int num_sms, bool nf4 = false) {
+  const int need = nf4 ? (cps + 3) / 4 : cps;
+  const int cap = nf4 ? kMaxStagesNF4 : kMaxStages;
+  if (ctas <= num_sms) return need < 2 ? 2 : (need > cap ? cap : need);
+  return 4;
+}
+
+int gemm_smem_bytes(int M, int stages, bool nf4 = false);
 cudaError_t gemm_init();
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
 
@@ -77,6 +102,7 @@ struct AttnArgs {
   int nq, nkv, hd, s_max, B, n_kv_chunks;
   float scale;
   int* err;
+  int merge_trace_id;      // timeline slot of the merge kernel
   RowSet rs;
 };
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl);
@@ -112,6 +138,6 @@ cudaError_t launch_reset(const SpecState& s, cudaStream_t st);
 cudaError_t launch_copy_draft(const SpecState& s, int* d_draft, cudaStream_t st);
 void nf4_levels(double out[16]);
 cudaError_t launch_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8_t* packed,
-                                __half* scales, cudaStream_t st);
+                                __half* scales, int scale_ld, cudaStream_t st);
 
 }  // namespace sf

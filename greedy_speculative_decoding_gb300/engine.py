@@ -12,6 +12,7 @@ import torch
 from . import _lib as L
 
 LAYER_TENSORS = ("ln1", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "ln2", "wg", "wu", "wd")
+LINEAR = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
 
 
 def model_cfg(shape, wdtype: int = L.SF_WDTYPE_BF16) -> L.ModelCfg:
@@ -25,19 +26,28 @@ def model_cfg(shape, wdtype: int = L.SF_WDTYPE_BF16) -> L.ModelCfg:
         rope_theta=float(shape.rope_theta), rms_eps=float(shape.rms_eps), wdtype=wdtype)
 
 
-def weight_order(shape) -> list:
-    """Names in the order of the C ABI's weight pointer array."""
+def weight_order(shape, nf4: bool = False) -> list:
+    """Names in the order of the C ABI's weight pointer array. With NF4 each
+    linear map `w` is followed by its block scales `w.scales`."""
     names = ["embed"]
     for i in range(shape.layers):
-        names += [f"layers.{i}.{t}" for t in LAYER_TENSORS]
+        for t in LAYER_TENSORS:
+            names.append(f"layers.{i}.{t}")
+            if nf4 and t in LINEAR:
+                names.append(f"layers.{i}.{t}.scales")
     names.append("norm")
     if not shape.tied:
         names.append("lm_head")
     return names
 
 
+def is_nf4(weights: dict) -> bool:
+    return any(k.endswith(".scales") for k in weights)
+
+
 def _ptr_array(shape, weights: dict):
-    names = weight_order(shape)
+    nf4 = is_nf4(weights)
+    names = weight_order(shape, nf4)
     arr = (ctypes.c_void_p * len(names))()
     keep = []
     for i, n in enumerate(names):
@@ -45,8 +55,13 @@ def _ptr_array(shape, weights: dict):
         if t is None:
             arr[i] = None
             continue
-        if not t.is_cuda or t.dtype != torch.bfloat16:
-            raise ValueError(f"{n}: expected a bf16 CUDA tensor, got {t.dtype} on {t.device}")
+        want = torch.bfloat16
+        if nf4 and n.split(".")[-1] in LINEAR:
+            want = torch.uint8
+        elif n.endswith(".scales"):
+            want = torch.float16
+        if not t.is_cuda or t.dtype != want:
+            raise ValueError(f"{n}: expected a {want} CUDA tensor, got {t.dtype} on {t.device}")
         if t.dim() == 2 and t.stride(1) != 1:
             raise ValueError(f"{n}: rows must be contiguous")
         if n == "embed":
@@ -77,8 +92,10 @@ class SpecEngine:
         self.lib = L.load()
         self.B, self.K, self.s_max = batch, K, s_max
         self.target_shape, self.draft_shape = target_shape, draft_shape
-        self.tc = model_cfg(target_shape)
-        self.dc = model_cfg(draft_shape) if draft_shape is not None else None
+        self.tc = model_cfg(target_shape, L.SF_WDTYPE_NF4 if is_nf4(target_w) else L.SF_WDTYPE_BF16)
+        self.dc = None
+        if draft_shape is not None:
+            self.dc = model_cfg(draft_shape, L.SF_WDTYPE_NF4 if is_nf4(draft_w) else L.SF_WDTYPE_BF16)
         pdc = ctypes.byref(self.dc) if self.dc is not None else None
         ws = self.lib.sf_workspace_bytes(ctypes.byref(self.tc), pdc, batch, K, s_max)
         if ws == 0:
@@ -174,6 +191,24 @@ class SpecEngine:
         L.check(self.lib.sf_get_accept_hist(self.h, _i32(hst)))
         return hst
 
+    def trace_count(self) -> int:
+        """Launches enqueued so far (SF_TRACE=1), the id the next one gets."""
+        return self.lib.sf_trace(self.h, None, 0)
+
+    def trace(self, first: int = 0, count: int = None):
+        """Launch timeline recorded with SF_TRACE=1 for launch ids first ..
+        first + count - 1: list of (label, start_ns, wait_done_ns)."""
+        slots = 8192
+        buf = (ctypes.c_uint64 * (2 * slots))()
+        n = self.lib.sf_trace(self.h, buf, slots)
+        if count is None:
+            count = min(n, slots)
+        out = []
+        for i in range(first, first + count):
+            j = i % slots
+            out.append((self.lib.sf_trace_label(self.h, j).decode(), buf[2 * j], buf[2 * j + 1]))
+        return out
+
     # ------------------------------------------------------------ views
     def kv_view(self, which: str = "target") -> torch.Tensor:
         """[layers][2][batch][n_kv_heads][s_max][head_dim] bf16 view of a cache."""
@@ -200,13 +235,31 @@ def linear(w: torch.Tensor, x: torch.Tensor, out: torch.Tensor = None, workspace
     return out
 
 
+def nf4_scale_ld(cols: int) -> int:
+    """Row stride (in scales) of the NF4 block-scale matrix: cols/64 rounded up to 8."""
+    return (cols // 64 + 7) // 8 * 8
+
+
 def nf4_quantize(w: torch.Tensor, stream=None):
-    """Blockwise NF4 codes and fp16 scales of a bf16 CUDA matrix (rows, cols % 64 == 0)."""
+    """Blockwise NF4 codes [rows, cols/2] and fp16 scales [rows, nf4_scale_ld(cols)]
+    (padding zero) of a bf16 CUDA matrix (cols % 64 == 0)."""
     lib = L.load()
     rows, cols = w.shape
     packed = torch.empty((rows, cols // 2), dtype=torch.uint8, device=w.device)
-    scales = torch.empty((rows, cols // 64), dtype=torch.float16, device=w.device)
+    scales = torch.zeros((rows, nf4_scale_ld(cols)), dtype=torch.float16, device=w.device)
     st = stream if stream is not None else torch.cuda.current_stream()
     L.check(lib.sf_nf4_quantize(w.data_ptr(), rows, cols, w.stride(0), packed.data_ptr(), scales.data_ptr(),
                                 ctypes.c_void_p(st.cuda_stream)))
     return packed, scales
+
+
+def quantize_model_nf4(shape, weights: dict, stream=None) -> dict:
+    """NF4 copy of a bf16 weight dict: every linear map becomes codes + scales
+    (quantised on the GPU); embedding, norms, biases and LM head stay bf16."""
+    out = {}
+    for k, v in weights.items():
+        if v is not None and k.split(".")[-1] in LINEAR:
+            out[k], out[k + ".scales"] = nf4_quantize(v, stream)
+        else:
+            out[k] = v
+    return out

@@ -99,7 +99,9 @@ typedef struct {
  * lm_head [vocab, hidden] (omitted when tied).
  * With SF_WDTYPE_NF4 each of wq, wk, wv, wo, wg, wu, wd takes two consecutive
  * slots: packed codes (uint8 [out, in/2], element 2i in the low nibble) then
- * block scales (fp16 [out, in/64]).
+ * block scales (fp16 [out, ld_s], ld_s = 8 * ceil(in / 512): the in/64 scales
+ * of a row padded to a 16-byte row stride), as sf_nf4_quantize writes them;
+ * in must be a multiple of 64.
  * Every row must start on a 16-byte boundary.
  * Returns the number of slots, or -1 for an invalid cfg.
  */
@@ -197,6 +199,20 @@ SF_API sf_status sf_get_lengths(sf_handle h, int32_t* h_len_t, int32_t* h_len_d)
 /* Accept-length histogram since prefill: host [batch][K+1]. */
 SF_API sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist);
 
+/*
+ * Launch timeline, for profiling. Only when the environment variable
+ * SF_TRACE=1 was set at sf_create: every kernel of the forward passes
+ * stamps the GPU global timer (ns) when it starts and when its wait on the
+ * preceding kernel returns. sf_trace copies up to max_launches pairs
+ * {start, wait_done} into h_out (host, 2 x uint64 each) for launch slots
+ * 0.. (launch n uses slot n mod 8192; graph replays rewrite their slots) and
+ * returns the count; with h_out NULL it returns the number of launches
+ * enqueued so far; 0 when tracing is off. sf_trace_label(i) names slot i ("qkv",
+ * "attention", "merge", "o_proj", "gate_up", "down", "lm_head", "embed").
+ */
+SF_API int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches);
+SF_API const char* sf_trace_label(sf_handle h, int32_t i);
+
 SF_API const char* sf_status_str(sf_status s);
 SF_API const char* sf_last_error(void);
 SF_API void sf_destroy(sf_handle h);
@@ -241,7 +257,8 @@ SF_API sf_status sf_linear_noalloc(const void* d_w, int32_t N, int32_t K, int32_
  * Blockwise NF4 quantisation of a bf16 matrix on the device (a preparation
  * step for SF_WDTYPE_NF4 weights): w [rows, cols] with row stride ld
  * elements, cols a multiple of 64; writes packed codes [rows, cols/2] and fp16
- * block scales [rows, cols/64]. Codebook: the NormalFloat construction of
+ * block scales [rows, 8 * ceil(cols / 512)] (padding entries untouched).
+ * Codebook: the NormalFloat construction of
  * Dettmers et al., "QLoRA" (2023), section 3 (format named in "The Numbers").
  */
 SF_API sf_status sf_nf4_quantize(const void* d_w, int32_t rows, int32_t cols, int32_t ld,
