@@ -172,6 +172,172 @@ def launches_per_round(t_shape, d_shape, K) -> int:
     return K * per_fwd(d_shape) + per_fwd(t_shape) + 1
 
 
+# ---------------------------------------------------------------------------- other workloads
+def _timed(fn, stream, reps):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _gen_rate(eng, n_new=256):
+    """(committed tokens/s, mean committed per round) of one sf_generate run
+    from the prefilled prompt, timed with CUDA events on the engine stream."""
+    import torch
+    eng.reset()
+    eng.generate(8)          # warm: graph captured, clocks up
+    eng.reset()
+    rounds = [0]
+
+    def run():
+        _, r = eng.generate(n_new)
+        rounds[0] = r
+    ms = _timed(run, eng.stream, 1)
+    return n_new / (ms / 1e3), n_new / max(1, rounds[0])
+
+
+def extra_workloads(pkg, tw, peak):
+    """The other workloads of the suite, each bounded to a few seconds:
+    the 0.5B-shape draft decode step at context 512 (standalone, vocabulary
+    151936), sigma-perturbed target copies as drafts, prompt-lookup drafting
+    on repetitive prompts, and the 14B-shape NF4 target at batch 1."""
+    import torch
+    from synth import (QWEN05B, QWEN14B, QWEN7B, make_weights, ngram_prompt, perturbed_copy,
+                       repeated_fraction, shared_embedding_draft, uniform_prompt)
+    out = {}
+    # 0.5B-shape decode step, context 512: the model drafts for itself.
+    try:
+        w5 = make_weights(QWEN05B, seed=0, device="cuda")
+        e5 = pkg.SpecEngine(QWEN05B, w5, QWEN05B, w5, batch=1, K=K_GUESS, s_max=S_MAX)
+        e5.prefill([uniform_prompt(512, QWEN05B.vocab, seed=101).numpy()])
+
+        def one():
+            e5.draft()
+            e5.verify()
+            e5.accept_rollback()
+        one()
+        e5.reset()
+        ms = []
+        for _ in range(10):
+            ms.append(_timed(e5.draft, e5.stream, 1))
+            e5.verify()
+            e5.accept_rollback()
+        step_ms = statistics.median(ms) / K_GUESS
+        b = weight_bytes(QWEN05B) + kv_bytes(QWEN05B, 512 + 8, 1)
+        out["draft_05b_ctx512"] = {"ms_per_decode_step": round(step_ms, 4), "bytes": b,
+                                   "gbs": round(b / step_ms / 1e6, 1), "frac_of_measured_peak": round(b / step_ms / 1e6 / peak, 4),
+                                   "frac_of_8TBs": round(b / step_ms / 8e9, 4)}
+        e5.close()
+        del w5, e5
+    except Exception as ex:
+        out["draft_05b_ctx512"] = {"error": repr(ex)[:200]}
+    torch.cuda.empty_cache()
+    # Target copies perturbed by N(0, sigma) as drafts (7B-shape draft).
+    prompt = uniform_prompt(PROMPT_LEN, QWEN7B.vocab, seed=102).numpy()
+    for sigma in (0.0, 0.002, 0.01):
+        try:
+            dcopy = perturbed_copy(tw, sigma, seed=3)
+            es = pkg.SpecEngine(QWEN7B, tw, QWEN7B, dcopy, batch=1, K=K_GUESS, s_max=S_MAX)
+            es.prefill([prompt])
+            rate, mean_c = _gen_rate(es)
+            out[f"sigma_{sigma}"] = {"tokens_per_s": round(rate, 2), "mean_committed_per_round": round(mean_c, 3)}
+            es.close()
+            del dcopy, es
+        except Exception as ex:
+            out[f"sigma_{sigma}"] = {"error": repr(ex)[:200]}
+        torch.cuda.empty_cache()
+    # Prompt lookup on repetitive prompts (K = 4).
+    for r in (0.2, 0.5, 0.8):
+        try:
+            p, mask = ngram_prompt(1024, r, QWEN7B.vocab, seed=200 + int(10 * r))
+            en = pkg.SpecEngine(QWEN7B, tw, batch=1, K=4, s_max=S_MAX)
+            en.prefill([p.numpy()])
+            rate, mean_c = _gen_rate(en)
+            out[f"ngram_r{r}"] = {"tokens_per_s": round(rate, 2), "mean_committed_per_round": round(mean_c, 3),
+                                  "repeated_fraction": round(repeated_fraction(mask), 3)}
+            en.close()
+        except Exception as ex:
+            out[f"ngram_r{r}"] = {"error": repr(ex)[:200]}
+    torch.cuda.empty_cache()
+    return out
+
+
+def nf4_workload(pkg, peak):
+    """14B-shape target with NF4 linear maps (quantised on the GPU), batch 1,
+    K = 8 with the 0.5B-shape draft on the target's first 896 embedding
+    columns: verify step at context 2048 and committed tokens/s."""
+    import torch
+    from synth import QWEN05B, QWEN14B, make_weights, shared_embedding_draft, uniform_prompt
+    tw = make_weights(QWEN14B, seed=0, device="cuda")
+    tq = pkg.quantize_model_nf4(QWEN14B, tw)
+    for k in list(tw):
+        if k.split(".")[-1] in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+            tw[k] = None
+    torch.cuda.empty_cache()
+    d_shape = QWEN05B.with_(vocab=QWEN14B.vocab, embed_ld=QWEN14B.hidden)
+    dw = shared_embedding_draft(make_weights(QWEN05B, seed=2, device="cuda"), tq["embed"], QWEN05B.hidden)
+    eng = pkg.SpecEngine(QWEN14B, tq, d_shape, dw, batch=1, K=K_GUESS, s_max=S_MAX)
+    eng.prefill([uniform_prompt(VERIFY_CTX, QWEN14B.vocab, seed=301).numpy()])
+    v = []
+    for i in range(8):
+        eng.draft()
+        v.append(_timed(eng.verify, eng.stream, 1))
+        eng.accept_rollback()
+    vms = statistics.median(v[2:])
+    h, f = QWEN14B.hidden, QWEN14B.ffn
+    lin = QWEN14B.layers * (h * QWEN14B.q_dim + 2 * h * QWEN14B.kv_dim + QWEN14B.q_dim * h + 3 * h * f)
+    nbytes = lin // 2 + lin // 64 * 2 + 2 * QWEN14B.vocab * h + kv_bytes(QWEN14B, VERIFY_CTX, K_GUESS + 1)
+    eng.prefill([uniform_prompt(PROMPT_LEN, QWEN14B.vocab, seed=302).numpy()])
+    rate, mean_c = _gen_rate(eng)
+    eng.close()
+    return {"verify_ms": round(vms, 4), "verify_bytes": nbytes, "verify_gbs": round(nbytes / vms / 1e6, 1),
+            "verify_frac_of_measured_peak": round(nbytes / vms / 1e6 / peak, 4), "tokens_per_s": round(rate, 2),
+            "mean_committed_per_round": round(mean_c, 3), "batch": 1}
+
+
+def run_trace(args):
+    """Launch timeline of replayed rounds (the engine records it when SF_TRACE=1
+    is set): per kernel kind, the time each launch adds to the dependent chain
+    (the gap between consecutive 'producer done' stamps)."""
+    import collections
+    import torch
+    if os.environ.get("SF_TRACE") != "1":
+        raise SystemExit("run with SF_TRACE=1 in the environment")
+    torch.cuda.set_device(0)
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as pkg
+    from synth import uniform_prompt
+    t_shape, d_shape = _shapes()
+    tw, dw = _weights("cuda")
+    eng = pkg.SpecEngine(t_shape, tw, d_shape, dw, batch=1, K=K_GUESS, s_max=S_MAX)
+    eng.prefill([uniform_prompt(VERIFY_CTX, t_shape.vocab, seed=103).numpy()])
+    first = eng.trace_count()
+    for _ in range(5):
+        eng.step()
+    tr = eng.trace(first, eng.trace_count() - first)
+    agg = collections.OrderedDict()
+    phase, heads = "draft", 0
+    for i in range(len(tr) - 1):
+        lab, st, wd = tr[i]
+        a = agg.setdefault((phase, lab), [0, 0.0, 0.0])
+        a[0] += 1
+        a[1] += (tr[i + 1][2] - wd) / 1e3
+        a[2] += (wd - st) / 1e3
+        if lab == "lm_head":
+            heads += 1
+            if heads == K_GUESS:
+                phase = "verify"
+    rows = [{"phase": ph, "kernel": lab, "launches": n, "total_us": round(t, 1), "avg_us": round(t / n, 2),
+             "early_start_us": round(w / n, 2)} for (ph, lab), (n, t, w) in agg.items()]
+    print(json.dumps({"trace": rows, "round_span_us": round((tr[-1][2] - tr[0][1]) / 1e3, 1)}))
+
+
 # ---------------------------------------------------------------------------- ours
 def run_gemm_only(args):
     """Small case for kernel profiling: the 7B gate+up matrix (271 MB, above
@@ -292,6 +458,10 @@ def run_ours(args):
     e2e_value = world * e2e_steps * N_NEW / _max_over_ranks(dist, e2e_s)
     eng.close()
 
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = extra_workloads(pkg, tw, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del eng
@@ -299,6 +469,13 @@ def run_ours(args):
             cpu = cpu_baseline(tw, dw)
         except Exception as ex:  # report, keep the GPU line
             cpu = {"value": None, "unit": "tokens/s", "kind": "oracle", "error": repr(ex)[:300]}
+    if rank == 0 and not args.no_extra:
+        del tw, dw
+        torch.cuda.empty_cache()
+        try:
+            extra["nf4_14b_b1"] = nf4_workload(pkg, peak)
+        except Exception as ex:
+            extra["nf4_14b_b1"] = {"error": repr(ex)[:300]}
 
     if rank == 0:
         mean_commit = float((hist * (np.arange(K_GUESS + 1) + 1)).sum() / max(1, hist.sum()))
@@ -330,6 +507,8 @@ def run_ours(args):
                        "rounds": rounds_total},
             "clocks": clk.summary(),
         }
+        if extra:
+            line["workloads"] = extra
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line))
@@ -420,12 +599,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--tokens", type=int, default=N_NEW, help="new tokens per step (profiling runs use fewer)")
     ap.add_argument("--gemm-only", action="store_true", help="small case for kernel profiling")
+    ap.add_argument("--trace", action="store_true", help="launch timeline of a round (needs SF_TRACE=1)")
     args = ap.parse_args()
     globals()["N_NEW"] = args.tokens
     if args.gemm_only:
         run_gemm_only(args)
+        return
+    if args.trace:
+        run_trace(args)
         return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -318,12 +318,22 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "LM head tensor map: %s", cudaGetErrorString(ce));
   }
   // The K splits of a row block run as one thread-block cluster.
+  // The splits of a row block form one cluster. Matrices of 24 MB and more
+  // are split for two CTAs per SM (bandwidth) in clusters of at most 8 (the
+  // portable size, which packs well into GPCs); smaller ones for one CTA per
+  // SM in clusters of up to 16, so that the next kernel's CTAs fit beside
+  // them and start streaming early.
   const int al = nf4 ? 4 : 1;
-  md.p_qkv = make_plan(nblocks_of(c, 0), H, e->slots, kMaxClusterSplit, al);
-  md.p_o = make_plan(nblocks_of(c, 1), c->n_heads * c->head_dim, e->slots, kMaxClusterSplit, al);
-  md.p_gu = make_plan(nblocks_of(c, 2), H, e->slots, kMaxClusterSplit, al);
-  md.p_d = make_plan(nblocks_of(c, 1), c->ffn, e->slots, kMaxClusterSplit, al);
-  md.p_lm = make_plan(nblocks_of(c, 3), H, e->slots, kMaxClusterSplit);
+  auto plan = [&](int nblocks, long rows, long k) {
+    const bool big = rows * k * (nf4 ? 1 : 2) >= (24l << 20);
+    return make_plan(nblocks, (int)k, big ? 2 * e->num_sms : e->num_sms, big ? 8 : kMaxClusterSplit, al);
+  };
+  const long QKV = (long)c->n_heads * c->head_dim + 2l * c->n_kv_heads * c->head_dim;
+  md.p_qkv = plan(nblocks_of(c, 0), QKV, H);
+  md.p_o = plan(nblocks_of(c, 1), H, (long)c->n_heads * c->head_dim);
+  md.p_gu = plan(nblocks_of(c, 2), 2l * c->ffn, H);
+  md.p_d = plan(nblocks_of(c, 1), H, c->ffn);
+  md.p_lm = make_plan(nblocks_of(c, 3), H, 2 * e->num_sms, 8);
   for (const Plan* p : {&md.p_qkv, &md.p_o, &md.p_gu, &md.p_d, &md.p_lm})
     if (p->nsplit > 1 && p->nblocks * p->nsplit > kMaxPlanTiles)
       return fail(SF_ERR_UNSUPPORTED, "split-K plan exceeds the scratch tiles");

@@ -408,6 +408,11 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
     stage_convert<T>(a, r, reinterpret_cast<uint2*>(act), rinv, min(nch, kWinChunks), M);
   }
   __syncthreads();
+  auto next_window = [&](int ch) {
+    __syncthreads();
+    stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
+    __syncthreads();
+  };
 
   float acc[T][4];
 #pragma unroll
@@ -425,11 +430,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
     const unsigned char* tile = my_ring + s * kTileBytes;
     if (!NF4) {
       const int ch = st;
-      if (ch > 0 && (ch % kWinChunks) == 0) {
-        __syncthreads();
-        stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
-        __syncthreads();
-      }
+      if (ch > 0 && (ch % kWinChunks) == 0) next_window(ch);
       uint4 w[4];
       w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
       w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
@@ -447,11 +448,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
       for (int q = 0; q < 4; ++q) {
         const int ch = 4 * st + q;
         if (ch >= nch) break;
-        if (ch > 0 && (ch % kWinChunks) == 0) {
-          __syncthreads();
-          stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
-          __syncthreads();
-        }
+        if (ch > 0 && (ch % kWinChunks) == 0) next_window(ch);
         // 8 code bytes (k = 16c .. 16c+15 of this chunk) of rows g and g+8,
         // at their 128-byte-swizzled positions; the scale of each row.
         const int cofs = ((((2 * q + (c >> 1)) ^ sw) << 4) + 8 * (c & 1));
@@ -663,16 +660,21 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
   return cudaLaunchKernelEx(&cfg, k_gemm<T, EPI, NF4>, a);
 }
 
+template <int T, int EPI, bool NF4>
+static cudaError_t init_one() {
+  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4);
+  cudaError_t e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
 template <int T, bool NF4>
 static cudaError_t init_t() {
-  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4);
-  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_QKV, NF4>, A, smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_RESID, NF4>, A, smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_SWIGLU, NF4>, A, smem))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemm<T, EPI_STORE, NF4>, A, smem))) return e;
-  return cudaFuncSetAttribute(k_gemm<T, EPI_ARGMAX, NF4>, A, smem);
+  if ((e = init_one<T, EPI_QKV, NF4>()) || (e = init_one<T, EPI_RESID, NF4>()) ||
+      (e = init_one<T, EPI_SWIGLU, NF4>()) || (e = init_one<T, EPI_STORE, NF4>()))
+    return e;
+  return init_one<T, EPI_ARGMAX, NF4>();
 }
 
 // Raise the dynamic shared-memory limit of every instantiation (current device).

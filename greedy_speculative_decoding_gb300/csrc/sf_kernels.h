@@ -64,19 +64,19 @@ cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const 
                           int rows, int K);
 cudaError_t set_nf4_levels(const float levels[16]);
 
-constexpr int kMaxClusterSplit = 8;   // portable cluster size
+constexpr int kMaxClusterSplit = 16;  // cluster size (above 8 is non-portable; allowed per kernel)
 constexpr int kMaxStages = 11;        // deepest bf16 weight ring that fits next to 16 token rows
 constexpr int kMaxStagesNF4 = 10;     // NF4 stages also carry their block scales
 
-// Ring depth for a plan: when the whole grid fits on the GPU at one CTA per
-// SM, every weight tile of a CTA is requested up front (before the kernel
-// waits on its producer); otherwise four tiles per warp keep two CTAs per SM.
-// An NF4 stage holds four 64-k chunks.
+// Ring depth for a plan. A grid of at most one CTA per SM gets rings of up
+// to five stages (under 114 KB of shared memory), so that one CTA of this
+// kernel and one of the next fit on an SM together: the next kernel's CTAs
+// start early and stream their weights while this one finishes. Larger
+// grids run two CTAs per SM with four stages. An NF4 stage holds four chunks.
 inline int pick_stages(int ctas, int cps, int num_sms, bool nf4 = false) {
   const int need = nf4 ? (cps + 3) / 4 : cps;
-  const int cap = nf4 ? kMaxStagesNF4 : kMaxStages;
-  if (ctas <= num_sms) return need < 2 ? 2 : (need > cap ? cap : need);
-  return 4;
+  if (ctas <= num_sms) return need < 2 ? 2 : (need > 5 ? 5 : need);
+  return kStages;
 }
 
 int gemm_smem_bytes(int M, int stages, bool nf4 = false);
