@@ -271,16 +271,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   }
 }
 
-// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), chunks in
-// order. One CTA per (row, head), one thread per output dimension; every
-// chunk's (max, sum) pair is loaded at once, and the output sums load eight
-// chunks at a time so the global loads overlap.
+// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M). One CTA
+// per (row, head) of 256 threads: thread (g, d) with g = tid / hd adds the
+// chunks g, g + G, g + 2G, ... (G = 256 / hd) in order, up to kMergeLoads of
+// them loaded at once, and the G partial sums are then added in order g =
+// 0, 1, ...; every chunk's (max, sum) pair is loaded in the same round, so a
+// merge costs two dependent global loads, not one per few chunks.
 constexpr int kMaxKvChunks = 256;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeLoads = 24;
 
-__global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_constant__ AttnArgs a) {
   __shared__ float wgt[kMaxKvChunks];
   __shared__ float lw[kMaxKvChunks];
-  __shared__ float red[4];
+  __shared__ float opart[kMergeThreads];
+  __shared__ float red[kMergeThreads / 32];
   __shared__ float s_mx, s_l;
   RowSet rs1 = a.rs;
   rs1.trace_id = a.merge_trace_id;
@@ -289,52 +294,66 @@ __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
   trace_mark(rs1, 1);
   pdl_launch_next();
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
-  const int d = threadIdx.x, lane = d & 31, warp = d >> 5, nwarps = blockDim.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = kMergeThreads / a.hd;
+  const int grp = tid / a.hd, d = tid - grp * a.hd;
   const int nch = row_pos(a.rs, m) / kKvChunk + 1;
   const int stride = a.hd + 2;
   const float* src = a.part + ((size_t)m * a.nq + h) * a.n_kv_chunks * stride;
-  float mc[2], lc[2];
+  // Round one: every chunk's (max, sum) and this thread's first output terms.
+  const float mc = tid < nch ? src[(size_t)tid * stride + a.hd] : -INFINITY;
+  const float lc = tid < nch ? src[(size_t)tid * stride + a.hd + 1] : 0.f;
+  float v[kMergeLoads];
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int c = d + r * blockDim.x;
-    mc[r] = c < nch ? src[(size_t)c * stride + a.hd] : -INFINITY;
-    lc[r] = c < nch ? src[(size_t)c * stride + a.hd + 1] : 0.f;
+  for (int q = 0; q < kMergeLoads; ++q) {
+    const int c = grp + q * G;
+    v[q] = c < nch ? src[(size_t)c * stride + d] : 0.f;
   }
-  const float wm = warp_max(fmaxf(mc[0], mc[1]));
+  const float wm = warp_max(mc);
   if (lane == 0) red[warp] = wm;
   __syncthreads();
-  if (d == 0) {
-    float v = red[0];
-    for (int w = 1; w < nwarps; ++w) v = fmaxf(v, red[w]);
-    s_mx = v;
+  if (tid == 0) {
+    float x = red[0];
+    for (int w = 1; w < kMergeThreads / 32; ++w) x = fmaxf(x, red[w]);
+    s_mx = x;
   }
   __syncthreads();
-  const float mx = s_mx;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int c = d + r * blockDim.x;
-    if (c < nch) {
-      wgt[c] = expf(mc[r] - mx);
-      lw[c] = lc[r];
-    }
+  if (tid < nch) {
+    wgt[tid] = expf(mc - s_mx);
+    lw[tid] = lc;
   }
   __syncthreads();
-  if (d == 0) {
+  if (tid == 0) {
     float l = 0.f;
     for (int c = 0; c < nch; ++c) l = fmaf(lw[c], wgt[c], l);
     s_l = l;
   }
   float o = 0.f;
-  for (int c0 = 0; c0 < nch; c0 += 8) {
-    float v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = c0 + q < nch ? src[(size_t)(c0 + q) * stride + d] : 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (c0 + q < nch) o = fmaf(v[q], wgt[c0 + q], o);
+  for (int q = 0; q < kMergeLoads; ++q) {
+    const int c = grp + q * G;
+    if (c < nch) o = fmaf(v[q], wgt[c], o);
   }
+  // Longer contexts: further rounds of kMergeLoads chunks per thread.
+  for (int c0 = kMergeLoads * G; c0 < nch; c0 += kMergeLoads * G) {
+#pragma unroll
+    for (int q = 0; q < kMergeLoads; ++q) {
+      const int c = c0 + grp + q * G;
+      v[q] = c < nch ? src[(size_t)c * stride + d] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kMergeLoads; ++q) {
+      const int c = c0 + grp + q * G;
+      if (c < nch) o = fmaf(v[q], wgt[c], o);
+    }
+  }
+  opart[tid] = o;
   __syncthreads();
-  a.out[(size_t)m * a.nq * a.hd + (size_t)h * a.hd + d] = o / s_l;
+  if (grp == 0) {
+    float t = opart[d];
+    for (int g2 = 1; g2 < G; ++g2) t += opart[g2 * a.hd + d];
+    a.out[(size_t)m * a.nq * a.hd + (size_t)h * a.hd + d] = t / s_l;
+  }
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl) {
@@ -357,7 +376,7 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bo
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.rs.M * a.nq);
-  cfg2.blockDim = dim3(a.hd);
+  cfg2.blockDim = dim3(kMergeThreads);
   cfg2.stream = st;
   cfg2.attrs = attr;
   cfg2.numAttrs = pdl ? 1 : 0;

@@ -162,7 +162,7 @@ struct EpiPre {
 };
 
 template <int T, int EPI>
-__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, EpiPre<T>& pre) {
+__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, EpiPre<T>& pre, const int* pos) {
   constexpr int kE = EpiPre<T>::kE;
   if (EPI == EPI_RESID) {
 #pragma unroll
@@ -189,7 +189,7 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, E
         if (bias) pre.v0[e] = __bfloat162float(bias[local]);
         if (s < 2 && d < half) {
           if (bias) pre.v1[e] = __bfloat162float(bias[local + half]);
-          pre.cs[e] = a.rope[(size_t)row_pos(a.rs, m) * half + d];
+          pre.cs[e] = a.rope[(size_t)pos[m] * half + d];
         }
       }
     }
@@ -226,7 +226,7 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M, const Epi
 }
 
 template <int T>
-__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const EpiPre<T>& pre) {
+__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const EpiPre<T>& pre, const int* spos) {
   constexpr int kE = EpiPre<T>::kE;
   const int half = a.hd >> 1;
   const int n0 = rb * kBlockRows;
@@ -240,7 +240,7 @@ __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const
     const int local = n0 + r - seg0;
     const int d = local % a.hd;
     const int b = m / a.rs.rps;
-    const int pos = row_pos(a.rs, m);
+    const int pos = spos[m];
     if (s == 2) {
       const int kvh = local / a.hd;
       a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(ys[i] + pre.v0[e]);
@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   float* rinv = ys + 4 * T * kBlockRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);           // [8][kStages]
   __shared__ int s_flag;
+  __shared__ int s_pos[kRows];
   __shared__ uint32_t lut[NF4 ? 256 : 1];   // NF4: byte (two codes) -> bf16 pair of levels
   trace_mark(a.rs, 0);
 
@@ -382,14 +383,19 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
     const uint32_t i = tid;   // 256 threads, 256 byte values
     lut[i] = pack_bf16x2(__float2bfloat16_rn(c_nf4_levels[i & 15]), __float2bfloat16_rn(c_nf4_levels[i >> 4]));
   }
-  __syncwarp();
+  // Token positions (QKV: RoPE angle and cache slot), read before the wait:
+  // the sequence lengths are written only by the acceptance and reset
+  // kernels and by host copies, never by the kernel that directly precedes a
+  // projection (the only one that can still be running at this point).
+  if (EPI == EPI_QKV && tid < a.rs.M) s_pos[tid] = row_pos(a.rs, tid);
+  __syncthreads();
 
   pdl_wait();
   trace_mark(a.rs, 1);
   pdl_launch_next();
   const int M = a.rs.M;
   EpiPre<T> pre;
-  if (!(a.cluster && a.nsplit > 1) || cluster_rank() == 0) epi_prefetch<T, EPI>(a, rb, M, pre);
+  if (!(a.cluster && a.nsplit > 1) || cluster_rank() == 0) epi_prefetch<T, EPI>(a, rb, M, pre, s_pos);
   {
     // The first activation window and the RMSNorm sums are loaded together.
     StageRegs<T> r;
@@ -503,39 +509,49 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
 
   if (a.nsplit > 1 && a.cluster) {
     // The K slices of this row block are the CTAs of one cluster: after the
-    // barrier every partial tile sits in its CTA's shared memory; rank 0 adds
-    // them in rank order and runs the epilogue; the second barrier keeps the
-    // other CTAs' shared memory alive until it has read them.
-    cluster_sync();
+    // barrier every partial tile sits in its CTA's shared memory and rank 0
+    // adds them in rank order, loading up to kG slices per round. The other
+    // CTAs keep their shared memory alive until rank 0 has arrived on the
+    // second barrier, which rank 0 does as soon as it has read them.
+    // Rank 0 publishes nothing in the first phase: its arrival is relaxed (a
+    // releasing one would also wait for its epilogue prefetch loads).
     const uint32_t rank = cluster_rank();
-    if (rank == 0) {
-      constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
-      const uint32_t ys_s = smem_u32(ys);
-      float sum[kE];
-#pragma unroll
-      for (int e = 0; e < kE; ++e) sum[e] = 0.f;
-      for (int p0 = 0; p0 < a.nsplit; p0 += 4) {
-        float v[4][kE];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int e = 0; e < kE; ++e) {
-            const int i = tid + e * kGemmThreads;
-            v[q][e] = (p0 + q < a.nsplit && i < M * kBlockRows) ? ld_dsmem(dsmem_addr(ys_s + 4 * i, p0 + q)) : 0.f;
-          }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int e = 0; e < kE; ++e) sum[e] += v[q][e];
-      }
-#pragma unroll
-      for (int e = 0; e < kE; ++e) {
-        const int i = tid + e * kGemmThreads;
-        if (i < M * kBlockRows) ys[i] = sum[e];
-      }
+    if (rank != 0) {
+      cluster_sync();
+      cluster_arrive();
+      cluster_wait();
+      return;
     }
-    cluster_sync();
-    if (rank != 0) return;
+    cluster_arrive_relaxed();
+    cluster_wait();
+    constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
+    constexpr int kG = kE <= 2 ? 16 : (kE <= 4 ? 8 : 4);   // at most 32 loads in flight per thread
+    const uint32_t ys_s = smem_u32(ys);
+    float sum[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) sum[e] = 0.f;
+    for (int p0 = 0; p0 < a.nsplit; p0 += kG) {
+      float v[kG][kE];
+#pragma unroll
+      for (int q = 0; q < kG; ++q)
+#pragma unroll
+        for (int e = 0; e < kE; ++e) {
+          const int i = tid + e * kGemmThreads;
+          v[q][e] = (p0 + q < a.nsplit && i < M * kBlockRows) ? ld_dsmem(dsmem_addr(ys_s + 4 * i, p0 + q)) : 0.f;
+        }
+#pragma unroll
+      for (int q = 0; q < kG; ++q)
+#pragma unroll
+        for (int e = 0; e < kE; ++e) sum[e] += v[q][e];
+    }
+    cluster_arrive();   // releasing: the loads above have completed before the others may exit
+    __syncthreads();    // every thread's loads of this CTA's own tile are done
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      const int i = tid + e * kGemmThreads;
+      if (i < M * kBlockRows) ys[i] = sum[e];
+    }
+    __syncthreads();
   } else if (a.nsplit > 1) {
     float* mine = a.part + ((size_t)rb * a.nsplit + sp) * (kRows * kBlockRows);
     for (int i = tid; i < M * kBlockRows; i += kGemmThreads) __stcg(mine + i, ys[i]);
@@ -578,10 +594,11 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   }
 
   if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, M, pre);
-  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M, pre);
+  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M, pre, s_pos);
   else if (EPI == EPI_SWIGLU) epi_swiglu(a, ys, rb, M);
   else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
   else epi_argmax(a, ys, rb, M, &s_flag);
+  if (a.nsplit > 1 && a.cluster) cluster_wait();
 }
 
 int gemm_smem_bytes(int M, int stages, bool nf4) {
