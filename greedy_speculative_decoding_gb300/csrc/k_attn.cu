@@ -2,13 +2,12 @@
 //
 // Attention is split over the cache ("flash decoding"): one work item is
 // (sequence, KV head, 64-slot chunk). Its keys and values are contiguous in
-// the cache; one warp brings them into padded shared-memory rows with bulk
-// (TMA) copies completing on an mbarrier, and the CTA then serves every
-// query that reads this KV head (all rows of the sequence times the query
-// heads of the group) on the tensor cores, 16 queries per warp. The chunk's
-// partial result (row max, sum of exponentials, unnormalised output) goes to
-// scratch; a second kernel merges the chunks of every (row, head) in fixed
-// chunk order.
+// the cache; the CTA brings them into padded shared-memory rows and serves
+// every query that reads this KV head (all rows of the sequence times the
+// query heads of the group) on the tensor cores, 16 queries at a time with
+// all eight warps on each tile. The chunk's partial result (row max, sum of
+// exponentials, unnormalised output) goes to scratch; a second kernel merges
+// the chunks of every (row, head) in fixed chunk order.
 //
 // Chunk boundaries are fixed multiples of 64 slots and a row at position p
 // reads slots 0..p, so a row's result does not depend on the other rows.
@@ -55,8 +54,6 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl) {
 }
 
 // ------------------------------------------------------------------ attention
-constexpr uint32_t kWaitIters = 1u << 24;
-
 __device__ __forceinline__ void ldsm_x2_trans(uint32_t& r0, uint32_t& r1, const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
                : "=r"(r0), "=r"(r1)
@@ -69,23 +66,44 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uin
   lo = pack_bf16x2(__float2bfloat16_rn(x - __bfloat162float(hx)), __float2bfloat16_rn(y - __bfloat162float(hy)));
 }
 
-// One work item = (sequence b, KV head, 64-slot chunk c). Each warp takes a
-// tile of 16 queries (rows of the sequence x query heads of the group):
-//   S = Q K^T with mma.sync m16n8k16 (Q as an fp32-accurate bf16 hi+lo pair,
-//   the head dimension walked in an order that makes each thread's key
-//   fragment one 8-byte shared load), masked to the slots each row may see,
-//   row max / exp / row sum on the accumulators (quad shuffles), then
-//   O = P V with P (hi+lo) taken straight from the S accumulators and V
-//   fragments from ldmatrix.trans.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// One work item = (sequence b, KV head, 64-slot chunk c). Its keys and values
+// come into padded shared-memory rows with 16-byte asynchronous copies
+// (slots past the last row's position are zero-filled instead: a zero
+// probability times a stale NaN would still be NaN). The queries that read
+// this KV head (rows of the sequence x query heads of the group) go through
+// in tiles of 16, and all eight warps share each tile:
+//   S = Q K^T   warp w computes the 8 keys 8w..8w+7 over the whole head
+//               dimension (mma.sync m16n8k16, Q as an fp32-accurate bf16
+//               hi+lo pair, the head dimension walked in an order that makes
+//               each key fragment one 8-byte shared load);
+//   softmax     row max and row sum combined across the warps through
+//               shared memory (sums in warp order);
+//   O = P V     P (hi+lo) through shared memory, warp w producing output
+//               dimensions w*HD/8 .. (w+1)*HD/8 - 1 from all 64 keys.
+// The split is the same for every tile and every launch, so a row's result
+// does not depend on how many other rows the launch carries.
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_constant__ AttnArgs a) {
-  constexpr int KP = HD * 2 + 32;   // key row pitch: 8-bank shift per row for the 8-byte fragment loads
+  constexpr int KP = HD * 2 + 32;   // key row pitch (bytes): 8-bank shift per row for the 8-byte fragment loads
   constexpr int VP = HD * 2 + 16;   // value row pitch: 4-bank shift per row for ldmatrix
   constexpr int KS = HD / 16;       // k-steps over the head dimension
-  constexpr int NT = HD / 8;        // n-tiles of the output
-  __shared__ __align__(128) unsigned char ks[kKvChunk * KP];
-  __shared__ __align__(128) unsigned char vs[kKvChunk * VP];
-  __shared__ __align__(8) uint64_t bar;
+  constexpr int NTW = HD / 64;      // output n-tiles (8 dimensions each) per warp
+  constexpr int HP = HD + 16;       // query hi / lo row pitch (bf16): 8-bank shift per row
+  constexpr int PP = kKvChunk + 8;  // probability tile row pitch (bf16)
+  constexpr int kPieces = kKvChunk * HD / 8;   // 16-byte pieces of a chunk's keys (and of its values)
+  static_assert(kAttnThreads == 256 && kKvChunk == 64, "eight warps of eight keys");
+  extern __shared__ __align__(128) unsigned char attn_smem[];
+  unsigned char* ks = attn_smem;                                   // [64][KP]
+  unsigned char* vs = ks + kKvChunk * KP;                          // [64][VP]
+  bf16* sph = reinterpret_cast<bf16*>(vs + kKvChunk * VP);         // [16][PP] P hi
+  bf16* spl = sph + 16 * PP;                                       // [16][PP] P lo
+  __shared__ float red_mx[8][16], red_l[8][16];
 
   trace_mark(a.rs, 0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -93,11 +111,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   const int group = a.nq / a.nkv;
   const int rps = a.rs.rps;
   const int Mq = rps * group;
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
+  const int qrows = (Mq + 15) / 16 * 16;
+  bf16* sqh = spl + 16 * PP;                                       // [tiles * 16][HP] queries, hi
+  bf16* sql = sqh + qrows * HP;                                    // [tiles * 16][HP] queries, lo
 
   // The lengths were written by kernels that finished before the preceding
   // one started, so they (and the cache slots below this pass's first
@@ -118,24 +134,27 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
     kvh = rest / nch;
     c = rest - kvh * nch;
   };
-  auto issue = [&](int b, int kvh, int c) {
+  // Copy slots [0, nvalid) of the chunk; zero the rest of the tile.
+  auto issue = [&](int b, int kvh, int c, int nvalid) {
     const size_t off = (((size_t)b * a.nkv + kvh) * a.s_max + (size_t)c * kKvChunk) * HD;
-    if (warp == 0) {
-      if (lane == 0) mbar_expect_tx(&bar, 2u * kKvChunk * HD * sizeof(bf16));
-      __syncwarp();
-      fence_proxy_async();   // earlier generic accesses of ks/vs before the async writes
-      for (int r = lane; r < kKvChunk; r += 32) {
-        bulk_g2s(ks + r * KP, a.kc + off + (size_t)r * HD, HD * sizeof(bf16), &bar);
-        bulk_g2s(vs + r * VP, a.vc + off + (size_t)r * HD, HD * sizeof(bf16), &bar);
+    for (int i = tid; i < kPieces; i += kAttnThreads) {
+      const int r = i / (HD / 8), u = i - r * (HD / 8);
+      if (r < nvalid) {
+        cp_async16(ks + r * KP + 16 * u, a.kc + off + (size_t)r * HD + 8 * u);
+        cp_async16(vs + r * VP + 16 * u, a.vc + off + (size_t)r * HD + 8 * u);
+      } else {
+        *reinterpret_cast<uint4*>(ks + r * KP + 16 * u) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vs + r * VP + 16 * u) = make_uint4(0, 0, 0, 0);
       }
     }
+    cp_async_commit();
   };
   bool issued = false;
   if ((int)blockIdx.x < total) {
     int b, kvh, c;
     locate(blockIdx.x, b, kvh, c);
     if ((c + 1) * kKvChunk <= a.rs.pos_base[b] + a.rs.pos_off) {   // no slot of this pass in the chunk
-      issue(b, kvh, c);
+      issue(b, kvh, c, kKvChunk);
       issued = true;
     }
   }
@@ -143,131 +162,173 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   trace_mark(a.rs, 1);
   pdl_launch_next();
 
-  uint32_t phase = 0;
+  // All query rows of the item -> shared memory as bf16 hi + lo pairs (rows
+  // past Mq are zero), eight 16-byte loads per thread in flight at a time.
+  auto stage_q = [&](int b, int kvh) {
+    constexpr int kBatch = 8;
+    const int n4 = qrows * (HD / 4);
+    for (int i0 = 0; i0 < n4; i0 += kBatch * kAttnThreads) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int e = 0; e < kBatch; ++e) {
+        const int i = i0 + tid + e * kAttnThreads;
+        const int qi = i / (HD / 4), u = i - qi * (HD / 4);
+        v[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n4 && qi < Mq) {
+          const int j = qi / group, hh = qi - j * group;
+          v[e] = *reinterpret_cast<const float4*>(a.q + ((size_t)(b * rps + j) * a.nq + kvh * group + hh) * HD + 4 * u);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kBatch; ++e) {
+        const int i = i0 + tid + e * kAttnThreads;
+        if (i >= n4) break;
+        const int qi = i / (HD / 4), u = i - qi * (HD / 4);
+        uint2 h, l;
+        split_bf16x2(v[e].x, v[e].y, h.x, l.x);
+        split_bf16x2(v[e].z, v[e].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(sqh + qi * HP + 4 * u) = h;
+        *reinterpret_cast<uint2*>(sql + qi * HP + 4 * u) = l;
+      }
+    }
+  };
+
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
     int b, kvh, c;
     locate(item, b, kvh, c);
-    if (!issued) issue(b, kvh, c);
-    issued = false;
-    if (!mbar_wait(&bar, phase, kWaitIters)) {
-      if (tid == 0) atomicOr(a.err, kErrWait);
-      mbar_wait(&bar, phase, kWaitIters);
-      return;
-    }
-    phase ^= 1u;
-
     const int p0 = a.rs.pos_base[b] + a.rs.pos_off;
-    // Slots past the last row's position hold stale or never-written cache
-    // entries; a zero probability times a NaN there would still be NaN in
-    // the P V product, so clear those rows of the tile.
-    const int nvalid = min(kKvChunk, p0 + rps - c * kKvChunk);
-    if (nvalid < kKvChunk) {
-      for (int i = tid; i < (kKvChunk - nvalid) * (HD / 8); i += kAttnThreads) {
-        const int r = nvalid + i / (HD / 8), u = i % (HD / 8);
-        *reinterpret_cast<uint4*>(ks + r * KP + 16 * u) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(vs + r * VP + 16 * u) = make_uint4(0, 0, 0, 0);
-      }
-      __syncthreads();
-    }
-    for (int qt = warp; qt * 16 < Mq; qt += kAttnThreads / 32) {
-      // Rows g and g+8 of the tile.
+    if (!issued) issue(b, kvh, c, min(kKvChunk, p0 + rps - c * kKvChunk));
+    issued = false;
+    stage_q(b, kvh);
+    cp_async_wait_all();
+    __syncthreads();
+
+    for (int qt = 0; qt * 16 < Mq; ++qt) {
+      const bf16* qht = sqh + qt * 16 * HP;
+      const bf16* qlt = sql + qt * 16 * HP;
+      // Rows g and g+8 of the tile: slots this row may see within the chunk.
       int nk[2];
-      const float* qrow[2];
-      int mrow[2], hrow[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int qi = qt * 16 + g + 8 * r;
-        const int j = qi / group, hh = qi - j * group;
-        mrow[r] = b * rps + j;
-        hrow[r] = kvh * group + hh;
+        const int j = qi / group;
         nk[r] = qi < Mq ? min(kKvChunk, p0 + j - c * kKvChunk + 1) : 0;
-        qrow[r] = a.q + ((size_t)mrow[r] * a.nq + hrow[r]) * HD;
       }
-      // S = Q K^T
-      float sacc[8][4];
+      // S for keys 8w .. 8w+7: four independent accumulation chains (hi / lo
+      // part of Q x even / odd k-step), added in a fixed order at the end.
+      float sa[4][4];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      for (int i = 0; i < 4; ++i) sa[i][0] = sa[i][1] = sa[i][2] = sa[i][3] = 0.f;
+      const unsigned char* krow = ks + (8 * warp + g) * KP + 8 * c4;
 #pragma unroll
       for (int k = 0; k < KS; ++k) {
-        uint32_t qh[4], ql[4];
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 q0 = nk[0] > 0 ? *reinterpret_cast<const float4*>(qrow[0] + 16 * k + 4 * c4) : z;
-        const float4 q1 = nk[1] > 0 ? *reinterpret_cast<const float4*>(qrow[1] + 16 * k + 4 * c4) : z;
-        split_bf16x2(q0.x, q0.y, qh[0], ql[0]);
-        split_bf16x2(q1.x, q1.y, qh[1], ql[1]);
-        split_bf16x2(q0.z, q0.w, qh[2], ql[2]);
-        split_bf16x2(q1.z, q1.w, qh[3], ql[3]);
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const uint2 kb = *reinterpret_cast<const uint2*>(ks + (8 * nt + g) * KP + 32 * k + 8 * c4);
-          mma_bf16_16816(sacc[nt], qh[0], qh[1], qh[2], qh[3], kb.x, kb.y);
-          mma_bf16_16816(sacc[nt], ql[0], ql[1], ql[2], ql[3], kb.x, kb.y);
-        }
+        // Elements 16k + 4c4 .. +3 of rows g and g+8: (a0, a2) and (a1, a3).
+        const uint2 h0 = *reinterpret_cast<const uint2*>(qht + g * HP + 16 * k + 4 * c4);
+        const uint2 h1 = *reinterpret_cast<const uint2*>(qht + (g + 8) * HP + 16 * k + 4 * c4);
+        const uint2 l0 = *reinterpret_cast<const uint2*>(qlt + g * HP + 16 * k + 4 * c4);
+        const uint2 l1 = *reinterpret_cast<const uint2*>(qlt + (g + 8) * HP + 16 * k + 4 * c4);
+        const uint2 kb = *reinterpret_cast<const uint2*>(krow + 32 * k);
+        mma_bf16_16816(sa[k & 1], h0.x, h1.x, h0.y, h1.y, kb.x, kb.y);
+        mma_bf16_16816(sa[2 + (k & 1)], l0.x, l1.x, l0.y, l1.y, kb.x, kb.y);
       }
-      // Softmax pieces per row: max, exp, sum (rows g: e = 0,1; g+8: e = 2,3).
-      float mx[2] = {-INFINITY, -INFINITY};
+      float sacc[4];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
+      for (int e = 0; e < 4; ++e) sacc[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+      // sacc[e]: row g (e < 2) or g+8, key 8w + 2c4 + (e & 1).
+      float mx[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = e >> 1, key = 8 * nt + 2 * c4 + (e & 1);
-          sacc[nt][e] = key < nk[r] ? sacc[nt][e] * a.scale : -INFINITY;
-          mx[r] = fmaxf(mx[r], sacc[nt][e]);
-        }
-      float l[2] = {0.f, 0.f};
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1, key = 8 * warp + 2 * c4 + (e & 1);
+        sacc[e] = key < nk[r] ? sacc[e] * a.scale : -INFINITY;
+      }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(sacc[2 * r], sacc[2 * r + 1]);
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        if (c4 == 0) red_mx[warp][g + 8 * r] = mx[r];
       }
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = e >> 1, key = 8 * nt + 2 * c4 + (e & 1);
-          const float pe = key < nk[r] ? expf(sacc[nt][e] - mx[r]) : 0.f;
-          sacc[nt][e] = pe;
-          l[r] += pe;
-        }
+      __syncthreads();   // red_mx complete
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-      }
-      // O = P V
-      float oacc[NT][4];
+        float m8 = red_mx[0][g + 8 * r];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
+        for (int w = 1; w < 8; ++w) m8 = fmaxf(m8, red_mx[w][g + 8 * r]);
+        mx[r] = m8;
+      }
+      float pe[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1, key = 8 * warp + 2 * c4 + (e & 1);
+        pe[e] = key < nk[r] ? expf(sacc[e] - mx[r]) : 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float l = pe[2 * r] + pe[2 * r + 1];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (c4 == 0) red_l[warp][g + 8 * r] = l;
+        uint32_t h, lo;
+        split_bf16x2(pe[2 * r], pe[2 * r + 1], h, lo);
+        *reinterpret_cast<uint32_t*>(sph + (g + 8 * r) * PP + 8 * warp + 2 * c4) = h;
+        *reinterpret_cast<uint32_t*>(spl + (g + 8 * r) * PP + 8 * warp + 2 * c4) = lo;
+      }
+      __syncthreads();
+
+      // O = P V for this warp's output dimensions (P hi and P lo in two
+      // accumulation chains, added at the end).
+      float oh[NTW][4], ol[NTW][4];
+#pragma unroll
+      for (int t = 0; t < NTW; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oh[t][e] = ol[t][e] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < kKvChunk / 16; ++kk) {
         uint32_t ph[4], pl[4];
-        split_bf16x2(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
-        split_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
-        split_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
-        split_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
+        const int k0 = 16 * kk + 2 * c4;
+        ph[0] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0);
+        ph[1] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0);
+        ph[2] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0 + 8);
+        ph[3] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0 + 8);
+        pl[0] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0);
+        pl[1] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0);
+        pl[2] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0 + 8);
+        pl[3] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0 + 8);
         const unsigned char* vrow = vs + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * VP;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int t = 0; t < NTW; ++t) {
           uint32_t b0, b1;
-          ldsm_x2_trans(b0, b1, vrow + 16 * nt);
-          mma_bf16_16816(oacc[nt], ph[0], ph[1], ph[2], ph[3], b0, b1);
-          mma_bf16_16816(oacc[nt], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          ldsm_x2_trans(b0, b1, vrow + 16 * (warp * NTW + t));
+          mma_bf16_16816(oh[t], ph[0], ph[1], ph[2], ph[3], b0, b1);
+          mma_bf16_16816(ol[t], pl[0], pl[1], pl[2], pl[3], b0, b1);
         }
       }
+      float oacc[NTW][4];
+#pragma unroll
+      for (int t = 0; t < NTW; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[t][e] = oh[t][e] + ol[t][e];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         if (nk[r] <= 0) continue;
-        float* dst = a.part + (((size_t)mrow[r] * a.nq + hrow[r]) * a.n_kv_chunks + c) * (HD + 2);
+        const int qi = qt * 16 + g + 8 * r;
+        const int j = qi / group, hh = qi - j * group;
+        const int m = b * rps + j, h = kvh * group + hh;
+        float* dst = a.part + (((size_t)m * a.nq + h) * a.n_kv_chunks + c) * (HD + 2);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          *reinterpret_cast<float2*>(dst + 8 * nt + 2 * c4) = make_float2(oacc[nt][2 * r], oacc[nt][2 * r + 1]);
-        if (c4 == 0) {
+        for (int t = 0; t < NTW; ++t)
+          *reinterpret_cast<float2*>(dst + 8 * (warp * NTW + t) + 2 * c4) =
+              make_float2(oacc[t][2 * r], oacc[t][2 * r + 1]);
+        if (warp == 0 && c4 == 0) {
+          float l = red_l[0][g + 8 * r];
+#pragma unroll
+          for (int w = 1; w < 8; ++w) l += red_l[w][g + 8 * r];
           dst[HD] = mx[r];
-          dst[HD + 1] = l[r];
+          dst[HD + 1] = l;
         }
       }
+      __syncthreads();   // P and red_* are free again
     }
-    __syncthreads();   // everyone is done with ks/vs before the next copy
   }
 }
 
@@ -356,6 +417,24 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
   }
 }
 
+// Dynamic shared memory of the chunk kernel: keys, values, P hi + lo, and
+// the item's query rows (padded to whole tiles of 16).
+static int attn_smem_bytes(int hd, int mq) {
+  return kKvChunk * (hd * 2 + 32) + kKvChunk * (hd * 2 + 16) + 2 * 16 * (kKvChunk + 8) * 2 +
+         2 * (mq + 15) / 16 * 16 * (hd + 16) * 2;
+}
+
+// Raise the dynamic shared-memory limit of the chunk kernels to what the
+// largest query group (rows x heads per KV head) needs.
+cudaError_t attn_init(int max_mq) {
+  if (attn_smem_bytes(128, max_mq) > 200 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(k_attn_chunks<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       attn_smem_bytes(128, max_mq));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_attn_chunks<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              attn_smem_bytes(64, max_mq));
+}
+
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -370,6 +449,7 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bo
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
+  cfg.dynamicSmemBytes = attn_smem_bytes(a.hd, a.rs.rps * (a.nq / a.nkv));
   if (a.hd == 128) e = cudaLaunchKernelEx(&cfg, k_attn_chunks<128>, a);
   else if (a.hd == 64) e = cudaLaunchKernelEx(&cfg, k_attn_chunks<64>, a);
   else return cudaErrorInvalidValue;
