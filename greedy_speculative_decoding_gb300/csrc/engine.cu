@@ -45,6 +45,7 @@ sf_status fail(sf_status s, const char* fmt, ...) {
 
 struct Plan {
   int nblocks = 0, nsplit = 1, cps = 1;
+  bool cluster = true;   // K slices reduced through a cluster's shared memory (else global scratch)
 };
 
 // Split K only when the row blocks alone cannot fill the GPU; the split
@@ -117,7 +118,7 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
 }
 
 struct Layout {
-  size_t x, ssq, q, attn_o, act, apart, gpart, counters, keys, done, zeros, rope_t, rope_d, state, trace, total;
+  size_t x, ssq, q, apart, gpart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, total;
   int n_kv_chunks, max_blocks;
 };
 
@@ -192,14 +193,20 @@ Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, i
   L.x = take((size_t)kRows * H * 4);
   L.ssq = take((size_t)(H / 128) * kRows * 4);
   L.q = take((size_t)kRows * QD * 4);
-  L.attn_o = take((size_t)kRows * QD * 4);
-  L.act = take((size_t)kRows * ((F + 3) / 4 * 4) * 4);
   L.apart = take((size_t)kRows * NQ * L.n_kv_chunks * (HD + 2) * 4);
   L.gpart = take((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
   L.counters = take((size_t)L.max_blocks * 4);
   L.keys = take((size_t)kRows * 8);
   L.done = take(4);
   L.zeros = take((size_t)B * 4);
+  // Fragment-ordered GEMM inputs (zeroed at creation: features past K stay 0):
+  // normed residual for QKV / LM head, normed residual for gate/up,
+  // attention output, SwiGLU activation.
+  const int kTiles = (kRows + 3) / 4;
+  L.fx = take(frag_bytes(H, kTiles));
+  L.fh = take(frag_bytes(H, kTiles));
+  L.fo = take(frag_bytes(QD, kTiles));
+  L.fa = take(frag_bytes(F, kTiles));
   L.rope_t = take((size_t)s_max * (t->head_dim / 2) * 8);
   L.rope_d = d ? take((size_t)s_max * (d->head_dim / 2) * 8) : p;
   L.state = take(state_offsets(B, K, s_max).n_ints * 4);
@@ -232,7 +239,8 @@ struct sf_engine {
   unsigned char* ws = nullptr;
   Layout lay{};
   StateOff so{};
-  float *x = nullptr, *ssq = nullptr, *q = nullptr, *attn_o = nullptr, *act = nullptr, *apart = nullptr,
+  bf16 *fx = nullptr, *fh = nullptr, *fo = nullptr, *fa = nullptr;
+  float *x = nullptr, *ssq = nullptr, *q = nullptr, *apart = nullptr,
         *gpart = nullptr;
   int *counters = nullptr, *done = nullptr, *zeros = nullptr;
   unsigned long long* keys = nullptr;
@@ -323,10 +331,25 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   // portable size, which packs well into GPCs); smaller ones for one CTA per
   // SM in clusters of up to 16, so that the next kernel's CTAs fit beside
   // them and start streaming early.
+  // The K splits of a row block form one cluster. Matrices of 24 MB and more
+  // are split for two CTAs per SM (bandwidth) in clusters of at most 8;
+  // smaller ones for one CTA per SM in clusters of up to 16, so that the
+  // next kernel's CTAs fit beside them and start streaming early. Clusters
+  // are placed within GPCs, and a kernel's CTAs start while the preceding
+  // kernel still holds part of the GPU: the split is lowered until the
+  // clusters fit with a fifth of the cluster slots to spare (checked for the
+  // 9..12-row footprint), so that fragmented free space still takes them all.
   const int al = nf4 ? 4 : 1;
   auto plan = [&](int nblocks, long rows, long k) {
     const bool big = rows * k * (nf4 ? 1 : 2) >= (24l << 20);
-    return make_plan(nblocks, (int)k, big ? 2 * e->num_sms : e->num_sms, big ? 8 : kMaxClusterSplit, al);
+    const int slots = big ? 2 * e->num_sms : e->num_sms;
+    Plan p = make_plan(nblocks, (int)k, slots, big ? 8 : kMaxClusterSplit, al);
+    while (p.nsplit > 1) {
+      const int stages = pick_stages(p.nblocks * p.nsplit, p.cps, e->num_sms, nf4);
+      if (5 * p.nblocks <= 4 * gemm_max_clusters(p.nsplit, 12, stages, p.cps)) break;
+      p = make_plan(nblocks, (int)k, slots, p.nsplit - 1, al);
+    }
+    return p;
   };
   const long QKV = (long)c->n_heads * c->head_dim + 2l * c->n_kv_heads * c->head_dim;
   md.p_qkv = plan(nblocks_of(c, 0), QKV, H);
@@ -348,7 +371,7 @@ GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& r
   a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, e->num_sms);
   a.part = e->gpart;
   a.counter = e->counters;
-  a.cluster = 1;
+  a.cluster = p.cluster ? 1 : 0;
   a.err = e->st.err;
   a.rs = rs;
   a.eps = md.c.rms_eps;
@@ -390,6 +413,8 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.err = e->st.err;
   ea.x = e->x;
   ea.ssq = e->ssq;
+  ea.frag = e->fx;
+  ea.gain = md.L[0].ln1;
   ea.rs = traced(e, rs, "embed");
   CK(launch_embed(ea, s, e->pdl));
   const size_t layer_elems = (size_t)2 * e->B * c.n_kv_heads * e->s_max * c.head_dim;
@@ -420,11 +445,9 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.nseg = 3;
     a.N = QD + 2 * KVD;
     a.K = H;
-    a.in = e->x;
-    a.in_ld = H;
+    a.in = reinterpret_cast<const uint4*>(e->fx);
     a.ssq = e->ssq;
     a.nssq = H / 128;
-    a.gain = lw.ln1;
     a.inv_k = 1.0f / H;
     a.out = e->q;
     a.out_ld = QD;
@@ -444,7 +467,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     t.kc = kc;
     t.vc = vc;
     t.part = e->apart;
-    t.out = e->attn_o;
+    t.out = e->fo;
     t.nq = c.n_heads;
     t.nkv = c.n_kv_heads;
     t.hd = c.head_dim;
@@ -468,11 +491,12 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.nseg = 1;
     a.N = H;
     a.K = QD;
-    a.in = e->attn_o;
-    a.in_ld = QD;
+    a.in = reinterpret_cast<const uint4*>(e->fo);
     a.out = e->x;
     a.out_ld = H;
     a.ssq_out = e->ssq;
+    a.frag_out = e->fh;
+    a.frag_gain = lw.ln2;
     a.rs = traced(e, rs, "o_proj");
     CK(launch_gemm(a, EPI_RESID, s, e->pdl));
     // gate/up + SwiGLU
@@ -489,14 +513,11 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.nseg = 2;
     a.N = c.ffn;
     a.K = H;
-    a.in = e->x;
-    a.in_ld = H;
+    a.in = reinterpret_cast<const uint4*>(e->fh);
     a.ssq = e->ssq;
     a.nssq = H / 128;
-    a.gain = lw.ln2;
     a.inv_k = 1.0f / H;
-    a.out = e->act;
-    a.out_ld = (c.ffn + 3) / 4 * 4;
+    a.frag_out = e->fa;
     a.rs = traced(e, rs, "gate_up");
     CK(launch_gemm(a, EPI_SWIGLU, s, e->pdl));
     // down + residual
@@ -511,11 +532,12 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.nseg = 1;
     a.N = H;
     a.K = c.ffn;
-    a.in = e->act;
-    a.in_ld = (c.ffn + 3) / 4 * 4;
+    a.in = reinterpret_cast<const uint4*>(e->fa);
     a.out = e->x;
     a.out_ld = H;
     a.ssq_out = e->ssq;
+    a.frag_out = e->fx;   // the next layer's QKV input, or the LM head's
+    a.frag_gain = l + 1 < c.layers ? md.L[l + 1].ln1 : md.norm;
     a.rs = traced(e, rs, "down");
     CK(launch_gemm(a, EPI_RESID, s, e->pdl));
   }
@@ -528,11 +550,9 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   a.nseg = 1;
   a.N = c.vocab;
   a.K = H;
-  a.in = e->x;
-  a.in_ld = H;
+  a.in = reinterpret_cast<const uint4*>(e->fx);
   a.ssq = e->ssq;
   a.nssq = H / 128;
-  a.gain = md.norm;
   a.inv_k = 1.0f / H;
   a.keys = e->keys;
   a.done = e->done;
@@ -743,6 +763,10 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
       cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return bail(fail(SF_ERR_CUDA, "no CUDA device"));
   e->slots = 2 * e->num_sms;
+  {
+    const cudaError_t ge = gemm_init();   // before planning: cluster occupancy queries need it
+    if (ge != cudaSuccess) return bail(fail(SF_ERR_CUDA, "gemm_init: %s", cudaGetErrorString(ge)));
+  }
   sf_status r = bind_model(e, e->tgt, tgt, tgt_w, static_cast<bf16*>(kv_t));
   if (r != SF_OK) return bail(r);
   if (dft && (r = bind_model(e, e->dft, dft, dft_w, static_cast<bf16*>(kv_d))) != SF_OK) return bail(r);
@@ -754,8 +778,10 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->x = reinterpret_cast<float*>(ws + e->lay.x);
   e->ssq = reinterpret_cast<float*>(ws + e->lay.ssq);
   e->q = reinterpret_cast<float*>(ws + e->lay.q);
-  e->attn_o = reinterpret_cast<float*>(ws + e->lay.attn_o);
-  e->act = reinterpret_cast<float*>(ws + e->lay.act);
+  e->fx = reinterpret_cast<bf16*>(ws + e->lay.fx);
+  e->fh = reinterpret_cast<bf16*>(ws + e->lay.fh);
+  e->fo = reinterpret_cast<bf16*>(ws + e->lay.fo);
+  e->fa = reinterpret_cast<bf16*>(ws + e->lay.fa);
   e->apart = reinterpret_cast<float*>(ws + e->lay.apart);
   e->gpart = reinterpret_cast<float*>(ws + e->lay.gpart);
   e->counters = reinterpret_cast<int*>(ws + e->lay.counters);
@@ -787,7 +813,6 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->C.assign(batch, 0);
 
   cudaError_t ce;
-  if ((ce = gemm_init()) != cudaSuccess) return bail(fail(SF_ERR_CUDA, "gemm_init: %s", cudaGetErrorString(ce)));
   {
     int group = tgt->n_heads / tgt->n_kv_heads;
     if (dft) group = std::max(group, dft->n_heads / dft->n_kv_heads);
@@ -1034,7 +1059,8 @@ sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist) {
 
 size_t sf_linear_workspace_bytes(int32_t N, int32_t K) {
   if (N < 1 || K < 8 || K % 8) return 0;
-  return align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4) + align256((size_t)((N + 127) / 128) * 4);
+  return align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4) + align256((size_t)((N + 127) / 128) * 4) +
+         align256(frag_bytes(K, (kRows + 3) / 4));
 }
 
 sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M, float* d_y,
@@ -1055,6 +1081,9 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   const size_t part_bytes = align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * 4, st));
+  // x -> fragment order (the GEMM's B-operand layout) in the workspace.
+  bf16* xf = reinterpret_cast<bf16*>(ws + part_bytes + align256((size_t)((N + 127) / 128) * 4));
+  CK(launch_to_frag(d_x, M, K, K, xf, st));
   GemmArgs a{};
   CK(make_weight_map(&a.tm[0], d_w, N, K, ld));
   a.w[0] = d_w;
@@ -1067,8 +1096,7 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   a.nsplit = p.nsplit;
   a.cps = p.cps;
   a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, sms);
-  a.in = d_x;
-  a.in_ld = K;
+  a.in = reinterpret_cast<const uint4*>(xf);
   a.part = reinterpret_cast<float*>(ws);
   a.counter = reinterpret_cast<int*>(ws + part_bytes);
   a.out = d_y;

@@ -16,8 +16,8 @@
 namespace sf {
 
 // ------------------------------------------------------------------ embedding
-// x[m][:] = E[tok_m][:] in fp32, plus the per-128-feature sums of squares the
-// next RMSNorm needs.
+// x[m][:] = E[tok_m][:] in fp32, the per-128-feature sums of squares the next
+// RMSNorm needs, and x * gain in fragment order (that RMSNorm's GEMM input).
 __global__ void __launch_bounds__(128) k_embed(const __grid_constant__ EmbedArgs a) {
   trace_mark(a.rs, 0);
   pdl_wait();
@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(128) k_embed(const __grid_constant__ EmbedArgs
   const int n = blk * 128 + i;
   const float v = __bfloat162float(a.E[(size_t)tok * a.ld + n]);
   a.x[(size_t)m * a.H + n] = v;
+  frag_store(a.frag, m, n, (a.rs.M + 3) / 4, v * __bfloat162float(a.gain[n]));
   const float s = warp_sum(v * v);
   if ((i & 31) == 0) part[i >> 5] = s;
   __syncthreads();
@@ -65,12 +66,6 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uin
   hi = pack_bf16x2(hx, hy);
   lo = pack_bf16x2(__float2bfloat16_rn(x - __bfloat162float(hx)), __float2bfloat16_rn(y - __bfloat162float(hy)));
 }
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // One work item = (sequence b, KV head, 64-slot chunk c). Its keys and values
 // come into padded shared-memory rows with 16-byte asynchronous copies
@@ -332,7 +327,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   }
 }
 
-// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M). One CTA
+// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), written
+// in fragment order for the output projection. One CTA
 // per (row, head) of 256 threads: thread (g, d) with g = tid / hd adds the
 // chunks g, g + G, g + 2G, ... (G = 256 / hd) in order, up to kMergeLoads of
 // them loaded at once, and the G partial sums are then added in order g =
@@ -413,7 +409,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
   if (grp == 0) {
     float t = opart[d];
     for (int g2 = 1; g2 < G; ++g2) t += opart[g2 * a.hd + d];
-    a.out[(size_t)m * a.nq * a.hd + (size_t)h * a.hd + d] = t / s_l;
+    frag_store(a.out, m, h * a.hd + d, (a.rs.M + 3) / 4, t / s_l);
   }
 }
 
@@ -431,8 +427,18 @@ cudaError_t attn_init(int max_mq) {
   cudaError_t e = cudaFuncSetAttribute(k_attn_chunks<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        attn_smem_bytes(128, max_mq));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_attn_chunks<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              attn_smem_bytes(64, max_mq));
+  e = cudaFuncSetAttribute(k_attn_chunks<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           attn_smem_bytes(64, max_mq));
+  if (e != cudaSuccess) return e;
+  // Largest shared-memory carve-out for every kernel of the chain (see gemm_init).
+  const void* fns[] = {reinterpret_cast<const void*>(k_attn_chunks<128>),
+                       reinterpret_cast<const void*>(k_attn_chunks<64>),
+                       reinterpret_cast<const void*>(k_attn_merge), reinterpret_cast<const void*>(k_embed)};
+  for (const void* f : fns)
+    if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+  return cudaSuccess;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl) {

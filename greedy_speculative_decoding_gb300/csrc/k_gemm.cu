@@ -8,14 +8,19 @@
 // cp.async.bulk.tensor loads that complete on per-stage mbarriers, so about
 // 80 KB of weights per CTA are in flight without holding registers. The tiles
 // feed mma.sync m16n8k16 as the A operand ("swap AB": weights are the M
-// side, tokens the N side). The token activations are staged in
-// shared memory, converted to a bf16 pair (hi + lo) so that the product keeps
-// about 16 mantissa bits of the fp32 activation; hi and lo of one token sit
-// in adjacent columns of the n8 tile and are summed in the epilogue.
+// side, tokens the N side). The token activations arrive from the producing
+// kernel already as bf16 pairs (hi + lo, about 16 mantissa bits of the fp32
+// value) in "fragment order": each lane reads its B operand for a 64-k chunk
+// with two 16-byte loads per token tile, straight from global memory (L1
+// serves the other warps of the CTA), one chunk ahead of the MMAs, so no
+// warp ever waits for the others inside the main loop. hi and lo of one
+// token sit in adjacent columns of the n8 tile and are summed at the end.
+// An RMSNorm input is stored as x * gain; the 1 / rms(x) row factor is
+// applied to the finished dot products.
 //
 // Inside an MMA the order of k does not matter as long as A and B agree, so
-// each thread takes 16 consecutive k of its rows and the activation tile is
-// laid out in the matching "fragment order" (conflict-free 128-bit reads).
+// each thread takes 16 consecutive k of its rows and the activations are
+// laid out in the matching order (frag_index).
 //
 // Every row's arithmetic is independent of how many rows are present (same
 // K split, same MMA sequence, same reduction order), so a verify row equals
@@ -49,96 +54,26 @@ __device__ __forceinline__ int warp_tile_row(const GemmArgs& a, int rb, int w, i
   return n - (s ? a.seg_end[s - 1] : 0) + 16 * w;
 }
 
-// Stage activation chunks [wc0, wc0 + nwc) of this CTA (absolute chunk index
-// c0 + wc) into fragment order: [wc][t][h][lane][8] bf16, lane = 4*col + c
-// with col = 2*(m%4) + {0: hi, 1: lo}, and k = 64*chunk + 16*c + 8*h + e.
+// B operand of chunk j (absolute) for this lane: per token tile, the two
+// 16-byte units of halves h = 0, 1.
 template <int T>
-struct StageRegs {
-  static constexpr int kItems = (4 * T * kWinChunks * 16 + kGemmThreads - 1) / kGemmThreads;
-  float4 v[kItems];
-  uint2 gg[kItems];
-};
-
-// Load this thread's share of activation chunks [cabs0, cabs0 + nwc) (and
-// the RMSNorm gains) into registers: all loads issued before any is used.
-template <int T>
-__device__ __forceinline__ void stage_load(const GemmArgs& a, StageRegs<T>& r, int cabs0, int nwc, int M) {
-  const int per_m = nwc * 16;  // groups of 4 k per token row
-  const int total = 4 * T * per_m;
-#pragma unroll
-  for (int it = 0; it < StageRegs<T>::kItems; ++it) {
-    const int idx = threadIdx.x + it * kGemmThreads;
-    const int m = idx / per_m;
-    const int k = cabs0 * kChunk + (idx - m * per_m) * 4;
-    r.v[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-    r.gg[it] = make_uint2(0, 0);
-    if (idx < total && m < M && k < a.K) {
-      r.v[it] = *reinterpret_cast<const float4*>(a.in + (size_t)m * a.in_ld + k);
-      if (a.gain) r.gg[it] = *reinterpret_cast<const uint2*>(a.gain + k);
-    }
-  }
-}
-
-// Apply the RMSNorm (when a.gain), split into bf16 hi + lo and store in
-// fragment order: [wc][t][h][lane][8] bf16, lane = 4*col + c with
-// col = 2*(m%4) + {0: hi, 1: lo}, and k = 64*chunk + 16*c + 8*h + e.
-template <int T>
-__device__ __forceinline__ void stage_convert(const GemmArgs& a, const StageRegs<T>& r, uint2* act,
-                                              const float* rinv, int nwc, int M) {
-  const int per_m = nwc * 16;
-  const int total = 4 * T * per_m;
-#pragma unroll
-  for (int it = 0; it < StageRegs<T>::kItems; ++it) {
-    const int idx = threadIdx.x + it * kGemmThreads;
-    if (idx >= total) continue;
-    const int m = idx / per_m;
-    const int q4 = idx - m * per_m;
-    float4 x = r.v[it];
-    if (a.gain && m < M) {
-      const float rr = rinv[m];
-      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.gg[it].x));
-      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.gg[it].y));
-      x.x = (x.x * rr) * g01.x;
-      x.y = (x.y * rr) * g01.y;
-      x.z = (x.z * rr) * g23.x;
-      x.w = (x.w * rr) * g23.y;
-    }
-    const bf16 h0 = __float2bfloat16_rn(x.x), h1 = __float2bfloat16_rn(x.y);
-    const bf16 h2 = __float2bfloat16_rn(x.z), h3 = __float2bfloat16_rn(x.w);
-    const bf16 l0 = __float2bfloat16_rn(x.x - __bfloat162float(h0));
-    const bf16 l1 = __float2bfloat16_rn(x.y - __bfloat162float(h1));
-    const bf16 l2 = __float2bfloat16_rn(x.z - __bfloat162float(h2));
-    const bf16 l3 = __float2bfloat16_rn(x.w - __bfloat162float(h3));
-    const int wc = q4 >> 4;
-    const int kk = (q4 & 15) * 4;
-    const int c = kk >> 4, h = (kk >> 3) & 1, e = kk & 7;
-    const int t = m >> 2, col = 2 * (m & 3);
-    const int base = ((wc * T + t) * 2 + h) * 32;     // in 16-byte units
-    // uint2 index: 16-byte unit * 2 + (e / 4)
-    act[(base + 4 * col + c) * 2 + (e >> 2)] = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-    act[(base + 4 * (col + 1) + c) * 2 + (e >> 2)] = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
-  }
-}
-
-template <int T>
-__device__ __forceinline__ void stage_acts(const GemmArgs& a, uint2* act, const float* rinv, int cabs0,
-                                           int nwc, int M) {
-  StageRegs<T> r;
-  stage_load<T>(a, r, cabs0, nwc, M);
-  stage_convert<T>(a, r, act, rinv, nwc, M);
-}
-
-template <int T>
-__device__ __forceinline__ void mma_chunk(float (&acc)[T][4], const uint4 (&w)[4], const uint4* act, int wc,
-                                          int lane) {
+__device__ __forceinline__ void load_b(uint4 (&b)[T][2], const uint4* in, int j, int lane) {
+  const uint4* p = in + (size_t)j * (T * 64) + lane;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    const uint4 b0 = act[((wc * T + t) * 2 + 0) * 32 + lane];
-    const uint4 b1 = act[((wc * T + t) * 2 + 1) * 32 + lane];
-    mma_bf16_16816(acc[t], w[0].x, w[2].x, w[0].y, w[2].y, b0.x, b0.y);
-    mma_bf16_16816(acc[t], w[0].z, w[2].z, w[0].w, w[2].w, b0.z, b0.w);
-    mma_bf16_16816(acc[t], w[1].x, w[3].x, w[1].y, w[3].y, b1.x, b1.y);
-    mma_bf16_16816(acc[t], w[1].z, w[3].z, w[1].w, w[3].w, b1.z, b1.w);
+    b[t][0] = p[(2 * t) * 32];
+    b[t][1] = p[(2 * t + 1) * 32];
+  }
+}
+
+template <int T>
+__device__ __forceinline__ void mma_chunk(float (&acc)[T][4], const uint4 (&w)[4], const uint4 (&b)[T][2]) {
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    mma_bf16_16816(acc[t], w[0].x, w[2].x, w[0].y, w[2].y, b[t][0].x, b[t][0].y);
+    mma_bf16_16816(acc[t], w[0].z, w[2].z, w[0].w, w[2].w, b[t][0].z, b[t][0].w);
+    mma_bf16_16816(acc[t], w[1].x, w[3].x, w[1].y, w[3].y, b[t][1].x, b[t][1].y);
+    mma_bf16_16816(acc[t], w[1].z, w[3].z, w[1].w, w[3].w, b[t][1].z, b[t][1].w);
   }
 }
 
@@ -170,6 +105,7 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, E
       const int i = threadIdx.x + e * kGemmThreads;
       const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
       pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)m * a.out_ld + n] : 0.f;
+      pre.v1[e] = (a.frag_gain && n < a.N) ? __bfloat162float(a.frag_gain[n]) : 0.f;
     }
   } else if (EPI == EPI_QKV) {
     const int half = a.hd >> 1;
@@ -208,6 +144,7 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M, const Epi
     if (n < a.N) {
       v = pre.v0[e] + ys[i];
       a.out[(size_t)m * a.out_ld + n] = v;
+      if (a.frag_out) frag_store(a.frag_out, m, n, T, v * pre.v1[e]);
     }
     ys[i] = v;
   }
@@ -265,6 +202,7 @@ __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const
   }
 }
 
+template <int T>
 __device__ void epi_swiglu(const GemmArgs& a, const float* ys, int rb, int M) {
   for (int i = threadIdx.x; i < M * 64; i += kGemmThreads) {
     const int m = i >> 6, j = i & 63;
@@ -272,7 +210,7 @@ __device__ void epi_swiglu(const GemmArgs& a, const float* ys, int rb, int M) {
     if (f >= a.N) continue;
     const float gte = ys[m * kBlockRows + j];
     const float up = ys[m * kBlockRows + 64 + j];
-    a.out[(size_t)m * a.out_ld + f] = gte / (1.0f + expf(-gte)) * up;
+    frag_store(a.frag_out, m, f, T, gte / (1.0f + expf(-gte)) * up);
   }
 }
 
@@ -334,10 +272,10 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   // NF4: each stage also carries the block scales of its rows ([16][8] fp16).
   unsigned char* sring = smem + 8 * kStages * kTileBytes;                // [8][kStages][kScaleTileBytes]
   unsigned char* after_ring = sring + (NF4 ? 8 * kStages * kScaleTileBytes : 0);
-  uint4* act = reinterpret_cast<uint4*>(after_ring);
-  float* ys = reinterpret_cast<float*>(after_ring + kWinChunks * T * 1024);
+  float* ys = reinterpret_cast<float*>(after_ring);
   float* rinv = ys + 4 * T * kBlockRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);           // [8][kStages]
+  uint4* bstage = reinterpret_cast<uint4*>(bars + 8 * kStages);         // staged B operand (if any)
   __shared__ int s_flag;
   __shared__ int s_pos[kRows];
   __shared__ uint32_t lut[NF4 ? 256 : 1];   // NF4: byte (two codes) -> bf16 pair of levels
@@ -394,31 +332,40 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   trace_mark(a.rs, 1);
   pdl_launch_next();
   const int M = a.rs.M;
+  // The CTAs that run the epilogue: all of them, except that in a cluster
+  // split only rank 0 does.
+  const bool finisher = !(a.cluster && a.nsplit > 1) || cluster_rank() == 0;
+  // First chunk's activations, then the epilogue's operands and the RMSNorm
+  // partial sums (rows warp and warp + 8, one or two per lane), all in
+  // flight together; the sums are only needed after the main loop.
+  // B operand source: global memory, or this CTA's chunks staged in shared
+  // memory (short K slices: one copy instead of a global round trip per chunk).
+  const uint4* bsrc = a.in;
+  int jb = 0;   // chunk index of bsrc[0]
+  if (staged_b_bytes(T, a.cps) && nch > 0) {
+    const uint4* src = a.in + (size_t)c0 * (T * 64);
+    for (int i = tid; i < nch * T * 64; i += kGemmThreads) cp_async16(bstage + i, src + i);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    bsrc = bstage;
+    jb = c0;
+  }
+  uint4 bq[T][2];
+  if (nch > 0) load_b<T>(bq, bsrc, c0 - jb, lane);
   EpiPre<T> pre;
-  if (!(a.cluster && a.nsplit > 1) || cluster_rank() == 0) epi_prefetch<T, EPI>(a, rb, M, pre, s_pos);
-  {
-    // The first activation window and the RMSNorm sums are loaded together.
-    StageRegs<T> r;
-    stage_load<T>(a, r, c0, min(nch, kWinChunks), M);
-    if (a.gain) {
-      // 1 / rms of each token row from the per-128-feature sums of squares:
-      // one warp per row, one load per lane (at most 64 partial sums).
-      for (int m = warp; m < M; m += kGemmThreads / 32) {
-        float s0 = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
-        float s1 = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
-        const float s = warp_sum(s0 + s1);
-        if (lane == 0) rinv[m] = 1.0f / sqrtf(s * a.inv_k + a.eps);
+  if (finisher) epi_prefetch<T, EPI>(a, rb, M, pre, s_pos);
+  float ssq_part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  if (a.ssq && finisher) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int m = warp + 8 * j;
+      if (m < M) {
+        ssq_part[j][0] = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
+        ssq_part[j][1] = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
       }
     }
-    __syncthreads();
-    stage_convert<T>(a, r, reinterpret_cast<uint2*>(act), rinv, min(nch, kWinChunks), M);
   }
-  __syncthreads();
-  auto next_window = [&](int ch) {
-    __syncthreads();
-    stage_acts<T>(a, reinterpret_cast<uint2*>(act), rinv, c0 + ch, min(nch - ch, kWinChunks), M);
-    __syncthreads();
-  };
 
   float acc[T][4];
 #pragma unroll
@@ -435,8 +382,8 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
     if (!mbar_wait(&my_bar[s], (st / kStages) & 1, kWaitIters)) timed_out = true;
     const unsigned char* tile = my_ring + s * kTileBytes;
     if (!NF4) {
-      const int ch = st;
-      if (ch > 0 && (ch % kWinChunks) == 0) next_window(ch);
+      uint4 bn[T][2];
+      if (st + 1 < nch) load_b<T>(bn, bsrc, c0 + st + 1 - jb, lane);
       uint4 w[4];
       w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
       w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
@@ -447,14 +394,22 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
         fence_proxy_async();   // the warp's reads of this stage before the async refill
         issue(s, st + kStages);
       }
-      mma_chunk<T>(acc, w, act, ch % kWinChunks, lane);
+      mma_chunk<T>(acc, w, bq);
+      if (st + 1 < nch) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          bq[t][0] = bn[t][0];
+          bq[t][1] = bn[t][1];
+        }
+      }
     } else {
       const __half* sct = reinterpret_cast<const __half*>(my_sring + s * kScaleTileBytes);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int ch = 4 * st + q;
         if (ch >= nch) break;
-        if (ch > 0 && (ch % kWinChunks) == 0) next_window(ch);
+        uint4 bn[T][2];
+        if (ch + 1 < nch) load_b<T>(bn, bsrc, c0 + ch + 1 - jb, lane);
         // 8 code bytes (k = 16c .. 16c+15 of this chunk) of rows g and g+8,
         // at their 128-byte-swizzled positions; the scale of each row.
         const int cofs = ((((2 * q + (c >> 1)) ^ sw) << 4) + 8 * (c & 1));
@@ -473,7 +428,14 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
         float part[T][4];
 #pragma unroll
         for (int t = 0; t < T; ++t) part[t][0] = part[t][1] = part[t][2] = part[t][3] = 0.f;
-        mma_chunk<T>(part, w, act, ch % kWinChunks, lane);
+        mma_chunk<T>(part, w, bq);
+        if (ch + 1 < nch) {
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            bq[t][0] = bn[t][0];
+            bq[t][1] = bn[t][1];
+          }
+        }
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           acc[t][0] = fmaf(s_lo, part[t][0], acc[t][0]);
@@ -593,18 +555,32 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
     __syncthreads();
   }
 
+  if (a.ssq) {
+    // RMSNorm input: scale row m by 1 / rms(x_m).
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int m = warp + 8 * j;
+      if (m < M) {
+        const float sq = warp_sum(ssq_part[j][0] + ssq_part[j][1]);
+        if (lane == 0) rinv[m] = 1.0f / sqrtf(sq * a.inv_k + a.eps);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < M * kBlockRows; i += kGemmThreads) ys[i] *= rinv[i / kBlockRows];
+    __syncthreads();
+  }
   if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, M, pre);
   else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M, pre, s_pos);
-  else if (EPI == EPI_SWIGLU) epi_swiglu(a, ys, rb, M);
+  else if (EPI == EPI_SWIGLU) epi_swiglu<T>(a, ys, rb, M);
   else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
   else epi_argmax(a, ys, rb, M, &s_flag);
   if (a.nsplit > 1 && a.cluster) cluster_wait();
 }
 
-int gemm_smem_bytes(int M, int stages, bool nf4) {
+int gemm_smem_bytes(int M, int stages, bool nf4, int cps) {
   const int T = (M + 3) / 4;
   return 1024 /* alignment slack */ + 8 * stages * (kTileBytes + (nf4 ? kScaleTileBytes : 0)) +
-         kWinChunks * T * 1024 + 4 * T * kBlockRows * 4 + 4 * T * 4 + 8 * stages * 8;
+         4 * T * kBlockRows * 4 + 4 * T * 4 + 8 * stages * 8 + staged_b_bytes(T, cps);
 }
 
 cudaError_t set_nf4_levels(const float levels[16]) {
@@ -656,7 +632,7 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nblocks * a.nsplit);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4, a.cps);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -679,8 +655,14 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
 
 template <int T, int EPI, bool NF4>
 static cudaError_t init_one() {
-  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4);
+  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4, 0) + kMaxStagedB;
   cudaError_t e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // Every kernel of the chain asks for the largest shared-memory carve-out,
+  // so an SM running one of them can take the next kernel's CTAs early
+  // (programmatic dependent launch) without first changing its L1 / shared split.
+  e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
@@ -692,6 +674,27 @@ static cudaError_t init_t() {
       (e = init_one<T, EPI_SWIGLU, NF4>()) || (e = init_one<T, EPI_STORE, NF4>()))
     return e;
   return init_one<T, EPI_ARGMAX, NF4>();
+}
+
+// Largest number of clusters of `csize` CTAs that can be resident at once
+// for a launch with this shared-memory footprint (clusters are placed within
+// GPCs, so this can be below SMs x CTAs per SM / csize). Measured on the
+// 9..12-row instantiation with the QKV epilogue (the most registers of the
+// two-CTAs-per-SM kernels); 0 if the query fails.
+int gemm_max_clusters(int csize, int M, int stages, int cps) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize * 512);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(M, stages, false, cps);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = csize;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  return cudaOccupancyMaxActiveClusters(&n, k_gemm<3, EPI_QKV, false>, &cfg) == cudaSuccess ? n : 0;
 }
 
 // Raise the dynamic shared-memory limit of every instantiation (current device).
@@ -725,6 +728,40 @@ static cudaError_t launch_f(const GemmArgs& a, int epi, cudaStream_t st, bool pd
     case EPI_STORE: return launch_e<EPI_STORE, NF4>(a, st, pdl);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// One thread per 16-byte unit of the fragment-ordered output.
+__global__ void k_to_frag(const float* x, int M, int K, int ld, int T, uint4* out, long units) {
+  const long u = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int lane = (int)(u & 31);
+  const int h = (int)((u >> 5) & 1);
+  const long r = u >> 6;
+  const int t = (int)(r % T), j = (int)(r / T);
+  const int col = lane >> 2, c = lane & 3;
+  const int m = 4 * t + (col >> 1);
+  const bool lo = col & 1;
+  uint32_t p[4];
+#pragma unroll
+  for (int e2 = 0; e2 < 4; ++e2) {
+    bf16 v2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int k = 64 * j + 16 * c + 8 * h + 2 * e2 + q;
+      const float v = (m < M && k < K) ? x[(size_t)m * ld + k] : 0.f;
+      const bf16 hi = __float2bfloat16_rn(v);
+      v2[q] = lo ? __float2bfloat16_rn(v - __bfloat162float(hi)) : hi;
+    }
+    p[e2] = pack_bf16x2(v2[0], v2[1]);
+  }
+  out[u] = make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cudaStream_t st) {
+  const int T = (M + 3) / 4;
+  const long units = (long)frag_bytes(K, T) / 16;
+  k_to_frag<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(x, M, K, ld, T, reinterpret_cast<uint4*>(out), units);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {

@@ -17,13 +17,9 @@ constexpr int kRows = SF_MAX_ROWS;     // tokens per forward, at most
 constexpr int kBlockRows = 128;        // output rows (features) per GEMM CTA
 constexpr int kGemmThreads = 256;      // 8 warps x 16 rows
 constexpr int kChunk = 64;             // k per pipeline step (one 128-byte line per weight row)
-#ifndef SF_WIN_CHUNKS
-#define SF_WIN_CHUNKS 8
-#endif
 #ifndef SF_STAGES
 #define SF_STAGES 4
 #endif
-constexpr int kWinChunks = SF_WIN_CHUNKS;   // chunks of activations staged at once
 constexpr int kStages = SF_STAGES;          // weight tiles in flight per warp (TMA ring)
 constexpr int kTileBytes = 16 * kChunk * 2;   // one warp's 16 rows x 64 k of bf16
 constexpr int kKvChunk = 64;           // cache slots per attention work item
@@ -136,6 +132,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (LDGSTS), its group commit and wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -197,6 +200,34 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 
 __device__ __forceinline__ int key_index(unsigned long long k) {
   return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+// ------------------------------------------------ fragment-ordered activations
+// The GEMM's B operand (token activations) lives in global memory already in
+// the order its warps read it: for T = ceil(M / 4) token tiles, 64-feature
+// chunk j, tile t and half h (features 8h..8h+7 of each 16), lane l holds 8
+// bf16 in 16 bytes at unit ((j * T + t) * 2 + h) * 32 + l. Lane l = 4 * col + c
+// serves MMA column col = 2 * (m % 4) + {0: hi, 1: lo} of token m = 4t + m % 4
+// and features k = 64j + 16c + 8h + e (e = 0..7). Each value is stored as a
+// bf16 pair (hi = bf16(v), lo = bf16(v - hi)), so products keep about 16
+// mantissa bits of the fp32 value. Bytes for K features: frag_bytes(K, T).
+__host__ __device__ __forceinline__ size_t frag_bytes(int K, int T) {
+  return (size_t)((K + 63) / 64) * T * 1024;
+}
+
+// bf16 index of the hi part of (token m, feature k); the lo part is 32 further.
+__device__ __forceinline__ size_t frag_index(int m, int k, int T) {
+  const int j = k >> 6, kk = k & 63;
+  const int c = kk >> 4, h = (kk >> 3) & 1, e = kk & 7;
+  const int t = m >> 2, col = 2 * (m & 3);
+  return ((((size_t)j * T + t) * 2 + h) * 32 + 4 * col + c) * 8 + e;
+}
+
+__device__ __forceinline__ void frag_store(bf16* f, int m, int k, int T, float v) {
+  const size_t i = frag_index(m, k, T);
+  const bf16 hi = __float2bfloat16_rn(v);
+  f[i] = hi;
+  f[i + 32] = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

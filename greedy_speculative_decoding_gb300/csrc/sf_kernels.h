@@ -27,13 +27,17 @@ struct GemmArgs {
   int cluster;                // 1: the splits of a row block form one thread-block
                               // cluster and are summed through distributed shared
                               // memory; 0: through `part` in global memory
-  // input activations fp32 [M][in_ld]; RMSNorm applied when gain != nullptr
-  const float* in;
-  int in_ld;
-  const float* ssq;           // [nssq][kRows] partial sums of squares of `in`
+  // Input activations in fragment order (frag_index, T = ceil(M / 4)). For
+  // the input of an RMSNorm they hold x * gain and ssq is set: the epilogue
+  // scales row m by 1 / rms(x_m), computed from the partial sums of squares.
+  const uint4* in;
+  const float* ssq;           // [nssq][kRows] partial sums of squares of x, or null
   int nssq;
-  const bf16* gain;
   float eps, inv_k;
+  // Fragment-ordered copy of the epilogue's result for the next GEMM: RESID
+  // writes x * frag_gain (the next RMSNorm's input), SWIGLU the activation.
+  bf16* frag_out;
+  const bf16* frag_gain;
   // split-K scratch: partial tiles and per-row-block arrival counters
   float* part;
   int* counter;
@@ -68,6 +72,10 @@ constexpr int kMaxClusterSplit = 16;  // cluster size (above 8 is non-portable; 
 constexpr int kMaxStages = 11;        // deepest bf16 weight ring that fits next to 16 token rows
 constexpr int kMaxStagesNF4 = 10;     // NF4 stages also carry their block scales
 
+// fp32 rows x [M][ld] (features 0..K-1) -> fragment order, zero past K and
+// past M within the last token tile (the input of sf_linear).
+cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cudaStream_t st);
+
 // Ring depth for a plan. A grid of at most one CTA per SM gets rings of up
 // to five stages (under 114 KB of shared memory), so that one CTA of this
 // kernel and one of the next fit on an SM together: the next kernel's CTAs
@@ -79,7 +87,15 @@ inline int pick_stages(int ctas, int cps, int num_sms, bool nf4 = false) {
   return kStages;
 }
 
-int gemm_smem_bytes(int M, int stages, bool nf4 = false);
+// A CTA with at least two chunks whose B operand (all its chunks, all token
+// tiles) fits in kMaxStagedB bytes copies it into shared memory once after
+// its wait instead of loading it from global memory chunk by chunk.
+constexpr int kMaxStagedB = 24 * 1024;
+__host__ __device__ inline int staged_b_bytes(int T, int cps) {
+  return (cps >= 2 && cps * T * 1024 <= kMaxStagedB) ? cps * T * 1024 : 0;
+}
+int gemm_smem_bytes(int M, int stages, bool nf4, int cps);
+int gemm_max_clusters(int csize, int M, int stages, int cps);
 cudaError_t gemm_init();
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
 
@@ -89,6 +105,8 @@ struct EmbedArgs {
   int* err;
   float* x;      // [M][H]
   float* ssq;    // [H/128][kRows]
+  bf16* frag;    // x * gain in fragment order (the first RMSNorm's input)
+  const bf16* gain;
   RowSet rs;
 };
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl);
@@ -98,7 +116,7 @@ struct AttnArgs {
   const bf16* kc;          // layer key cache [B][nkv][s_max][hd]
   const bf16* vc;
   float* part;             // [M*nq][n_kv_chunks][hd + 2]
-  float* out;              // [M][nq*hd]
+  bf16* out;               // attention output [M][nq*hd] in fragment order
   int nq, nkv, hd, s_max, B, n_kv_chunks;
   float scale;
   int* err;

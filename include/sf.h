@@ -224,8 +224,9 @@ SF_API void sf_destroy(sf_handle h);
  * multiples of 8, 16-byte aligned rows); x: device fp32 [M, K]; y: device
  * fp32 [M, N]. d_workspace: device scratch of
  * sf_linear_workspace_bytes(N, K) bytes, 256-byte aligned, for split-K
- * partial tiles and arrival counters (zeroed by the call). Enqueued on
- * cuda_stream; returns without synchronising.
+ * partial tiles, arrival counters (zeroed by the call) and a bf16 hi/lo copy
+ * of x in the GEMM's operand order. Enqueued on cuda_stream; returns without
+ * synchronising.
  */
 SF_API size_t sf_linear_workspace_bytes(int32_t N, int32_t K);
 SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M,
@@ -240,15 +241,15 @@ SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, co
  * sf_linear minus d_workspace. (The pages describe no such call; it has no
  * counterpart there.)
  *
- * The split-K scratch is a file-scope device array of about 8 MB inside the
- * library (enough for N up to 1,048,576 rows); every GPU that loads the
+ * The scratch is a file-scope device array of about 12 MB inside the
+ * library (enough for N up to 1,048,576 rows and K up to 65,536); every GPU that loads the
  * library keeps it until the process exits. The call allocates nothing: the
  * first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current, so make that first call
  * before any stream capture. All calls share the array: it keeps the last
  * call's contents, the counters that must start at zero are cleared by each
- * call, and calls that overlap on the GPU race with each other. N beyond the
- * limit returns SF_ERR_ARG with a message in sf_last_error().
+ * call, and calls that overlap on the GPU race with each other. N or K beyond
+ * the limits returns SF_ERR_ARG with a message in sf_last_error().
  */
 SF_API sf_status sf_linear_noalloc(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x,
                                    int32_t M, float* d_y, void* cuda_stream);
