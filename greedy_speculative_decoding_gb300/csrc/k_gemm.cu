@@ -459,6 +459,19 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
       mbar_wait(&my_bar[st % kStages], (st / kStages) & 1, kWaitIters);
   }
 
+  // RMSNorm input: 1 / rms(x_m) of rows warp and warp + 8 (visible to the
+  // CTA after the barrier below).
+  if (a.ssq && finisher) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int m = warp + 8 * j;
+      if (m < M) {
+        const float sq = warp_sum(ssq_part[j][0] + ssq_part[j][1]);
+        if (lane == 0) rinv[m] = 1.0f / sqrtf(sq * a.inv_k + a.eps);
+      }
+    }
+  }
+
   // Token m = 4t + c: hi in column 2c, lo in column 2c + 1.
   const int r0 = warp * 16 + g;
 #pragma unroll
@@ -506,13 +519,15 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
 #pragma unroll
         for (int e = 0; e < kE; ++e) sum[e] += v[q][e];
     }
-    cluster_arrive();   // releasing: the loads above have completed before the others may exit
-    __syncthreads();    // every thread's loads of this CTA's own tile are done
+    // Each thread rewrites only the elements it summed (its own loads of
+    // this CTA's tile are done); the stores consume every loaded value, so
+    // once they have issued the other CTAs may go (relaxed arrival).
 #pragma unroll
     for (int e = 0; e < kE; ++e) {
       const int i = tid + e * kGemmThreads;
-      if (i < M * kBlockRows) ys[i] = sum[e];
+      if (i < M * kBlockRows) ys[i] = a.ssq ? sum[e] * rinv[i / kBlockRows] : sum[e];
     }
+    cluster_arrive_relaxed();
     __syncthreads();
   } else if (a.nsplit > 1) {
     float* mine = a.part + ((size_t)rb * a.nsplit + sp) * (kRows * kBlockRows);
@@ -549,23 +564,14 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
 #pragma unroll
     for (int e = 0; e < kE; ++e) {
       const int i = tid + e * kGemmThreads;
-      if (i < M * kBlockRows) ys[i] = sum[e];
+      if (i < M * kBlockRows) ys[i] = a.ssq ? sum[e] * rinv[i / kBlockRows] : sum[e];
     }
     if (tid == 0) a.counter[rb] = 0;
     __syncthreads();
   }
 
-  if (a.ssq) {
-    // RMSNorm input: scale row m by 1 / rms(x_m).
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int m = warp + 8 * j;
-      if (m < M) {
-        const float sq = warp_sum(ssq_part[j][0] + ssq_part[j][1]);
-        if (lane == 0) rinv[m] = 1.0f / sqrtf(sq * a.inv_k + a.eps);
-      }
-    }
-    __syncthreads();
+  if (a.ssq && a.nsplit == 1) {
+    // RMSNorm input without a K split: scale row m by 1 / rms(x_m) here.
     for (int i = tid; i < M * kBlockRows; i += kGemmThreads) ys[i] *= rinv[i / kBlockRows];
     __syncthreads();
   }
