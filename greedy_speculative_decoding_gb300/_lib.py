@@ -22,7 +22,7 @@ EXPORTS = (
     "sf_ngram_draft", "sf_verify", "sf_accept_rollback", "sf_step", "sf_generate", "sf_reset",
     "sf_set_drafter", "sf_get_lengths", "sf_get_accept_hist", "sf_status_str", "sf_last_error",
     "sf_destroy", "sf_nf4_quantize", "sf_linear_workspace_bytes", "sf_linear", "sf_linear_noalloc",
-    "sf_trace", "sf_trace_label",
+    "sf_trace", "sf_trace_label", "sf_frag_bytes", "sf_to_frag", "sf_linear_frag",
 )
 
 
@@ -80,6 +80,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sf_linear": (ST, [P, I32, I32, I32, P, I32, P, P, P]),
         "sf_linear_noalloc": (ST, [P, I32, I32, I32, P, I32, P, P]),
         "sf_trace": (I32, [P, ctypes.POINTER(ctypes.c_uint64), I32]),
+        "sf_frag_bytes": (SZ, [I32, I32]),
+        "sf_to_frag": (ST, [P, I32, I32, I32, P, P]),
+        "sf_linear_frag": (ST, [P, I32, I32, I32, P, I32, P, P, P]),
         "sf_trace_label": (ctypes.c_char_p, [P, I32]),
     }
     for name, (res, args) in sig.items():

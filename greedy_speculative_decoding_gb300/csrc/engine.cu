@@ -1063,14 +1063,28 @@ size_t sf_linear_workspace_bytes(int32_t N, int32_t K) {
          align256(frag_bytes(K, (kRows + 3) / 4));
 }
 
-sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M, float* d_y,
-                    void* d_workspace, void* cuda_stream) {
-  if (!d_w || !d_x || !d_y || !d_workspace) return fail(SF_ERR_ARG, "null pointer");
+size_t sf_frag_bytes(int32_t K, int32_t M) {
+  if (K < 8 || K % 8 || M < 1 || M > SF_MAX_ROWS) return 0;
+  return frag_bytes(K, (M + 3) / 4);
+}
+
+sf_status sf_to_frag(const float* d_x, int32_t M, int32_t K, int32_t ld, void* d_frag, void* cuda_stream) {
+  if (!d_x || !d_frag) return fail(SF_ERR_ARG, "null pointer");
+  if (K < 8 || K % 8 || ld < K || M < 1 || M > SF_MAX_ROWS)
+    return fail(SF_ERR_ARG, "need K a multiple of 8, ld >= K, 1 <= M <= %d", SF_MAX_ROWS);
+  if (reinterpret_cast<uintptr_t>(d_frag) & 15) return fail(SF_ERR_ARG, "d_frag must be 16-byte aligned");
+  CK(launch_to_frag(d_x, M, K, ld, static_cast<bf16*>(d_frag), static_cast<cudaStream_t>(cuda_stream)));
+  return SF_OK;
+}
+
+sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, const void* d_frag, int32_t M,
+                         float* d_y, void* d_workspace, void* cuda_stream) {
+  if (!d_w || !d_frag || !d_y || !d_workspace) return fail(SF_ERR_ARG, "null pointer");
   if (N < 1 || K < 8 || K % 8 || ld < K || ld % 8 || M < 1 || M > SF_MAX_ROWS)
     return fail(SF_ERR_ARG, "need N >= 1, K and ld multiples of 8 with ld >= K, 1 <= M <= %d", SF_MAX_ROWS);
-  if ((reinterpret_cast<uintptr_t>(d_w) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
+  if ((reinterpret_cast<uintptr_t>(d_w) & 15) || (reinterpret_cast<uintptr_t>(d_frag) & 15) ||
       (reinterpret_cast<uintptr_t>(d_workspace) & 255))
-    return fail(SF_ERR_ARG, "W and x must be 16-byte aligned, the workspace 256-byte aligned");
+    return fail(SF_ERR_ARG, "W and the fragment copy must be 16-byte aligned, the workspace 256-byte aligned");
   int dev = 0, sms = 0;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -1081,9 +1095,6 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   const size_t part_bytes = align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * 4, st));
-  // x -> fragment order (the GEMM's B-operand layout) in the workspace.
-  bf16* xf = reinterpret_cast<bf16*>(ws + part_bytes + align256((size_t)((N + 127) / 128) * 4));
-  CK(launch_to_frag(d_x, M, K, K, xf, st));
   GemmArgs a{};
   CK(make_weight_map(&a.tm[0], d_w, N, K, ld));
   a.w[0] = d_w;
@@ -1096,7 +1107,7 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   a.nsplit = p.nsplit;
   a.cps = p.cps;
   a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, sms);
-  a.in = reinterpret_cast<const uint4*>(xf);
+  a.in = static_cast<const uint4*>(d_frag);
   a.part = reinterpret_cast<float*>(ws);
   a.counter = reinterpret_cast<int*>(ws + part_bytes);
   a.out = d_y;
@@ -1105,6 +1116,22 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
   a.rs.rps = M;
   CK(launch_gemm(a, EPI_STORE, st, false));
   return SF_OK;
+}
+
+sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M, float* d_y,
+                    void* d_workspace, void* cuda_stream) {
+  if (!d_w || !d_x || !d_y || !d_workspace) return fail(SF_ERR_ARG, "null pointer");
+  if (N < 1 || K < 8 || K % 8 || ld < K || ld % 8 || M < 1 || M > SF_MAX_ROWS)
+    return fail(SF_ERR_ARG, "need N >= 1, K and ld multiples of 8 with ld >= K, 1 <= M <= %d", SF_MAX_ROWS);
+  if ((reinterpret_cast<uintptr_t>(d_w) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
+      (reinterpret_cast<uintptr_t>(d_workspace) & 255))
+    return fail(SF_ERR_ARG, "W and x must be 16-byte aligned, the workspace 256-byte aligned");
+  // x -> fragment order in the workspace's last region, then the GEMM.
+  unsigned char* ws = static_cast<unsigned char*>(d_workspace);
+  void* xf = ws + align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4) + align256((size_t)((N + 127) / 128) * 4);
+  sf_status r = sf_to_frag(d_x, M, K, K, xf, cuda_stream);
+  if (r != SF_OK) return r;
+  return sf_linear_frag(d_w, N, K, ld, xf, M, d_y, d_workspace, cuda_stream);
 }
 
 int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches) {

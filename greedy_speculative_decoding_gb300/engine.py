@@ -235,6 +235,32 @@ def linear(w: torch.Tensor, x: torch.Tensor, out: torch.Tensor = None, workspace
     return out
 
 
+def to_frag(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp32 CUDA rows x [M, K] -> the fragment-ordered bf16 hi/lo copy the
+    projections read (uint8 buffer of sf_frag_bytes(K, M) bytes)."""
+    lib = L.load()
+    M, K = x.shape
+    out = torch.empty(lib.sf_frag_bytes(K, M), dtype=torch.uint8, device=x.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    L.check(lib.sf_to_frag(x.data_ptr(), M, K, x.stride(0), out.data_ptr(), ctypes.c_void_p(st.cuda_stream)))
+    return out
+
+
+def linear_frag(w: torch.Tensor, xf: torch.Tensor, M: int, out: torch.Tensor = None,
+                workspace: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """y = x @ w.T from the fragment-ordered copy xf = to_frag(x) of M rows."""
+    lib = L.load()
+    N, K = w.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=w.device)
+    if workspace is None:
+        workspace = torch.empty(lib.sf_linear_workspace_bytes(N, K), dtype=torch.uint8, device=w.device)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    L.check(lib.sf_linear_frag(w.data_ptr(), N, K, w.stride(0), xf.data_ptr(), M, out.data_ptr(),
+                               workspace.data_ptr(), ctypes.c_void_p(st.cuda_stream)))
+    return out
+
+
 def nf4_scale_ld(cols: int) -> int:
     """Row stride (in scales) of the NF4 block-scale matrix: cols/64 rounded up to 8."""
     return (cols // 64 + 7) // 8 * 8

@@ -233,6 +233,26 @@ SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, co
                            float* d_y, void* d_workspace, void* cuda_stream);
 
 /*
+ * The two halves of sf_linear. Every projection reads its token rows as
+ * bf16 pairs (hi = bf16(v), lo = bf16(v - hi), about 16 mantissa bits of the
+ * fp32 value) in the order the GEMM's MMA lanes consume them ("fragment
+ * order"): with T = ceil(M / 4) token tiles, the 16-byte unit
+ * ((j * T + t) * 2 + h) * 32 + l holds, for 64-feature chunk j, tile t, half h
+ * and lane l = 4 * col + c, the 8 features 64j + 16c + 8h + 0..7 of token
+ * 4t + col / 2, hi parts for even col and lo parts for odd col. Features past
+ * K and tokens past M are zero.
+ *   sf_frag_bytes(K, M): size of that copy (0 if invalid).
+ *   sf_to_frag: x (device fp32 [M, ld], features 0..K-1) -> d_frag (device,
+ *     16-byte aligned, sf_frag_bytes(K, M) bytes), enqueued on cuda_stream.
+ *   sf_linear_frag: sf_linear reading the copy instead of x (same W, y and
+ *     workspace rules); reuse one copy for several matrices that share x.
+ */
+SF_API size_t sf_frag_bytes(int32_t K, int32_t M);
+SF_API sf_status sf_to_frag(const float* d_x, int32_t M, int32_t K, int32_t ld, void* d_frag, void* cuda_stream);
+SF_API sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, const void* d_frag, int32_t M,
+                                float* d_y, void* d_workspace, void* cuda_stream);
+
+/*
  * sf_linear without any caller-provided scratch, for callers that cannot
  * allocate device memory where they need the projection: code running while
  * a stream is captured into a CUDA graph, plug-ins whose host framework owns

@@ -63,3 +63,47 @@ def test_deterministic_and_row_independent(pkg):
     for m in range(9):
         ym = pkg.linear(w, x[m:m + 1].contiguous())
         assert torch.equal(ym[0], y1[m]), m
+
+
+def _frag_reference(x):
+    """The fragment order written out element by element (test-side
+    restatement of the layout the header documents): bf16 hi/lo pairs of x
+    [M, K] as a uint16 array of the library's byte size."""
+    M, K = x.shape
+    T = (M + 3) // 4
+    nch = (K + 63) // 64
+    out = torch.zeros(nch * T * 2 * 32 * 8, dtype=torch.int16)
+    hi = x.to(torch.bfloat16)
+    lo = (x - hi.float()).to(torch.bfloat16)
+    hi16, lo16 = hi.view(torch.int16), lo.view(torch.int16)
+    for m in range(M):
+        for k in range(K):
+            j, kk = divmod(k, 64)
+            c, h, e = kk // 16, (kk // 8) % 2, kk % 8
+            t, col = m // 4, 2 * (m % 4)
+            unit = ((j * T + t) * 2 + h) * 32 + 4 * col + c
+            out[unit * 8 + e] = hi16[m, k]
+            out[(unit + 4) * 8 + e] = lo16[m, k]
+    return out
+
+
+@pytest.mark.parametrize("M,K", [(1, 64), (3, 72), (9, 200), (16, 128)])
+def test_to_frag_layout(pkg, M, K):
+    g = torch.Generator(device="cuda").manual_seed(M * 1000 + K)
+    x = torch.randn(M, K, generator=g, device="cuda")
+    xf = pkg.to_frag(x)
+    torch.cuda.synchronize()
+    ref = _frag_reference(x.cpu())
+    assert xf.numel() == 2 * ref.numel()
+    assert torch.equal(xf.cpu().view(torch.int16), ref)
+
+
+@pytest.mark.parametrize("N,K,M", [(37888, 3584, 9), (1000, 904, 3), (129, 72, 16), (5, 8, 1)])
+def test_linear_frag_equals_linear(pkg, N, K, M):
+    g = torch.Generator(device="cuda").manual_seed(N + K + M)
+    w = (torch.randn(N, K, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    x = torch.randn(M, K, generator=g, device="cuda")
+    ref = pkg.linear(w, x)
+    y = pkg.linear_frag(w, pkg.to_frag(x), M)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
