@@ -813,12 +813,7 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->C.assign(batch, 0);
 
   cudaError_t ce;
-  {
-    int group = tgt->n_heads / tgt->n_kv_heads;
-    if (dft) group = std::max(group, dft->n_heads / dft->n_kv_heads);
-    if ((ce = attn_init(SF_MAX_ROWS * group)) != cudaSuccess)
-      return bail(fail(SF_ERR_UNSUPPORTED, "attention: %d query heads per KV head: %s", group, cudaGetErrorString(ce)));
-  }
+  if ((ce = attn_init()) != cudaSuccess) return bail(fail(SF_ERR_CUDA, "attn_init: %s", cudaGetErrorString(ce)));
   if (tgt->wdtype == SF_WDTYPE_NF4 || (dft && dft->wdtype == SF_WDTYPE_NF4)) {
     double lv[16];
     float lf[16];

@@ -106,28 +106,32 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   const int group = a.nq / a.nkv;
   const int rps = a.rs.rps;
   const int Mq = rps * group;
-  const int qrows = (Mq + 15) / 16 * 16;
-  bf16* sqh = spl + 16 * PP;                                       // [tiles * 16][HP] queries, hi
-  bf16* sql = sqh + qrows * HP;                                    // [tiles * 16][HP] queries, lo
+  const int ntiles = (Mq + 15) / 16;
+  bf16* sqh = spl + 16 * PP;                                       // [16][HP] queries of the tile, hi
+  bf16* sql = sqh + 16 * HP;                                       // [16][HP] queries of the tile, lo
 
   // The lengths were written by kernels that finished before the preceding
   // one started, so they (and the cache slots below this pass's first
   // position) can be read before waiting on the preceding kernel.
+  // Work item = (sequence b, KV head, chunk c, query tile qt); the tiles of
+  // one chunk are consecutive items (their CTAs share the chunk through L2).
   int total = 0;
   for (int b = 0; b < a.B; ++b) {
     const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
-    total += a.nkv * (p_last / kKvChunk + 1);
+    total += a.nkv * (p_last / kKvChunk + 1) * ntiles;
   }
-  auto locate = [&](int item, int& b, int& kvh, int& c) {
+  auto locate = [&](int item, int& b, int& kvh, int& c, int& qt) {
     int rest = item, nch = 0;
     for (b = 0; b < a.B; ++b) {
       const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
       nch = p_last / kKvChunk + 1;
-      if (rest < a.nkv * nch) break;
-      rest -= a.nkv * nch;
+      if (rest < a.nkv * nch * ntiles) break;
+      rest -= a.nkv * nch * ntiles;
     }
-    kvh = rest / nch;
-    c = rest - kvh * nch;
+    kvh = rest / (nch * ntiles);
+    rest -= kvh * nch * ntiles;
+    c = rest / ntiles;
+    qt = rest - c * ntiles;
   };
   // Copy slots [0, nvalid) of the chunk; zero the rest of the tile.
   auto issue = [&](int b, int kvh, int c, int nvalid) {
@@ -146,8 +150,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   };
   bool issued = false;
   if ((int)blockIdx.x < total) {
-    int b, kvh, c;
-    locate(blockIdx.x, b, kvh, c);
+    int b, kvh, c, qt;
+    locate(blockIdx.x, b, kvh, c, qt);
     if ((c + 1) * kKvChunk <= a.rs.pos_base[b] + a.rs.pos_off) {   // no slot of this pass in the chunk
       issue(b, kvh, c, kKvChunk);
       issued = true;
@@ -157,17 +161,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   trace_mark(a.rs, 1);
   pdl_launch_next();
 
-  // All query rows of the item -> shared memory as bf16 hi + lo pairs (rows
-  // past Mq are zero), eight 16-byte loads per thread in flight at a time.
-  auto stage_q = [&](int b, int kvh) {
-    constexpr int kBatch = 8;
-    const int n4 = qrows * (HD / 4);
+  // The item's 16 query rows -> shared memory as bf16 hi + lo pairs (rows
+  // past Mq are zero), all loads of a thread in flight at once.
+  auto stage_q = [&](int b, int kvh, int qt) {
+    constexpr int kBatch = 16 * (HD / 4) / kAttnThreads;
+    const int n4 = 16 * (HD / 4);
     for (int i0 = 0; i0 < n4; i0 += kBatch * kAttnThreads) {
       float4 v[kBatch];
 #pragma unroll
       for (int e = 0; e < kBatch; ++e) {
         const int i = i0 + tid + e * kAttnThreads;
-        const int qi = i / (HD / 4), u = i - qi * (HD / 4);
+        const int qi = qt * 16 + i / (HD / 4), u = i % (HD / 4);
         v[e] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < n4 && qi < Mq) {
           const int j = qi / group, hh = qi - j * group;
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
       for (int e = 0; e < kBatch; ++e) {
         const int i = i0 + tid + e * kAttnThreads;
         if (i >= n4) break;
-        const int qi = i / (HD / 4), u = i - qi * (HD / 4);
+        const int qi = i / (HD / 4), u = i - qi * (HD / 4);   // row within the tile
         uint2 h, l;
         split_bf16x2(v[e].x, v[e].y, h.x, l.x);
         split_bf16x2(v[e].z, v[e].w, h.y, l.y);
@@ -189,18 +193,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   };
 
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    int b, kvh, c;
-    locate(item, b, kvh, c);
+    int b, kvh, c, qt;
+    locate(item, b, kvh, c, qt);
     const int p0 = a.rs.pos_base[b] + a.rs.pos_off;
     if (!issued) issue(b, kvh, c, min(kKvChunk, p0 + rps - c * kKvChunk));
     issued = false;
-    stage_q(b, kvh);
+    stage_q(b, kvh, qt);
     cp_async_wait_all();
     __syncthreads();
 
-    for (int qt = 0; qt * 16 < Mq; ++qt) {
-      const bf16* qht = sqh + qt * 16 * HP;
-      const bf16* qlt = sql + qt * 16 * HP;
+    {
+      const bf16* qht = sqh;
+      const bf16* qlt = sql;
       // Rows g and g+8 of the tile: slots this row may see within the chunk.
       int nk[2];
 #pragma unroll
@@ -415,20 +419,17 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
 
 // Dynamic shared memory of the chunk kernel: keys, values, P hi + lo, and
 // the item's query rows (padded to whole tiles of 16).
-static int attn_smem_bytes(int hd, int mq) {
-  return kKvChunk * (hd * 2 + 32) + kKvChunk * (hd * 2 + 16) + 2 * 16 * (kKvChunk + 8) * 2 +
-         2 * (mq + 15) / 16 * 16 * (hd + 16) * 2;
+static int attn_smem_bytes(int hd) {
+  return kKvChunk * (hd * 2 + 32) + kKvChunk * (hd * 2 + 16) + 2 * 16 * (kKvChunk + 8) * 2 + 2 * 16 * (hd + 16) * 2;
 }
 
-// Raise the dynamic shared-memory limit of the chunk kernels to what the
-// largest query group (rows x heads per KV head) needs.
-cudaError_t attn_init(int max_mq) {
-  if (attn_smem_bytes(128, max_mq) > 200 * 1024) return cudaErrorInvalidValue;
+// Dynamic shared-memory limits of the chunk kernels and the largest
+// shared-memory carve-out for every kernel of the chain.
+cudaError_t attn_init() {
   cudaError_t e = cudaFuncSetAttribute(k_attn_chunks<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       attn_smem_bytes(128, max_mq));
+                                       attn_smem_bytes(128));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_attn_chunks<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           attn_smem_bytes(64, max_mq));
+  e = cudaFuncSetAttribute(k_attn_chunks<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(64));
   if (e != cudaSuccess) return e;
   // Largest shared-memory carve-out for every kernel of the chain (see gemm_init).
   const void* fns[] = {reinterpret_cast<const void*>(k_attn_chunks<128>),
@@ -448,14 +449,14 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bo
   cudaLaunchConfig_t cfg = {};
   // Enough CTAs for the largest item count this launch can see (the count
   // itself lives on the device): B * nkv * chunks of the whole cache, capped.
-  const int max_items = a.B * a.nkv * a.n_kv_chunks;
+  const int max_items = a.B * a.nkv * a.n_kv_chunks * ((a.rs.rps * (a.nq / a.nkv) + 15) / 16);
   cfg.gridDim = dim3(max(1, min(max_items, 2 * num_sms)));
   cfg.blockDim = dim3(kAttnThreads);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  cfg.dynamicSmemBytes = attn_smem_bytes(a.hd, a.rs.rps * (a.nq / a.nkv));
+  cfg.dynamicSmemBytes = attn_smem_bytes(a.hd);
   if (a.hd == 128) e = cudaLaunchKernelEx(&cfg, k_attn_chunks<128>, a);
   else if (a.hd == 64) e = cudaLaunchKernelEx(&cfg, k_attn_chunks<64>, a);
   else return cudaErrorInvalidValue;

@@ -124,9 +124,8 @@ struct AttnArgs {
   RowSet rs;
 };
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl);
-// Shared-memory limits of the attention kernels (current device) for up to
-// max_mq query rows per KV head (rows per sequence x query heads per KV head).
-cudaError_t attn_init(int max_mq);
+// Shared-memory limits and carve-out of the attention kernels (current device).
+cudaError_t attn_init();
 
 cudaError_t launch_rope_table(float2* table, int s_max, int hd, float theta, cudaStream_t st);
 
