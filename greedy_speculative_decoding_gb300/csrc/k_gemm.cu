@@ -276,9 +276,15 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   float* rinv = ys + 4 * T * kBlockRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);           // [8][kStages]
   uint4* bstage = reinterpret_cast<uint4*>(bars + 8 * kStages);         // staged B operand (if any)
+  float* recv = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bstage) +
+                                         staged_b_bytes(T, a.cps));     // push: ranks 1.. tiles [M][128]
   __shared__ int s_flag;
   __shared__ int s_pos[kRows];
-  __shared__ uint32_t lut[NF4 ? 256 : 1];   // NF4: byte (two codes) -> bf16 pair of levels
+  __shared__ __align__(8) uint64_t recv_bar;   // push: the other ranks' tiles have landed
+  // NF4: byte (two codes) -> bf16 pair of levels, one copy of the 256-entry
+  // table per lane (entry b of lane l at 32 b + l: every lookup of a warp
+  // hits its own bank, whatever the codes).
+  __shared__ uint32_t lut[NF4 ? 256 * 32 : 1];
   trace_mark(a.rs, 0);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -318,15 +324,30 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
     for (int s = 0; s < kStages && s < nst; ++s) issue(s, s);
   }
   if (NF4) {
-    const uint32_t i = tid;   // 256 threads, 256 byte values
-    lut[i] = pack_bf16x2(__float2bfloat16_rn(c_nf4_levels[i & 15]), __float2bfloat16_rn(c_nf4_levels[i >> 4]));
+    for (int i = tid; i < 256 * 32; i += kGemmThreads) {
+      const int b = i >> 5;
+      lut[i] = pack_bf16x2(__float2bfloat16_rn(c_nf4_levels[b & 15]), __float2bfloat16_rn(c_nf4_levels[b >> 4]));
+    }
   }
   // Token positions (QKV: RoPE angle and cache slot), read before the wait:
   // the sequence lengths are written only by the acceptance and reset
   // kernels and by host copies, never by the kernel that directly precedes a
   // projection (the only one that can still be running at this point).
   if (EPI == EPI_QKV && tid < a.rs.M) s_pos[tid] = row_pos(a.rs, tid);
-  __syncthreads();
+  if (a.push) {
+    // Rank 0's landing barrier expects every other rank's tile; the cluster
+    // barrier that starts here (and is waited on only after the main loop)
+    // publishes its initialisation before any rank stores into it.
+    if (cluster_rank() == 0 && tid == 0) {
+      mbar_init(&recv_bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      mbar_expect_tx(&recv_bar, (uint32_t)push_bytes(a.nsplit, a.rs.M));
+    }
+    __syncthreads();
+    cluster_arrive();
+  } else {
+    __syncthreads();
+  }
 
   pdl_wait();
   trace_mark(a.rs, 1);
@@ -419,10 +440,15 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
         const float s_lo = __half2float(sct[g * 8 + scol]);
         const float s_hi = __half2float(sct[(g + 8) * 8 + scol]);
         uint4 w[4];
-        w[0] = make_uint4(lut[b0.x & 255], lut[(b0.x >> 8) & 255], lut[(b0.x >> 16) & 255], lut[b0.x >> 24]);
-        w[1] = make_uint4(lut[b0.y & 255], lut[(b0.y >> 8) & 255], lut[(b0.y >> 16) & 255], lut[b0.y >> 24]);
-        w[2] = make_uint4(lut[b1.x & 255], lut[(b1.x >> 8) & 255], lut[(b1.x >> 16) & 255], lut[b1.x >> 24]);
-        w[3] = make_uint4(lut[b1.y & 255], lut[(b1.y >> 8) & 255], lut[(b1.y >> 16) & 255], lut[b1.y >> 24]);
+        const uint32_t* lt = lut + lane;
+        w[0] = make_uint4(lt[(b0.x & 255) << 5], lt[((b0.x >> 8) & 255) << 5], lt[((b0.x >> 16) & 255) << 5],
+                          lt[(b0.x >> 24) << 5]);
+        w[1] = make_uint4(lt[(b0.y & 255) << 5], lt[((b0.y >> 8) & 255) << 5], lt[((b0.y >> 16) & 255) << 5],
+                          lt[(b0.y >> 24) << 5]);
+        w[2] = make_uint4(lt[(b1.x & 255) << 5], lt[((b1.x >> 8) & 255) << 5], lt[((b1.x >> 16) & 255) << 5],
+                          lt[(b1.x >> 24) << 5]);
+        w[3] = make_uint4(lt[(b1.y & 255) << 5], lt[((b1.y >> 8) & 255) << 5], lt[((b1.y >> 16) & 255) << 5],
+                          lt[(b1.y >> 24) << 5]);
         // Levels are unscaled; one chunk shares one scale per row, applied
         // to the chunk's product before it joins the running sum.
         float part[T][4];
@@ -482,7 +508,34 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   }
   __syncthreads();
 
-  if (a.nsplit > 1 && a.cluster) {
+  if (a.push) {
+    // The K slices of this row block are the CTAs of one cluster. Every other
+    // rank stores its tile into rank 0's landing area with asynchronous
+    // remote stores counted on rank 0's barrier and leaves; rank 0 adds the
+    // tiles in rank order.
+    const uint32_t rank = cluster_rank();
+    cluster_wait();
+    if (rank != 0) {
+      const uint32_t dst = dsmem_addr(smem_u32(recv), 0) + (rank - 1) * (uint32_t)(M * kBlockRows * 4);
+      const uint32_t bar = dsmem_addr(smem_u32(&recv_bar), 0);
+      const float4* mine = reinterpret_cast<const float4*>(ys);
+      for (int i = tid; i < M * (kBlockRows / 4); i += kGemmThreads) st_async_v4(dst + 16 * i, mine[i], bar);
+      return;
+    }
+    if (!mbar_wait_cluster(&recv_bar, 0, kWaitIters)) {
+      // A tile never arrived: report, give the stores one more bounded
+      // chance to land in this CTA's shared memory, and skip the epilogue.
+      if (tid == 0) atomicOr(a.err, kErrWait);
+      mbar_wait_cluster(&recv_bar, 0, kWaitIters);
+      return;
+    }
+    for (int i = tid; i < M * kBlockRows; i += kGemmThreads) {
+      float v = ys[i];
+      for (int r = 1; r < a.nsplit; ++r) v += recv[(r - 1) * (M * kBlockRows) + i];
+      ys[i] = a.ssq ? v * rinv[i / kBlockRows] : v;
+    }
+    __syncthreads();
+  } else if (a.nsplit > 1 && a.cluster) {
     // The K slices of this row block are the CTAs of one cluster: after the
     // barrier every partial tile sits in its CTA's shared memory and rank 0
     // adds them in rank order, loading up to kG slices per round. The other
@@ -580,13 +633,13 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   else if (EPI == EPI_SWIGLU) epi_swiglu<T>(a, ys, rb, M);
   else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
   else epi_argmax(a, ys, rb, M, &s_flag);
-  if (a.nsplit > 1 && a.cluster) cluster_wait();
+  if (a.nsplit > 1 && a.cluster && !a.push) cluster_wait();
 }
 
-int gemm_smem_bytes(int M, int stages, bool nf4, int cps) {
+int gemm_smem_bytes(int M, int stages, bool nf4, int cps, int push) {
   const int T = (M + 3) / 4;
   return 1024 /* alignment slack */ + 8 * stages * (kTileBytes + (nf4 ? kScaleTileBytes : 0)) +
-         4 * T * kBlockRows * 4 + 4 * T * 4 + 8 * stages * 8 + staged_b_bytes(T, cps);
+         4 * T * kBlockRows * 4 + 4 * T * 4 + 8 * stages * 8 + staged_b_bytes(T, cps) + push;
 }
 
 cudaError_t set_nf4_levels(const float levels[16]) {
@@ -638,7 +691,7 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nblocks * a.nsplit);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4, a.cps);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4, a.cps, a.push ? push_bytes(a.nsplit, a.rs.M) : 0);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -661,7 +714,7 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
 
 template <int T, int EPI, bool NF4>
 static cudaError_t init_one() {
-  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4, 0) + kMaxStagedB;
+  const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4, 0, kMaxPushBytes) + kMaxStagedB;
   cudaError_t e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // Every kernel of the chain asks for the largest shared-memory carve-out,
@@ -775,7 +828,14 @@ cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
   if (a.cluster && a.nsplit > kMaxClusterSplit) return cudaErrorInvalidValue;
   if (a.stages < 2 || a.stages > (a.nf4 ? kMaxStagesNF4 : kMaxStages)) return cudaErrorInvalidValue;
   if (a.nf4 && (a.K % 64 || (a.cps * a.nsplit > 1 && a.cps % 4))) return cudaErrorInvalidValue;
-  return a.nf4 ? launch_f<true>(a, epi, st, pdl) : launch_f<false>(a, epi, st, pdl);
+  // Push when the landing area fits and keeps the CTA within half an SM's
+  // shared memory (two CTAs per SM: this kernel's and the next one's, or two
+  // of this kernel's); otherwise rank 0 pulls the tiles.
+  GemmArgs b = a;
+  const int pb = push_bytes(a.nsplit, a.rs.M);
+  b.push = a.cluster && a.nsplit > 1 && pb <= kMaxPushBytes &&
+           gemm_smem_bytes(a.rs.M, a.stages, a.nf4, a.cps, pb) <= kHalfSmBytes;
+  return b.nf4 ? launch_f<true>(b, epi, st, pdl) : launch_f<false>(b, epi, st, pdl);
 }
 
 }  // namespace sf

@@ -176,6 +176,32 @@ __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
   return v;
 }
 
+// 16-byte asynchronous store into another CTA's shared memory (cluster
+// address), counted in bytes on that CTA's mbarrier (cluster address).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+               : "memory");
+}
+
+// Bounded wait on an mbarrier phase completed by other CTAs of the cluster
+// (acquire at cluster scope). Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t it = 0; it < max_iter; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start its prologue.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

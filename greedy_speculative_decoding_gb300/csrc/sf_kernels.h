@@ -24,6 +24,7 @@ struct GemmArgs {
   int N, K;                   // output rows (SWIGLU: ffn features), reduction length
   int nblocks, nsplit, cps;   // row blocks, K splits, chunks per split
   int stages;                 // weight tiles in flight per warp (2..kMaxStages)
+  int push;                   // cluster split: ranks push their tiles into rank 0 (set by launch_gemm)
   int cluster;                // 1: the splits of a row block form one thread-block
                               // cluster and are summed through distributed shared
                               // memory; 0: through `part` in global memory
@@ -69,8 +70,8 @@ cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const 
 cudaError_t set_nf4_levels(const float levels[16]);
 
 constexpr int kMaxClusterSplit = 16;  // cluster size (above 8 is non-portable; allowed per kernel)
-constexpr int kMaxStages = 11;        // deepest bf16 weight ring that fits next to 16 token rows
-constexpr int kMaxStagesNF4 = 10;     // NF4 stages also carry their block scales
+constexpr int kMaxStages = 9;         // deepest bf16 weight ring (beside 16 token rows and their operands)
+constexpr int kMaxStagesNF4 = 6;      // NF4 stages also carry their block scales (and a 32 KB table)
 
 // fp32 rows x [M][ld] (features 0..K-1) -> fragment order, zero past K and
 // past M within the last token tile (the input of sf_linear).
@@ -94,7 +95,13 @@ constexpr int kMaxStagedB = 24 * 1024;
 __host__ __device__ inline int staged_b_bytes(int T, int cps) {
   return (cps >= 2 && cps * T * 1024 <= kMaxStagedB) ? cps * T * 1024 : 0;
 }
-int gemm_smem_bytes(int M, int stages, bool nf4, int cps);
+// A cluster split whose ranks' partial tiles for rank 0 fit in kMaxPushBytes
+// pushes them there with asynchronous remote stores (one hop, no barrier
+// round trip); larger ones are pulled by rank 0 after a cluster barrier.
+constexpr int kMaxPushBytes = 32 * 1024;
+constexpr int kHalfSmBytes = 112 * 1024;   // dynamic shared memory that still lets two CTAs share an SM
+__host__ __device__ inline int push_bytes(int nsplit, int M) { return (nsplit - 1) * M * kBlockRows * 4; }
+int gemm_smem_bytes(int M, int stages, bool nf4, int cps, int push = 0);
 int gemm_max_clusters(int csize, int M, int stages, int cps);
 cudaError_t gemm_init();
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
