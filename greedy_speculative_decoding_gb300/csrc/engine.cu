@@ -356,7 +356,9 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   md.p_o = plan(nblocks_of(c, 1), H, (long)c->n_heads * c->head_dim);
   md.p_gu = plan(nblocks_of(c, 2), 2l * c->ffn, H);
   md.p_d = plan(nblocks_of(c, 1), H, c->ffn);
-  md.p_lm = make_plan(nblocks_of(c, 3), H, 2 * e->num_sms, 8);
+  md.p_lm.nblocks = nblocks_of(c, 3);   // the persistent LM head: no K split
+  md.p_lm.nsplit = 1;
+  md.p_lm.cps = (H + kChunk - 1) / kChunk;
   for (const Plan* p : {&md.p_qkv, &md.p_o, &md.p_gu, &md.p_d, &md.p_lm})
     if (p->nsplit > 1 && p->nblocks * p->nsplit > kMaxPlanTiles)
       return fail(SF_ERR_UNSUPPORTED, "split-K plan exceeds the scratch tiles");
@@ -563,8 +565,9 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   a.logits = to.logits;
   a.lg_stride = to.lg_stride;
   a.lg_off = to.lg_off;
+  a.stages = 5;
   a.rs = traced(e, rs, "lm_head");
-  CK(launch_gemm(a, EPI_ARGMAX, s, e->pdl));
+  CK(launch_lmhead(a, e->num_sms, s, e->pdl));
   return SF_OK;
 }
 

@@ -29,6 +29,8 @@
 // Split-K partial tiles go to a global scratch area; the last CTA of a row
 // block (arrival counter) adds them in fixed slice order and runs the
 // epilogue, so results are deterministic without float atomics.
+#include <algorithm>
+
 #include "sf_kernels.h"
 
 namespace sf {
@@ -636,6 +638,180 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   if (a.nsplit > 1 && a.cluster && !a.push) cluster_wait();
 }
 
+// ------------------------------------------------------------------ LM head
+// Persistent form of the GEMM with the argmax epilogue, for the vocabulary
+// projection (one K slice, far more 128-row blocks than CTAs): CTA b of G
+// takes row blocks b, b + G, b + 2G, ...; each warp's TMA ring runs over the
+// concatenated (block, chunk) sequence, so the weight stream never drains at
+// a block boundary; the running best (value, index) of every token row stays
+// in shared memory and is merged into the global keys once per CTA. The
+// per-row arithmetic is that of k_gemm with one K slice (same chunk order,
+// same MMA sequence, same 1 / rms scaling), so logits are bit-identical.
+template <int T>
+__global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const __grid_constant__ GemmArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int kStages = a.stages;
+  unsigned char* ring = smem;                                            // [8][kStages][kTileBytes]
+  float* ys = reinterpret_cast<float*>(smem + 8 * kStages * kTileBytes);   // [4T][128]
+  float* rinv = ys + 4 * T * kBlockRows;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);            // [8][kStages]
+  uint4* bstage = reinterpret_cast<uint4*>(bars + 8 * kStages);          // staged B operand (if any)
+  __shared__ unsigned long long s_best[kRows];
+  __shared__ int s_flag;
+  trace_mark(a.rs, 0);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int nch = (a.K + kChunk - 1) / kChunk;
+  const int G = gridDim.x;
+  const int nmine = (a.nblocks - (int)blockIdx.x + G - 1) / G;   // launch: G <= nblocks
+  const long total = (long)nmine * nch;                             // this warp's tiles, all blocks
+  unsigned char* my_ring = ring + warp * kStages * kTileBytes;
+  uint64_t* my_bar = bars + warp * kStages;
+  auto issue = [&](int s, long q) {
+    const int i = (int)(q / nch), j = (int)(q - (long)i * nch);
+    const int rb = blockIdx.x + i * G;
+    mbar_expect_tx(&my_bar[s], kTileBytes);
+    tma_load_2d(my_ring + s * kTileBytes, &a.tm[0], j * kChunk, rb * kBlockRows + 16 * warp, &my_bar[s],
+                policy_evict_first());
+  };
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&my_bar[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < kStages && s < total; ++s) issue(s, s);   // weights: before the wait
+  }
+  if (tid < kRows) s_best[tid] = 0ull;
+  __syncthreads();
+
+  pdl_wait();
+  trace_mark(a.rs, 1);
+  pdl_launch_next();
+  const int M = a.rs.M;
+  float ssq_part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  if (a.ssq) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int m = warp + 8 * j;
+      if (m < M) {
+        ssq_part[j][0] = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
+        ssq_part[j][1] = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
+      }
+    }
+  }
+  // The B operand is the same for every block: staged once when it is small.
+  const uint4* bsrc = a.in;
+  if (staged_b_bytes(T, nch)) {
+    for (int i = tid; i < nch * T * 64; i += kGemmThreads) cp_async16(bstage + i, a.in + i);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    bsrc = bstage;
+  }
+  uint4 bq[T][2];
+  load_b<T>(bq, bsrc, 0, lane);
+
+  const int sw = g & 7;
+  const int off_lo = g * 128 + (((2 * c) ^ sw) << 4);
+  const int off_hi = g * 128 + (((2 * c + 1) ^ sw) << 4);
+  bool timed_out = false;
+  long q = 0;
+  for (int i = 0; i < nmine; ++i) {
+    const int rb = blockIdx.x + i * G;
+    float acc[T][4];
+#pragma unroll
+    for (int t = 0; t < T; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    for (int j = 0; j < nch; ++j, ++q) {
+      const int s = (int)(q % kStages);
+      const bool more = j + 1 < nch || i + 1 < nmine;
+      uint4 bn[T][2];
+      if (more) load_b<T>(bn, bsrc, j + 1 < nch ? j + 1 : 0, lane);
+      if (!mbar_wait(&my_bar[s], (uint32_t)((q / kStages) & 1), kWaitIters)) timed_out = true;
+      const unsigned char* tile = my_ring + s * kTileBytes;
+      uint4 w[4];
+      w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
+      w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
+      w[2] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_lo);
+      w[3] = *reinterpret_cast<const uint4*>(tile + 8 * 128 + off_hi);
+      __syncwarp();
+      if (lane == 0 && q + kStages < total) {
+        fence_proxy_async();   // the warp's reads of this stage before the async refill
+        issue(s, q + kStages);
+      }
+      mma_chunk<T>(acc, w, bq);
+      if (more) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          bq[t][0] = bn[t][0];
+          bq[t][1] = bn[t][1];
+        }
+      }
+    }
+    if (i == 0 && a.ssq) {
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int m = warp + 8 * jj;
+        if (m < M) {
+          const float sq = warp_sum(ssq_part[jj][0] + ssq_part[jj][1]);
+          if (lane == 0) rinv[m] = 1.0f / sqrtf(sq * a.inv_k + a.eps);
+        }
+      }
+    }
+    const int r0 = warp * 16 + g;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int m = 4 * t + c;
+      ys[m * kBlockRows + r0] = acc[t][0] + acc[t][1];
+      ys[m * kBlockRows + r0 + 8] = acc[t][2] + acc[t][3];
+    }
+    __syncthreads();
+    for (int m = warp; m < M; m += kGemmThreads / 32) {
+      unsigned long long best = 0ull;
+      bool bad = false;
+      const int mb = m / a.rs.rps, mj = m - mb * a.rs.rps;
+      const int lg_row = mj >= a.tok_skip ? mb * a.lg_stride + a.lg_off + mj - a.tok_skip : -1;
+      const float sc = a.ssq ? rinv[m] : 1.f;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int r = lane + 32 * jj;
+        const int n = rb * kBlockRows + r;
+        if (n < a.N) {
+          const float v = a.ssq ? ys[m * kBlockRows + r] * sc : ys[m * kBlockRows + r];
+          if (a.logits && lg_row >= 0) a.logits[(size_t)lg_row * a.N + n] = v;
+          bad |= !isfinite(v);
+          const unsigned long long k = argmax_key(v, n);
+          best = k > best ? k : best;
+        }
+      }
+      best = shfl_max_u64(best);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, kErrNonfinite);
+      if (lane == 0 && best > s_best[m]) s_best[m] = best;
+    }
+    __syncthreads();   // ys is free for the next block
+  }
+  if (timed_out) {
+    if (lane == 0) atomicOr(a.err, kErrWait);
+    for (long st = (total > kStages ? total - kStages : 0); st < total; ++st)
+      mbar_wait(&my_bar[st % kStages], (uint32_t)((st / kStages) & 1), kWaitIters);
+  }
+  // Merge the CTA's bests; the last CTA to arrive writes the tokens and
+  // leaves the keys and the counter at zero for the next launch.
+  if (tid < M) atomicMax(a.keys + tid, s_best[tid]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_flag = (atomicAdd(a.done, 1) == G - 1);
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  if (tid < M) {
+    const int m = tid;
+    const unsigned long long k = atomicExch(a.keys + m, 0ull);
+    const int b = m / a.rs.rps, j = m - b * a.rs.rps;
+    if (j >= a.tok_skip) a.tok_out[b * a.tok_stride + a.tok_off + j - a.tok_skip] = key_index(k);
+  }
+  if (tid == 0) *a.done = 0;
+}
+
 int gemm_smem_bytes(int M, int stages, bool nf4, int cps, int push) {
   const int T = (M + 3) / 4;
   return 1024 /* alignment slack */ + 8 * stages * (kTileBytes + (nf4 ? kScaleTileBytes : 0)) +
@@ -756,9 +932,19 @@ int gemm_max_clusters(int csize, int M, int stages, int cps) {
   return cudaOccupancyMaxActiveClusters(&n, k_gemm<3, EPI_QKV, false>, &cfg) == cudaSuccess ? n : 0;
 }
 
+template <int T>
+static cudaError_t init_lm() {
+  const int smem = gemm_smem_bytes(4 * T, kMaxStages, false, 0) + kMaxStagedB;
+  cudaError_t e = cudaFuncSetAttribute(k_lmhead<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_lmhead<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 // Raise the dynamic shared-memory limit of every instantiation (current device).
 cudaError_t gemm_init() {
   cudaError_t e;
+  if ((e = init_lm<1>()) || (e = init_lm<2>()) || (e = init_lm<3>()) || (e = init_lm<4>())) return e;
   if ((e = init_t<1, false>()) || (e = init_t<2, false>()) || (e = init_t<3, false>()) ||
       (e = init_t<4, false>()) || (e = init_t<1, true>()) || (e = init_t<2, true>()) ||
       (e = init_t<3, true>()) || (e = init_t<4, true>()))
@@ -821,6 +1007,33 @@ cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cuda
   const long units = (long)frag_bytes(K, T) / 16;
   k_to_frag<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(x, M, K, ld, T, reinterpret_cast<uint4*>(out), units);
   return cudaGetLastError();
+}
+
+template <int T>
+static cudaError_t launch_lm_t(const GemmArgs& a, int ctas, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, false, (a.K + kChunk - 1) / kChunk);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_lmhead<T>, a);
+}
+
+cudaError_t launch_lmhead(const GemmArgs& a, int num_sms, cudaStream_t st, bool pdl) {
+  const int T = (a.rs.M + 3) / 4;
+  if (a.rs.M < 1 || a.rs.M > kRows || a.nf4 || a.stages < 2 || a.stages > kMaxStages) return cudaErrorInvalidValue;
+  const int ctas = std::max(1, std::min(a.nblocks, (T <= 3 ? 2 : 1) * num_sms));
+  switch (T) {
+    case 1: return launch_lm_t<1>(a, ctas, st, pdl);
+    case 2: return launch_lm_t<2>(a, ctas, st, pdl);
+    case 3: return launch_lm_t<3>(a, ctas, st, pdl);
+    default: return launch_lm_t<4>(a, ctas, st, pdl);
+  }
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {

@@ -105,6 +105,9 @@ int gemm_smem_bytes(int M, int stages, bool nf4, int cps, int push = 0);
 int gemm_max_clusters(int csize, int M, int stages, int cps);
 cudaError_t gemm_init();
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
+// The LM head with its argmax as a persistent kernel (one K slice, at most
+// two CTAs per SM walking the row blocks); same arguments as EPI_ARGMAX.
+cudaError_t launch_lmhead(const GemmArgs& a, int num_sms, cudaStream_t st, bool pdl);
 
 struct EmbedArgs {
   const bf16* E;
