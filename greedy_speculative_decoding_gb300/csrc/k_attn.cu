@@ -344,10 +344,9 @@ constexpr int kMergeLoads = 24;
 
 __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_constant__ AttnArgs a) {
   __shared__ float wgt[kMaxKvChunks];
-  __shared__ float lw[kMaxKvChunks];
   __shared__ float opart[kMergeThreads];
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float s_mx, s_l;
+  __shared__ float red[kMergeThreads / 32], red_l[kMergeThreads / 32];
+  __shared__ float s_l;
   RowSet rs1 = a.rs;
   rs1.trace_id = a.merge_trace_id;
   trace_mark(rs1, 0);
@@ -370,23 +369,23 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
     const int c = grp + q * G;
     v[q] = c < nch ? src[(size_t)c * stride + d] : 0.f;
   }
+  // M = max_c m_c (every thread combines the eight warp maxima itself);
+  // chunk weights e^(m_c - M); l = sum_c l_c e^(m_c - M) in a fixed tree
+  // (within warps, then warps in order).
   const float wm = warp_max(mc);
   if (lane == 0) red[warp] = wm;
   __syncthreads();
-  if (tid == 0) {
-    float x = red[0];
-    for (int w = 1; w < kMergeThreads / 32; ++w) x = fmaxf(x, red[w]);
-    s_mx = x;
-  }
-  __syncthreads();
-  if (tid < nch) {
-    wgt[tid] = expf(mc - s_mx);
-    lw[tid] = lc;
-  }
+  float mx = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+  const float wc = tid < nch ? expf(mc - mx) : 0.f;
+  if (tid < nch) wgt[tid] = wc;
+  const float lsum = warp_sum(lc * wc);
+  if (lane == 0) red_l[warp] = lsum;
   __syncthreads();
   if (tid == 0) {
-    float l = 0.f;
-    for (int c = 0; c < nch; ++c) l = fmaf(lw[c], wgt[c], l);
+    float l = red_l[0];
+    for (int w = 1; w < kMergeThreads / 32; ++w) l += red_l[w];
     s_l = l;
   }
   float o = 0.f;
