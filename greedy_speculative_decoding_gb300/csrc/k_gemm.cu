@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   float* rinv = ys + 4 * T * kBlockRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);           // [8][kStages]
   uint4* bstage = reinterpret_cast<uint4*>(bars + 8 * kStages);         // staged B operand (if any)
-  float* recv = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bstage) +
-                                         staged_b_bytes(T, a.cps));     // push: ranks 1.. tiles [M][128]
+  const int sb = a.stage_b ? staged_b_bytes(T, a.cps) : 0;             // staged B operand bytes
+  float* recv = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bstage) + sb);   // push landing area
   __shared__ int s_flag;
   __shared__ int s_pos[kRows];
   __shared__ __align__(8) uint64_t recv_bar;   // push: the other ranks' tiles have landed
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const _
   // memory (short K slices: one copy instead of a global round trip per chunk).
   const uint4* bsrc = a.in;
   int jb = 0;   // chunk index of bsrc[0]
-  if (staged_b_bytes(T, a.cps) && nch > 0) {
+  if (sb && nch > 0) {
     const uint4* src = a.in + (size_t)c0 * (T * 64);
     for (int i = tid; i < nch * T * 64; i += kGemmThreads) cp_async16(bstage + i, src + i);
     cp_async_commit();
@@ -867,7 +867,8 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nblocks * a.nsplit);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4, a.cps, a.push ? push_bytes(a.nsplit, a.rs.M) : 0);
+  cfg.dynamicSmemBytes =
+      gemm_smem_bytes(4 * T, a.stages, NF4, a.stage_b ? a.cps : 0, a.push ? push_bytes(a.nsplit, a.rs.M) : 0);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -1044,10 +1045,17 @@ cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
   // Push when the landing area fits and keeps the CTA within half an SM's
   // shared memory (two CTAs per SM: this kernel's and the next one's, or two
   // of this kernel's); otherwise rank 0 pulls the tiles.
+  // Staging the B operand and the landing area compete for that space; the
+  // push reduction wins when both do not fit.
   GemmArgs b = a;
   const int pb = push_bytes(a.nsplit, a.rs.M);
-  b.push = a.cluster && a.nsplit > 1 && pb <= kMaxPushBytes &&
-           gemm_smem_bytes(a.rs.M, a.stages, a.nf4, a.cps, pb) <= kHalfSmBytes;
+  const bool split = a.cluster && a.nsplit > 1 && pb <= kMaxPushBytes;
+  b.stage_b = staged_b_bytes((a.rs.M + 3) / 4, a.cps) > 0;
+  b.push = split && gemm_smem_bytes(a.rs.M, a.stages, a.nf4, a.cps, pb) <= kHalfSmBytes;
+  if (split && !b.push && gemm_smem_bytes(a.rs.M, a.stages, a.nf4, 0, pb) <= kHalfSmBytes) {
+    b.stage_b = 0;
+    b.push = 1;
+  }
   return b.nf4 ? launch_f<true>(b, epi, st, pdl) : launch_f<false>(b, epi, st, pdl);
 }
 

@@ -25,6 +25,7 @@ struct GemmArgs {
   int nblocks, nsplit, cps;   // row blocks, K splits, chunks per split
   int stages;                 // weight tiles in flight per warp (2..kMaxStages)
   int push;                   // cluster split: ranks push their tiles into rank 0 (set by launch_gemm)
+  int stage_b;                // B operand copied into shared memory first (set by launch_gemm)
   int cluster;                // 1: the splits of a row block form one thread-block
                               // cluster and are summed through distributed shared
                               // memory; 0: through `part` in global memory
