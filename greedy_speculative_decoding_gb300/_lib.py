@@ -22,7 +22,7 @@ EXPORTS = (
     "sf_ngram_draft", "sf_verify", "sf_accept_rollback", "sf_step", "sf_generate", "sf_reset",
     "sf_set_drafter", "sf_get_lengths", "sf_get_accept_hist", "sf_status_str", "sf_last_error",
     "sf_destroy", "sf_nf4_quantize", "sf_linear_workspace_bytes", "sf_linear", "sf_linear_noalloc",
-    "sf_trace", "sf_trace_label", "sf_frag_bytes", "sf_to_frag", "sf_linear_frag",
+    "sf_trace", "sf_trace_label", "sf_frag_bytes", "sf_to_frag", "sf_linear_frag", "sf_round_launches",
 )
 
 
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sf_to_frag": (ST, [P, I32, I32, I32, P, P]),
         "sf_linear_frag": (ST, [P, I32, I32, I32, P, I32, P, P, P]),
         "sf_trace_label": (ctypes.c_char_p, [P, I32]),
+        "sf_round_launches": (ctypes.c_int64, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

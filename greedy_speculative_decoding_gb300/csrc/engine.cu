@@ -247,6 +247,7 @@ struct sf_engine {
   SpecState st{};
   int* pin = nullptr;   // pinned host copy of the report block
   cudaGraphExec_t graph[2] = {nullptr, nullptr};   // whole round, per drafter
+  size_t graph_kernels[2] = {0, 0};                 // kernel launches in each round graph
   cudaGraphExec_t g_draft = nullptr, g_verify = nullptr;
   int drafter = SF_DRAFT_NEURAL, ng_min = 2, ng_max = 4;
   std::vector<int> C;   // committed tokens per sequence (host mirror)
@@ -652,6 +653,10 @@ sf_status build_graph(sf_engine* e, int what) {
     return r;
   }
   if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(ce));
+  if (what == CAP_ROUND_NEURAL || what == CAP_ROUND_NGRAM) {
+    size_t n = 0;
+    if (cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess) e->graph_kernels[what] = n;
+  }
   ce = cudaGraphInstantiate(slot, g, 0);
   cudaGraphDestroy(g);
   if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(ce));
@@ -1142,6 +1147,11 @@ int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches) {
       return 0;
   }
   return n;
+}
+
+int64_t sf_round_launches(sf_handle h) {
+  if (!h) return 0;
+  return (int64_t)h->graph_kernels[h->drafter == SF_DRAFT_NGRAM ? CAP_ROUND_NGRAM : CAP_ROUND_NEURAL];
 }
 
 const char* sf_trace_label(sf_handle h, int32_t i) {

@@ -11,7 +11,7 @@
 //
 // Chunk boundaries are fixed multiples of 64 slots and a row at position p
 // reads slots 0..p, so a row's result does not depend on the other rows.
-#include "sf_kernels.h"
+#include "attn_merge.cuh"
 
 namespace sf {
 
@@ -331,22 +331,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   }
 }
 
-// out[m][h*hd + d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), written
-// in fragment order for the output projection. One CTA
-// per (row, head) of 256 threads: thread (g, d) with g = tid / hd adds the
-// chunks g, g + G, g + 2G, ... (G = 256 / hd) in order, up to kMergeLoads of
-// them loaded at once, and the G partial sums are then added in order g =
-// 0, 1, ...; every chunk's (max, sum) pair is loaded in the same round, so a
-// merge costs two dependent global loads, not one per few chunks.
-constexpr int kMaxKvChunks = 256;
-constexpr int kMergeThreads = 256;
-constexpr int kMergeLoads = 24;
-
+// The merge kernel: one CTA of kMergeThreads per (row, head); writes the
+// output projection's input in fragment order.
 __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_constant__ AttnArgs a) {
-  __shared__ float wgt[kMaxKvChunks];
-  __shared__ float opart[kMergeThreads];
-  __shared__ float red[kMergeThreads / 32], red_l[kMergeThreads / 32];
-  __shared__ float s_l;
+  __shared__ MergeSmem sm;
   RowSet rs1 = a.rs;
   rs1.trace_id = a.merge_trace_id;
   trace_mark(rs1, 0);
@@ -354,66 +342,9 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
   trace_mark(rs1, 1);
   pdl_launch_next();
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = kMergeThreads / a.hd;
-  const int grp = tid / a.hd, d = tid - grp * a.hd;
   const int nch = row_pos(a.rs, m) / kKvChunk + 1;
-  const int stride = a.hd + 2;
-  const float* src = a.part + ((size_t)m * a.nq + h) * a.n_kv_chunks * stride;
-  // Round one: every chunk's (max, sum) and this thread's first output terms.
-  const float mc = tid < nch ? src[(size_t)tid * stride + a.hd] : -INFINITY;
-  const float lc = tid < nch ? src[(size_t)tid * stride + a.hd + 1] : 0.f;
-  float v[kMergeLoads];
-#pragma unroll
-  for (int q = 0; q < kMergeLoads; ++q) {
-    const int c = grp + q * G;
-    v[q] = c < nch ? src[(size_t)c * stride + d] : 0.f;
-  }
-  // M = max_c m_c (every thread combines the eight warp maxima itself);
-  // chunk weights e^(m_c - M); l = sum_c l_c e^(m_c - M) in a fixed tree
-  // (within warps, then warps in order).
-  const float wm = warp_max(mc);
-  if (lane == 0) red[warp] = wm;
-  __syncthreads();
-  float mx = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, red[w]);
-  const float wc = tid < nch ? expf(mc - mx) : 0.f;
-  if (tid < nch) wgt[tid] = wc;
-  const float lsum = warp_sum(lc * wc);
-  if (lane == 0) red_l[warp] = lsum;
-  __syncthreads();
-  if (tid == 0) {
-    float l = red_l[0];
-    for (int w = 1; w < kMergeThreads / 32; ++w) l += red_l[w];
-    s_l = l;
-  }
-  float o = 0.f;
-#pragma unroll
-  for (int q = 0; q < kMergeLoads; ++q) {
-    const int c = grp + q * G;
-    if (c < nch) o = fmaf(v[q], wgt[c], o);
-  }
-  // Longer contexts: further rounds of kMergeLoads chunks per thread.
-  for (int c0 = kMergeLoads * G; c0 < nch; c0 += kMergeLoads * G) {
-#pragma unroll
-    for (int q = 0; q < kMergeLoads; ++q) {
-      const int c = c0 + grp + q * G;
-      v[q] = c < nch ? src[(size_t)c * stride + d] : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < kMergeLoads; ++q) {
-      const int c = c0 + grp + q * G;
-      if (c < nch) o = fmaf(v[q], wgt[c], o);
-    }
-  }
-  opart[tid] = o;
-  __syncthreads();
-  if (grp == 0) {
-    float t = opart[d];
-    for (int g2 = 1; g2 < G; ++g2) t += opart[g2 * a.hd + d];
-    frag_store(a.out, m, h * a.hd + d, (a.rs.M + 3) / 4, t / s_l);
-  }
+  const float v = merge_row_head(a.part, a.nq, a.hd, a.n_kv_chunks, m, h, nch, sm);
+  if ((int)threadIdx.x < a.hd) frag_store(a.out, m, h * a.hd + threadIdx.x, (a.rs.M + 3) / 4, v);
 }
 
 // Dynamic shared memory of the chunk kernel: keys, values, P hi + lo, and

@@ -191,6 +191,10 @@ class SpecEngine:
         L.check(self.lib.sf_get_accept_hist(self.h, _i32(hst)))
         return hst
 
+    def round_launches(self) -> int:
+        """Kernel launches in one replay of the round graph (0 before it is built)."""
+        return int(self.lib.sf_round_launches(self.h))
+
     def trace_count(self) -> int:
         """Launches enqueued so far (SF_TRACE=1), the id the next one gets."""
         return self.lib.sf_trace(self.h, None, 0)

@@ -213,6 +213,11 @@ SF_API sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist);
 SF_API int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches);
 SF_API const char* sf_trace_label(sf_handle h, int32_t i);
 
+/* Kernel launches in one replay of the round graph of the current drafter
+ * (its node count; every node is a kernel), or 0 before the graph has been
+ * built by sf_step / sf_generate. */
+SF_API int64_t sf_round_launches(sf_handle h);
+
 SF_API const char* sf_status_str(sf_status s);
 SF_API const char* sf_last_error(void);
 SF_API void sf_destroy(sf_handle h);
