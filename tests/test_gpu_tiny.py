@@ -333,3 +333,21 @@ def test_head_shapes_with_poisoned_caches(pkg, name):
     assert worst < LOGIT_TOL_BF16
     eng.accept_rollback()
     eng.close()
+
+
+def test_round_graph_kernel_count(pkg, tiny):
+    """One replay of the round graph launches: per forward an embedding, six
+    kernels per layer (QKV, attention chunks, merge, O, gate/up, down) and the
+    LM head; K draft forwards, one verify forward and the acceptance kernel
+    (the n-gram round: the lookup kernel instead of the draft forwards)."""
+    K = 4
+    eng = make_engine(pkg, tiny, K=K)
+    assert eng.round_launches() == 0          # no round graph yet
+    eng.prefill([uniform_prompt(32, 1024, seed=100).tolist()])
+    eng.step()
+    per_fwd = lambda s: 2 + 6 * s.layers
+    assert eng.round_launches() == K * per_fwd(TINY_DRAFT) + per_fwd(TINY_TARGET) + 1
+    eng.set_drafter(pkg.SF_DRAFT_NGRAM)
+    eng.step()
+    assert eng.round_launches() == 1 + per_fwd(TINY_TARGET) + 1
+    eng.close()
