@@ -1,13 +1,13 @@
 // Embedding gather, GQA attention over the static KV cache, RoPE table.
 //
 // Attention is split over the cache ("flash decoding"): one work item is
-// (sequence, KV head, 64-slot chunk). Its keys and values are contiguous in
-// the cache; the CTA brings them into padded shared-memory rows and serves
-// every query that reads this KV head (all rows of the sequence times the
-// query heads of the group) on the tensor cores, 16 queries at a time with
-// all eight warps on each tile. The chunk's partial result (row max, sum of
+// (sequence, KV head, 64-slot chunk, tile of 16 queries), the queries being
+// all rows of the sequence times the query heads that read this KV head.
+// The chunk's keys and values are contiguous in the cache; the CTA brings
+// them into padded shared-memory rows and computes its tile on the tensor
+// cores with all eight warps. The chunk's partial result (row max, sum of
 // exponentials, unnormalised output) goes to scratch; a second kernel merges
-// the chunks of every (row, head) in fixed chunk order.
+// the chunks of every (row, head) in a fixed order (attn_merge.cuh).
 //
 // Chunk boundaries are fixed multiples of 64 slots and a row at position p
 // reads slots 0..p, so a row's result does not depend on the other rows.

@@ -26,9 +26,14 @@
 // K split, same MMA sequence, same reduction order), so a verify row equals
 // the decode of the same token at the same position bit for bit.
 //
-// Split-K partial tiles go to a global scratch area; the last CTA of a row
-// block (arrival counter) adds them in fixed slice order and runs the
-// epilogue, so results are deterministic without float atomics.
+// Split K: the slices of a row block are one thread-block cluster; every
+// rank but 0 pushes its partial tile into rank 0's shared memory with
+// asynchronous remote stores (or, when that area does not fit, rank 0 pulls
+// the tiles after a cluster barrier), and rank 0 adds them in rank order and
+// runs the epilogue. sf_linear splits without clusters: partial tiles go to
+// a global scratch area and the last CTA of a row block (arrival counter)
+// adds them in slice order. Either way results are deterministic without
+// float atomics.
 #include <algorithm>
 
 #include "sf_kernels.h"
