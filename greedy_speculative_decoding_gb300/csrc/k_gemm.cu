@@ -270,7 +270,7 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, in
 }  // namespace
 
 template <int T, int EPI, bool NF4>
-__global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_gemm(const __grid_constant__ GemmArgs a) {
+__global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_QKV) ? 2 : 1)) k_gemm(const __grid_constant__ GemmArgs a) {
   extern __shared__ unsigned char smem_raw[];
   // The swizzled TMA tiles need a 1024-byte aligned base.
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
