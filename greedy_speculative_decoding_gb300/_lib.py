@@ -15,7 +15,7 @@ SF_OK, SF_ERR_ARG, SF_ERR_CAPACITY, SF_ERR_CUDA, SF_ERR_NONFINITE, SF_ERR_STATE,
     SF_ERR_DEVICE = range(8)
 SF_WDTYPE_BF16, SF_WDTYPE_NF4 = 0, 1
 SF_DRAFT_NEURAL, SF_DRAFT_NGRAM = 0, 1
-SF_MAX_ROWS = 16
+SF_MAX_ROWS = 80
 
 EXPORTS = (
     "sf_weight_count", "sf_kv_bytes", "sf_workspace_bytes", "sf_create", "sf_prefill", "sf_draft",

@@ -45,7 +45,6 @@ sf_status fail(sf_status s, const char* fmt, ...) {
 
 struct Plan {
   int nblocks = 0, nsplit = 1, cps = 1;
-  bool cluster = true;   // K slices reduced through a cluster's shared memory (else global scratch)
 };
 
 // Split K only when the row blocks alone cannot fill the GPU; the split
@@ -90,7 +89,10 @@ struct Model {
   int kv_dim() const { return c.n_kv_heads * c.head_dim; }
 };
 
-constexpr int kMaxPlanTiles = 1024;   // split-K partial tiles the scratch holds
+// sf_linear's split-K scratch: partial tiles of 16 token rows x 128 outputs
+// (row blocks x K slices x row groups).
+constexpr int kLinearTiles = 2048;
+constexpr size_t kLinearPartBytes = (size_t)kLinearTiles * kGroupRows * kBlockRows * 4;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -118,7 +120,7 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
 }
 
 struct Layout {
-  size_t x, ssq, q, apart, gpart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, total;
+  size_t x, ssq, q, apart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, total;
   int n_kv_chunks, max_blocks;
 };
 
@@ -194,8 +196,7 @@ Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, i
   L.ssq = take((size_t)(H / 128) * kRows * 4);
   L.q = take((size_t)kRows * QD * 4);
   L.apart = take((size_t)kRows * NQ * L.n_kv_chunks * (HD + 2) * 4);
-  L.gpart = take((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
-  L.counters = take((size_t)L.max_blocks * 4);
+  L.counters = take((size_t)L.max_blocks * kMaxGroups * 4);
   L.keys = take((size_t)kRows * 8);
   L.done = take(4);
   L.zeros = take((size_t)B * 4);
@@ -240,8 +241,7 @@ struct sf_engine {
   Layout lay{};
   StateOff so{};
   bf16 *fx = nullptr, *fh = nullptr, *fo = nullptr, *fa = nullptr;
-  float *x = nullptr, *ssq = nullptr, *q = nullptr, *apart = nullptr,
-        *gpart = nullptr;
+  float *x = nullptr, *ssq = nullptr, *q = nullptr, *apart = nullptr;
   int *counters = nullptr, *done = nullptr, *zeros = nullptr;
   unsigned long long* keys = nullptr;
   SpecState st{};
@@ -251,7 +251,7 @@ struct sf_engine {
   cudaGraphExec_t g_draft = nullptr, g_verify = nullptr;
   int drafter = SF_DRAFT_NEURAL, ng_min = 2, ng_max = 4;
   std::vector<int> C;   // committed tokens per sequence (host mirror)
-  int P = 0;            // prompt length
+  std::vector<int> P;   // prompt length per sequence
   int phase = 0;        // 0: no prompt, 1: ready, 2: drafted, 3: verified
   int drafted_mode = SF_DRAFT_NEURAL;
   bool draft_stale = false;
@@ -360,9 +360,6 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   md.p_lm.nblocks = nblocks_of(c, 3);   // the persistent LM head: no K split
   md.p_lm.nsplit = 1;
   md.p_lm.cps = (H + kChunk - 1) / kChunk;
-  for (const Plan* p : {&md.p_qkv, &md.p_o, &md.p_gu, &md.p_d, &md.p_lm})
-    if (p->nsplit > 1 && p->nblocks * p->nsplit > kMaxPlanTiles)
-      return fail(SF_ERR_UNSUPPORTED, "split-K plan exceeds the scratch tiles");
   return SF_OK;
 }
 
@@ -372,9 +369,8 @@ GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& r
   a.nsplit = p.nsplit;
   a.cps = p.cps;
   a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, e->num_sms);
-  a.part = e->gpart;
   a.counter = e->counters;
-  a.cluster = p.cluster ? 1 : 0;
+  a.cluster = 1;   // the K slices of a row block are one cluster
   a.err = e->st.err;
   a.rs = rs;
   a.eps = md.c.rms_eps;
@@ -404,7 +400,10 @@ struct TokOut {
 
 // Enqueue one forward pass of `md` over the rows `rs`. With `lm` the final
 // norm + LM head + argmax run too and write tokens (and optional logits).
-sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokOut& to, cudaStream_t s) {
+// seq >= 0: every row belongs to sequence `seq` alone (its cache is addressed
+// as a batch of one; rs.pos_base then has one entry).
+sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokOut& to, cudaStream_t s,
+                  int seq = -1) {
   const sf_model_cfg& c = md.c;
   const int nf4 = c.wdtype == SF_WDTYPE_NF4 ? 1 : 0;
   const int H = c.hidden, QD = md.q_dim(), KVD = md.kv_dim();
@@ -420,11 +419,16 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.gain = md.L[0].ln1;
   ea.rs = traced(e, rs, "embed");
   CK(launch_embed(ea, s, e->pdl));
-  const size_t layer_elems = (size_t)2 * e->B * c.n_kv_heads * e->s_max * c.head_dim;
+  const size_t seq_elems = (size_t)c.n_kv_heads * e->s_max * c.head_dim;   // one sequence's keys of a layer
+  const size_t layer_elems = 2 * e->B * seq_elems;
   for (int l = 0; l < c.layers; ++l) {
     const LayerW& lw = md.L[l];
     bf16* kc = md.kv + (size_t)l * layer_elems;
     bf16* vc = kc + layer_elems / 2;
+    if (seq >= 0) {
+      kc += seq * seq_elems;
+      vc += seq * seq_elems;
+    }
     // q, k, v (+ bias, RoPE, cache append)
     GemmArgs a = base_args(e, md, md.p_qkv, rs);
     a.w[0] = lw.w[W_Q];
@@ -475,7 +479,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     t.nkv = c.n_kv_heads;
     t.hd = c.head_dim;
     t.s_max = e->s_max;
-    t.B = e->B;
+    t.B = seq >= 0 ? 1 : e->B;
     t.n_kv_chunks = e->lay.n_kv_chunks;
     t.scale = 1.0f / sqrtf((float)c.head_dim);
     t.err = e->st.err;
@@ -677,7 +681,7 @@ sf_status sync_report(sf_engine* e) {
     return fail(SF_ERR_CAPACITY, "cache capacity or token range exceeded on the device (flag %d)", err);
   }
   const int* tot = e->pin + (e->so.total - e->so.report);
-  for (int b = 0; b < e->B; ++b) e->C[b] = e->P + tot[b];
+  for (int b = 0; b < e->B; ++b) e->C[b] = e->P[b] + tot[b];
   return SF_OK;
 }
 
@@ -737,7 +741,7 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   if (!cfg_ok(tgt, &why)) return fail(SF_ERR_ARG, "target: %s", why.c_str());
   if (dft && !cfg_ok(dft, &why)) return fail(SF_ERR_ARG, "draft: %s", why.c_str());
   if (!tgt_w || (dft && !dft_w)) return fail(SF_ERR_ARG, "weight pointer array is null");
-  if (batch < 1 || K < 1 || K > 15) return fail(SF_ERR_ARG, "batch must be >= 1 and K in 1..15");
+  if (batch < 1 || batch > 32 || K < 1 || K > 15) return fail(SF_ERR_ARG, "need batch in 1..32 and K in 1..15");
   if (batch * (K + 1) > SF_MAX_ROWS || batch * 2 > SF_MAX_ROWS)
     return fail(SF_ERR_UNSUPPORTED, "batch*(K+1) = %d exceeds %d rows", batch * (K + 1), SF_MAX_ROWS);
   if (s_max < 64 || s_max % kKvChunk || s_max > 16384)
@@ -791,7 +795,6 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->fo = reinterpret_cast<bf16*>(ws + e->lay.fo);
   e->fa = reinterpret_cast<bf16*>(ws + e->lay.fa);
   e->apart = reinterpret_cast<float*>(ws + e->lay.apart);
-  e->gpart = reinterpret_cast<float*>(ws + e->lay.gpart);
   e->counters = reinterpret_cast<int*>(ws + e->lay.counters);
   e->keys = reinterpret_cast<unsigned long long*>(ws + e->lay.keys);
   e->done = reinterpret_cast<int*>(ws + e->lay.done);
@@ -857,36 +860,50 @@ void sf_destroy(sf_handle h) {
 
 sf_status sf_prefill(sf_handle h, const int32_t* h_tokens, const int32_t* h_lens, int32_t stride) {
   if (!h || !h_tokens || !h_lens) return fail(SF_ERR_ARG, "null argument");
-  const int P = h_lens[0];
-  for (int b = 0; b < h->B; ++b)
-    if (h_lens[b] != P) return fail(SF_ERR_UNSUPPORTED, "prompts of different lengths are not supported yet");
-  if (P < 2 || stride < P) return fail(SF_ERR_ARG, "prompt length must be >= 2 and <= stride");
-  if (P + h->K + 1 > h->s_max) return fail(SF_ERR_CAPACITY, "prompt of %d tokens leaves no room for a round", P);
-  for (int b = 0; b < h->B; ++b)
+  std::vector<int> lens(h_lens, h_lens + h->B);
+  bool equal = true;
+  for (int b = 0; b < h->B; ++b) {
+    const int P = lens[b];
+    if (P < 2 || stride < P) return fail(SF_ERR_ARG, "prompt %d: length must be >= 2 and <= stride", b);
+    if (P + h->K + 1 > h->s_max)
+      return fail(SF_ERR_CAPACITY, "prompt %d of %d tokens leaves no room for a round", b, P);
     for (int i = 0; i < P; ++i) {
       const int t = h_tokens[(size_t)b * stride + i];
       if (t < 0 || t >= h->tgt.c.vocab) return fail(SF_ERR_ARG, "token %d out of range at [%d][%d]", t, b, i);
     }
+    equal = equal && P == lens[0];
+  }
   for (int b = 0; b < h->B; ++b)
-    CK(cudaMemcpyAsync(h->st.hist + (size_t)b * h->s_max, h_tokens + (size_t)b * stride, P * sizeof(int),
+    CK(cudaMemcpyAsync(h->st.hist + (size_t)b * h->s_max, h_tokens + (size_t)b * stride, lens[b] * sizeof(int),
                        cudaMemcpyHostToDevice, h->user));
-  std::vector<int> lens(h->B, P);
   CK(cudaMemcpyAsync(h->st.prompt_len, lens.data(), h->B * sizeof(int), cudaMemcpyHostToDevice, h->user));
   CK(launch_reset(h->st, h->user));
-  // Fill the caches with prompt[0..P-1) in chunks of SF_MAX_ROWS rows.
-  const int cl = SF_MAX_ROWS / h->B;
+  // Fill the caches with prompt[0..P-1) in chunks of up to SF_MAX_ROWS rows:
+  // all sequences side by side when the prompts have one length, else one
+  // sequence at a time.
   for (Model* md : {&h->tgt, &h->dft}) {
     if (md == &h->dft && !h->has_dft) continue;
-    for (int start = 0; start < P - 1; start += cl) {
-      const int n = std::min(cl, P - 1 - start);
-      RowSet rs{h->st.hist, h->s_max, start, n, h->B * n, h->zeros, start};
-      sf_status r = forward(h, *md, rs, false, TokOut(), h->user);
-      if (r != SF_OK) return r;
+    if (equal) {
+      const int P = lens[0], cl = SF_MAX_ROWS / h->B;
+      for (int start = 0; start < P - 1; start += cl) {
+        const int n = std::min(cl, P - 1 - start);
+        RowSet rs{h->st.hist, h->s_max, start, n, h->B * n, h->zeros, start};
+        sf_status r = forward(h, *md, rs, false, TokOut(), h->user);
+        if (r != SF_OK) return r;
+      }
+      continue;
     }
+    for (int b = 0; b < h->B; ++b)
+      for (int start = 0; start < lens[b] - 1; start += SF_MAX_ROWS) {
+        const int n = std::min(SF_MAX_ROWS, lens[b] - 1 - start);
+        RowSet rs{h->st.hist + (size_t)b * h->s_max, h->s_max, start, n, n, h->zeros, start};
+        sf_status r = forward(h, *md, rs, false, TokOut(), h->user, b);
+        if (r != SF_OK) return r;
+      }
   }
   CK(cudaStreamSynchronize(h->user));
-  h->P = P;
-  h->C.assign(h->B, P);
+  h->P = lens;
+  h->C = lens;
   h->phase = 1;
   h->draft_stale = false;
   return SF_OK;
@@ -897,7 +914,7 @@ sf_status sf_reset(sf_handle h) {
   if (h->phase == 0) return fail(SF_ERR_STATE, "no prompt loaded");
   CK(launch_reset(h->st, h->user));
   CK(cudaStreamSynchronize(h->user));
-  h->C.assign(h->B, h->P);
+  h->C = h->P;
   h->phase = 1;
   h->draft_stale = false;
   return SF_OK;
@@ -1022,7 +1039,7 @@ sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rou
   int rounds = 0;
   for (;;) {
     int gen_min = 1 << 30;
-    for (int b = 0; b < h->B; ++b) gen_min = std::min(gen_min, h->C[b] - h->P);
+    for (int b = 0; b < h->B; ++b) gen_min = std::min(gen_min, h->C[b] - h->P[b]);
     const int remaining = n_new - gen_min;
     if (remaining <= 0) break;
     // Each round commits at most K+1 tokens, so this many rounds never
@@ -1038,8 +1055,8 @@ sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rou
   }
   if (h_out)
     for (int b = 0; b < h->B; ++b)
-      CK(cudaMemcpyAsync(h_out + (size_t)b * n_new, h->st.hist + (size_t)b * h->s_max + h->P, n_new * sizeof(int),
-                         cudaMemcpyDeviceToHost, h->user));
+      CK(cudaMemcpyAsync(h_out + (size_t)b * n_new, h->st.hist + (size_t)b * h->s_max + h->P[b],
+                         n_new * sizeof(int), cudaMemcpyDeviceToHost, h->user));
   CK(cudaStreamSynchronize(h->user));
   if (h_rounds) *h_rounds = rounds;
   return SF_OK;
@@ -1062,7 +1079,7 @@ sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist) {
 
 size_t sf_linear_workspace_bytes(int32_t N, int32_t K) {
   if (N < 1 || K < 8 || K % 8) return 0;
-  return align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4) + align256((size_t)((N + 127) / 128) * 4) +
+  return align256(kLinearPartBytes) + align256((size_t)((N + 127) / 128) * kMaxGroups * 4) +
          align256(frag_bytes(K, (kRows + 3) / 4));
 }
 
@@ -1092,12 +1109,14 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const Plan p = make_plan((N + 127) / 128, K, 2 * sms, 1 << 30);
-  if (p.nsplit > 1 && p.nblocks * p.nsplit > kMaxPlanTiles) return fail(SF_ERR_UNSUPPORTED, "plan too large");
+  const int groups = (M + kGroupRows - 1) / kGroupRows;
+  if (p.nsplit > 1 && p.nblocks * p.nsplit * groups > kLinearTiles)
+    return fail(SF_ERR_UNSUPPORTED, "plan too large");
   CK(gemm_init());
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
-  const size_t part_bytes = align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4);
+  const size_t part_bytes = align256(kLinearPartBytes);
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * 4, st));
+  if (p.nsplit > 1) CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * groups * 4, st));   // arrival counters
   GemmArgs a{};
   CK(make_weight_map(&a.tm[0], d_w, N, K, ld));
   a.w[0] = d_w;
@@ -1131,7 +1150,7 @@ sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const flo
     return fail(SF_ERR_ARG, "W and x must be 16-byte aligned, the workspace 256-byte aligned");
   // x -> fragment order in the workspace's last region, then the GEMM.
   unsigned char* ws = static_cast<unsigned char*>(d_workspace);
-  void* xf = ws + align256((size_t)kMaxPlanTiles * kRows * kBlockRows * 4) + align256((size_t)((N + 127) / 128) * 4);
+  void* xf = ws + align256(kLinearPartBytes) + align256((size_t)((N + 127) / 128) * kMaxGroups * 4);
   sf_status r = sf_to_frag(d_x, M, K, K, xf, cuda_stream);
   if (r != SF_OK) return r;
   return sf_linear_frag(d_w, N, K, ld, xf, M, d_y, d_workspace, cuda_stream);

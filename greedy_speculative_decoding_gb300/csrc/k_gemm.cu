@@ -1,8 +1,12 @@
 // Skinny bf16 GEMM for decode (1-2 rows) and verify (K+1 rows) on sm_103a.
 //
 // The work is weight streaming: y[m][n] = sum_k a[m][k] W[n][k] with at most
-// SF_MAX_ROWS token rows m, so every weight byte is read once and used by all
-// rows. Each CTA owns 128 output rows (8 warps x 16) and one slice of K.
+// 16 token rows m per CTA, so every weight byte is read once and used by all
+// rows. Each CTA owns 128 output rows (8 warps x 16) and one slice of K. A
+// launch of more rows (up to SF_MAX_ROWS) runs one CTA per 16-row group,
+// neighbours in launch order: the first to ask for a weight tile brings it
+// from HBM, the others find it in L2 (normal eviction priority instead of
+// evict-first).
 // Every warp runs its own TMA pipeline: a ring of kStages shared-memory
 // tiles (16 weight rows x 64 k, 128-byte swizzle) filled by
 // cp.async.bulk.tensor loads that complete on per-stage mbarriers, so about
@@ -35,12 +39,15 @@
 // adds them in slice order. Either way results are deterministic without
 // float atomics.
 #include <algorithm>
+#include <mutex>
 
 #include "sf_kernels.h"
 
 namespace sf {
 
 namespace {
+
+constexpr int kMaxDevices = 64;
 
 constexpr uint32_t kWaitIters = 1u << 24;
 constexpr int kScaleTileBytes = 16 * 8 * 2;   // NF4: 16 rows x 8 block scales (fp16)
@@ -61,16 +68,35 @@ __device__ __forceinline__ int warp_tile_row(const GemmArgs& a, int rb, int w, i
   return n - (s ? a.seg_end[s - 1] : 0) + 16 * w;
 }
 
-// B operand of chunk j (absolute) for this lane: per token tile, the two
-// 16-byte units of halves h = 0, 1.
+// B operand of chunk j for this lane: per token tile, the two 16-byte units
+// of halves h = 0, 1. Chunks are `stride` units apart; tiles t >= tl (past
+// the last token tile of the layout, in the last row group) read as zero.
 template <int T>
-__device__ __forceinline__ void load_b(uint4 (&b)[T][2], const uint4* in, int j, int lane) {
-  const uint4* p = in + (size_t)j * (T * 64) + lane;
+__device__ __forceinline__ void load_b(uint4 (&b)[T][2], const uint4* in, size_t stride, int j, int tl, int lane) {
+  const uint4* p = in + (size_t)j * stride + lane;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    b[t][0] = p[(2 * t) * 32];
-    b[t][1] = p[(2 * t + 1) * 32];
+    if (t < tl) {
+      b[t][0] = p[(2 * t) * 32];
+      b[t][1] = p[(2 * t + 1) * 32];
+    } else {
+      b[t][0] = b[t][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
+}
+
+// Copy the B operand of chunks [c0, c0 + nch) of this CTA's token tiles into
+// shared memory (T tiles per chunk, contiguous); tiles t >= tl become zero.
+template <int T>
+__device__ __forceinline__ void stage_b_copy(uint4* dst, const uint4* src, size_t stride, int nch, int tl) {
+  for (int i = threadIdx.x; i < nch * T * 64; i += kGemmThreads) {
+    const int ci = i / (T * 64), r = i - ci * (T * 64);
+    if (r / 64 < tl) cp_async16(dst + i, src + (size_t)ci * stride + r);
+    else dst[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
 }
 
 template <int T>
@@ -103,15 +129,17 @@ struct EpiPre {
   float2 cs[kE];
 };
 
+// Rows m < M of the CTA are token rows m0 + m of the forward.
 template <int T, int EPI>
-__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, EpiPre<T>& pre, const int* pos) {
+__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, int M, EpiPre<T>& pre,
+                                             const int* pos) {
   constexpr int kE = EpiPre<T>::kE;
   if (EPI == EPI_RESID) {
 #pragma unroll
     for (int e = 0; e < kE; ++e) {
       const int i = threadIdx.x + e * kGemmThreads;
       const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
-      pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)m * a.out_ld + n] : 0.f;
+      pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)(m0 + m) * a.out_ld + n] : 0.f;
       pre.v1[e] = (a.frag_gain && n < a.N) ? __bfloat162float(a.frag_gain[n]) : 0.f;
     }
   } else if (EPI == EPI_QKV) {
@@ -140,7 +168,7 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int M, E
 }
 
 template <int T>
-__device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M, const EpiPre<T>& pre) {
+__device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int m0, int M, int Tt, const EpiPre<T>& pre) {
   constexpr int kE = EpiPre<T>::kE;
 #pragma unroll
   for (int e = 0; e < kE; ++e) {
@@ -150,8 +178,8 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M, const Epi
     float v = 0.f;
     if (n < a.N) {
       v = pre.v0[e] + ys[i];
-      a.out[(size_t)m * a.out_ld + n] = v;
-      if (a.frag_out) frag_store(a.frag_out, m, n, T, v * pre.v1[e]);
+      a.out[(size_t)(m0 + m) * a.out_ld + n] = v;
+      if (a.frag_out) frag_store(a.frag_out, m0 + m, n, Tt, v * pre.v1[e]);
     }
     ys[i] = v;
   }
@@ -165,12 +193,13 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int M, const Epi
       s = fmaf(v, v, s);
     }
     s = warp_sum(s);
-    if (lane == 0) a.ssq_out[rb * kRows + m] = s;
+    if (lane == 0) a.ssq_out[rb * kRows + m0 + m] = s;
   }
 }
 
 template <int T>
-__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const EpiPre<T>& pre, const int* spos) {
+__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int m0, int M, const EpiPre<T>& pre,
+                        const int* spos) {
   constexpr int kE = EpiPre<T>::kE;
   const int half = a.hd >> 1;
   const int n0 = rb * kBlockRows;
@@ -183,7 +212,7 @@ __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const
     if (m >= M || n0 + r >= a.N) continue;
     const int local = n0 + r - seg0;
     const int d = local % a.hd;
-    const int b = m / a.rs.rps;
+    const int b = (m0 + m) / a.rs.rps;
     const int pos = spos[m];
     if (s == 2) {
       const int kvh = local / a.hd;
@@ -197,7 +226,7 @@ __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const
     const float y1 = x1 * cs.x - x2 * cs.y;
     const float y2 = x2 * cs.x + x1 * cs.y;
     if (s == 0) {
-      float* q = a.out + (size_t)m * a.out_ld + local;
+      float* q = a.out + (size_t)(m0 + m) * a.out_ld + local;
       q[0] = y1;
       q[half] = y2;
     } else {
@@ -209,32 +238,33 @@ __device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int M, const
   }
 }
 
-template <int T>
-__device__ void epi_swiglu(const GemmArgs& a, const float* ys, int rb, int M) {
+__device__ void epi_swiglu(const GemmArgs& a, const float* ys, int rb, int m0, int M, int Tt) {
   for (int i = threadIdx.x; i < M * 64; i += kGemmThreads) {
     const int m = i >> 6, j = i & 63;
     const int f = rb * 64 + j;
     if (f >= a.N) continue;
     const float gte = ys[m * kBlockRows + j];
     const float up = ys[m * kBlockRows + 64 + j];
-    frag_store(a.frag_out, m, f, T, gte / (1.0f + expf(-gte)) * up);
+    frag_store(a.frag_out, m0 + m, f, Tt, gte / (1.0f + expf(-gte)) * up);
   }
 }
 
-__device__ void epi_store(const GemmArgs& a, const float* ys, int rb, int M) {
+__device__ void epi_store(const GemmArgs& a, const float* ys, int rb, int m0, int M) {
   for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
     const int m = i / kBlockRows, r = i - m * kBlockRows;
     const int n = rb * kBlockRows + r;
-    if (n < a.N) a.out[(size_t)m * a.out_ld + n] = ys[i];
+    if (n < a.N) a.out[(size_t)(m0 + m) * a.out_ld + n] = ys[i];
   }
 }
 
-__device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, int* s_flag) {
+// `finishers`: CTAs that run this epilogue in the launch (row blocks x row
+// groups); the last to arrive writes the tokens of all rows of the forward.
+__device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int m0, int M, int finishers, int* s_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int m = warp; m < M; m += kGemmThreads / 32) {
     unsigned long long best = 0ull;
     bool bad = false;
-    const int mb = m / a.rs.rps, mj = m - mb * a.rs.rps;
+    const int mb = (m0 + m) / a.rs.rps, mj = (m0 + m) - mb * a.rs.rps;
     const int lg_row = mj >= a.tok_skip ? mb * a.lg_stride + a.lg_off + mj - a.tok_skip : -1;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -250,15 +280,15 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, in
     }
     best = shfl_max_u64(best);
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, kErrNonfinite);
-    if (lane == 0) atomicMax(a.keys + m, best);
+    if (lane == 0) atomicMax(a.keys + m0 + m, best);
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.done, 1) == a.nblocks - 1);
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.done, 1) == finishers - 1);
   __syncthreads();
   if (!*s_flag) return;
   __threadfence();
-  if (threadIdx.x < M) {
+  if (threadIdx.x < a.rs.M) {
     const int m = threadIdx.x;
     const unsigned long long k = atomicExch(a.keys + m, 0ull);
     const int b = m / a.rs.rps, j = m - b * a.rs.rps;
@@ -269,7 +299,9 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int M, in
 
 }  // namespace
 
-template <int T, int EPI, bool NF4>
+// GRP: the launch has more than 16 token rows (T = 4, one CTA per row group);
+// without it the row-group arithmetic folds away at compile time.
+template <int T, int EPI, bool NF4, bool GRP>
 __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_QKV) ? 2 : 1)) k_gemm(const __grid_constant__ GemmArgs a) {
   extern __shared__ unsigned char smem_raw[];
   // The swizzled TMA tiles need a 1024-byte aligned base.
@@ -286,7 +318,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   const int sb = a.stage_b ? staged_b_bytes(T, a.cps) : 0;             // staged B operand bytes
   float* recv = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(bstage) + sb);   // push landing area
   __shared__ int s_flag;
-  __shared__ int s_pos[kRows];
+  __shared__ int s_pos[kGroupRows];
   __shared__ __align__(8) uint64_t recv_bar;   // push: the other ranks' tiles have landed
   // NF4: byte (two codes) -> bf16 pair of levels, one copy of the 256-entry
   // table per lane (entry b of lane l at 32 b + l: every lookup of a warp
@@ -296,7 +328,17 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int rb = blockIdx.x / a.nsplit, sp = blockIdx.x - rb * a.nsplit;
+  // Block = (row block rb, token row group gi, K slice sp). The slices of one
+  // (rb, gi) are consecutive (one cluster), and the row groups of a row block
+  // are neighbours in launch order, so they read its weight tiles at about
+  // the same time: from HBM once, then from L2.
+  const int G = GRP ? (a.rs.M + kGroupRows - 1) / kGroupRows : 1;
+  const int Tt = GRP ? (a.rs.M + 3) / 4 : T;        // token tiles of the fragment layout
+  const int qb = blockIdx.x / a.nsplit, sp = blockIdx.x - qb * a.nsplit;
+  const int rb = GRP ? qb / G : qb, gi = GRP ? qb - rb * G : 0;
+  const int m0 = gi * kGroupRows;
+  const int M = GRP ? min(kGroupRows, a.rs.M - m0) : a.rs.M;   // token rows of this CTA
+  const int tl = GRP ? min(T, Tt - 4 * gi) : T;     // token tiles present in this group
   const int nch_total = (a.K + kChunk - 1) / kChunk;
   const int c0 = sp * a.cps;
   const int nch = min(a.cps, nch_total - c0);
@@ -312,15 +354,16 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   // 128 bytes of codes) plus the 8-block scale group that holds them.
   const int per_stage = NF4 ? 4 : 1;
   const int nst = (nch + per_stage - 1) / per_stage;
+  const uint64_t pol = GRP ? policy_evict_normal() : policy_evict_first();
   auto issue = [&](int s, int st) {
     if (NF4) {
       const int cabs = c0 + 4 * st;
       mbar_expect_tx(&my_bar[s], kTileBytes + kScaleTileBytes);
-      tma_load_2d(my_ring + s * kTileBytes, map, cabs * (kChunk / 2), trow, &my_bar[s], policy_evict_first());
-      tma_load_2d(my_sring + s * kScaleTileBytes, smap, (cabs / 8) * 8, trow, &my_bar[s], policy_evict_first());
+      tma_load_2d(my_ring + s * kTileBytes, map, cabs * (kChunk / 2), trow, &my_bar[s], pol);
+      tma_load_2d(my_sring + s * kScaleTileBytes, smap, (cabs / 8) * 8, trow, &my_bar[s], pol);
     } else {
       mbar_expect_tx(&my_bar[s], kTileBytes);
-      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + st) * kChunk, trow, &my_bar[s], policy_evict_first());
+      tma_load_2d(my_ring + s * kTileBytes, map, (c0 + st) * kChunk, trow, &my_bar[s], pol);
     }
   };
   if (lane == 0) {
@@ -340,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   // the sequence lengths are written only by the acceptance and reset
   // kernels and by host copies, never by the kernel that directly precedes a
   // projection (the only one that can still be running at this point).
-  if (EPI == EPI_QKV && tid < a.rs.M) s_pos[tid] = row_pos(a.rs, tid);
+  if (EPI == EPI_QKV && tid < M) s_pos[tid] = row_pos(a.rs, m0 + tid);
   if (a.push) {
     // Rank 0's landing barrier expects every other rank's tile; the cluster
     // barrier that starts here (and is waited on only after the main loop)
@@ -348,7 +391,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
     if (cluster_rank() == 0 && tid == 0) {
       mbar_init(&recv_bar, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      mbar_expect_tx(&recv_bar, (uint32_t)push_bytes(a.nsplit, a.rs.M));
+      mbar_expect_tx(&recv_bar, (uint32_t)push_bytes(a.nsplit, M));
     }
     __syncthreads();
     cluster_arrive();
@@ -359,7 +402,6 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   pdl_wait();
   trace_mark(a.rs, 1);
   pdl_launch_next();
-  const int M = a.rs.M;
   // The CTAs that run the epilogue: all of them, except that in a cluster
   // split only rank 0 does.
   const bool finisher = !(a.cluster && a.nsplit > 1) || cluster_rank() == 0;
@@ -368,29 +410,27 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   // flight together; the sums are only needed after the main loop.
   // B operand source: global memory, or this CTA's chunks staged in shared
   // memory (short K slices: one copy instead of a global round trip per chunk).
-  const uint4* bsrc = a.in;
-  int jb = 0;   // chunk index of bsrc[0]
+  const uint4* bsrc = a.in + (size_t)(4 * gi) * 64;   // this group's first token tile
+  size_t bstride = (size_t)Tt * 64;                    // 16-byte units per chunk
+  int jb = 0;                                          // chunk index of bsrc[0]
   if (sb && nch > 0) {
-    const uint4* src = a.in + (size_t)c0 * (T * 64);
-    for (int i = tid; i < nch * T * 64; i += kGemmThreads) cp_async16(bstage + i, src + i);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
+    stage_b_copy<T>(bstage, bsrc + (size_t)c0 * bstride, bstride, nch, tl);
     bsrc = bstage;
+    bstride = (size_t)T * 64;
     jb = c0;
   }
   uint4 bq[T][2];
-  if (nch > 0) load_b<T>(bq, bsrc, c0 - jb, lane);
+  if (nch > 0) load_b<T>(bq, bsrc, bstride, c0 - jb, tl, lane);
   EpiPre<T> pre;
-  if (finisher) epi_prefetch<T, EPI>(a, rb, M, pre, s_pos);
+  if (finisher) epi_prefetch<T, EPI>(a, rb, m0, M, pre, s_pos);
   float ssq_part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   if (a.ssq && finisher) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int m = warp + 8 * j;
       if (m < M) {
-        ssq_part[j][0] = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
-        ssq_part[j][1] = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
+        ssq_part[j][0] = lane < a.nssq ? a.ssq[lane * kRows + m0 + m] : 0.f;
+        ssq_part[j][1] = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m0 + m] : 0.f;
       }
     }
   }
@@ -411,7 +451,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
     const unsigned char* tile = my_ring + s * kTileBytes;
     if (!NF4) {
       uint4 bn[T][2];
-      if (st + 1 < nch) load_b<T>(bn, bsrc, c0 + st + 1 - jb, lane);
+      if (st + 1 < nch) load_b<T>(bn, bsrc, bstride, c0 + st + 1 - jb, tl, lane);
       uint4 w[4];
       w[0] = *reinterpret_cast<const uint4*>(tile + off_lo);
       w[1] = *reinterpret_cast<const uint4*>(tile + off_hi);
@@ -437,7 +477,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
         const int ch = 4 * st + q;
         if (ch >= nch) break;
         uint4 bn[T][2];
-        if (ch + 1 < nch) load_b<T>(bn, bsrc, c0 + ch + 1 - jb, lane);
+        if (ch + 1 < nch) load_b<T>(bn, bsrc, bstride, c0 + ch + 1 - jb, tl, lane);
         // 8 code bytes (k = 16c .. 16c+15 of this chunk) of rows g and g+8,
         // at their 128-byte-swizzled positions; the scale of each row.
         const int cofs = ((((2 * q + (c >> 1)) ^ sw) << 4) + 8 * (c & 1));
@@ -590,17 +630,17 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
     cluster_arrive_relaxed();
     __syncthreads();
   } else if (a.nsplit > 1) {
-    float* mine = a.part + ((size_t)rb * a.nsplit + sp) * (kRows * kBlockRows);
+    float* mine = a.part + ((size_t)qb * a.nsplit + sp) * (kGroupRows * kBlockRows);
     for (int i = tid; i < M * kBlockRows; i += kGemmThreads) __stcg(mine + i, ys[i]);
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_flag = (atomicAdd(a.counter + rb, 1) == a.nsplit - 1);
+    if (tid == 0) s_flag = (atomicAdd(a.counter + qb, 1) == a.nsplit - 1);
     __syncthreads();
     if (!s_flag) return;
     __threadfence();
     // Sum the slices in fixed order 0, 1, ..., loading four slices' worth of
     // this thread's elements at a time so the loads overlap.
-    const float* src = a.part + (size_t)rb * a.nsplit * (kRows * kBlockRows);
+    const float* src = a.part + (size_t)qb * a.nsplit * (kGroupRows * kBlockRows);
     constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
     float sum[kE];
 #pragma unroll
@@ -613,7 +653,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
         for (int e = 0; e < kE; ++e) {
           const int i = tid + e * kGemmThreads;
           v[q][e] = (p0 + q < a.nsplit && i < M * kBlockRows)
-                        ? __ldcg(src + (size_t)(p0 + q) * (kRows * kBlockRows) + i)
+                        ? __ldcg(src + (size_t)(p0 + q) * (kGroupRows * kBlockRows) + i)
                         : 0.f;
         }
 #pragma unroll
@@ -626,7 +666,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
       const int i = tid + e * kGemmThreads;
       if (i < M * kBlockRows) ys[i] = a.ssq ? sum[e] * rinv[i / kBlockRows] : sum[e];
     }
-    if (tid == 0) a.counter[rb] = 0;
+    if (tid == 0) a.counter[qb] = 0;
     __syncthreads();
   }
 
@@ -635,11 +675,11 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
     for (int i = tid; i < M * kBlockRows; i += kGemmThreads) ys[i] *= rinv[i / kBlockRows];
     __syncthreads();
   }
-  if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, M, pre);
-  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, M, pre, s_pos);
-  else if (EPI == EPI_SWIGLU) epi_swiglu<T>(a, ys, rb, M);
-  else if (EPI == EPI_STORE) epi_store(a, ys, rb, M);
-  else epi_argmax(a, ys, rb, M, &s_flag);
+  if (EPI == EPI_RESID) epi_resid<T>(a, ys, rb, m0, M, Tt, pre);
+  else if (EPI == EPI_QKV) epi_qkv<T>(a, ys, rb, m0, M, pre, s_pos);
+  else if (EPI == EPI_SWIGLU) epi_swiglu(a, ys, rb, m0, M, Tt);
+  else if (EPI == EPI_STORE) epi_store(a, ys, rb, m0, M);
+  else epi_argmax(a, ys, rb, m0, M, a.nblocks * G, &s_flag);
   if (a.nsplit > 1 && a.cluster && !a.push) cluster_wait();
 }
 
@@ -652,7 +692,10 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
 // in shared memory and is merged into the global keys once per CTA. The
 // per-row arithmetic is that of k_gemm with one K slice (same chunk order,
 // same MMA sequence, same 1 / rms scaling), so logits are bit-identical.
-template <int T>
+// A forward of more than 16 token rows runs one set of CTAs per 16-row group,
+// interleaved in launch order (CTA i of every group side by side), so the
+// groups walk the same row blocks together and share them through L2.
+template <int T, bool GRP>
 __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const __grid_constant__ GemmArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -662,59 +705,63 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
   float* rinv = ys + 4 * T * kBlockRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(rinv + 4 * T);            // [8][kStages]
   uint4* bstage = reinterpret_cast<uint4*>(bars + 8 * kStages);          // staged B operand (if any)
-  __shared__ unsigned long long s_best[kRows];
+  __shared__ unsigned long long s_best[kGroupRows];
   __shared__ int s_flag;
   trace_mark(a.rs, 0);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int nch = (a.K + kChunk - 1) / kChunk;
-  const int G = gridDim.x;
-  const int nmine = (a.nblocks - (int)blockIdx.x + G - 1) / G;   // launch: G <= nblocks
+  const int G = GRP ? (a.rs.M + kGroupRows - 1) / kGroupRows : 1;   // token row groups
+  const int Tt = GRP ? (a.rs.M + 3) / 4 : T;                     // token tiles of the fragment layout
+  const int cta = GRP ? blockIdx.x / G : blockIdx.x, gi = GRP ? blockIdx.x - cta * G : 0;
+  const int m0 = gi * kGroupRows;
+  const int M = GRP ? min(kGroupRows, a.rs.M - m0) : a.rs.M;     // token rows of this CTA
+  const int tl = GRP ? min(T, Tt - 4 * gi) : T;
+  const int nc = GRP ? gridDim.x / G : gridDim.x;                // CTAs per group (launch: <= nblocks)
+  const int nmine = (a.nblocks - cta + nc - 1) / nc;
   const long total = (long)nmine * nch;                             // this warp's tiles, all blocks
   unsigned char* my_ring = ring + warp * kStages * kTileBytes;
   uint64_t* my_bar = bars + warp * kStages;
+  const uint64_t pol = GRP ? policy_evict_normal() : policy_evict_first();
   auto issue = [&](int s, long q) {
     const int i = (int)(q / nch), j = (int)(q - (long)i * nch);
-    const int rb = blockIdx.x + i * G;
+    const int rb = cta + i * nc;
     mbar_expect_tx(&my_bar[s], kTileBytes);
-    tma_load_2d(my_ring + s * kTileBytes, &a.tm[0], j * kChunk, rb * kBlockRows + 16 * warp, &my_bar[s],
-                policy_evict_first());
+    tma_load_2d(my_ring + s * kTileBytes, &a.tm[0], j * kChunk, rb * kBlockRows + 16 * warp, &my_bar[s], pol);
   };
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&my_bar[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int s = 0; s < kStages && s < total; ++s) issue(s, s);   // weights: before the wait
   }
-  if (tid < kRows) s_best[tid] = 0ull;
+  if (tid < kGroupRows) s_best[tid] = 0ull;
   __syncthreads();
 
   pdl_wait();
   trace_mark(a.rs, 1);
   pdl_launch_next();
-  const int M = a.rs.M;
   float ssq_part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   if (a.ssq) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int m = warp + 8 * j;
       if (m < M) {
-        ssq_part[j][0] = lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f;
-        ssq_part[j][1] = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f;
+        ssq_part[j][0] = lane < a.nssq ? a.ssq[lane * kRows + m0 + m] : 0.f;
+        ssq_part[j][1] = lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m0 + m] : 0.f;
       }
     }
   }
   // The B operand is the same for every block: staged once when it is small.
-  const uint4* bsrc = a.in;
+  const uint4* bsrc = a.in + (size_t)(4 * gi) * 64;
+  size_t bstride = (size_t)Tt * 64;
   if (staged_b_bytes(T, nch)) {
-    for (int i = tid; i < nch * T * 64; i += kGemmThreads) cp_async16(bstage + i, a.in + i);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
+    stage_b_copy<T>(bstage, bsrc, bstride, nch, tl);
     bsrc = bstage;
+    bstride = (size_t)T * 64;
   }
   uint4 bq[T][2];
-  load_b<T>(bq, bsrc, 0, lane);
+  load_b<T>(bq, bsrc, bstride, 0, tl, lane);
 
   const int sw = g & 7;
   const int off_lo = g * 128 + (((2 * c) ^ sw) << 4);
@@ -722,7 +769,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
   bool timed_out = false;
   long q = 0;
   for (int i = 0; i < nmine; ++i) {
-    const int rb = blockIdx.x + i * G;
+    const int rb = cta + i * nc;
     float acc[T][4];
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -730,7 +777,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
       const int s = (int)(q % kStages);
       const bool more = j + 1 < nch || i + 1 < nmine;
       uint4 bn[T][2];
-      if (more) load_b<T>(bn, bsrc, j + 1 < nch ? j + 1 : 0, lane);
+      if (more) load_b<T>(bn, bsrc, bstride, j + 1 < nch ? j + 1 : 0, tl, lane);
       if (!mbar_wait(&my_bar[s], (uint32_t)((q / kStages) & 1), kWaitIters)) timed_out = true;
       const unsigned char* tile = my_ring + s * kTileBytes;
       uint4 w[4];
@@ -773,7 +820,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
     for (int m = warp; m < M; m += kGemmThreads / 32) {
       unsigned long long best = 0ull;
       bool bad = false;
-      const int mb = m / a.rs.rps, mj = m - mb * a.rs.rps;
+      const int mb = (m0 + m) / a.rs.rps, mj = (m0 + m) - mb * a.rs.rps;
       const int lg_row = mj >= a.tok_skip ? mb * a.lg_stride + a.lg_off + mj - a.tok_skip : -1;
       const float sc = a.ssq ? rinv[m] : 1.f;
 #pragma unroll
@@ -801,14 +848,14 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
   }
   // Merge the CTA's bests; the last CTA to arrive writes the tokens and
   // leaves the keys and the counter at zero for the next launch.
-  if (tid < M) atomicMax(a.keys + tid, s_best[tid]);
+  if (tid < M) atomicMax(a.keys + m0 + tid, s_best[tid]);
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_flag = (atomicAdd(a.done, 1) == G - 1);
+  if (tid == 0) s_flag = (atomicAdd(a.done, 1) == (int)gridDim.x - 1);
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
-  if (tid < M) {
+  if (tid < a.rs.M) {
     const int m = tid;
     const unsigned long long k = atomicExch(a.keys + m, 0ull);
     const int b = m / a.rs.rps, j = m - b * a.rs.rps;
@@ -818,7 +865,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
 }
 
 int gemm_smem_bytes(int M, int stages, bool nf4, int cps, int push) {
-  const int T = (M + 3) / 4;
+  const int T = (std::min(M, kGroupRows) + 3) / 4;   // token tiles of one row group
   return 1024 /* alignment slack */ + 8 * stages * (kTileBytes + (nf4 ? kScaleTileBytes : 0)) +
          4 * T * kBlockRows * 4 + 4 * T * 4 + 8 * stages * 8 + staged_b_bytes(T, cps) + push;
 }
@@ -867,13 +914,14 @@ cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const 
                    8, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int T, int EPI, bool NF4>
+template <int T, int EPI, bool NF4, bool GRP>
 static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
+  const int G = (a.rs.M + kGroupRows - 1) / kGroupRows;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.nblocks * a.nsplit);
+  cfg.gridDim = dim3(a.nblocks * a.nsplit * G);
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes =
-      gemm_smem_bytes(4 * T, a.stages, NF4, a.stage_b ? a.cps : 0, a.push ? push_bytes(a.nsplit, a.rs.M) : 0);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(4 * T, a.stages, NF4, a.stage_b ? a.cps : 0,
+                                         a.push ? push_bytes(a.nsplit, std::min(a.rs.M, kGroupRows)) : 0);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -891,30 +939,30 @@ static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st, bool pdl) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, k_gemm<T, EPI, NF4>, a);
+  return cudaLaunchKernelEx(&cfg, k_gemm<T, EPI, NF4, GRP>, a);
 }
 
-template <int T, int EPI, bool NF4>
+template <int T, int EPI, bool NF4, bool GRP>
 static cudaError_t init_one() {
   const int smem = gemm_smem_bytes(4 * T, NF4 ? kMaxStagesNF4 : kMaxStages, NF4, 0, kMaxPushBytes) + kMaxStagedB;
-  cudaError_t e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // Every kernel of the chain asks for the largest shared-memory carve-out,
   // so an SM running one of them can take the next kernel's CTAs early
   // (programmatic dependent launch) without first changing its L1 / shared split.
-  e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(k_gemm<T, EPI, NF4, GRP>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_gemm<T, EPI, NF4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(k_gemm<T, EPI, NF4, GRP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int T, bool NF4>
+template <int T, bool NF4, bool GRP = false>
 static cudaError_t init_t() {
   cudaError_t e;
-  if ((e = init_one<T, EPI_QKV, NF4>()) || (e = init_one<T, EPI_RESID, NF4>()) ||
-      (e = init_one<T, EPI_SWIGLU, NF4>()) || (e = init_one<T, EPI_STORE, NF4>()))
+  if ((e = init_one<T, EPI_QKV, NF4, GRP>()) || (e = init_one<T, EPI_RESID, NF4, GRP>()) ||
+      (e = init_one<T, EPI_SWIGLU, NF4, GRP>()) || (e = init_one<T, EPI_STORE, NF4, GRP>()))
     return e;
-  return init_one<T, EPI_ARGMAX, NF4>();
+  return init_one<T, EPI_ARGMAX, NF4, GRP>();
 }
 
 // Largest number of clusters of `csize` CTAs that can be resident at once
@@ -935,36 +983,56 @@ int gemm_max_clusters(int csize, int M, int stages, int cps) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  return cudaOccupancyMaxActiveClusters(&n, k_gemm<3, EPI_QKV, false>, &cfg) == cudaSuccess ? n : 0;
+  return cudaOccupancyMaxActiveClusters(&n, k_gemm<3, EPI_QKV, false, false>, &cfg) == cudaSuccess ? n : 0;
 }
 
-template <int T>
+template <int T, bool GRP = false>
 static cudaError_t init_lm() {
   const int smem = gemm_smem_bytes(4 * T, kMaxStages, false, 0) + kMaxStagedB;
-  cudaError_t e = cudaFuncSetAttribute(k_lmhead<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(k_lmhead<T, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_lmhead<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  return cudaFuncSetAttribute(k_lmhead<T, GRP>, cudaFuncAttributePreferredSharedMemoryCarveout,
                               cudaSharedmemCarveoutMaxShared);
 }
 
 // Raise the dynamic shared-memory limit of every instantiation (current device).
-cudaError_t gemm_init() {
+static cudaError_t gemm_init_all() {
   cudaError_t e;
-  if ((e = init_lm<1>()) || (e = init_lm<2>()) || (e = init_lm<3>()) || (e = init_lm<4>())) return e;
+  if ((e = init_lm<1>()) || (e = init_lm<2>()) || (e = init_lm<3>()) || (e = init_lm<4>()) ||
+      (e = init_lm<4, true>()))
+    return e;
   if ((e = init_t<1, false>()) || (e = init_t<2, false>()) || (e = init_t<3, false>()) ||
       (e = init_t<4, false>()) || (e = init_t<1, true>()) || (e = init_t<2, true>()) ||
-      (e = init_t<3, true>()) || (e = init_t<4, true>()))
+      (e = init_t<3, true>()) || (e = init_t<4, true>()) || (e = init_t<4, false, true>()) ||
+      (e = init_t<4, true, true>()))
     return e;
+  return cudaSuccess;
+}
+
+// Once per device (the attributes persist for the process): about 130
+// attribute calls, too slow to repeat before every sf_linear launch.
+cudaError_t gemm_init() {
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return gemm_init_all();
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev]) return cudaSuccess;
+  if ((e = gemm_init_all()) != cudaSuccess) return e;
+  done[dev] = true;
   return cudaSuccess;
 }
 
 template <int EPI, bool NF4>
 static cudaError_t launch_e(const GemmArgs& a, cudaStream_t st, bool pdl) {
+  if (a.rs.M > kGroupRows) return launch_t<4, EPI, NF4, true>(a, st, pdl);
   switch ((a.rs.M + 3) / 4) {
-    case 1: return launch_t<1, EPI, NF4>(a, st, pdl);
-    case 2: return launch_t<2, EPI, NF4>(a, st, pdl);
-    case 3: return launch_t<3, EPI, NF4>(a, st, pdl);
-    case 4: return launch_t<4, EPI, NF4>(a, st, pdl);
+    case 1: return launch_t<1, EPI, NF4, false>(a, st, pdl);
+    case 2: return launch_t<2, EPI, NF4, false>(a, st, pdl);
+    case 3: return launch_t<3, EPI, NF4, false>(a, st, pdl);
+    case 4: return launch_t<4, EPI, NF4, false>(a, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1015,7 +1083,8 @@ cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cuda
   return cudaGetLastError();
 }
 
-template <int T>
+// ctas: CTAs of the whole launch (per row group x row groups).
+template <int T, bool GRP>
 static cudaError_t launch_lm_t(const GemmArgs& a, int ctas, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
@@ -1027,18 +1096,20 @@ static cudaError_t launch_lm_t(const GemmArgs& a, int ctas, cudaStream_t st, boo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_lmhead<T>, a);
+  return cudaLaunchKernelEx(&cfg, k_lmhead<T, GRP>, a);
 }
 
 cudaError_t launch_lmhead(const GemmArgs& a, int num_sms, cudaStream_t st, bool pdl) {
-  const int T = (a.rs.M + 3) / 4;
+  const int T = (std::min(a.rs.M, kGroupRows) + 3) / 4;
+  const int G = (a.rs.M + kGroupRows - 1) / kGroupRows;
   if (a.rs.M < 1 || a.rs.M > kRows || a.nf4 || a.stages < 2 || a.stages > kMaxStages) return cudaErrorInvalidValue;
-  const int ctas = std::max(1, std::min(a.nblocks, (T <= 3 ? 2 : 1) * num_sms));
+  const int ctas = G * std::max(1, std::min(a.nblocks, (T <= 3 ? 2 : 1) * num_sms / G));
+  if (G > 1) return launch_lm_t<4, true>(a, ctas, st, pdl);
   switch (T) {
-    case 1: return launch_lm_t<1>(a, ctas, st, pdl);
-    case 2: return launch_lm_t<2>(a, ctas, st, pdl);
-    case 3: return launch_lm_t<3>(a, ctas, st, pdl);
-    default: return launch_lm_t<4>(a, ctas, st, pdl);
+    case 1: return launch_lm_t<1, false>(a, ctas, st, pdl);
+    case 2: return launch_lm_t<2, false>(a, ctas, st, pdl);
+    case 3: return launch_lm_t<3, false>(a, ctas, st, pdl);
+    default: return launch_lm_t<4, false>(a, ctas, st, pdl);
   }
 }
 
@@ -1053,9 +1124,10 @@ cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
   // Staging the B operand and the landing area compete for that space; the
   // push reduction wins when both do not fit.
   GemmArgs b = a;
-  const int pb = push_bytes(a.nsplit, a.rs.M);
+  const int mg = std::min(a.rs.M, kGroupRows);   // token rows of one CTA
+  const int pb = push_bytes(a.nsplit, mg);
   const bool split = a.cluster && a.nsplit > 1 && pb <= kMaxPushBytes;
-  b.stage_b = staged_b_bytes((a.rs.M + 3) / 4, a.cps) > 0;
+  b.stage_b = staged_b_bytes((mg + 3) / 4, a.cps) > 0;
   b.push = split && gemm_smem_bytes(a.rs.M, a.stages, a.nf4, a.cps, pb) <= kHalfSmBytes;
   if (split && !b.push && gemm_smem_bytes(a.rs.M, a.stages, a.nf4, 0, pb) <= kHalfSmBytes) {
     b.stage_b = 0;

@@ -9,9 +9,9 @@
 // synchronisation is not acceptable. For them the split-K scratch lives in a
 // file-scope device array that is part of the loaded library image.
 //
-// The array is sized for sf_linear's workspace at up to kMaxRows output rows
-// and kMaxK inputs (about 12 MB); every GPU that loads the library holds it until the process
-// exits. All calls share it and it keeps the previous call's contents: the
+// The array is sized for sf_linear's workspace at up to kMaxRows output rows,
+// kMaxK inputs and SF_MAX_ROWS token rows (about 37 MB); every GPU that loads
+// the library holds it until the process exits. All calls share it and it keeps the previous call's contents: the
 // arrival counters that must start at zero are cleared by every call, and
 // calls that overlap on the GPU (e.g. on two streams at once) race on it.
 #include <mutex>
@@ -21,9 +21,9 @@
 namespace {
 
 constexpr int kMaxRows = 1 << 20;   // largest N accepted
-constexpr size_t kPartBytes = (size_t)1024 * sf::kRows * sf::kBlockRows * 4;   // sf_linear's tile area
+constexpr size_t kPartBytes = (size_t)2048 * sf::kGroupRows * sf::kBlockRows * 4;   // sf_linear's tile area
 constexpr int kMaxK = 1 << 16;      // largest K accepted (fragment-ordered copy of x)
-constexpr size_t kScratchBytes = kPartBytes + (size_t)(kMaxRows / sf::kBlockRows) * 4 + 256 +
+constexpr size_t kScratchBytes = kPartBytes + (size_t)(kMaxRows / sf::kBlockRows) * sf::kMaxGroups * 4 + 3 * 256 +
                                  (size_t)(kMaxK / 64) * ((sf::kRows + 3) / 4) * 1024;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];

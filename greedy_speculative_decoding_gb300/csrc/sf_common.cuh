@@ -14,6 +14,9 @@ namespace sf {
 typedef __nv_bfloat16 bf16;
 
 constexpr int kRows = SF_MAX_ROWS;     // tokens per forward, at most
+constexpr int kGroupRows = 16;         // token rows of one GEMM CTA (a forward of more rows runs
+                                       // ceil(M / 16) row groups side by side)
+constexpr int kMaxGroups = kRows / kGroupRows;
 constexpr int kBlockRows = 128;        // output rows (features) per GEMM CTA
 constexpr int kGemmThreads = 256;      // 8 warps x 16 rows
 constexpr int kChunk = 64;             // k per pipeline step (one 128-byte line per weight row)
@@ -112,6 +115,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// For weight tiles that other row groups of the same launch read again.
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

@@ -8,8 +8,8 @@ namespace sf {
 enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3, EPI_STORE = 4 };
 
 // Skinny GEMM y[m][n] = sum_k a[m][k] * W[n][k] over up to SF_MAX_ROWS token
-// rows, with a fused prologue (optional RMSNorm of the fp32 input) and one of
-// five epilogues. Weights are bf16 row-major, or NF4 (packed codes + fp16
+// rows (16 per CTA; more run as 16-row groups), with a fused prologue
+// (optional RMSNorm of the fp32 input) and one of five epilogues. Weights are bf16 row-major, or NF4 (packed codes + fp16
 // block scales) when nf4 != 0.
 struct GemmArgs {
   CUtensorMap tm[3];          // per segment: 2-D map {K, rows}, box {64, 16}, 128-byte swizzle
@@ -40,7 +40,8 @@ struct GemmArgs {
   // writes x * frag_gain (the next RMSNorm's input), SWIGLU the activation.
   bf16* frag_out;
   const bf16* frag_gain;
-  // split-K scratch: partial tiles and per-row-block arrival counters
+  // split-K scratch without clusters: partial tiles [row block x row group][split][16][128]
+  // and one arrival counter per (row block, row group)
   float* part;
   int* counter;
   // epilogue outputs

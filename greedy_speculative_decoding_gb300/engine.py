@@ -134,10 +134,16 @@ class SpecEngine:
 
     # ------------------------------------------------------------ the calls
     def prefill(self, prompts):
-        p = np.ascontiguousarray(np.asarray(prompts, dtype=np.int32).reshape(self.B, -1))
-        lens = np.full(self.B, p.shape[1], dtype=np.int32)
-        L.check(self.lib.sf_prefill(self.h, _i32(p), _i32(lens), p.shape[1]))
-        self.prompt_len = p.shape[1]
+        """prompts: one token list per sequence; lengths may differ."""
+        if len(prompts) != self.B:
+            raise ValueError(f"expected {self.B} prompts, got {len(prompts)}")
+        lens = np.array([len(q) for q in prompts], dtype=np.int32)
+        width = int(lens.max())
+        p = np.zeros((self.B, width), np.int32)
+        for b, q in enumerate(prompts):
+            p[b, :len(q)] = np.asarray(q, dtype=np.int32)
+        L.check(self.lib.sf_prefill(self.h, _i32(p), _i32(lens), width))
+        self.prompt_len = lens.copy()
 
     def draft(self, out: torch.Tensor = None, logits: torch.Tensor = None):
         L.check(self.lib.sf_draft(self.h, None if out is None else out.data_ptr(),

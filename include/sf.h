@@ -42,7 +42,10 @@
  *     calling thread's last failure.
  *   - Batch: sequences are independent; per-sequence lengths and accept
  *     lengths are kept on the device.
- *   - Rows per forward (batch * (K + 1)) are limited to SF_MAX_ROWS.
+ *   - Rows per forward (batch * (K + 1)) are limited to SF_MAX_ROWS. Up to 16
+ *     rows run in one pass over the weights per CTA; a forward with more
+ *     rows runs one CTA per 16-row group side by side (weights from HBM once,
+ *     then from L2).
  */
 #ifndef SF_H_
 #define SF_H_
@@ -60,7 +63,7 @@ extern "C" {
 #define SF_API
 #endif
 
-#define SF_MAX_ROWS 16
+#define SF_MAX_ROWS 80
 
 typedef struct sf_engine* sf_handle;
 
@@ -117,7 +120,8 @@ SF_API size_t sf_workspace_bytes(const sf_model_cfg* tgt, const sf_model_cfg* df
 /*
  * Bind caller-owned buffers and build the engine. kv_d may be NULL when dft
  * is NULL. workspace must hold sf_workspace_bytes(...) bytes, 256-byte
- * aligned. K: guesses per round (1..15, batch*(K+1) <= SF_MAX_ROWS).
+ * aligned. batch: 1..32 independent sequences. K: guesses per round (1..15,
+ * batch*(K+1) <= SF_MAX_ROWS).
  * s_max: cache slots per sequence, a multiple of 64.
  * cuda_stream: a cudaStream_t (NULL = legacy default stream).
  * The engine starts with SF_DRAFT_NEURAL when dft is given, else
@@ -131,8 +135,10 @@ SF_API sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w,
 
 /*
  * Load prompts and fill both caches. h_tokens: host [batch][stride] int32,
- * h_lens: host [batch] prompt lengths (>= 2, all equal in this build). After
- * it, each cache holds the prompt except its last token, which is pending.
+ * h_lens: host [batch] prompt lengths (each >= 2 and <= stride; they may
+ * differ). After it, each cache holds its prompt except the last token,
+ * which is pending. Prompts of one length are filled side by side in chunks
+ * of up to SF_MAX_ROWS rows; otherwise each sequence is filled on its own.
  */
 SF_API sf_status sf_prefill(sf_handle h, const int32_t* h_tokens, const int32_t* h_lens, int32_t stride);
 

@@ -71,6 +71,9 @@ def test_create_rejects_bad_arguments_without_gpu_work(lib):
     assert st == L.SF_ERR_ARG and h.value is None
     # too many rows per forward
     arr = (ctypes.c_void_p * lib.sf_weight_count(ctypes.byref(c)))()
-    st = lib.sf_create(ctypes.byref(c), arr, None, None, 2, 8, 256, 256, None, 256, None, ctypes.byref(h))
+    st = lib.sf_create(ctypes.byref(c), arr, None, None, 8, 15, 256, 256, None, 256, None, ctypes.byref(h))
     assert st == L.SF_ERR_UNSUPPORTED
     assert b"exceeds" in lib.sf_last_error()
+    # more sequences than the acceptance kernel's one-warp-per-sequence block holds
+    st = lib.sf_create(ctypes.byref(c), arr, None, None, 33, 1, 256, 256, None, 256, None, ctypes.byref(h))
+    assert st == L.SF_ERR_ARG and h.value is None

@@ -1,6 +1,7 @@
 """GPU parity of the weight-streaming GEMM (sf_linear) against a float64
 matrix product, over shapes that span several 128-row blocks and 64-wide K
-chunks with ragged tails, every row count 1..16, and K splits across CTAs.
+chunks with ragged tails, every row count 1..16, row counts above 16 (one
+CTA per 16-row group, the last one partial), and K splits across CTAs.
 
 Error bound: the activation is carried as a bf16 pair (hi + lo, about 16
 mantissa bits) and products are summed in fp32, so |y - y_ref| stays within
@@ -65,6 +66,30 @@ def test_deterministic_and_row_independent(pkg):
         assert torch.equal(ym[0], y1[m]), m
 
 
+@pytest.mark.parametrize("M", [17, 24, 33, 40, 72, 80])
+def test_rows_above_16(pkg, M):
+    _check(pkg, N=1000, K=904, M=M, seed=M)
+
+
+@pytest.mark.parametrize("N,K,M", [(3584, 18944, 72), (4608, 3584, 40), (129, 72, 80), (896, 4864, 18)])
+def test_row_groups_equal_separate_launches(pkg, N, K, M):
+    """Each 16-row group of a launch gives the same bits as a launch of its
+    rows alone, and any row the same bits as that row alone: a row's
+    arithmetic does not depend on the other rows (K splits included)."""
+    g = torch.Generator(device="cuda").manual_seed(N + K + M)
+    w = (torch.randn(N, K, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    x = torch.randn(M, K, generator=g, device="cuda")
+    y = pkg.linear(w, x)
+    for m0 in range(0, M, 16):
+        part = pkg.linear(w, x[m0:m0 + 16].contiguous())
+        assert torch.equal(part, y[m0:m0 + 16]), m0
+    for m in (0, M // 2, M - 1):
+        assert torch.equal(pkg.linear(w, x[m:m + 1].contiguous())[0], y[m]), m
+    wd, xd = w.double(), x.double()
+    err = (y.double() - xd @ wd.t()).abs()
+    assert bool((err <= 1e-4 * (xd.abs() @ wd.abs().t()) + 1e-30).all())
+
+
 def _frag_reference(x):
     """The fragment order written out element by element (test-side
     restatement of the layout the header documents): bf16 hi/lo pairs of x
@@ -87,7 +112,7 @@ def _frag_reference(x):
     return out
 
 
-@pytest.mark.parametrize("M,K", [(1, 64), (3, 72), (9, 200), (16, 128)])
+@pytest.mark.parametrize("M,K", [(1, 64), (3, 72), (9, 200), (16, 128), (40, 136), (72, 72)])
 def test_to_frag_layout(pkg, M, K):
     g = torch.Generator(device="cuda").manual_seed(M * 1000 + K)
     x = torch.randn(M, K, generator=g, device="cuda")
@@ -98,7 +123,7 @@ def test_to_frag_layout(pkg, M, K):
     assert torch.equal(xf.cpu().view(torch.int16), ref)
 
 
-@pytest.mark.parametrize("N,K,M", [(37888, 3584, 9), (1000, 904, 3), (129, 72, 16), (5, 8, 1)])
+@pytest.mark.parametrize("N,K,M", [(37888, 3584, 9), (1000, 904, 3), (129, 72, 16), (5, 8, 1), (1000, 904, 72)])
 def test_linear_frag_equals_linear(pkg, N, K, M):
     g = torch.Generator(device="cuda").manual_seed(N + K + M)
     w = (torch.randn(N, K, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
