@@ -107,3 +107,45 @@ def test_14b_shape_nf4_two_layers(pkg):
     worst = _check_model(pkg, shape, seed=41, prompt_len=12, s_max=1024)
     print(f"14B shape NF4 (2 layers): max logit error / range = {worst:.3e}")
     assert worst < NF4_TOL
+
+
+@pytest.mark.parametrize("name,B,K,lens", [
+    ("tiny", 4, 4, [40, 23, 57, 31]),
+    ("14b2", 8, 8, [12, 30, 19, 44, 9, 27, 36, 15]),
+])
+def test_nf4_row_groups_ragged_batch(pkg, name, B, K, lens):
+    """Sequences with prompts of different lengths whose verify forward has
+    more than 16 rows (tiny: 20 rows, two 16-row groups; 14B shape: 72 rows,
+    five groups), NF4 weights. Target = draft, so every guess is accepted and
+    each draft row (at most 16 rows per launch: the single-group kernels)
+    equals its verify row (the row-group kernels) bit for bit; every
+    sequence's verify logits are within the NF4 tolerance of the oracle."""
+    shape = TINY_TARGET.with_(ffn=768) if name == "tiny" else QWEN14B.with_(layers=2)
+    w = make_weights(shape, seed=51)
+    gw, rw = _oracle_nf4(shape, w)
+    prompts = [uniform_prompt(n, shape.vocab, seed=60 + b).tolist() for b, n in enumerate(lens)]
+    eng = pkg.SpecEngine(shape, gw, shape, gw, batch=B, K=K, s_max=256)
+    eng.kv_t.fill_(0xFF)
+    eng.kv_d.fill_(0xFF)
+    eng.prefill(prompts)
+    d_out = torch.zeros(B, K, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros(B, K, shape.vocab, dtype=torch.float32, device="cuda")
+    t_log = torch.zeros(B, K + 1, shape.vocab, dtype=torch.float32, device="cuda")
+    eng.draft(d_out, d_log)
+    eng.verify(None, t_log)
+    torch.cuda.synchronize()
+    assert torch.equal(d_log, t_log[:, :K])
+    n_acc, _ = eng.accept_rollback()
+    assert [int(n) for n in n_acc] == [K] * B
+    lt, _ = eng.lengths()
+    assert [int(x) for x in lt] == [n + K for n in lens]
+    eng.close()
+    m = om.Model(shape, rw, rowwise=shape.hidden < 1024)
+    worst = 0.0
+    for b in range(B):
+        c = m.new_cache()
+        m.forward(prompts[b][:-1], c, logit_rows=[])
+        ref = m.forward([prompts[b][-1]] + d_out[b].cpu().tolist(), c)
+        worst = max(worst, max(logit_err(t_log[b, j], ref[j]) for j in range(K + 1)))
+    print(f"{name} NF4 batch {B}: max logit error / range = {worst:.3e}")
+    assert worst < NF4_TOL
