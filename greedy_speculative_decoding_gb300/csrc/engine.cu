@@ -326,20 +326,15 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     const cudaError_t ce = make_weight_map(&md.lm_tm, md.lm, c->vocab, H, md.lm_ld);
     if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "LM head tensor map: %s", cudaGetErrorString(ce));
   }
-  // The K splits of a row block run as one thread-block cluster.
-  // The splits of a row block form one cluster. Matrices of 24 MB and more
-  // are split for two CTAs per SM (bandwidth) in clusters of at most 8 (the
-  // portable size, which packs well into GPCs); smaller ones for one CTA per
-  // SM in clusters of up to 16, so that the next kernel's CTAs fit beside
-  // them and start streaming early.
-  // The K splits of a row block form one cluster. Matrices of 24 MB and more
-  // are split for two CTAs per SM (bandwidth) in clusters of at most 8;
-  // smaller ones for one CTA per SM in clusters of up to 16, so that the
-  // next kernel's CTAs fit beside them and start streaming early. Clusters
-  // are placed within GPCs, and a kernel's CTAs start while the preceding
-  // kernel still holds part of the GPU: the split is lowered until the
-  // clusters fit with a fifth of the cluster slots to spare (checked for the
-  // 9..12-row footprint), so that fragmented free space still takes them all.
+  // The K splits of a row block form one thread-block cluster. Matrices of
+  // 24 MB and more are split for two CTAs per SM (bandwidth) in clusters of
+  // at most 8 (the portable size, which packs well into GPCs); smaller ones
+  // for one CTA per SM in clusters of up to 16, so that the next kernel's
+  // CTAs fit beside them and start streaming early. Clusters are placed
+  // within GPCs, and a kernel's CTAs start while the preceding kernel still
+  // holds part of the GPU: the split is lowered until the clusters fit with a
+  // fifth of the cluster slots to spare (checked for the 9..12-row
+  // footprint), so that fragmented free space still takes them all.
   const int al = nf4 ? 4 : 1;
   auto plan = [&](int nblocks, long rows, long k) {
     const bool big = rows * k * (nf4 ? 1 : 2) >= (24l << 20);
