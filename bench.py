@@ -246,7 +246,8 @@ def extra_workloads(pkg, tw, peak):
             es = pkg.SpecEngine(QWEN7B, tw, QWEN7B, dcopy, batch=1, K=K_GUESS, s_max=S_MAX)
             es.prefill([prompt])
             rate, mean_c = _gen_rate(es)
-            out[f"sigma_{sigma}"] = {"tokens_per_s": round(rate, 2), "mean_committed_per_round": round(mean_c, 3)}
+            out[f"sigma_{sigma}"] = {"tokens_per_s": round(rate, 2), "mean_committed_per_round": round(mean_c, 3),
+                                     "accept_hist": es.accept_hist()[0].tolist()}
             es.close()
             del dcopy, es
         except Exception as ex:
@@ -264,6 +265,20 @@ def extra_workloads(pkg, tw, peak):
             en.close()
         except Exception as ex:
             out[f"ngram_r{r}"] = {"error": repr(ex)[:200]}
+    torch.cuda.empty_cache()
+    # Plain greedy decoding of the same target (no drafter: each round verifies
+    # the pending token and commits the target's own choice), the baseline the
+    # speculative rounds are measured against.
+    try:
+        eg = pkg.SpecEngine(QWEN7B, tw, batch=1, K=1, s_max=S_MAX)
+        eg.set_drafter(pkg.SF_DRAFT_NONE)
+        eg.prefill([prompt])
+        rate, mean_c = _gen_rate(eg)
+        out["plain_greedy"] = {"tokens_per_s": round(rate, 2), "mean_committed_per_round": round(mean_c, 3),
+                               "what": "7B-shape target alone, one verify forward (2 rows) per token"}
+        eg.close()
+    except Exception as ex:
+        out["plain_greedy"] = {"error": repr(ex)[:200]}
     torch.cuda.empty_cache()
     return out
 
@@ -352,42 +367,77 @@ def nf4_batch_workload(pkg, peak, tq, d_shape, dw, lin):
             "rounds": rounds[0], "prefill_s": round(prefill_s, 2)}
 
 
-def run_trace(args):
-    """Launch timeline of replayed rounds (the engine records it when SF_TRACE=1
-    is set): per kernel kind, the time each launch adds to the dependent chain
-    (the gap between consecutive 'producer done' stamps)."""
+def _kernel_bytes(shape, label, ctx):
+    """Algorithmic bytes one launch of a forward kernel moves (weights it
+    streams; for attention the keys and values it reads at context ctx)."""
+    h, f = shape.hidden, shape.ffn
+    w = {"qkv": (shape.q_dim + 2 * shape.kv_dim) * h * 2, "o_proj": h * shape.q_dim * 2,
+         "gate_up": 2 * f * h * 2, "down": h * f * 2, "lm_head": shape.vocab * h * 2,
+         "attention": 2 * shape.n_kv_heads * shape.head_dim * 2 * ctx}
+    return w.get(label)
+
+
+def trace_breakdown(pkg, t_shape, tw, d_shape, dw, rounds=5, ctx=VERIFY_CTX, peak=None):
+    """Per (phase, kernel) of replayed rounds: the time each launch adds to the
+    dependent chain (gap between consecutive 'producer done' stamps of the
+    launch timeline the engine records with SF_TRACE=1) and, for the kernels
+    that stream weights or the cache, bytes / that time."""
     import collections
-    import torch
-    if os.environ.get("SF_TRACE") != "1":
-        raise SystemExit("run with SF_TRACE=1 in the environment")
-    torch.cuda.set_device(0)
-    import __graft_entry__ as g
-    g.build()
-    import greedy_speculative_decoding_gb300 as pkg
     from synth import uniform_prompt
-    t_shape, d_shape = _shapes()
-    tw, dw = _weights("cuda")
-    eng = pkg.SpecEngine(t_shape, tw, d_shape, dw, batch=1, K=K_GUESS, s_max=S_MAX)
-    eng.prefill([uniform_prompt(VERIFY_CTX, t_shape.vocab, seed=103).numpy()])
+    old = os.environ.get("SF_TRACE")
+    os.environ["SF_TRACE"] = "1"
+    try:
+        eng = pkg.SpecEngine(t_shape, tw, d_shape, dw, batch=1, K=K_GUESS, s_max=S_MAX)
+    finally:
+        if old is None:
+            del os.environ["SF_TRACE"]
+        else:
+            os.environ["SF_TRACE"] = old
+    eng.prefill([uniform_prompt(ctx, t_shape.vocab, seed=103).numpy()])
+    # The round graph is captured on the first step; every replay rewrites the
+    # same timeline slots, so the stamps describe the last round replayed.
     first = eng.trace_count()
-    for _ in range(5):
+    for _ in range(rounds):
         eng.step()
     tr = eng.trace(first, eng.trace_count() - first)
+    eng.close()
     agg = collections.OrderedDict()
-    phase, heads = "draft", 0
+    heads = 0
     for i in range(len(tr) - 1):
         lab, st, wd = tr[i]
+        phase = "draft" if heads < K_GUESS else "verify"
         a = agg.setdefault((phase, lab), [0, 0.0, 0.0])
         a[0] += 1
         a[1] += (tr[i + 1][2] - wd) / 1e3
         a[2] += (wd - st) / 1e3
         if lab == "lm_head":
             heads += 1
-            if heads == K_GUESS:
-                phase = "verify"
-    rows = [{"phase": ph, "kernel": lab, "launches": n, "total_us": round(t, 1), "avg_us": round(t / n, 2),
-             "early_start_us": round(w / n, 2)} for (ph, lab), (n, t, w) in agg.items()]
-    print(json.dumps({"trace": rows, "round_span_us": round((tr[-1][2] - tr[0][1]) / 1e3, 1)}))
+    rows = []
+    for (ph, lab), (n, t, w) in agg.items():
+        r = {"phase": ph, "kernel": lab, "launches": n, "total_us": round(t, 1), "avg_us": round(t / n, 2),
+             "early_start_us": round(w / n, 2)}
+        b = _kernel_bytes(t_shape if ph == "verify" else d_shape, lab, ctx)
+        if b:
+            r["bytes"] = b
+            r["gbs"] = round(b / (t / n) / 1e3, 1)
+            if peak:
+                r["frac_of_measured_peak"] = round(b / (t / n) / 1e3 / peak, 4)
+        rows.append(r)
+    return rows, round((tr[-1][2] - tr[0][1]) / 1e3, 1)
+
+
+def run_trace(args):
+    """Launch timeline of replayed rounds at context 2048: per kernel kind,
+    the time each launch adds to the dependent chain."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as pkg
+    t_shape, d_shape = _shapes()
+    tw, dw = _weights("cuda")
+    rows, span = trace_breakdown(pkg, t_shape, tw, d_shape, dw, peak=_peaks()[0])
+    print(json.dumps({"trace": rows, "round_span_us": span}))
 
 
 # ---------------------------------------------------------------------------- ours
@@ -517,6 +567,13 @@ def run_ours(args):
     extra = {}
     if rank == 0 and not args.no_extra:
         extra = extra_workloads(pkg, tw, peak)
+        try:
+            rows, span = trace_breakdown(pkg, t_shape, tw, d_shape, dw, peak=peak)
+            extra["round_kernels"] = {"ctx": VERIFY_CTX, "round_span_us": span, "kernels": rows,
+                                      "how": "SF_TRACE=1 launch timeline of one replayed round: time each launch "
+                                             "adds to the dependent chain; bytes = weights (attention: KV) per launch"}
+        except Exception as ex:
+            extra["round_kernels"] = {"error": repr(ex)[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -573,50 +630,98 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------------------- oracle
-def oracle_round_sample(tw_cpu, dw_cpu, ctx=32, rounds=1):
-    """Time the CPU oracle on one speculative round of the same workload
-    (same weights, K = 8) at a 32-token context; prefill is not timed.
-    Returns (committed tokens, seconds)."""
+def _synthetic_cache(model, n, seed):
+    """The oracle's KV cache holding n slots of N(0, 1) keys and values: the
+    state a prefill of n tokens leaves, for timing the round after it without
+    running that prefill."""
     import torch
-    from oracle import decode as od
-    from oracle import model as om
-    from synth import uniform_prompt
-    t_shape, d_shape = _shapes()
-    tm = om.Model(t_shape, tw_cpu, memoize=False, rowwise=False)
-    dm = om.Model(d_shape, dw_cpu, memoize=False, rowwise=False)
-    prompt = uniform_prompt(ctx, t_shape.vocab, seed=102).tolist()
-    tc, dc = tm.new_cache(), dm.new_cache()
-    tm.forward(prompt[:-1], tc, logit_rows=[])
-    dm.forward(prompt[:-1], dc, logit_rows=[])
-    seq = list(prompt)
-    committed = 0
-    t0 = time.perf_counter()
-    for _ in range(rounds):
-        feed, guesses = [seq[-1]], []
+    g = torch.Generator().manual_seed(seed)
+    s = model.shape
+    c = model.new_cache()
+    for l in range(s.layers):
+        k = torch.randn(n, s.n_kv_heads, s.head_dim, generator=g, dtype=torch.float64)
+        v = torch.randn(n, s.n_kv_heads, s.head_dim, generator=g, dtype=torch.float64)
+        for j in range(n):
+            c.append(l, k[j], v[j])
+    return c
+
+
+class OracleRounds:
+    """The CPU oracle on the benchmark's workload: speculative rounds of the
+    0.5B-shape draft (K = 8) and the 7B-shape target at the prompt's context
+    (512), with both caches holding that context already."""
+
+    def __init__(self, tw_cpu, dw_cpu, ctx=PROMPT_LEN):
+        from oracle import model as om
+        from synth import uniform_prompt
+        t_shape, d_shape = _shapes()
+        self.tm = om.Model(t_shape, tw_cpu, memoize=False, rowwise=False)
+        self.dm = om.Model(d_shape, dw_cpu, memoize=False, rowwise=False)
+        self.seq = uniform_prompt(ctx, t_shape.vocab, seed=102).tolist()
+        self.tc = _synthetic_cache(self.tm, ctx - 1, 1)
+        self.dc = _synthetic_cache(self.dm, ctx - 1, 2)
+
+    def round(self):
+        """One round; returns (committed tokens, seconds, seconds of the draft
+        steps, seconds of the verify pass)."""
+        from oracle import decode as od
+        from oracle import model as om
+        t0 = time.perf_counter()
+        feed, guesses = [self.seq[-1]], []
         for _ in range(K_GUESS):
-            lg = dm.forward(feed, dc)[0]
+            lg = self.dm.forward(feed, self.dc)[0]
             guesses.append(om.first_argmax(lg))
             feed = [guesses[-1]]
-        lg = tm.forward([seq[-1]] + guesses, tc)
+        t1 = time.perf_counter()
+        lg = self.tm.forward([self.seq[-1]] + guesses, self.tc)
         choice = [om.first_argmax(lg[i]) for i in range(K_GUESS + 1)]
+        t2 = time.perf_counter()
         n = od.accept_length(guesses, choice)
-        seq += guesses[:n] + [choice[n]]
-        tc.truncate(len(seq) - 1)
-        dc.truncate(min(dc.length, len(seq) - 1))
-        committed += n + 1
-    return committed, time.perf_counter() - t0
+        self.seq += guesses[:n] + [choice[n]]
+        self.tc.truncate(len(self.seq) - 1)
+        self.dc.truncate(min(self.dc.length, len(self.seq) - 1))
+        return n + 1, time.perf_counter() - t0, t1 - t0, t2 - t1
 
 
-def cpu_baseline(tw, dw):
+def _tiny_end_to_end():
+    """The tiny correctness workload end to end on the oracle: prefill of the
+    32-token prompt and 64 tokens of speculative decoding (K = 4, one-layer
+    draft). Returns (tokens, seconds)."""
+    from oracle import decode as od
+    from oracle import model as om
+    from synth import TINY_DRAFT, TINY_TARGET, draft_from_target_layer0, make_weights, uniform_prompt
+    tw = make_weights(TINY_TARGET, seed=0)
+    dw = draft_from_target_layer0(tw, TINY_DRAFT, 0.005, seed=1)
+    prompt = uniform_prompt(32, TINY_TARGET.vocab, seed=100).tolist()
+    t0 = time.perf_counter()
+    r = od.spec_decode(om.Model(TINY_TARGET, tw), om.Model(TINY_DRAFT, dw), prompt, 4, 64)
+    return len(r["tokens"]), time.perf_counter() - t0
+
+
+def _cores():
     import torch
+    return {"nproc": os.cpu_count(), "torch_threads": torch.get_num_threads()}
+
+
+def cpu_baseline(tw, dw, rounds=3):
     cpu = lambda w: {k: (None if v is None else v.detach().to("cpu")) for k, v in w.items()}
-    tw_c, dw_c = cpu(tw), cpu(dw)
-    n, s = oracle_round_sample(tw_c, dw_c)
-    return {"value": round(n / s, 5), "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "sample": "one speculative round (8 draft steps of the 0.5B-shape draft, one 9-row verify of the "
-                      "7B-shape target, accept) at a 32-token context instead of 512, fp64 torch CPU, prefill "
-                      "untimed; weights are 99% of the work at either context",
-            "seconds": round(s, 2), "committed": n}
+    orc = OracleRounds(cpu(tw), cpu(dw))
+    orc.round()                          # warm: first touch of the weights
+    n = s = sd = sv = 0.0
+    for _ in range(rounds):
+        c, t, td, tv = orc.round()
+        n, s, sd, sv = n + c, s + t, sd + td, sv + tv
+    tn, ts = _tiny_end_to_end()
+    cores = _cores()
+    return {"value": round(n / s, 5), "unit": "tokens/s", "cores": cores["torch_threads"], "nproc": cores["nproc"],
+            "kind": "oracle",
+            "sample": f"{rounds} speculative rounds of the benchmark workload (8 steps of the 0.5B-shape draft, "
+                      "one 9-row verify of the 7B-shape target, accept) at the 512-token context, caches holding "
+                      "that context already (prefill not run); fp64 torch CPU",
+            "seconds": round(s, 2), "committed": int(n),
+            "draft_decode_step_s": round(sd / rounds / K_GUESS, 4), "verify_step_s": round(sv / rounds, 3),
+            "tiny_end_to_end": {"tokens_per_s": round(tn / ts, 2), "seconds": round(ts, 2),
+                                "what": "tiny workload: prefill + 64 tokens, K=4"}}
 
 
 def run_reference(args):
@@ -625,24 +730,27 @@ def run_reference(args):
     if rank != 0:
         return
     tw, dw = _weights("cpu")
-    steps, tot_n, tot_s = args.steps, 0, 0.0
+    orc = OracleRounds(tw, dw)
     for _ in range(min(args.warmup, 1)):
-        oracle_round_sample(tw, dw)
+        orc.round()
+    steps, tot_n, tot_s = args.steps, 0, 0.0
     for _ in range(steps):
-        n, s = oracle_round_sample(tw, dw)
+        n, s, _, _ = orc.round()
         tot_n += n
         tot_s += s
     value = tot_n / tot_s
+    cores = _cores()
+    sample = ("one speculative round per step (8 draft steps of the 0.5B-shape draft, one 9-row verify of the "
+              "7B-shape target, accept) at the 512-token context, caches holding it already; fp64 torch CPU")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tot_s / steps, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic: random-init weights N(0,0.02), uniform prompt",
-        "config": {"workload": "Qwen2.5-7B-shape bf16 target + Qwen2.5-0.5B-shape draft, K=8, batch 1; each step "
-                               "one speculative round at a 32-token context"},
+        "config": {"workload": "Qwen2.5-7B-shape bf16 target + Qwen2.5-0.5B-shape draft, K=8, batch 1, 512-token "
+                               "context; each step one speculative round"},
         "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "kind": "oracle",
-                         "cores": torch.get_num_threads(),
-                         "sample": "one speculative round per step at a 32-token context, prefill untimed"},
+                         "cores": cores["torch_threads"], "nproc": cores["nproc"], "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

@@ -232,6 +232,7 @@ struct sf_engine {
   Model tgt, dft;
   bool has_dft = false;
   bool pdl = true;      // programmatic dependent launch between the round's kernels
+  bool expire_waits = false;   // SF_TEST_WAIT_EXPIRE=1: every GEMM reports an expired wait (error-path test)
   unsigned long long* trace = nullptr;     // launch timeline (SF_TRACE=1), kTraceSlots entries
   int trace_next = 0;
   std::vector<std::string> trace_labels;
@@ -246,8 +247,8 @@ struct sf_engine {
   unsigned long long* keys = nullptr;
   SpecState st{};
   int* pin = nullptr;   // pinned host copy of the report block
-  cudaGraphExec_t graph[2] = {nullptr, nullptr};   // whole round, per drafter
-  size_t graph_kernels[2] = {0, 0};                 // kernel launches in each round graph
+  cudaGraphExec_t graph[3] = {nullptr, nullptr, nullptr};   // whole round, per drafter (SF_DRAFT_*)
+  size_t graph_kernels[3] = {0, 0, 0};                      // kernel launches in each round graph
   cudaGraphExec_t g_draft = nullptr, g_verify = nullptr;
   int drafter = SF_DRAFT_NEURAL, ng_min = 2, ng_max = 4;
   std::vector<int> C;   // committed tokens per sequence (host mirror)
@@ -367,6 +368,7 @@ GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& r
   a.counter = e->counters;
   a.cluster = 1;   // the K slices of a row block are one cluster
   a.err = e->st.err;
+  a.expire_first_wait = e->expire_waits ? 1 : 0;
   a.rs = rs;
   a.eps = md.c.rms_eps;
   return a;
@@ -619,15 +621,19 @@ sf_status enqueue_round(sf_engine* e, int mode, cudaStream_t s) {
   sf_status r;
   if (mode == SF_DRAFT_NEURAL) {
     if ((r = enqueue_draft(e, nullptr, s)) != SF_OK) return r;
-  } else {
+  } else if (mode == SF_DRAFT_NGRAM) {
     CK(launch_ngram(e->st, e->K, e->ng_min, e->ng_max, nullptr, nullptr, s, e->pdl));
+  } else {
+    // No drafter: the lookup kernel with an empty range of n proposes nothing,
+    // so the round commits the target's own next token (plain greedy decoding).
+    CK(launch_ngram(e->st, e->K, 1, 0, nullptr, nullptr, s, e->pdl));
   }
   if ((r = enqueue_verify(e, nullptr, s)) != SF_OK) return r;
   CK(launch_accept(e->st, mode, s, e->pdl));
   return SF_OK;
 }
 
-enum { CAP_ROUND_NEURAL = 0, CAP_ROUND_NGRAM = 1, CAP_DRAFT = 2, CAP_VERIFY = 3 };
+enum { CAP_ROUND_NEURAL = 0, CAP_ROUND_NGRAM = 1, CAP_ROUND_NONE = 2, CAP_DRAFT = 3, CAP_VERIFY = 4 };
 
 cudaGraphExec_t* graph_slot(sf_engine* e, int what) {
   if (what == CAP_DRAFT) return &e->g_draft;
@@ -652,7 +658,7 @@ sf_status build_graph(sf_engine* e, int what) {
     return r;
   }
   if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(ce));
-  if (what == CAP_ROUND_NEURAL || what == CAP_ROUND_NGRAM) {
+  if (what == CAP_ROUND_NEURAL || what == CAP_ROUND_NGRAM || what == CAP_ROUND_NONE) {
     size_t n = 0;
     if (cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess) e->graph_kernels[what] = n;
   }
@@ -758,6 +764,10 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   // SF_PDL=0 in the environment launches the kernels without programmatic
   // dependent launch (for comparing the two; results are identical).
   if (const char* v = getenv("SF_PDL")) e->pdl = v[0] != '0';
+  // SF_TEST_WAIT_EXPIRE=1: the first weight-tile wait of every projection
+  // gives up at once and reports it (the wait then completes normally), so
+  // tests can drive the device error path without stalling a kernel.
+  if (const char* v = getenv("SF_TEST_WAIT_EXPIRE")) e->expire_waits = v[0] == '1';
   // SF_TRACE=1: kernels stamp a launch timeline (see sf_trace).
   const char* tr = getenv("SF_TRACE");
   const bool trace_on = tr && tr[0] == '1';
@@ -917,7 +927,8 @@ sf_status sf_reset(sf_handle h) {
 
 sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n) {
   if (!h) return fail(SF_ERR_ARG, "null handle");
-  if (mode != SF_DRAFT_NEURAL && mode != SF_DRAFT_NGRAM) return fail(SF_ERR_ARG, "unknown drafter");
+  if (mode != SF_DRAFT_NEURAL && mode != SF_DRAFT_NGRAM && mode != SF_DRAFT_NONE)
+    return fail(SF_ERR_ARG, "unknown drafter");
   if (mode == SF_DRAFT_NEURAL && !h->has_dft) return fail(SF_ERR_STATE, "no draft model");
   if (mode == SF_DRAFT_NGRAM && (min_n < 1 || max_n < min_n || max_n > 64))
     return fail(SF_ERR_ARG, "need 1 <= min_n <= max_n <= 64");
@@ -998,7 +1009,7 @@ sf_status sf_accept_rollback(sf_handle h, int32_t* h_n_accepted, int32_t* h_comm
   if (h->phase != 3) return fail(SF_ERR_STATE, "sf_accept_rollback needs a verify first");
   CK(launch_accept(h->st, h->drafted_mode, h->user, false));
   h->phase = 1;
-  if (h->drafted_mode == SF_DRAFT_NGRAM && h->has_dft) h->draft_stale = true;
+  if (h->drafted_mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
   sf_status r = sync_report(h);
   if (r != SF_OK) return r;
   copy_out(h, h_n_accepted, h_committed, h_n_committed);
@@ -1015,7 +1026,7 @@ sf_status sf_step(sf_handle h, int32_t* h_n_committed, int32_t* h_committed) {
   sf_status r = build_graph(h, mode);
   if (r != SF_OK) return r;
   CK(cudaGraphLaunch(h->graph[mode], h->user));
-  if (mode == SF_DRAFT_NGRAM && h->has_dft) h->draft_stale = true;
+  if (mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
   if ((r = sync_report(h)) != SF_OK) return r;
   copy_out(h, nullptr, h_committed, h_n_committed);
   return SF_OK;
@@ -1045,7 +1056,7 @@ sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rou
     if (R < 1) return fail(SF_ERR_CAPACITY, "s_max reached after %d new tokens", gen_min);
     for (int i = 0; i < R; ++i) CK(cudaGraphLaunch(h->graph[mode], h->user));
     rounds += R;
-    if (mode == SF_DRAFT_NGRAM && h->has_dft) h->draft_stale = true;
+    if (mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
     if ((r = sync_report(h)) != SF_OK) return r;
   }
   if (h_out)
@@ -1165,7 +1176,7 @@ int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches) {
 
 int64_t sf_round_launches(sf_handle h) {
   if (!h) return 0;
-  return (int64_t)h->graph_kernels[h->drafter == SF_DRAFT_NGRAM ? CAP_ROUND_NGRAM : CAP_ROUND_NEURAL];
+  return (int64_t)h->graph_kernels[h->drafter];
 }
 
 const char* sf_trace_label(sf_handle h, int32_t i) {

@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(128) k_embed(const __grid_constant__ EmbedArgs
   const int b = m / a.rs.rps, j = m - b * a.rs.rps;
   int tok = a.rs.tok[b * a.rs.tok_stride + a.rs.tok_off + j];
   if (tok < 0 || tok >= a.vocab) {
-    if (i == 0 && blk == 0) atomicOr(a.err, kErrCapacity);
+    if (i == 0 && blk == 0) report_err(a.err, kErrCapacity);
     tok = 0;
   }
   const int n = blk * 128 + i;

@@ -279,7 +279,7 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int m0, i
       }
     }
     best = shfl_max_u64(best);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, kErrNonfinite);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report_err(a.err, kErrNonfinite);
     if (lane == 0) atomicMax(a.keys + m0 + m, best);
   }
   __threadfence();
@@ -447,6 +447,9 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   bool timed_out = false;
   for (int st = 0; st < nst; ++st) {
     const int s = st % kStages;
+    // Test hook for the error path: a first wait with no iterations always
+    // gives up; the full wait that follows keeps the data and the flow intact.
+    if (st == 0 && a.expire_first_wait && !mbar_wait(&my_bar[s], 0, 0)) timed_out = true;
     if (!mbar_wait(&my_bar[s], (st / kStages) & 1, kWaitIters)) timed_out = true;
     const unsigned char* tile = my_ring + s * kTileBytes;
     if (!NF4) {
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   if (timed_out) {
     // A tile never arrived: report, and give every copy of this warp one more
     // bounded chance to land before the CTA's shared memory is released.
-    if (lane == 0) atomicOr(a.err, kErrWait);
+    if (lane == 0) report_err(a.err, kErrWait);
     for (int st = max(0, nst - kStages); st < nst; ++st)
       mbar_wait(&my_bar[st % kStages], (st / kStages) & 1, kWaitIters);
   }
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
     if (!mbar_wait_cluster(&recv_bar, 0, kWaitIters)) {
       // A tile never arrived: report, give the stores one more bounded
       // chance to land in this CTA's shared memory, and skip the epilogue.
-      if (tid == 0) atomicOr(a.err, kErrWait);
+      if (tid == 0) report_err(a.err, kErrWait);
       mbar_wait_cluster(&recv_bar, 0, kWaitIters);
       return;
     }
@@ -836,13 +839,13 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 ? 2 : 1)) k_lmhead(const
         }
       }
       best = shfl_max_u64(best);
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, kErrNonfinite);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) report_err(a.err, kErrNonfinite);
       if (lane == 0 && best > s_best[m]) s_best[m] = best;
     }
     __syncthreads();   // ys is free for the next block
   }
   if (timed_out) {
-    if (lane == 0) atomicOr(a.err, kErrWait);
+    if (lane == 0) report_err(a.err, kErrWait);
     for (long st = (total > kStages ? total - kStages : 0); st < total; ++st)
       mbar_wait(&my_bar[st % kStages], (uint32_t)((st / kStages) & 1), kWaitIters);
   }

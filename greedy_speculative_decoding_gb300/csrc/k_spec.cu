@@ -65,7 +65,7 @@ cudaError_t launch_accept(const SpecState& s, int mode, cudaStream_t st, bool pd
   cfg.stream = st;
   cfg.attrs = &attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_accept, s, mode == SF_DRAFT_NGRAM ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg, k_accept, s, mode != SF_DRAFT_NEURAL ? 1 : 0);
 }
 
 // ---------------------------------------------------------------- n-gram

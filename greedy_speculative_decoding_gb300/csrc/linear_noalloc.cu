@@ -2,18 +2,20 @@
 // cannot hand the library any scratch memory.
 //
 // Some callers cannot call cudaMalloc at the point where they need a
-// projection: code that runs while a stream is being captured into a CUDA
-// graph (an allocation there would break or serialise the capture), plug-ins
-// whose host framework owns every device allocation through its own pool,
-// and latency-critical loops where cudaMalloc's implicit device
-// synchronisation is not acceptable. For them the split-K scratch lives in a
-// file-scope device array that is part of the loaded library image.
+// projection: plug-ins whose host framework owns every device allocation
+// through its own pool, and latency-critical loops where cudaMalloc's
+// implicit device synchronisation is not acceptable. For them the split-K
+// scratch lives in a file-scope device array that is part of the loaded
+// library image.
 //
 // The array is sized for sf_linear's workspace at up to kMaxRows output rows,
-// kMaxK inputs and SF_MAX_ROWS token rows (about 37 MB); every GPU that loads
-// the library holds it until the process exits. All calls share it and it keeps the previous call's contents: the
-// arrival counters that must start at zero are cleared by every call, and
-// calls that overlap on the GPU (e.g. on two streams at once) race on it.
+// kMaxK inputs and SF_MAX_ROWS token rows (about 38 MB); every GPU that loads
+// the library holds it until the process exits. All calls share it and it
+// keeps the previous call's contents: the arrival counters that must start at
+// zero are cleared by every call, and calls that overlap on the GPU (e.g. on
+// two streams at once) race on it. The array's device address is looked up
+// once per device index and kept for the life of the process, so a context
+// reset (cudaDeviceReset) after the first call is not supported.
 #include <mutex>
 
 #include "sf_kernels.h"
@@ -58,8 +60,10 @@ extern "C" sf_status sf_linear_noalloc(const void* d_w, int32_t N, int32_t K, in
   if (N < 1 || N > kMaxRows)
     return sf::set_error(SF_ERR_ARG, "sf_linear_noalloc: N = %d is outside 1..%d, the limit of the static scratch",
                          N, kMaxRows);
+  if (K < 8 || K % 8)
+    return sf::set_error(SF_ERR_ARG, "sf_linear_noalloc: K = %d must be a positive multiple of 8", K);
   const size_t need = sf_linear_workspace_bytes(N, K);
-  if (need == 0 || need > kScratchBytes)
+  if (need > kScratchBytes)
     return sf::set_error(SF_ERR_ARG, "sf_linear_noalloc: N = %d, K = %d needs %zu scratch bytes, the static "
                          "scratch holds %zu", N, K, need, kScratchBytes);
   void* scratch = nullptr;

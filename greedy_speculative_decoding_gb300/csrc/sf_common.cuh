@@ -57,6 +57,12 @@ __device__ __forceinline__ void trace_mark(const RowSet& rs, int k) {
   }
 }
 
+// Set an error bit in the caller's status word; launches made outside an
+// engine (sf_linear) carry no status word and report nothing.
+__device__ __forceinline__ void report_err(int* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
 __device__ __forceinline__ int row_pos(const RowSet& rs, int m) {
   return rs.pos_base[m / rs.rps] + rs.pos_off + m % rs.rps;
 }

@@ -58,7 +58,8 @@ struct GemmArgs {
   int tok_stride, tok_skip, tok_off;   // rows with j < tok_skip produce nothing
   float* logits;              // ARGMAX: optional fp32 rows, row (b*lg_stride + lg_off + j - tok_skip)
   int lg_stride, lg_off;
-  int* err;
+  int* err;                   // status word (kErr* bits), or null
+  int expire_first_wait;      // test hook: the first weight-tile wait reports an expiry
   RowSet rs;
 };
 

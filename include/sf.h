@@ -79,7 +79,10 @@ typedef enum {
 } sf_status;
 
 enum { SF_WDTYPE_BF16 = 0, SF_WDTYPE_NF4 = 1 };
-enum { SF_DRAFT_NEURAL = 0, SF_DRAFT_NGRAM = 1 };
+/* Drafters: the draft model, prompt lookup, or none (each round then commits
+ * only the target's own next token: plain greedy decoding, the baseline the
+ * speculative rounds are measured against). */
+enum { SF_DRAFT_NEURAL = 0, SF_DRAFT_NGRAM = 1, SF_DRAFT_NONE = 2 };
 
 /* Decoder shape (Qwen2-style: GQA attention with RoPE, RMSNorm, SwiGLU MLP). */
 typedef struct {
@@ -113,12 +116,18 @@ SF_API int32_t sf_weight_count(const sf_model_cfg* cfg);
 /* Bytes of one KV cache: layout [layers][2 (k, v)][batch][n_kv_heads][s_max][head_dim] bf16. */
 SF_API size_t sf_kv_bytes(const sf_model_cfg* cfg, int32_t batch, int32_t s_max);
 
-/* Bytes of device workspace sf_create needs (dft may be NULL: n-gram only). */
+/* Bytes of device workspace sf_create needs (dft may be NULL: n-gram only);
+ * 0 for an invalid configuration. The caller allocates it once: the pages'
+ * fix for graph replays is a static, preallocated cache and in-place
+ * intermediates ("Why It Kept Breaking (and How I Fixed It)", fixes 1-2). */
 SF_API size_t sf_workspace_bytes(const sf_model_cfg* tgt, const sf_model_cfg* dft, int32_t batch,
                           int32_t K, int32_t s_max);
 
 /*
- * Bind caller-owned buffers and build the engine. kv_d may be NULL when dft
+ * Bind caller-owned buffers and build the engine ("Speculative Decoding: The
+ * Idea": a small draft model beside the target; for an n-gram-only engine,
+ * "Speculative decoding: correct, but slower (for now)" on the Sangama
+ * page). kv_d may be NULL when dft
  * is NULL. workspace must hold sf_workspace_bytes(...) bytes, 256-byte
  * aligned. batch: 1..32 independent sequences. K: guesses per round (1..15,
  * batch*(K+1) <= SF_MAX_ROWS).
@@ -134,7 +143,9 @@ SF_API sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w,
                     sf_handle* out);
 
 /*
- * Load prompts and fill both caches. h_tokens: host [batch][stride] int32,
+ * Load prompts and fill both caches (the step before the speculative loop;
+ * "Qwen3.5-397B on 20 GPUs", "What made it faster": prompts go through in
+ * pieces). h_tokens: host [batch][stride] int32,
  * h_lens: host [batch] prompt lengths (each >= 2 and <= stride; they may
  * differ). After it, each cache holds its prompt except the last token,
  * which is pending. Prompts of one length are filled side by side in chunks
@@ -143,7 +154,9 @@ SF_API sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w,
 SF_API sf_status sf_prefill(sf_handle h, const int32_t* h_tokens, const int32_t* h_lens, int32_t stride);
 
 /*
- * Neural draft: K greedy decode steps of the draft model. Writes the guesses
+ * Neural draft ("Speculative Decoding: The Idea": the small model guesses K
+ * tokens one at a time; "CUDA Graphs: What They Are and Why They Helped":
+ * the K steps replay as one graph): K greedy decode steps of the draft model. Writes the guesses
  * to the engine's device state and, when not NULL, to d_draft (device
  * [batch][K] int32) and their logits to d_logits (device [batch][K][vocab]
  * fp32). The first step runs two rows (the last two committed tokens) so the
@@ -153,7 +166,9 @@ SF_API sf_status sf_prefill(sf_handle h, const int32_t* h_tokens, const int32_t*
 SF_API sf_status sf_draft(sf_handle h, int32_t* d_draft, float* d_logits);
 
 /*
- * Prompt-lookup draft: for n = max_n down to min_n, the rightmost earlier
+ * Prompt-lookup draft ("Speculative decoding: correct, but slower (for
+ * now)", Sangama page: guess what followed the last 2-4 tokens the last time
+ * they appeared): for n = max_n down to min_n, the rightmost earlier
  * occurrence of the last n committed tokens; up to max_guess tokens that
  * followed it are proposed (cut at the end of the context). Optional device
  * outputs: d_prop [batch][max_guess] (unused slots 0), d_count [batch].
@@ -163,7 +178,9 @@ SF_API sf_status sf_ngram_draft(sf_handle h, int32_t max_guess, int32_t min_n, i
                          int32_t* d_prop, int32_t* d_count);
 
 /*
- * Target verify: one causal pass over [pending, d_1..d_K] per sequence,
+ * Target verify ("Speculative Decoding: The Idea": the target checks all
+ * guesses in one forward pass; the Sangama page: the model's own choice at
+ * every position): one causal pass over [pending, d_1..d_K] per sequence,
  * appending K+1 entries to the target cache. Optional device outputs: the
  * target's argmax at every row (d_tgt_argmax [batch][K+1] int32) and the
  * logits (d_logits [batch][K+1][vocab] fp32). Ties go to the lowest index.
@@ -172,7 +189,9 @@ SF_API sf_status sf_ngram_draft(sf_handle h, int32_t max_guess, int32_t min_n, i
 SF_API sf_status sf_verify(sf_handle h, int32_t* d_tgt_argmax, float* d_logits);
 
 /*
- * Accept and roll back, per sequence: n = longest prefix of guesses equal to
+ * Accept and roll back ("Speculative Decoding: The Idea": keep the agreed
+ * tokens; "Why It Kept Breaking (and How I Fixed It)", fix 4: in-place KV
+ * rewind on rejection), per sequence: n = longest prefix of guesses equal to
  * the target's choices (capped at the number of real guesses); d_1..d_n and
  * the target's choice t_n are committed; both caches are cut back in place
  * to the committed length minus one. Host outputs (may be NULL):
@@ -181,8 +200,10 @@ SF_API sf_status sf_verify(sf_handle h, int32_t* d_tgt_argmax, float* d_logits);
 SF_API sf_status sf_accept_rollback(sf_handle h, int32_t* h_n_accepted, int32_t* h_committed,
                              int32_t* h_n_committed);
 
-/* draft (neural or n-gram, per sf_set_drafter) + verify + accept/rollback as
- * one CUDA graph replay. Host outputs as in sf_accept_rollback (may be NULL). */
+/* One whole round ("CUDA Graphs: What They Are and Why They Helped": one
+ * driver call instead of a launch per kernel): draft (neural or n-gram, per
+ * sf_set_drafter) + verify + accept/rollback as one CUDA graph replay. Host
+ * outputs as in sf_accept_rollback (may be NULL). */
 SF_API sf_status sf_step(sf_handle h, int32_t* h_n_committed, int32_t* h_committed);
 
 /*
@@ -196,10 +217,13 @@ SF_API sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t
 /* Rewind every sequence to its prompt (prefix already in the caches). */
 SF_API sf_status sf_reset(sf_handle h);
 
-/* Select the drafter used by sf_step / sf_generate. */
+/* Select the drafter used by sf_step / sf_generate (SF_DRAFT_*; min_n and
+ * max_n apply to SF_DRAFT_NGRAM only). */
 SF_API sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n);
 
-/* Current cache lengths per sequence (host [batch] each, may be NULL). */
+/* Current cache lengths per sequence (host [batch] each, may be NULL): the
+ * positions the in-place rewind left ("Why It Kept Breaking", fixes 3-4:
+ * explicit position updates, in-place rewind). */
 SF_API sf_status sf_get_lengths(sf_handle h, int32_t* h_len_t, int32_t* h_len_d);
 
 /* Accept-length histogram since prefill: host [batch][K+1]. */
@@ -224,8 +248,11 @@ SF_API const char* sf_trace_label(sf_handle h, int32_t i);
  * built by sf_step / sf_generate. */
 SF_API int64_t sf_round_launches(sf_handle h);
 
+/* Name of a status code; message of the calling thread's last failure. */
 SF_API const char* sf_status_str(sf_status s);
 SF_API const char* sf_last_error(void);
+/* Release the engine's graphs, stream and pinned host memory (the caller's
+ * device buffers stay the caller's). NULL is ignored. */
 SF_API void sf_destroy(sf_handle h);
 
 /*
@@ -237,7 +264,8 @@ SF_API void sf_destroy(sf_handle h);
  * sf_linear_workspace_bytes(N, K) bytes, 256-byte aligned, for split-K
  * partial tiles, arrival counters (zeroed by the call) and a bf16 hi/lo copy
  * of x in the GEMM's operand order. Enqueued on cuda_stream; returns without
- * synchronising.
+ * synchronising. There is no device status word here: should a weight-tile
+ * wait ever expire, the kernel returns normally and y is unspecified.
  */
 SF_API size_t sf_linear_workspace_bytes(int32_t N, int32_t K);
 SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x, int32_t M,
@@ -265,22 +293,23 @@ SF_API sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t l
 
 /*
  * sf_linear without any caller-provided scratch, for callers that cannot
- * allocate device memory where they need the projection: code running while
- * a stream is captured into a CUDA graph, plug-ins whose host framework owns
- * all device allocations, and latency-critical loops that cannot afford
- * cudaMalloc's implicit synchronisation. Same arguments and result as
- * sf_linear minus d_workspace. (The pages describe no such call; it has no
- * counterpart there.)
+ * allocate device memory where they need the projection: plug-ins whose
+ * host framework owns every device allocation through its own pool, and
+ * latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation. Same arguments and result as sf_linear minus d_workspace.
+ * (The pages have no counterpart of this call.)
  *
- * The scratch is a file-scope device array of about 12 MB inside the
- * library (enough for N up to 1,048,576 rows and K up to 65,536); every GPU that loads the
- * library keeps it until the process exits. The call allocates nothing: the
- * first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current, so make that first call
- * before any stream capture. All calls share the array: it keeps the last
- * call's contents, the counters that must start at zero are cleared by each
- * call, and calls that overlap on the GPU race with each other. N or K beyond
- * the limits returns SF_ERR_ARG with a message in sf_last_error().
+ * The scratch is a file-scope device array of about 38 MB inside the
+ * library, enough for N up to 1,048,576 output rows, K up to 65,536 inputs
+ * and M up to SF_MAX_ROWS token rows; every GPU that loads the library keeps
+ * it until the process exits. The call allocates nothing: the first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current and keeps it for the life of the process, so a
+ * context reset (cudaDeviceReset) after that first call is not supported.
+ * All calls share the array: it keeps the last call's contents, the counters
+ * that must start at zero are cleared by each call, and calls that overlap
+ * on the GPU race with each other. N, K or M beyond the limits returns
+ * SF_ERR_ARG with a message in sf_last_error().
  */
 SF_API sf_status sf_linear_noalloc(const void* d_w, int32_t N, int32_t K, int32_t ld, const float* d_x,
                                    int32_t M, float* d_y, void* cuda_stream);

@@ -51,6 +51,28 @@ def teacher_forced_stream_check(model: om.Model, prompt, stream, tol=LOGIT_TOL_B
     return near
 
 
+def stream_report(model: om.Model, prompt, stream, tol=LOGIT_TOL_BF16):
+    """Teacher-forced comparison of a GPU token stream with the oracle: at
+    every position the oracle scores the prefix the GPU committed. Returns
+    (positions, flips, near_ties): near_ties counts positions whose oracle
+    top-2 gap is below tol * the row's logit range (where the pages allow a
+    different choice), flips the positions where the GPU token is not the
+    oracle's argmax. Every flip must be a near tie (asserted)."""
+    cache = model.new_cache()
+    seq = list(prompt)
+    model.forward(seq[:-1], cache, logit_rows=[])
+    flips = near = 0
+    for t in stream:
+        ref = model.forward([seq[-1]], cache)[0]
+        top = torch.topk(ref, 2).values
+        if float(top[0] - top[1]) < tol * float(ref.max() - ref.min()):
+            near += 1
+        if check_token_against_oracle(int(t), ref, tol) == "near-tie":
+            flips += 1
+        seq.append(int(t))
+    return len(stream), flips, near
+
+
 def accept_brute(d, t, limit):
     n = 0
     for m in range(limit + 1):

@@ -1,0 +1,191 @@
+"""GPU parity at the contexts the benchmark times and on the longest code
+paths of attention, plus multi-round token streams at the full shapes.
+
+* The 7B-shape verify with the caches prefilled to 2048 slots, as the
+  benchmark's verify-step roofline measures it; two layers of the 7B shape
+  (the same matrix shapes, hence the same GEMM launch plans, as 28 layers)
+  with a two-layer 0.5B-shape draft on the target's first 896 embedding
+  columns, so the float64 oracle stays affordable.
+* Attention contexts whose chunk merge needs more than one round of loads:
+  more than 48 chunks of 64 slots at head dim 128 (3500 tokens) and more
+  than 96 at head dim 64 (6500 tokens), batch 1, and a batch of eight
+  ragged sequences (72 verify rows) whose longest one crosses the threshold.
+* Token streams over several replayed rounds at the 0.5B shape (drafting
+  for itself) and at the two-layer 7B shape with its draft, scored by the
+  oracle position by position: flips (GPU token != oracle argmax) must be
+  near ties of the oracle, and their count is printed beside the number of
+  near-tie positions.
+
+Logit rows within 3e-2 of each row's range; the caches start filled with NaN
+bytes, so a slot the kernels did not write cannot hide.
+"""
+
+import pytest
+import torch
+
+from oracle import model as om
+from synth import (QWEN05B, QWEN05B_SHARED, QWEN7B, TINY_TARGET, make_weights, shared_embedding_draft,
+                   uniform_prompt)
+
+from gpu_helpers import LOGIT_TOL_BF16, logit_err, stream_report, to_cpu, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+HD128_G7 = TINY_TARGET.with_(hidden=384, n_heads=14, n_kv_heads=2, head_dim=128)
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as p
+    return p
+
+
+def _poison(eng):
+    eng.kv_t.fill_(0xFF)
+    if eng.kv_d is not None:
+        eng.kv_d.fill_(0xFF)
+
+
+def test_7b_shape_verify_at_context_2048(pkg):
+    K = 8
+    t_shape = QWEN7B.with_(layers=2)
+    d_shape = QWEN05B_SHARED.with_(layers=2)
+    tw = make_weights(t_shape, seed=0, device="cuda")
+    dw = shared_embedding_draft(make_weights(QWEN05B.with_(layers=2), seed=2, device="cuda"), tw["embed"],
+                                d_shape.hidden)
+    eng = pkg.SpecEngine(t_shape, tw, d_shape, dw, batch=1, K=K, s_max=4096)
+    _poison(eng)
+    prompt = uniform_prompt(2048, t_shape.vocab, seed=103).tolist()
+    eng.prefill([prompt])
+    d_out = torch.zeros(K, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros(K, t_shape.vocab, dtype=torch.float32, device="cuda")
+    t_log = torch.zeros(K + 1, t_shape.vocab, dtype=torch.float32, device="cuda")
+    eng.draft(d_out, d_log)
+    eng.verify(None, t_log)
+    torch.cuda.synchronize()
+    eng.accept_rollback()
+    eng.close()
+    d = d_out.cpu().tolist()
+    tw_c, dw_c = to_cpu(tw), to_cpu(dw)
+    del tw, dw
+    torch.cuda.empty_cache()
+    dm = om.Model(d_shape, dw_c, rowwise=False)
+    dc = dm.new_cache()
+    dm.forward(prompt[:-1], dc, logit_rows=[])
+    feed, worst_d = [prompt[-1]], 0.0
+    for i in range(K):
+        worst_d = max(worst_d, logit_err(d_log[i], dm.forward(feed, dc)[0]))
+        feed = [d[i]]
+    tm = om.Model(t_shape, tw_c, rowwise=False)
+    tc = tm.new_cache()
+    tm.forward(prompt[:-1], tc, logit_rows=[])
+    ref = tm.forward([prompt[-1]] + d, tc)
+    worst_t = max(logit_err(t_log[j], ref[j]) for j in range(K + 1))
+    print(f"ctx 2048: draft {worst_d:.3e}, 7B-shape verify {worst_t:.3e} (max logit error / range)")
+    assert worst_d < LOGIT_TOL_BF16 and worst_t < LOGIT_TOL_BF16
+
+
+@pytest.mark.parametrize("name,shape,ctx,s_max", [
+    ("hd128_55_chunks", HD128_G7, 3500, 4096),
+    ("hd64_102_chunks", TINY_TARGET, 6500, 8192),
+])
+def test_attention_merge_beyond_one_round(pkg, name, shape, ctx, s_max):
+    K = 4
+    w = make_weights(shape, seed=23)
+    g = to_cuda(w)
+    eng = pkg.SpecEngine(shape, g, shape, g, batch=1, K=K, s_max=s_max)
+    _poison(eng)
+    prompt = uniform_prompt(ctx, shape.vocab, seed=24).tolist()
+    eng.prefill([prompt])
+    d_out = torch.zeros(K, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros(K, shape.vocab, dtype=torch.float32, device="cuda")
+    t_log = torch.zeros(K + 1, shape.vocab, dtype=torch.float32, device="cuda")
+    eng.draft(d_out, d_log)
+    eng.verify(None, t_log)
+    torch.cuda.synchronize()
+    assert torch.equal(d_log, t_log[:K])         # draft = target: decode rows equal verify rows
+    n_acc, _ = eng.accept_rollback()
+    assert int(n_acc[0]) == K
+    eng.close()
+    m = om.Model(shape, w)
+    c = m.new_cache()
+    m.forward(prompt[:-1], c, logit_rows=[])
+    ref = m.forward([prompt[-1]] + d_out.cpu().tolist(), c)
+    worst = max(logit_err(t_log[j], ref[j]) for j in range(K + 1))
+    print(f"{name}: max logit error / range = {worst:.3e}")
+    assert worst < LOGIT_TOL_BF16
+
+
+def test_batch8_ragged_long_contexts(pkg):
+    """Eight sequences, K = 8 (72 verify rows in five 16-row groups), the
+    longest at 3300 tokens: 52 chunks at head dim 128."""
+    K, shape = 8, HD128_G7
+    lens = [3300, 200, 1500, 40, 900, 3150, 12, 700]
+    B = len(lens)
+    w = make_weights(shape, seed=25)
+    g = to_cuda(w)
+    prompts = [uniform_prompt(n, shape.vocab, seed=400 + b).tolist() for b, n in enumerate(lens)]
+    eng = pkg.SpecEngine(shape, g, shape, g, batch=B, K=K, s_max=4096)
+    _poison(eng)
+    eng.prefill(prompts)
+    d_out = torch.zeros(B, K, dtype=torch.int32, device="cuda")
+    d_log = torch.zeros(B, K, shape.vocab, dtype=torch.float32, device="cuda")
+    t_log = torch.zeros(B, K + 1, shape.vocab, dtype=torch.float32, device="cuda")
+    eng.draft(d_out, d_log)
+    eng.verify(None, t_log)
+    torch.cuda.synchronize()
+    assert torch.equal(d_log, t_log[:, :K])
+    n_acc, _ = eng.accept_rollback()
+    assert [int(n) for n in n_acc] == [K] * B
+    lt, _ = eng.lengths()
+    assert [int(x) for x in lt] == [n + K for n in lens]
+    eng.close()
+    m = om.Model(shape, w)
+    worst = 0.0
+    for b in range(B):
+        c = m.new_cache()
+        m.forward(prompts[b][:-1], c, logit_rows=[])
+        ref = m.forward([prompts[b][-1]] + d_out[b].cpu().tolist(), c)
+        worst = max(worst, max(logit_err(t_log[b, j], ref[j]) for j in range(K + 1)))
+    print(f"batch 8, contexts up to 3300: max logit error / range = {worst:.3e}")
+    assert worst < LOGIT_TOL_BF16
+
+
+def test_05b_shape_stream_over_rounds(pkg):
+    """The 0.5B shape drafting for itself (every guess accepted), four
+    replayed rounds = 36 tokens, scored by the oracle at every position."""
+    w = make_weights(QWEN05B, seed=0, device="cuda")
+    eng = pkg.SpecEngine(QWEN05B, w, QWEN05B, w, batch=1, K=8, s_max=4096)
+    _poison(eng)
+    prompt = uniform_prompt(20, QWEN05B.vocab, seed=101).tolist()
+    eng.prefill([prompt])
+    out, rounds = eng.generate(36)
+    eng.close()
+    assert rounds == 4
+    m = om.Model(QWEN05B, to_cpu(w), memoize=True, rowwise=False)
+    n, flips, near = stream_report(m, prompt, out[0].tolist())
+    print(f"0.5B shape, {n} tokens over {rounds} rounds: {flips} flips, {near} near-tie positions")
+
+
+def test_7b_shape_stream_with_draft(pkg):
+    """Two-layer 7B shape with the two-layer shared-embedding 0.5B draft:
+    32 tokens from a 64-token prompt through replayed round graphs."""
+    t_shape = QWEN7B.with_(layers=2)
+    d_shape = QWEN05B_SHARED.with_(layers=2)
+    tw = make_weights(t_shape, seed=0, device="cuda")
+    dw = shared_embedding_draft(make_weights(QWEN05B.with_(layers=2), seed=2, device="cuda"), tw["embed"],
+                                d_shape.hidden)
+    eng = pkg.SpecEngine(t_shape, tw, d_shape, dw, batch=1, K=8, s_max=4096)
+    _poison(eng)
+    prompt = uniform_prompt(64, t_shape.vocab, seed=104).tolist()
+    eng.prefill([prompt])
+    out, rounds = eng.generate(32)
+    eng.close()
+    tw_c = to_cpu(tw)
+    del tw, dw
+    torch.cuda.empty_cache()
+    m = om.Model(t_shape, tw_c, memoize=True, rowwise=False)
+    n, flips, near = stream_report(m, prompt, out[0].tolist())
+    print(f"7B shape (2 layers), {n} tokens over {rounds} rounds: {flips} flips, {near} near-tie positions")

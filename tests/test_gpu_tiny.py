@@ -398,3 +398,46 @@ def test_round_graph_kernel_count(pkg, tiny):
     eng.step()
     assert eng.round_launches() == 1 + per_fwd(TINY_TARGET) + 1
     eng.close()
+
+
+def test_expired_wait_is_reported(pkg, tiny, monkeypatch):
+    """The device error path of the bounded waits: with SF_TEST_WAIT_EXPIRE=1
+    every projection's first weight-tile wait gives up at once (and then
+    completes normally), the kernels set the wait bit, and the next host
+    synchronisation returns SF_ERR_DEVICE; the CUDA context stays usable and
+    an engine created without the switch runs a correct round afterwards."""
+    from greedy_speculative_decoding_gb300 import SFError
+    from greedy_speculative_decoding_gb300 import _lib as L
+    prompt = uniform_prompt(32, 1024, seed=100).tolist()
+    monkeypatch.setenv("SF_TEST_WAIT_EXPIRE", "1")
+    eng = make_engine(pkg, tiny, K=4)
+    monkeypatch.delenv("SF_TEST_WAIT_EXPIRE")
+    eng.prefill([prompt])
+    with pytest.raises(SFError) as e:
+        eng.step()
+    assert e.value.status == L.SF_ERR_DEVICE
+    assert "bounded wait" in str(e.value)
+    eng.close()
+    ok = make_engine(pkg, tiny, K=4)
+    ok.prefill([prompt])
+    out, _ = ok.generate(8)
+    ok.close()
+    assert out[0].tolist() == od.greedy(om.Model(TINY_TARGET, tiny[0]), prompt, 8)
+
+
+def test_no_drafter_is_plain_greedy(pkg, tiny):
+    """SF_DRAFT_NONE: every round proposes nothing, verifies the pending
+    token and commits the target's own choice, i.e. plain greedy decoding;
+    the round graph is the (empty) lookup, one verify forward and the
+    acceptance kernel."""
+    tw = tiny[0]
+    prompt = uniform_prompt(32, 1024, seed=100).tolist()
+    eng = make_engine(pkg, tiny, K=1)
+    eng.prefill([prompt])
+    eng.set_drafter(pkg.SF_DRAFT_NONE)
+    out, rounds = eng.generate(20)
+    hist = eng.accept_hist()
+    assert rounds == 20 and hist[0].tolist() == [20, 0]
+    assert eng.round_launches() == 1 + (2 + 6 * TINY_TARGET.layers) + 1
+    eng.close()
+    assert out[0].tolist() == od.greedy(om.Model(TINY_TARGET, tw), prompt, 20)

@@ -157,3 +157,18 @@ def test_rollback_cache_equals_fresh_prefix(tiny_models):
         for l in range(TINY_TARGET.layers):
             assert torch.equal(tc.keys(l), fresh.keys(l))
             assert torch.equal(tc.values(l), fresh.values(l))
+
+
+def test_planted_prompts_give_every_accept_length():
+    """The prompts the GPU accept tests use: prompt lookup proposes K = 4
+    guesses of which exactly the first j agree with greedy decoding, for
+    every j in 0..4 (checked against the oracle's own greedy continuation)."""
+    from accept_prompts import planted_prompt
+    from synth import TINY_TARGET, make_weights
+    m = om.Model(TINY_TARGET, make_weights(TINY_TARGET, seed=0))
+    for j in range(5):
+        P, g = planted_prompt(m, TINY_TARGET.vocab, j, K=4, seed=7 + j, a_len=20 + 3 * j)
+        prop = od.ngram_propose(P, 4, 2, 4)
+        assert len(prop) == 4
+        assert od.accept_length(prop, g + [-1] * (5 - len(g)), 4) == j
+        assert g == od.greedy(m, P, j + 1)

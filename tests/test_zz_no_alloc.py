@@ -1,6 +1,6 @@
 """sf_linear_noalloc: the projection for callers that cannot allocate device
-memory (graph capture in progress, a host framework that owns every
-allocation, latency-critical loops). It must give the same result as
+memory (a host framework that owns every allocation, latency-critical loops
+that cannot take cudaMalloc's implicit synchronisation). It must give the same result as
 sf_linear with a caller-provided workspace, on consecutive calls that reuse
 the library's static scratch, and refuse sizes beyond its limit.
 
@@ -81,3 +81,11 @@ def test_noalloc_rejects_sizes_beyond_the_limit(lib):
     rc = lib.sf_linear_noalloc(w.data_ptr(), (1 << 20) + 1, 64, 64, x.data_ptr(), 1, y.data_ptr(), st)
     assert rc == L.SF_ERR_ARG
     assert b"static scratch" in lib.sf_last_error()
+    # N within its limit, but K one 64-wide chunk past what the scratch holds
+    # for the operand copy: refused by the byte check (no launch happens).
+    rc = lib.sf_linear_noalloc(w.data_ptr(), 1 << 20, 65600, 65600, x.data_ptr(), 1, y.data_ptr(), st)
+    assert rc == L.SF_ERR_ARG
+    assert b"static scratch" in lib.sf_last_error()
+    rc = lib.sf_linear_noalloc(w.data_ptr(), 8, 60, 64, x.data_ptr(), 1, y.data_ptr(), st)
+    assert rc == L.SF_ERR_ARG
+    assert b"multiple of 8" in lib.sf_last_error()
