@@ -137,8 +137,8 @@ int nblocks_of(const sf_model_cfg* c, int which) {
 // acc_hist, then the report block (ncommit, nacc, commit, total, err) that
 // one copy brings back to the host.
 struct StateOff {
-  size_t len_t, len_d, vtok, ttok, dtok0, nprop, hist, prompt_len, acc_hist, report, ncommit, nacc, commit,
-      total, err, n_ints, report_ints;
+  size_t len_t, len_d, vtok, ttok, dtok0, nprop, hist, prompt_len, acc_hist, loop_target, report, ncommit, nacc,
+      commit, total, err, rounds, n_ints, report_ints;
 };
 
 StateOff state_offsets(int B, int K, int s_max) {
@@ -159,6 +159,7 @@ StateOff state_offsets(int B, int K, int s_max) {
   o.hist = take((size_t)B * s_max);
   o.prompt_len = take(B);
   o.acc_hist = take(B * K1);
+  o.loop_target = take(1);
   o.report = p;
   o.ncommit = p;
   p += B;
@@ -169,6 +170,8 @@ StateOff state_offsets(int B, int K, int s_max) {
   o.total = p;
   p += B;
   o.err = p;
+  p += 1;
+  o.rounds = p;
   p += 1;
   o.report_ints = p - o.report;
   o.n_ints = p;
@@ -249,6 +252,8 @@ struct sf_engine {
   int* pin = nullptr;   // pinned host copy of the report block
   cudaGraphExec_t graph[3] = {nullptr, nullptr, nullptr};   // whole round, per drafter (SF_DRAFT_*)
   size_t graph_kernels[3] = {0, 0, 0};                      // kernel launches in each round graph
+  cudaGraphExec_t loop[3] = {nullptr, nullptr, nullptr};    // sf_generate: rounds in a device-side WHILE loop
+  bool host_loop = false;   // SF_HOST_LOOP=1: sf_generate replays the round graph from the host instead
   cudaGraphExec_t g_draft = nullptr, g_verify = nullptr;
   int drafter = SF_DRAFT_NEURAL, ng_min = 2, ng_max = 4;
   std::vector<int> C;   // committed tokens per sequence (host mirror)
@@ -668,6 +673,61 @@ sf_status build_graph(sf_engine* e, int what) {
   return SF_OK;
 }
 
+// The whole generation as one graph: a WHILE conditional node whose body is
+// the round of drafter `mode` followed by the loop control kernel (see
+// k_loop_ctl), captured into the body with the kernels' programmatic
+// dependent launches; if the body does not take them, it is captured without.
+sf_status build_loop_graph(sf_engine* e, int mode) {
+  if (e->loop[mode]) return SF_OK;
+  cudaError_t last = cudaSuccess;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    const bool pdl_saved = e->pdl;
+    if (attempt == 1) e->pdl = false;
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t ex = nullptr;
+    size_t nodes = 0;
+    sf_status r = SF_OK;
+    cudaError_t ce = cudaGraphCreate(&g, 0);
+    cudaGraphConditionalHandle hnd{};
+    if (ce == cudaSuccess) ce = cudaGraphConditionalHandleCreate(&hnd, g, 1, cudaGraphCondAssignDefault);
+    cudaGraph_t body = nullptr;
+    if (ce == cudaSuccess) {
+      cudaGraphNodeParams np = {};
+      np.type = cudaGraphNodeTypeConditional;
+      np.conditional.handle = hnd;
+      np.conditional.type = cudaGraphCondTypeWhile;
+      np.conditional.size = 1;
+      cudaGraphNode_t node;
+      ce = cudaGraphAddNode(&node, g, nullptr, nullptr, 0, &np);
+      if (ce == cudaSuccess) body = np.conditional.phGraph_out[0];
+    }
+    if (ce == cudaSuccess) ce = cudaStreamBeginCaptureToGraph(e->cap, body, nullptr, nullptr, 0,
+                                                              cudaStreamCaptureModeThreadLocal);
+    if (ce == cudaSuccess) {
+      r = enqueue_round(e, mode, e->cap);
+      const cudaError_t lc = r == SF_OK ? launch_loop_ctl(e->st, hnd, e->cap) : cudaSuccess;
+      cudaGraph_t out = nullptr;
+      ce = cudaStreamEndCapture(e->cap, &out);
+      if (ce == cudaSuccess) ce = lc;
+    }
+    if (ce == cudaSuccess && r == SF_OK) {
+      cudaGraphGetNodes(body, nullptr, &nodes);
+      ce = cudaGraphInstantiate(&ex, g, 0);
+    }
+    e->pdl = pdl_saved;
+    if (g) cudaGraphDestroy(g);
+    if (r != SF_OK) return r;
+    if (ce == cudaSuccess) {
+      e->loop[mode] = ex;
+      if (!e->graph_kernels[mode] && nodes > 0) e->graph_kernels[mode] = nodes - 1;   // the round without the control kernel
+      return SF_OK;
+    }
+    cudaGetLastError();   // clear a sticky launch error of the failed attempt
+    last = ce;
+  }
+  return fail(SF_ERR_CUDA, "device loop graph: %s", cudaGetErrorString(last));
+}
+
 // Copy the report block to pinned memory, wait, and turn device error bits
 // into a status (clearing them).
 sf_status sync_report(sf_engine* e) {
@@ -768,6 +828,9 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   // gives up at once and reports it (the wait then completes normally), so
   // tests can drive the device error path without stalling a kernel.
   if (const char* v = getenv("SF_TEST_WAIT_EXPIRE")) e->expire_waits = v[0] == '1';
+  // SF_HOST_LOOP=1: sf_generate replays the round graph from the host (for
+  // comparing with the device-resident loop; results are identical).
+  if (const char* v = getenv("SF_HOST_LOOP")) e->host_loop = v[0] == '1';
   // SF_TRACE=1: kernels stamp a launch timeline (see sf_trace).
   const char* tr = getenv("SF_TRACE");
   const bool trace_on = tr && tr[0] == '1';
@@ -823,6 +886,8 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   st.commit = S + e->so.commit;
   st.total = S + e->so.total;
   st.err = S + e->so.err;
+  st.loop_target = S + e->so.loop_target;
+  st.rounds = S + e->so.rounds;
   st.B = batch;
   st.K = K;
   st.s_max = s_max;
@@ -855,6 +920,8 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
 void sf_destroy(sf_handle h) {
   if (!h) return;
   for (auto& g : h->graph)
+    if (g) cudaGraphExecDestroy(g);
+  for (auto& g : h->loop)
     if (g) cudaGraphExecDestroy(g);
   if (h->g_draft) cudaGraphExecDestroy(h->g_draft);
   if (h->g_verify) cudaGraphExecDestroy(h->g_verify);
@@ -936,6 +1003,10 @@ sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n
     if (h->graph[SF_DRAFT_NGRAM]) {
       cudaGraphExecDestroy(h->graph[SF_DRAFT_NGRAM]);
       h->graph[SF_DRAFT_NGRAM] = nullptr;
+    }
+    if (h->loop[SF_DRAFT_NGRAM]) {
+      cudaGraphExecDestroy(h->loop[SF_DRAFT_NGRAM]);
+      h->loop[SF_DRAFT_NGRAM] = nullptr;
     }
     h->ng_min = min_n;
     h->ng_max = max_n;
@@ -1039,25 +1110,43 @@ sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rou
   const int mode = h->drafter;
   if (mode == SF_DRAFT_NEURAL && h->draft_stale)
     return fail(SF_ERR_STATE, "draft cache is behind after n-gram rounds; call sf_reset or sf_prefill");
-  sf_status r = build_graph(h, mode);
-  if (r != SF_OK) return r;
   const int K1 = h->K + 1;
+  auto gen_min = [&]() {
+    int g = 1 << 30;
+    for (int b = 0; b < h->B; ++b) g = std::min(g, h->C[b] - h->P[b]);
+    return g;
+  };
   int rounds = 0;
-  for (;;) {
-    int gen_min = 1 << 30;
-    for (int b = 0; b < h->B; ++b) gen_min = std::min(gen_min, h->C[b] - h->P[b]);
-    const int remaining = n_new - gen_min;
-    if (remaining <= 0) break;
-    // Each round commits at most K+1 tokens, so this many rounds never
-    // overshoots the target by more than one round's worth.
-    int R = (remaining + K1 - 1) / K1;
-    const int room = (h->s_max - h->K - 1 - max_committed(h)) / K1;
-    R = std::min(R, room);
-    if (R < 1) return fail(SF_ERR_CAPACITY, "s_max reached after %d new tokens", gen_min);
-    for (int i = 0; i < R; ++i) CK(cudaGraphLaunch(h->graph[mode], h->user));
-    rounds += R;
-    if (mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
-    if ((r = sync_report(h)) != SF_OK) return r;
+  sf_status r;
+  if (!h->host_loop) {
+    // Device-resident loop: one graph launch runs every round; the host
+    // synchronises once at the end.
+    if (gen_min() < n_new) {
+      if (max_committed(h) + 2 * K1 > h->s_max) return fail(SF_ERR_CAPACITY, "s_max reached after %d new tokens", gen_min());
+      if ((r = build_loop_graph(h, mode)) != SF_OK) return r;
+      CK(launch_loop_init(h->st, n_new, h->user));
+      CK(cudaGraphLaunch(h->loop[mode], h->user));
+      if (mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
+      if ((r = sync_report(h)) != SF_OK) return r;
+      rounds = h->pin[h->so.rounds - h->so.report];
+      if (gen_min() < n_new) return fail(SF_ERR_CAPACITY, "s_max reached after %d new tokens", gen_min());
+    }
+  } else {
+    if ((r = build_graph(h, mode)) != SF_OK) return r;
+    for (;;) {
+      const int remaining = n_new - gen_min();
+      if (remaining <= 0) break;
+      // Each round commits at most K+1 tokens, so this many rounds never
+      // overshoots the target by more than one round's worth.
+      int R = (remaining + K1 - 1) / K1;
+      const int room = (h->s_max - h->K - 1 - max_committed(h)) / K1;
+      R = std::min(R, room);
+      if (R < 1) return fail(SF_ERR_CAPACITY, "s_max reached after %d new tokens", gen_min());
+      for (int i = 0; i < R; ++i) CK(cudaGraphLaunch(h->graph[mode], h->user));
+      rounds += R;
+      if (mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
+      if ((r = sync_report(h)) != SF_OK) return r;
+    }
   }
   if (h_out)
     for (int b = 0; b < h->B; ++b)

@@ -131,6 +131,41 @@ cudaError_t launch_ngram(const SpecState& s, int max_guess, int min_n, int max_n
   return cudaLaunchKernelEx(&cfg, k_ngram, s, max_guess, min_n, max_n, d_prop, d_count);
 }
 
+// ---------------------------------------------------------------- device loop
+// sf_generate as one graph launch: a WHILE conditional node whose body is one
+// round followed by k_loop_ctl. The control kernel counts the round and lets
+// the loop run again while some sequence has fewer than the target number of
+// new tokens, every sequence has room for two more rounds (so acceptance
+// never raises the capacity flag), no error bit is set, and fewer rounds than
+// the target have run (each round commits at least one token per sequence,
+// so that bound never stops a loop that still has work).
+__global__ void k_loop_init(const __grid_constant__ SpecState s, int n_new) {
+  *s.loop_target = n_new;
+  *s.rounds = 0;
+}
+
+__global__ void k_loop_ctl(const __grid_constant__ SpecState s, cudaGraphConditionalHandle h) {
+  const int r = *s.rounds + 1;
+  *s.rounds = r;
+  const int target = *s.loop_target;
+  bool need = false, room = true;
+  for (int b = 0; b < s.B; ++b) {
+    need = need || s.total[b] < target;
+    room = room && s.len_t[b] + 1 + 2 * (s.K + 1) <= s.s_max;
+  }
+  cudaGraphSetConditional(h, (need && room && *s.err == 0 && r < target) ? 1u : 0u);
+}
+
+cudaError_t launch_loop_init(const SpecState& s, int n_new, cudaStream_t st) {
+  k_loop_init<<<1, 1, 0, st>>>(s, n_new);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loop_ctl(const SpecState& s, cudaGraphConditionalHandle h, cudaStream_t st) {
+  k_loop_ctl<<<1, 1, 0, st>>>(s, h);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- reset
 // Back to "prompt prefilled": caches hold prompt[0..P-1), prompt[P-1] pending.
 __global__ void k_reset(const __grid_constant__ SpecState s) {

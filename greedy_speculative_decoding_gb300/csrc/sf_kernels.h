@@ -158,6 +158,8 @@ struct SpecState {
   int* acc_hist;    // [B][K+1] accept-length histogram
   int* prompt_len;  // [B]
   int* err;
+  int* loop_target; // device-resident loop: new tokens per sequence to reach
+  int* rounds;      // device-resident loop: rounds run by the current sf_generate
   int B, K, s_max;
 };
 
@@ -168,6 +170,11 @@ cudaError_t launch_accept(const SpecState& s, int mode, cudaStream_t st, bool pd
 cudaError_t launch_ngram(const SpecState& s, int max_guess, int min_n, int max_n, int* d_prop,
                          int* d_count, cudaStream_t st, bool pdl);
 cudaError_t launch_reset(const SpecState& s, cudaStream_t st);
+// Device-resident round loop: set the target and clear the round count
+// (before the loop graph), and the control kernel at the end of every round
+// that decides whether the loop runs another round.
+cudaError_t launch_loop_init(const SpecState& s, int n_new, cudaStream_t st);
+cudaError_t launch_loop_ctl(const SpecState& s, cudaGraphConditionalHandle h, cudaStream_t st);
 cudaError_t launch_copy_draft(const SpecState& s, int* d_draft, cudaStream_t st);
 void nf4_levels(double out[16]);
 cudaError_t launch_nf4_quantize(const bf16* w, int rows, int cols, int ld, uint8_t* packed,

@@ -207,10 +207,17 @@ SF_API sf_status sf_accept_rollback(sf_handle h, int32_t* h_n_accepted, int32_t*
 SF_API sf_status sf_step(sf_handle h, int32_t* h_n_committed, int32_t* h_committed);
 
 /*
- * Run rounds until every sequence has at least n_new new tokens, replaying
- * the step graph back to back and synchronising only to count. h_out: host
- * [batch][n_new] (the first n_new generated tokens). h_rounds: rounds run
- * (may be NULL).
+ * Run rounds until every sequence has at least n_new new tokens since its
+ * prompt. The rounds run on the device as one graph launch: a WHILE
+ * conditional node repeats the round graph, and a control kernel at the end
+ * of each round decides on the device whether another round is needed and
+ * fits in s_max (the pages' single driver call for the draft, "CUDA Graphs:
+ * What They Are and Why They Helped", taken to the whole generation); the
+ * host synchronises once. With SF_HOST_LOOP=1 in the environment at
+ * sf_create the host replays the round graph instead, synchronising only to
+ * count (same tokens). h_out: host [batch][n_new] (the first n_new generated
+ * tokens). h_rounds: rounds run (may be NULL). SF_ERR_CAPACITY when s_max
+ * runs out first.
  */
 SF_API sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t* h_rounds);
 
@@ -243,9 +250,10 @@ SF_API sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist);
 SF_API int32_t sf_trace(sf_handle h, uint64_t* h_out, int32_t max_launches);
 SF_API const char* sf_trace_label(sf_handle h, int32_t i);
 
-/* Kernel launches in one replay of the round graph of the current drafter
- * (its node count; every node is a kernel), or 0 before the graph has been
- * built by sf_step / sf_generate. */
+/* Kernel launches in one round of the current drafter (the node count of
+ * its round graph; every node is a kernel; sf_generate's device loop adds one
+ * control kernel per round), or 0 before a round graph has been built by
+ * sf_step / sf_generate. */
 SF_API int64_t sf_round_launches(sf_handle h);
 
 /* Name of a status code; message of the calling thread's last failure. */

@@ -441,3 +441,32 @@ def test_no_drafter_is_plain_greedy(pkg, tiny):
     assert eng.round_launches() == 1 + (2 + 6 * TINY_TARGET.layers) + 1
     eng.close()
     assert out[0].tolist() == od.greedy(om.Model(TINY_TARGET, tw), prompt, 20)
+
+
+@pytest.mark.parametrize("batch,mode", [(1, "neural"), (4, "neural"), (1, "ngram"), (3, "none")])
+def test_device_loop_equals_host_loop(pkg, tiny, monkeypatch, batch, mode):
+    """sf_generate's device-resident loop (one graph launch: a WHILE
+    conditional node around the round, a control kernel deciding on the
+    device) gives the same tokens, round count and accept histogram as the
+    host replaying the round graph (SF_HOST_LOOP=1)."""
+    lens = [32, 45, 27, 38][:batch]
+    prompts = [uniform_prompt(n, 1024, seed=500 + b).tolist() for b, n in enumerate(lens)]
+    if mode == "ngram":
+        prompts = [ngram_prompt(96, 0.8, 1024, seed=201, base_len=48, seg_lo=8, seg_hi=16)[0].tolist()]
+    res = []
+    for host in ("1", "0"):
+        monkeypatch.setenv("SF_HOST_LOOP", host)
+        eng = make_engine(pkg, tiny, K=4, batch=batch, draft=mode == "neural")
+        monkeypatch.delenv("SF_HOST_LOOP")
+        eng.prefill(prompts)
+        if mode == "none":
+            eng.set_drafter(pkg.SF_DRAFT_NONE)
+        out, rounds = eng.generate(40)
+        out2, rounds2 = eng.generate(60)      # continues from 40 tokens
+        res.append((out.tolist(), rounds, out2.tolist(), rounds2, eng.accept_hist().tolist(), eng.lengths()))
+        eng.close()
+    (o1, r1, p1, q1, h1, l1), (o2, r2, p2, q2, h2, l2) = res
+    assert o1 == o2 and p1 == p2 and h1 == h2
+    assert r1 == r2 and q1 == q2, (r1, r2, q1, q2)
+    assert all((a == b).all() for a, b in zip(l1, l2))
+    assert r2 > 0 and q2 > 0
