@@ -68,6 +68,8 @@ enum { W_Q = 0, W_K, W_V, W_O, W_G, W_U, W_D };
 struct LayerW {
   CUtensorMap tm[7];
   CUtensorMap tms[7];      // NF4 block scales
+  CUtensorMap tmu[7];      // the same with 64-row boxes, for the tcgen05 GEMM (forwards of > 16 rows)
+  CUtensorMap tmsu[7];
   const void* w[7] = {};
   const void* sc[7] = {};  // NF4 block scales
   const bf16 *ln1 = nullptr, *ln2 = nullptr, *bq = nullptr, *bk = nullptr, *bv = nullptr;
@@ -85,6 +87,7 @@ struct Model {
   bf16* kv = nullptr;
   float2* rope = nullptr;
   Plan p_qkv, p_o, p_gu, p_d, p_lm;
+  Plan u_qkv, u_o, u_gu, u_d;   // tcgen05 GEMM plans (forwards of more than 16 rows)
   int q_dim() const { return c.n_heads * c.head_dim; }
   int kv_dim() const { return c.n_kv_heads * c.head_dim; }
 };
@@ -322,8 +325,11 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     const int rows[7] = {QD, KVD, KVD, H, F, F, H};
     const int ks[7] = {H, H, H, QD, H, H, F};
     for (int k = 0; k < 7; ++k) {
-      const cudaError_t ce = nf4 ? make_nf4_maps(&lw.tm[k], &lw.tms[k], lw.w[k], lw.sc[k], rows[k], ks[k])
-                                 : make_weight_map(&lw.tm[k], lw.w[k], rows[k], ks[k], ks[k]);
+      cudaError_t ce = nf4 ? make_nf4_maps(&lw.tm[k], &lw.tms[k], lw.w[k], lw.sc[k], rows[k], ks[k])
+                           : make_weight_map(&lw.tm[k], lw.w[k], rows[k], ks[k], ks[k]);
+      if (ce == cudaSuccess)
+        ce = nf4 ? make_nf4_maps(&lw.tmu[k], &lw.tmsu[k], lw.w[k], lw.sc[k], rows[k], ks[k], 64)
+                 : make_weight_map(&lw.tmu[k], lw.w[k], rows[k], ks[k], ks[k], 64);
       if (ce != cudaSuccess)
         return fail(SF_ERR_CUDA, "layer %d weight %d: tensor map: %s", l, k, cudaGetErrorString(ce));
     }
@@ -358,6 +364,19 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   md.p_o = plan(nblocks_of(c, 1), H, (long)c->n_heads * c->head_dim);
   md.p_gu = plan(nblocks_of(c, 2), 2l * c->ffn, H);
   md.p_d = plan(nblocks_of(c, 1), H, c->ffn);
+  // tcgen05 GEMM: two CTAs per SM whatever the row count, K slices in
+  // clusters of at most 8 that fit with a fifth of the cluster slots to spare.
+  auto uplan = [&](int nblocks, long k) {
+    const int stages = umma_stages(kRows, nf4);
+    Plan p = make_plan(nblocks, (int)k, 2 * e->num_sms, 8, al);
+    while (p.nsplit > 1 && 5 * p.nblocks > 4 * umma_max_clusters(p.nsplit, kRows, stages, nf4))
+      p = make_plan(nblocks, (int)k, 2 * e->num_sms, p.nsplit - 1, al);
+    return p;
+  };
+  md.u_qkv = uplan(nblocks_of(c, 0), H);
+  md.u_o = uplan(nblocks_of(c, 1), (long)c->n_heads * c->head_dim);
+  md.u_gu = uplan(nblocks_of(c, 2), H);
+  md.u_d = uplan(nblocks_of(c, 1), c->ffn);
   md.p_lm.nblocks = nblocks_of(c, 3);   // the persistent LM head: no K split
   md.p_lm.nsplit = 1;
   md.p_lm.cps = (H + kChunk - 1) / kChunk;
@@ -409,6 +428,20 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   const sf_model_cfg& c = md.c;
   const int nf4 = c.wdtype == SF_WDTYPE_NF4 ? 1 : 0;
   const int H = c.hidden, QD = md.q_dim(), KVD = md.kv_dim();
+  // More than 16 token rows: the projections run on the tcgen05 GEMM, whose
+  // inputs the producers write in the tensor-core operand order (the LM head
+  // keeps reading fragment order).
+  const bool tc = rs.M > kGroupRows;
+  auto gemm = [&](const GemmArgs& a, int epi) {
+    return tc ? launch_umma(a, epi, s, e->pdl) : launch_gemm(a, epi, s, e->pdl);
+  };
+  auto maps = [&](GemmArgs& a, const LayerW& lw, int slot, int w) {
+    a.tm[slot] = tc ? lw.tmu[w] : lw.tm[w];
+    a.tms[slot] = tc ? lw.tmsu[w] : lw.tms[w];
+  };
+  auto stages = [&](const GemmArgs& a) {
+    return tc ? umma_stages(rs.M, nf4) : pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
+  };
   EmbedArgs ea{};
   ea.E = md.embed;
   ea.ld = md.embed_ld;
@@ -419,6 +452,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.ssq = e->ssq;
   ea.frag = e->fx;
   ea.gain = md.L[0].ln1;
+  ea.umma = tc;
   ea.rs = traced(e, rs, "embed");
   CK(launch_embed(ea, s, e->pdl));
   const size_t seq_elems = (size_t)c.n_kv_heads * e->s_max * c.head_dim;   // one sequence's keys of a layer
@@ -432,18 +466,15 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
       vc += seq * seq_elems;
     }
     // q, k, v (+ bias, RoPE, cache append)
-    GemmArgs a = base_args(e, md, md.p_qkv, rs);
+    GemmArgs a = base_args(e, md, tc ? md.u_qkv : md.p_qkv, rs);
     a.w[0] = lw.w[W_Q];
     a.w[1] = lw.w[W_K];
     a.w[2] = lw.w[W_V];
-    a.tm[0] = lw.tm[W_Q];
-    a.tm[1] = lw.tm[W_K];
-    a.tm[2] = lw.tm[W_V];
-    a.tms[0] = lw.tms[W_Q];
-    a.tms[1] = lw.tms[W_K];
-    a.tms[2] = lw.tms[W_V];
+    maps(a, lw, 0, W_Q);
+    maps(a, lw, 1, W_K);
+    maps(a, lw, 2, W_V);
     a.nf4 = nf4;
-    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
+    a.stages = stages(a);
     a.bias[0] = lw.bq;
     a.bias[1] = lw.bk;
     a.bias[2] = lw.bv;
@@ -469,7 +500,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.vc = vc;
     a.rope = md.rope;
     a.rs = traced(e, rs, "qkv");
-    CK(launch_gemm(a, EPI_QKV, s, e->pdl));
+    CK(gemm(a, EPI_QKV));
     // attention
     AttnArgs t{};
     t.q = e->q;
@@ -485,16 +516,16 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     t.n_kv_chunks = e->lay.n_kv_chunks;
     t.scale = 1.0f / sqrtf((float)c.head_dim);
     t.err = e->st.err;
+    t.umma = tc;
     t.rs = traced(e, rs, "attention");
     t.merge_trace_id = traced(e, rs, "merge").trace_id;
     CK(launch_attention(t, e->num_sms, s, e->pdl));
     // o-projection + residual
-    a = base_args(e, md, md.p_o, rs);
+    a = base_args(e, md, tc ? md.u_o : md.p_o, rs);
     a.w[0] = lw.w[W_O];
-    a.tm[0] = lw.tm[W_O];
-    a.tms[0] = lw.tms[W_O];
+    maps(a, lw, 0, W_O);
     a.nf4 = nf4;
-    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
+    a.stages = stages(a);
     a.seg_end[0] = H;
     a.ld[0] = QD;
     a.nseg = 1;
@@ -506,18 +537,17 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.ssq_out = e->ssq;
     a.frag_out = e->fh;
     a.frag_gain = lw.ln2;
+    a.frag_umma = tc;
     a.rs = traced(e, rs, "o_proj");
-    CK(launch_gemm(a, EPI_RESID, s, e->pdl));
+    CK(gemm(a, EPI_RESID));
     // gate/up + SwiGLU
-    a = base_args(e, md, md.p_gu, rs);
+    a = base_args(e, md, tc ? md.u_gu : md.p_gu, rs);
     a.w[0] = lw.w[W_G];
     a.w[1] = lw.w[W_U];
-    a.tm[0] = lw.tm[W_G];
-    a.tm[1] = lw.tm[W_U];
-    a.tms[0] = lw.tms[W_G];
-    a.tms[1] = lw.tms[W_U];
+    maps(a, lw, 0, W_G);
+    maps(a, lw, 1, W_U);
     a.nf4 = nf4;
-    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
+    a.stages = stages(a);
     a.ld[0] = a.ld[1] = H;
     a.nseg = 2;
     a.N = c.ffn;
@@ -527,15 +557,15 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.nssq = H / 128;
     a.inv_k = 1.0f / H;
     a.frag_out = e->fa;
+    a.frag_umma = tc;
     a.rs = traced(e, rs, "gate_up");
-    CK(launch_gemm(a, EPI_SWIGLU, s, e->pdl));
+    CK(gemm(a, EPI_SWIGLU));
     // down + residual
-    a = base_args(e, md, md.p_d, rs);
+    a = base_args(e, md, tc ? md.u_d : md.p_d, rs);
     a.w[0] = lw.w[W_D];
-    a.tm[0] = lw.tm[W_D];
-    a.tms[0] = lw.tms[W_D];
+    maps(a, lw, 0, W_D);
     a.nf4 = nf4;
-    a.stages = pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
+    a.stages = stages(a);
     a.seg_end[0] = H;
     a.ld[0] = c.ffn;
     a.nseg = 1;
@@ -547,8 +577,9 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.ssq_out = e->ssq;
     a.frag_out = e->fx;   // the next layer's QKV input, or the LM head's
     a.frag_gain = l + 1 < c.layers ? md.L[l + 1].ln1 : md.norm;
+    a.frag_umma = tc && l + 1 < c.layers;   // the LM head reads fragment order
     a.rs = traced(e, rs, "down");
-    CK(launch_gemm(a, EPI_RESID, s, e->pdl));
+    CK(gemm(a, EPI_RESID));
   }
   if (!lm) return SF_OK;
   GemmArgs a = base_args(e, md, md.p_lm, rs);
@@ -900,7 +931,7 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
     float lf[16];
     nf4_levels(lv);
     for (int k = 0; k < 16; ++k) lf[k] = (float)lv[k];
-    if ((ce = set_nf4_levels(lf)) != cudaSuccess)
+    if ((ce = set_nf4_levels(lf)) != cudaSuccess || (ce = set_umma_nf4_levels(lf)) != cudaSuccess)
       return bail(fail(SF_ERR_CUDA, "NF4 levels: %s", cudaGetErrorString(ce)));
   }
   // Zero everything that must start at zero: counters, keys, state.
@@ -1203,6 +1234,7 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   int dev = 0, sms = 0;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const bool tc = M > kGroupRows;   // more than 16 rows: the tcgen05 GEMM
   const Plan p = make_plan((N + 127) / 128, K, 2 * sms, 1 << 30);
   const int groups = (M + kGroupRows - 1) / kGroupRows;
   if (p.nsplit > 1 && p.nblocks * p.nsplit * groups > kLinearTiles)
@@ -1213,7 +1245,7 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (p.nsplit > 1) CK(cudaMemsetAsync(ws + part_bytes, 0, (size_t)p.nblocks * groups * 4, st));   // arrival counters
   GemmArgs a{};
-  CK(make_weight_map(&a.tm[0], d_w, N, K, ld));
+  CK(make_weight_map(&a.tm[0], d_w, N, K, ld, tc ? 64 : 16));
   a.w[0] = d_w;
   a.seg_end[0] = N;
   a.ld[0] = ld;
@@ -1223,7 +1255,7 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   a.nblocks = p.nblocks;
   a.nsplit = p.nsplit;
   a.cps = p.cps;
-  a.stages = pick_stages(p.nblocks * p.nsplit, p.cps, sms);
+  a.stages = tc ? umma_stages(M, false) : pick_stages(p.nblocks * p.nsplit, p.cps, sms);
   a.in = static_cast<const uint4*>(d_frag);
   a.part = reinterpret_cast<float*>(ws);
   a.counter = reinterpret_cast<int*>(ws + part_bytes);
@@ -1231,7 +1263,7 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   a.out_ld = N;
   a.rs.M = M;
   a.rs.rps = M;
-  CK(launch_gemm(a, EPI_STORE, st, false));
+  CK(tc ? launch_umma(a, EPI_STORE, st, false) : launch_gemm(a, EPI_STORE, st, false));
   return SF_OK;
 }
 

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(128) k_embed(const __grid_constant__ EmbedArgs
   const int n = blk * 128 + i;
   const float v = __bfloat162float(a.E[(size_t)tok * a.ld + n]);
   a.x[(size_t)m * a.H + n] = v;
-  frag_store(a.frag, m, n, (a.rs.M + 3) / 4, v * __bfloat162float(a.gain[n]));
+  act_store(a.frag, m, n, (a.rs.M + 3) / 4, v * __bfloat162float(a.gain[n]), a.umma);
   const float s = warp_sum(v * v);
   if ((i & 31) == 0) part[i >> 5] = s;
   __syncthreads();
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
   const int nch = row_pos(a.rs, m) / kKvChunk + 1;
   const float v = merge_row_head(a.part, a.nq, a.hd, a.n_kv_chunks, m, h, nch, sm);
-  if ((int)threadIdx.x < a.hd) frag_store(a.out, m, h * a.hd + threadIdx.x, (a.rs.M + 3) / 4, v);
+  if ((int)threadIdx.x < a.hd) act_store(a.out, m, h * a.hd + threadIdx.x, (a.rs.M + 3) / 4, v, a.umma);
 }
 
 // Dynamic shared memory of the chunk kernel: keys, values, P hi + lo, and

@@ -41,7 +41,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "sf_kernels.h"
+#include "gemm_epi.cuh"
 
 namespace sf {
 
@@ -117,144 +117,6 @@ __device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v)
     v = w > v ? w : v;
   }
   return v;
-}
-
-// ---------------------------------------------------------------- epilogues
-// Global operands of the epilogue, loaded right after the kernel waits on
-// its producer so their latency overlaps the weight stream.
-template <int T>
-struct EpiPre {
-  static constexpr int kE = (4 * T * kBlockRows + kGemmThreads - 1) / kGemmThreads;
-  float v0[kE], v1[kE];
-  float2 cs[kE];
-};
-
-// Rows m < M of the CTA are token rows m0 + m of the forward.
-template <int T, int EPI>
-__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, int M, EpiPre<T>& pre,
-                                             const int* pos) {
-  constexpr int kE = EpiPre<T>::kE;
-  if (EPI == EPI_RESID) {
-#pragma unroll
-    for (int e = 0; e < kE; ++e) {
-      const int i = threadIdx.x + e * kGemmThreads;
-      const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
-      pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)(m0 + m) * a.out_ld + n] : 0.f;
-      pre.v1[e] = (a.frag_gain && n < a.N) ? __bfloat162float(a.frag_gain[n]) : 0.f;
-    }
-  } else if (EPI == EPI_QKV) {
-    const int half = a.hd >> 1;
-    const int n0 = rb * kBlockRows;
-    const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);   // one segment per block
-    const int seg0 = s ? a.seg_end[s - 1] : 0;
-    const bf16* bias = a.bias[s];
-#pragma unroll
-    for (int e = 0; e < kE; ++e) {
-      const int i = threadIdx.x + e * kGemmThreads;
-      const int m = i / kBlockRows, r = i - m * kBlockRows;
-      const int local = n0 + r - seg0;
-      const int d = local % a.hd;
-      pre.v0[e] = pre.v1[e] = 0.f;
-      pre.cs[e] = make_float2(1.f, 0.f);
-      if (m < M && n0 + r < a.N) {
-        if (bias) pre.v0[e] = __bfloat162float(bias[local]);
-        if (s < 2 && d < half) {
-          if (bias) pre.v1[e] = __bfloat162float(bias[local + half]);
-          pre.cs[e] = a.rope[(size_t)pos[m] * half + d];
-        }
-      }
-    }
-  }
-}
-
-template <int T>
-__device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int m0, int M, int Tt, const EpiPre<T>& pre) {
-  constexpr int kE = EpiPre<T>::kE;
-#pragma unroll
-  for (int e = 0; e < kE; ++e) {
-    const int i = threadIdx.x + e * kGemmThreads;
-    if (i >= M * kBlockRows) continue;
-    const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
-    float v = 0.f;
-    if (n < a.N) {
-      v = pre.v0[e] + ys[i];
-      a.out[(size_t)(m0 + m) * a.out_ld + n] = v;
-      if (a.frag_out) frag_store(a.frag_out, m0 + m, n, Tt, v * pre.v1[e]);
-    }
-    ys[i] = v;
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int m = warp; m < M; m += kGemmThreads / 32) {
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float v = ys[m * kBlockRows + lane + 32 * j];
-      s = fmaf(v, v, s);
-    }
-    s = warp_sum(s);
-    if (lane == 0) a.ssq_out[rb * kRows + m0 + m] = s;
-  }
-}
-
-template <int T>
-__device__ void epi_qkv(const GemmArgs& a, const float* ys, int rb, int m0, int M, const EpiPre<T>& pre,
-                        const int* spos) {
-  constexpr int kE = EpiPre<T>::kE;
-  const int half = a.hd >> 1;
-  const int n0 = rb * kBlockRows;
-  const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);
-  const int seg0 = s ? a.seg_end[s - 1] : 0;
-#pragma unroll
-  for (int e = 0; e < kE; ++e) {
-    const int i = threadIdx.x + e * kGemmThreads;
-    const int m = i / kBlockRows, r = i - m * kBlockRows;
-    if (m >= M || n0 + r >= a.N) continue;
-    const int local = n0 + r - seg0;
-    const int d = local % a.hd;
-    const int b = (m0 + m) / a.rs.rps;
-    const int pos = spos[m];
-    if (s == 2) {
-      const int kvh = local / a.hd;
-      a.vc[(((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d] = __float2bfloat16_rn(ys[i] + pre.v0[e]);
-      continue;
-    }
-    if (d >= half) continue;
-    const float x1 = ys[i] + pre.v0[e];
-    const float x2 = ys[i + half] + pre.v1[e];
-    const float2 cs = pre.cs[e];
-    const float y1 = x1 * cs.x - x2 * cs.y;
-    const float y2 = x2 * cs.x + x1 * cs.y;
-    if (s == 0) {
-      float* q = a.out + (size_t)(m0 + m) * a.out_ld + local;
-      q[0] = y1;
-      q[half] = y2;
-    } else {
-      const int kvh = local / a.hd;
-      bf16* kp = a.kc + (((size_t)b * a.nkv + kvh) * a.s_max + pos) * a.hd + d;
-      kp[0] = __float2bfloat16_rn(y1);
-      kp[half] = __float2bfloat16_rn(y2);
-    }
-  }
-}
-
-__device__ void epi_swiglu(const GemmArgs& a, const float* ys, int rb, int m0, int M, int Tt) {
-  for (int i = threadIdx.x; i < M * 64; i += kGemmThreads) {
-    const int m = i >> 6, j = i & 63;
-    const int f = rb * 64 + j;
-    if (f >= a.N) continue;
-    const float gte = ys[m * kBlockRows + j];
-    const float up = ys[m * kBlockRows + 64 + j];
-    frag_store(a.frag_out, m0 + m, f, Tt, gte / (1.0f + expf(-gte)) * up);
-  }
-}
-
-__device__ void epi_store(const GemmArgs& a, const float* ys, int rb, int m0, int M) {
-  for (int i = threadIdx.x; i < M * kBlockRows; i += kGemmThreads) {
-    const int m = i / kBlockRows, r = i - m * kBlockRows;
-    const int n = rb * kBlockRows + r;
-    if (n < a.N) a.out[(size_t)(m0 + m) * a.out_ld + n] = ys[i];
-  }
 }
 
 // `finishers`: CTAs that run this epilogue in the launch (row blocks x row
@@ -901,20 +763,20 @@ static cudaError_t encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const voi
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld) {
-  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, rows, (uint64_t)ld * 2, kChunk, 16,
+cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld, int box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, rows, (uint64_t)ld * 2, kChunk, box_rows,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int nf4_scale_ld(int K) { return ((K / 64 + 7) / 8) * 8; }
 
 cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const void* codes, const void* scales,
-                          int rows, int K) {
-  cudaError_t e = encode_2d(codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, rows, K / 2, 128, 16,
+                          int rows, int K, int box_rows) {
+  cudaError_t e = encode_2d(codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, rows, K / 2, 128, box_rows,
                             CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   return encode_2d(scale_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, K / 64, rows, (uint64_t)nf4_scale_ld(K) * 2,
-                   8, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   8, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int T, int EPI, bool NF4, bool GRP>
@@ -1009,7 +871,7 @@ static cudaError_t gemm_init_all() {
       (e = init_t<3, true>()) || (e = init_t<4, true>()) || (e = init_t<4, false, true>()) ||
       (e = init_t<4, true, true>()))
     return e;
-  return cudaSuccess;
+  return umma_init();
 }
 
 // Once per device (the attributes persist for the process): about 130
@@ -1052,24 +914,36 @@ static cudaError_t launch_f(const GemmArgs& a, int epi, cudaStream_t st, bool pd
   }
 }
 
-// One thread per 16-byte unit of the fragment-ordered output.
-__global__ void k_to_frag(const float* x, int M, int K, int ld, int T, uint4* out, long units) {
+// One thread per 16-byte unit of the output: fragment order, or (umma) the
+// tensor-core operand order (umma_index).
+__global__ void k_to_frag(const float* x, int M, int K, int ld, int T, uint4* out, long units, int umma) {
   const long u = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
-  const int lane = (int)(u & 31);
-  const int h = (int)((u >> 5) & 1);
-  const long r = u >> 6;
-  const int t = (int)(r % T), j = (int)(r / T);
-  const int col = lane >> 2, c = lane & 3;
-  const int m = 4 * t + (col >> 1);
-  const bool lo = col & 1;
+  int m, k0, lo;
+  if (umma) {
+    const int pos = (int)(u & 7), col = (int)((u >> 3) & 7);
+    const long r = u >> 6;
+    const int t = (int)(r % T), j = (int)(r / T);
+    m = 4 * t + (col >> 1);
+    lo = col & 1;
+    k0 = 64 * j + 8 * (pos ^ col);
+  } else {
+    const int lane = (int)(u & 31);
+    const int h = (int)((u >> 5) & 1);
+    const long r = u >> 6;
+    const int t = (int)(r % T), j = (int)(r / T);
+    const int col = lane >> 2, c = lane & 3;
+    m = 4 * t + (col >> 1);
+    lo = col & 1;
+    k0 = 64 * j + 16 * c + 8 * h;
+  }
   uint32_t p[4];
 #pragma unroll
   for (int e2 = 0; e2 < 4; ++e2) {
     bf16 v2[2];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int k = 64 * j + 16 * c + 8 * h + 2 * e2 + q;
+      const int k = k0 + 2 * e2 + q;
       const float v = (m < M && k < K) ? x[(size_t)m * ld + k] : 0.f;
       const bf16 hi = __float2bfloat16_rn(v);
       v2[q] = lo ? __float2bfloat16_rn(v - __bfloat162float(hi)) : hi;
@@ -1082,7 +956,8 @@ __global__ void k_to_frag(const float* x, int M, int K, int ld, int T, uint4* ou
 cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cudaStream_t st) {
   const int T = (M + 3) / 4;
   const long units = (long)frag_bytes(K, T) / 16;
-  k_to_frag<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(x, M, K, ld, T, reinterpret_cast<uint4*>(out), units);
+  k_to_frag<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(x, M, K, ld, T, reinterpret_cast<uint4*>(out), units,
+                                                            M > kGroupRows ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,473 @@
+// The weight-streaming GEMM on the tcgen05 tensor cores, for forwards of more
+// than 16 token rows (the verify pass of a batch of sequences, prefill
+// chunks): y[m][n] = sum_k x[m][k] W[n][k] for every token row m (up to
+// SF_MAX_ROWS) in one CTA per (128 weight rows, K slice).
+//
+// The mma.sync kernel (k_gemm.cu) covers at most 16 token rows per CTA, so a
+// 72-row verify ran as five row groups that each streamed (from L2) and, for
+// NF4 weights, dequantised every weight tile again. Here the whole token
+// block is the N side of one MMA: M = 128 weight rows, N = 8 columns per
+// token tile (hi and lo bf16 halves of four tokens), accumulated in tensor
+// memory, so every weight tile is read and dequantised once.
+//
+// Warp roles, 256 threads:
+//   thread 0      producer: weight tiles by TMA (two 64-row boxes, 128-byte
+//                 swizzle) or NF4 code tiles + block scales, and the token
+//                 operand of each 64-k chunk by one bulk copy (the producers
+//                 of the activations store them in exactly the tile layout
+//                 the MMA reads: umma_index in sf_common.cuh);
+//   thread 32     MMA issuer: four tcgen05.mma (K = 16 each) per chunk,
+//                 tcgen05.commit to the stage's "empty" barrier;
+//   warps 4-7     NF4 only: dequantise each chunk's codes into a bf16 weight
+//                 tile (level x block scale) in the MMA's layout;
+//   warps 4-7     afterwards: read the accumulator (tcgen05.ld, one weight row
+//                 per thread), add each token's hi and lo columns, and write
+//                 the CTA's tile ys[m][128] in shared memory.
+// Then all 256 threads sum the K slices (thread-block cluster, rank 0 reads
+// the other ranks' tiles; or global partial tiles and an arrival counter),
+// apply the RMSNorm row factor and run the same epilogues as k_gemm, one
+// 16-row group at a time.
+#include <algorithm>
+#include <mutex>
+
+#include "gemm_epi.cuh"
+#include "umma.cuh"
+
+namespace sf {
+
+namespace {
+
+constexpr uint32_t kUWaitIters = 1u << 24;
+constexpr int kUThreads = 256;
+constexpr int kUMaxStages = 6;
+constexpr int kATileBytes = 128 * 128;      // 128 weight rows x 64 k bf16 (also 128 rows x 256 k of NF4 codes)
+constexpr int kUScaleBytes = 128 * 16;      // NF4: 128 rows x 8 fp16 block scales
+constexpr int kCodeStage = kATileBytes + kUScaleBytes;
+constexpr int kCodeStages = 2;
+constexpr int kDeqStages = 2;
+
+__constant__ float c_levels[16];
+
+struct USmem {
+  uint64_t full[kUMaxStages], empty[kUMaxStages];   // token operand (+ bf16 weights) ring
+  uint64_t cfull[kCodeStages], cempty[kCodeStages];   // NF4 code ring
+  uint64_t afull[kDeqStages], aempty[kDeqStages];     // NF4 dequantised weight ring
+  uint64_t acc;                                       // accumulator complete
+  uint32_t tmem;
+  int flag;
+  int pos[kRows];
+  float rinv[kRows];
+  float levels[16];   // NF4 levels: 16 words in 16 banks, so lookups never conflict
+};
+
+__device__ __forceinline__ int tiles_padded(int T) { return (T + 1) & ~1; }
+
+// Tensor map, first weight row and row of the second 64-row box of row block
+// rb: SwiGLU blocks are 64 gate rows then the same 64 features' up rows.
+template <int EPI>
+__device__ __forceinline__ void block_rows(const GemmArgs& a, int rb, int* seg_lo, int* row_lo, int* seg_hi,
+                                           int* row_hi) {
+  if (EPI == EPI_SWIGLU) {
+    *seg_lo = 0;
+    *seg_hi = 1;
+    *row_lo = *row_hi = rb * 64;
+    return;
+  }
+  const int n = rb * kBlockRows;
+  int s = 0;
+  while (s < a.nseg - 1 && n >= a.seg_end[s]) ++s;
+  *seg_lo = *seg_hi = s;
+  *row_lo = n - (s ? a.seg_end[s - 1] : 0);
+  *row_hi = *row_lo + 64;
+}
+
+}  // namespace
+
+template <int EPI, bool NF4>
+__global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ GemmArgs a) {
+  extern __shared__ unsigned char usmem_raw[];
+  unsigned char* base = usmem_raw + ((1024 - (smem_u32(usmem_raw) & 1023)) & 1023);
+  __shared__ USmem sm;
+  trace_mark(a.rs, 0);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int M = a.rs.M;
+  const int T = (M + 3) / 4;              // token tiles of the operand layout
+  const int Tp = tiles_padded(T);         // MMA N = 8 * Tp (a multiple of 16)
+  const int N = 8 * Tp;
+  const int ncols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+  const int S = a.stages;
+  const int rb = blockIdx.x / a.nsplit, sp = blockIdx.x - rb * a.nsplit;
+  const int nch_total = (a.K + kChunk - 1) / kChunk;
+  const int c0 = sp * a.cps;
+  const int nch = min(a.cps, nch_total - c0);
+  const uint32_t btile = (uint32_t)T * 1024;   // bytes of one chunk's token operand
+
+  // Shared memory: bf16: S stages of [weights 16 KB | tokens Tp KB];
+  // NF4: 2 code stages [codes 16 KB | scales 2 KB], 2 dequantised weight
+  // tiles of 16 KB, S token stages of Tp KB. The result tile ys aliases it.
+  const int bstage = Tp * 1024;
+  auto wtile = [&](int s) -> unsigned char* { return base + (size_t)s * (kATileBytes + bstage); };
+  auto btile_p = [&](int s) -> unsigned char* {
+    return NF4 ? base + kCodeStages * kCodeStage + kDeqStages * kATileBytes + (size_t)s * bstage
+               : wtile(s) + kATileBytes;
+  };
+  auto ctile = [&](int s) -> unsigned char* { return base + (size_t)s * kCodeStage; };
+  auto dtile = [&](int s) -> unsigned char* { return base + kCodeStages * kCodeStage + (size_t)s * kATileBytes; };
+  float* ys = reinterpret_cast<float*>(base);
+
+  int seg_lo, row_lo, seg_hi, row_hi;
+  block_rows<EPI>(a, rb, &seg_lo, &row_lo, &seg_hi, &row_hi);
+
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem, ncols);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < kCodeStages; ++s) {
+      mbar_init(&sm.cfull[s], 1);
+      mbar_init(&sm.cempty[s], 128);
+    }
+    for (int s = 0; s < kDeqStages; ++s) {
+      mbar_init(&sm.afull[s], 128);
+      mbar_init(&sm.aempty[s], 1);
+    }
+    mbar_init(&sm.acc, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // An odd tile count leaves the last tile of every token stage unwritten by
+  // the copies: it reads as zero columns.
+  if (Tp > T)
+    for (int i = tid; i < S * 64; i += kUThreads)
+      reinterpret_cast<uint4*>(btile_p(i / 64) + (size_t)T * 1024)[i % 64] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async();
+  // Token positions (QKV epilogue), read before the wait: lengths are never
+  // written by the kernel that directly precedes a projection.
+  if (EPI == EPI_QKV && tid < M) sm.pos[tid] = row_pos(a.rs, tid);
+  if (NF4 && tid < 16) sm.levels[tid] = c_levels[tid];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_b = policy_evict_normal();
+  const int ncg = (nch + 3) / 4;          // NF4 code groups of this slice
+  (void)ncg;
+  auto issue_codes = [&](int q) {
+    const int s = q % kCodeStages;
+    const int cabs = c0 + 4 * q;
+    mbar_expect_tx(&sm.cfull[s], kCodeStage);
+    tma_load_2d(ctile(s), &a.tm[seg_lo], cabs * (kChunk / 2), row_lo, &sm.cfull[s], pol_w);
+    tma_load_2d(ctile(s) + kATileBytes / 2, &a.tm[seg_hi], cabs * (kChunk / 2), row_hi, &sm.cfull[s], pol_w);
+    tma_load_2d(ctile(s) + kATileBytes, &a.tms[seg_lo], (cabs / 8) * 8, row_lo, &sm.cfull[s], pol_w);
+    tma_load_2d(ctile(s) + kATileBytes + kUScaleBytes / 2, &a.tms[seg_hi], (cabs / 8) * 8, row_hi, &sm.cfull[s],
+                pol_w);
+  };
+  auto issue_w = [&](int st) {
+    const int s = st % S;
+    tma_load_2d(wtile(s), &a.tm[seg_lo], (c0 + st) * kChunk, row_lo, &sm.full[s], pol_w);
+    tma_load_2d(wtile(s) + kATileBytes / 2, &a.tm[seg_hi], (c0 + st) * kChunk, row_hi, &sm.full[s], pol_w);
+  };
+  auto issue_b = [&](int st) {
+    bulk_load(btile_p(st % S), reinterpret_cast<const unsigned char*>(a.in) + (size_t)(c0 + st) * btile, btile,
+              &sm.full[st % S], pol_b);
+  };
+  const int pre = min(S, nch);
+  // Weights are never written by the preceding kernels: start them first.
+  if (tid == 0) {
+    if (NF4) {
+      for (int q = 0; q < kCodeStages && q < ncg; ++q) issue_codes(q);
+      for (int st = 0; st < pre; ++st) mbar_expect_tx(&sm.full[st], btile);
+    } else {
+      for (int st = 0; st < pre; ++st) {
+        mbar_expect_tx(&sm.full[st], kATileBytes + btile);
+        issue_w(st);
+      }
+    }
+  }
+  pdl_wait();
+  trace_mark(a.rs, 1);
+  pdl_launch_next();
+
+  bool timed_out = false;
+  if (tid == 0) {
+    // ---- producer. NF4 code group q (chunks 4q .. 4q+3) reuses code stage
+    // q % 2 once the dequantisers released group q - 2; token stage s is
+    // refilled once the MMAs of chunk st - S committed.
+    for (int st = 0; st < nch; ++st) {
+      const int s = st % S;
+      if (NF4 && (st & 3) == 0 && st / 4 >= kCodeStages) {
+        const int q = st / 4;
+        if (!mbar_wait(&sm.cempty[q % kCodeStages], ((q / kCodeStages) + 1) & 1, kUWaitIters)) timed_out = true;
+        issue_codes(q);
+      }
+      if (st >= pre) {
+        if (!mbar_wait(&sm.empty[s], ((st / S) + 1) & 1, kUWaitIters)) timed_out = true;
+        mbar_expect_tx(&sm.full[s], NF4 ? btile : kATileBytes + btile);
+        if (!NF4) issue_w(st);
+      }
+      issue_b(st);
+    }
+  } else if (tid == 32) {
+    // ---- MMA issuer
+    const uint32_t idesc = umma_idesc_bf16(128, N);
+    for (int st = 0; st < nch; ++st) {
+      const int s = st % S;
+      if (!mbar_wait(&sm.full[s], (st / S) & 1, kUWaitIters)) timed_out = true;
+      const int ds = st % kDeqStages;
+      if (NF4 && !mbar_wait(&sm.afull[ds], (st / kDeqStages) & 1, kUWaitIters)) timed_out = true;
+      tc_fence_after();
+      const uint32_t aw = smem_u32(NF4 ? dtile(ds) : wtile(s));
+      const uint32_t bw = smem_u32(btile_p(s));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem, sw128_desc(aw + 32 * kk), sw128_desc(bw + 32 * kk), idesc, (st | kk) != 0);
+      umma_commit(&sm.empty[s]);
+      if (NF4) umma_commit(&sm.aempty[ds]);
+    }
+    umma_commit(&sm.acc);
+  } else if (NF4 && warp >= 4) {
+    // ---- dequantisers: thread r owns weight row r of the tile
+    const int r = tid - 128;
+    const int sw = r & 7;
+    const float* lv = sm.levels;
+    for (int st = 0; st < nch; ++st) {
+      const int q = st >> 2, sub = st & 3, cs = q % kCodeStages, ds = st % kDeqStages;
+      if (sub == 0 && !mbar_wait(&sm.cfull[cs], (q / kCodeStages) & 1, kUWaitIters)) timed_out = true;
+      if (!mbar_wait(&sm.aempty[ds], ((st / kDeqStages) + 1) & 1, kUWaitIters)) timed_out = true;
+      const unsigned char* crow = ctile(cs) + (r >> 3) * 1024 + sw * 128;
+      const uint4 b0 = *reinterpret_cast<const uint4*>(crow + (((2 * sub) ^ sw) << 4));
+      const uint4 b1 = *reinterpret_cast<const uint4*>(crow + (((2 * sub + 1) ^ sw) << 4));
+      const __half* sc = reinterpret_cast<const __half*>(ctile(cs) + kATileBytes) + r * 8;
+      const float scale = __half2float(sc[(c0 + st) & 7]);
+      const uint32_t cw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      unsigned char* drow = dtile(ds) + (r >> 3) * 1024 + sw * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {   // 8 weights per 16-byte piece: code word c
+        const uint32_t w = cw[c];
+        uint32_t p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t byte = (w >> (8 * e)) & 255u;
+          p[e] = pack_bf16x2(__float2bfloat16_rn(lv[byte & 15] * scale), __float2bfloat16_rn(lv[byte >> 4] * scale));
+        }
+        *reinterpret_cast<uint4*>(drow + ((c ^ sw) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+      }
+      fence_proxy_async();
+      mbar_arrive(&sm.afull[ds]);
+      if (sub == 3 || st == nch - 1) mbar_arrive(&sm.cempty[cs]);
+    }
+  }
+
+  // ---- accumulator -> ys[m][128] (warps 4-7: lane 32 * (warp - 4) + lane = weight row)
+  if (warp >= 4) {
+    if (!mbar_wait(&sm.acc, 0, kUWaitIters)) {
+      timed_out = true;
+      mbar_wait(&sm.acc, 0, kUWaitIters);
+    }
+    tc_fence_after();
+    const int row = 32 * (warp - 4) + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
+    for (int c16 = 0; c16 < N / 16; ++c16) {
+      uint32_t v[16];
+      tmem_ld16(taddr + 16 * c16, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int m = 8 * c16 + i;
+        if (m < M) ys[m * kBlockRows + row] = __uint_as_float(v[2 * i]) + __uint_as_float(v[2 * i + 1]);
+      }
+    }
+  }
+  if (timed_out) report_err(a.err, kErrWait);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+
+  // ---- RMSNorm row factors 1 / rms(x_m)
+  if (a.ssq)
+    for (int m = warp; m < M; m += kUThreads / 32) {
+      float sq = (lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f) + (lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f);
+      sq = warp_sum(sq);
+      if (lane == 0) sm.rinv[m] = 1.0f / sqrtf(sq * a.inv_k + a.eps);
+    }
+  __syncthreads();
+
+  // ---- sum the K slices in slice order, scale rows by 1 / rms
+  const int nel = M * kBlockRows;
+  if (a.nsplit > 1 && a.cluster) {
+    cluster_sync();   // every rank's tile is complete
+    const uint32_t rank = cluster_rank();
+    if (rank != 0) {
+      cluster_sync();   // rank 0 has read it
+      return;
+    }
+    const uint32_t ys_s = smem_u32(ys);
+    for (int i = tid; i < nel; i += kUThreads) {
+      float v = ys[i];
+      for (int r = 1; r < a.nsplit; ++r) v += ld_dsmem(dsmem_addr(ys_s + 4 * i, r));
+      ys[i] = a.ssq ? v * sm.rinv[i / kBlockRows] : v;
+    }
+    cluster_sync();
+  } else if (a.nsplit > 1) {
+    const int G = (M + kGroupRows - 1) / kGroupRows;
+    for (int i = tid; i < nel; i += kUThreads) {
+      const int m = i / kBlockRows, g = m / kGroupRows;
+      __stcg(a.part + (((size_t)(rb * G + g) * a.nsplit + sp) * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
+                 (i - m * kBlockRows),
+             ys[i]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.flag = (atomicAdd(a.counter + rb * G, 1) == a.nsplit - 1);
+    __syncthreads();
+    if (!sm.flag) return;
+    __threadfence();
+    for (int i = tid; i < nel; i += kUThreads) {
+      const int m = i / kBlockRows, g = m / kGroupRows;
+      const float* src = a.part + ((size_t)(rb * G + g) * a.nsplit * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
+                         (i - m * kBlockRows);
+      float v = 0.f;
+      for (int p = 0; p < a.nsplit; ++p) v += __ldcg(src + (size_t)p * kGroupRows * kBlockRows);
+      ys[i] = a.ssq ? v * sm.rinv[m] : v;
+    }
+    if (tid == 0) a.counter[rb * G] = 0;
+  } else if (a.ssq) {
+    for (int i = tid; i < nel; i += kUThreads) ys[i] *= sm.rinv[i / kBlockRows];
+  }
+  __syncthreads();
+
+  // ---- epilogue, one 16-row group at a time (the k_gemm epilogues)
+  for (int m0 = 0; m0 < M; m0 += kGroupRows) {
+    const int Mg = min(kGroupRows, M - m0);
+    float* yg = ys + m0 * kBlockRows;
+    EpiPre<4> pre_g;
+    epi_prefetch<4, EPI>(a, rb, m0, Mg, pre_g, sm.pos + m0);
+    if (EPI == EPI_RESID) epi_resid<4>(a, yg, rb, m0, Mg, T, pre_g);
+    else if (EPI == EPI_QKV) epi_qkv<4>(a, yg, rb, m0, Mg, pre_g, sm.pos + m0);
+    else if (EPI == EPI_SWIGLU) epi_swiglu(a, yg, rb, m0, Mg, T);
+    else epi_store(a, yg, rb, m0, Mg);
+  }
+}
+
+// Dynamic shared memory of a launch (plus 1 KB for the 1024-byte alignment).
+int umma_smem_bytes(int M, int stages, bool nf4) {
+  const int Tp = ((M + 3) / 4 + 1) & ~1;
+  const int ring = nf4 ? kCodeStages * kCodeStage + kDeqStages * kATileBytes + stages * Tp * 1024
+                       : stages * (kATileBytes + Tp * 1024);
+  return 1024 + std::max(ring, M * kBlockRows * 4);
+}
+
+// Deepest token ring that keeps two CTAs on an SM (each at most kHalfSmBytes).
+int umma_stages(int M, bool nf4) {
+  int s = kUMaxStages;
+  while (s > 2 && umma_smem_bytes(M, s, nf4) > kHalfSmBytes) --s;
+  return s;
+}
+
+cudaError_t set_umma_nf4_levels(const float levels[16]) {
+  return cudaMemcpyToSymbol(c_levels, levels, 16 * sizeof(float));
+}
+
+template <int EPI, bool NF4>
+static cudaError_t launch_ut(const GemmArgs& a, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nblocks * a.nsplit);
+  cfg.blockDim = dim3(kUThreads);
+  cfg.dynamicSmemBytes = umma_smem_bytes(a.rs.M, a.stages, NF4);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (a.cluster && a.nsplit > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = a.nsplit;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k_umma<EPI, NF4>, a);
+}
+
+template <bool NF4>
+static cudaError_t launch_uf(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
+  switch (epi) {
+    case EPI_QKV: return launch_ut<EPI_QKV, NF4>(a, st, pdl);
+    case EPI_RESID: return launch_ut<EPI_RESID, NF4>(a, st, pdl);
+    case EPI_SWIGLU: return launch_ut<EPI_SWIGLU, NF4>(a, st, pdl);
+    case EPI_STORE: return launch_ut<EPI_STORE, NF4>(a, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_umma(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
+  if (a.rs.M <= kGroupRows || a.rs.M > kRows) return cudaErrorInvalidValue;
+  if (a.cluster && a.nsplit > 8) return cudaErrorInvalidValue;
+  if (a.stages < 2 || a.stages > kUMaxStages) return cudaErrorInvalidValue;
+  if (umma_smem_bytes(a.rs.M, a.stages, a.nf4) > 227 * 1024) return cudaErrorInvalidValue;
+  if (a.nf4 && (a.K % 64 || (a.nsplit > 1 && a.cps % 4))) return cudaErrorInvalidValue;
+  return a.nf4 ? launch_uf<true>(a, epi, st, pdl) : launch_uf<false>(a, epi, st, pdl);
+}
+
+template <int EPI, bool NF4>
+static cudaError_t uinit_one() {
+  const int smem = umma_smem_bytes(kRows, kUMaxStages, NF4);
+  cudaError_t e = cudaFuncSetAttribute(k_umma<EPI, NF4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       std::min(smem, 227 * 1024));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_umma<EPI, NF4>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+template <bool NF4>
+static cudaError_t uinit_t() {
+  cudaError_t e;
+  if ((e = uinit_one<EPI_QKV, NF4>()) || (e = uinit_one<EPI_RESID, NF4>()) || (e = uinit_one<EPI_SWIGLU, NF4>()))
+    return e;
+  return uinit_one<EPI_STORE, NF4>();
+}
+
+// Attributes of every instantiation on the current device (called from
+// gemm_init, once per device).
+cudaError_t umma_init() {
+  cudaError_t e = uinit_t<false>();
+  if (e != cudaSuccess) return e;
+  return uinit_t<true>();
+}
+
+// Largest number of clusters of `csize` CTAs resident at once for this
+// launch footprint (0 if the query fails).
+int umma_max_clusters(int csize, int M, int stages, bool nf4) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize * 512);
+  cfg.blockDim = dim3(kUThreads);
+  cfg.dynamicSmemBytes = umma_smem_bytes(M, stages, nf4);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = csize;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e = nf4 ? cudaOccupancyMaxActiveClusters(&n, k_umma<EPI_QKV, true>, &cfg)
+                            : cudaOccupancyMaxActiveClusters(&n, k_umma<EPI_QKV, false>, &cfg);
+  return e == cudaSuccess ? n : 0;
+}
+
+}  // namespace sf

@@ -248,11 +248,36 @@ __device__ __forceinline__ size_t frag_index(int m, int k, int T) {
   return ((((size_t)j * T + t) * 2 + h) * 32 + 4 * col + c) * 8 + e;
 }
 
-__device__ __forceinline__ void frag_store(bf16* f, int m, int k, int T, float v) {
-  const size_t i = frag_index(m, k, T);
+
+// ------------------------------------------------ tensor-core operand order
+// Forwards of more than 16 token rows run their projections on the tcgen05
+// tensor cores, whose B operand is the canonical K-major tile with 128-byte
+// swizzle: for 64-feature chunk j and token tile t (tokens 4t .. 4t+3) one
+// 1024-byte block at byte (j * T + t) * 1024 holds 8 operand rows of 128
+// bytes, row col = 2 * (m % 4) + {0: hi, 1: lo}; the 16-byte piece with
+// features 8q .. 8q+7 of the chunk sits at position q ^ col of its row. A
+// chunk of all T tiles is therefore one contiguous T * 1024-byte block that a
+// single bulk copy brings into shared memory ready for the MMA.
+__device__ __forceinline__ size_t umma_index(int m, int k, int T, int lo) {
+  const int j = k >> 6, kk = k & 63;
+  const int t = m >> 2, col = 2 * (m & 3) + lo;
+  const int q = kk >> 3, e = kk & 7;
+  return (((size_t)j * T + t) * 1024 + col * 128 + ((q ^ col) << 4)) / 2 + e;
+}
+
+// Store one activation as a bf16 hi/lo pair in the order its consumer reads:
+// fragment order (mma.sync GEMMs) or the tensor-core operand order.
+__device__ __forceinline__ void act_store(bf16* f, int m, int k, int T, float v, int umma) {
   const bf16 hi = __float2bfloat16_rn(v);
-  f[i] = hi;
-  f[i + 32] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  const bf16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+  if (umma) {
+    f[umma_index(m, k, T, 0)] = hi;
+    f[umma_index(m, k, T, 1)] = lo;
+  } else {
+    const size_t i = frag_index(m, k, T);
+    f[i] = hi;
+    f[i + 32] = lo;
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -40,6 +40,7 @@ struct GemmArgs {
   // writes x * frag_gain (the next RMSNorm's input), SWIGLU the activation.
   bf16* frag_out;
   const bf16* frag_gain;
+  int frag_umma;              // frag_out in the tensor-core operand order (umma_index) instead of fragment order
   // split-K scratch without clusters: partial tiles [row block x row group][split][16][128]
   // and one arrival counter per (row block, row group)
   float* part;
@@ -64,12 +65,14 @@ struct GemmArgs {
 };
 
 // Tensor map of a bf16 weight matrix [rows, K] with row stride ld elements,
-// in the layout the GEMM's TMA ring expects.
-cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld);
+// in the layout the GEMM's TMA ring expects: boxes of 64 k x box_rows rows
+// with 128-byte swizzle (16 rows: one warp's tile of the mma.sync GEMM; 64
+// rows: half the 128-row tile of the tcgen05 GEMM).
+cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, int ld, int box_rows = 16);
 // NF4: codes [rows, K/2] bytes and fp16 block scales [rows, nf4_scale_ld(K)].
 int nf4_scale_ld(int K);
 cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const void* codes, const void* scales,
-                          int rows, int K);
+                          int rows, int K, int box_rows = 16);
 cudaError_t set_nf4_levels(const float levels[16]);
 
 constexpr int kMaxClusterSplit = 16;  // cluster size (above 8 is non-portable; allowed per kernel)
@@ -108,6 +111,17 @@ int gemm_smem_bytes(int M, int stages, bool nf4, int cps, int push = 0);
 int gemm_max_clusters(int csize, int M, int stages, int cps);
 cudaError_t gemm_init();
 cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
+// The same projections on the tcgen05 tensor cores for launches of 17 to
+// SF_MAX_ROWS token rows (k_umma.cu): one CTA per (128 weight rows, K slice)
+// covers every token row; the input is in the tensor-core operand order
+// (umma_index), the weight maps have 64-row boxes, the K slices of a row
+// block are one cluster (at most 8) or use `part` / `counter`.
+cudaError_t launch_umma(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
+cudaError_t umma_init();
+int umma_smem_bytes(int M, int stages, bool nf4);
+int umma_stages(int M, bool nf4);
+int umma_max_clusters(int csize, int M, int stages, bool nf4);
+cudaError_t set_umma_nf4_levels(const float levels[16]);
 // The LM head with its argmax as a persistent kernel (one K slice, at most
 // two CTAs per SM walking the row blocks); same arguments as EPI_ARGMAX.
 cudaError_t launch_lmhead(const GemmArgs& a, int num_sms, cudaStream_t st, bool pdl);
@@ -120,6 +134,7 @@ struct EmbedArgs {
   float* ssq;    // [H/128][kRows]
   bf16* frag;    // x * gain in fragment order (the first RMSNorm's input)
   const bf16* gain;
+  int umma;      // frag in the tensor-core operand order instead
   RowSet rs;
 };
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl);
@@ -130,6 +145,7 @@ struct AttnArgs {
   const bf16* vc;
   float* part;             // [M*nq][n_kv_chunks][hd + 2]
   bf16* out;               // attention output [M][nq*hd] in fragment order
+  int umma;                // out in the tensor-core operand order instead
   int nq, nkv, hd, s_max, B, n_kv_chunks;
   float scale;
   int* err;

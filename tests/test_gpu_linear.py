@@ -1,7 +1,8 @@
 """GPU parity of the weight-streaming GEMM (sf_linear) against a float64
 matrix product, over shapes that span several 128-row blocks and 64-wide K
-chunks with ragged tails, every row count 1..16, row counts above 16 (one
-CTA per 16-row group, the last one partial), and K splits across CTAs.
+chunks with ragged tails, every row count 1..16 (the mma.sync kernel), row
+counts above 16 (the tcgen05 kernel: all rows in one tensor-memory
+accumulator), and K splits across CTAs.
 
 Error bound: the activation is carried as a bf16 pair (hi + lo, about 16
 mantissa bits) and products are summed in fp32, so |y - y_ref| stays within
@@ -72,28 +73,32 @@ def test_rows_above_16(pkg, M):
 
 
 @pytest.mark.parametrize("N,K,M", [(3584, 18944, 72), (4608, 3584, 40), (129, 72, 80), (896, 4864, 18)])
-def test_row_groups_equal_separate_launches(pkg, N, K, M):
-    """Each 16-row group of a launch gives the same bits as a launch of its
-    rows alone, and any row the same bits as that row alone: a row's
-    arithmetic does not depend on the other rows (K splits included)."""
+def test_tensor_core_rows(pkg, N, K, M):
+    """Above 16 rows the tcgen05 kernel takes every row in one accumulator.
+    Its results are deterministic, a row's bits do not depend on how many
+    other rows (above 16) share the launch, and they agree with the 16-row
+    mma.sync launches of the same rows to float32 accumulation error."""
     g = torch.Generator(device="cuda").manual_seed(N + K + M)
     w = (torch.randn(N, K, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
     x = torch.randn(M, K, generator=g, device="cuda")
     y = pkg.linear(w, x)
+    assert torch.equal(y, pkg.linear(w, x))
+    assert torch.equal(pkg.linear(w, x[:17].contiguous()), y[:17])
+    wd, xd = w.double(), x.double()
+    bound = xd.abs() @ wd.abs().t()
+    err = (y.double() - xd @ wd.t()).abs()
+    assert bool((err <= 1e-4 * bound + 1e-30).all())
     for m0 in range(0, M, 16):
         part = pkg.linear(w, x[m0:m0 + 16].contiguous())
-        assert torch.equal(part, y[m0:m0 + 16]), m0
-    for m in (0, M // 2, M - 1):
-        assert torch.equal(pkg.linear(w, x[m:m + 1].contiguous())[0], y[m]), m
-    wd, xd = w.double(), x.double()
-    err = (y.double() - xd @ wd.t()).abs()
-    assert bool((err <= 1e-4 * (xd.abs() @ wd.abs().t()) + 1e-30).all())
+        assert bool(((part.double() - y[m0:m0 + 16].double()).abs() <= 1e-5 * bound[m0:m0 + 16] + 1e-30).all()), m0
 
 
 def _frag_reference(x):
-    """The fragment order written out element by element (test-side
-    restatement of the layout the header documents): bf16 hi/lo pairs of x
-    [M, K] as a uint16 array of the library's byte size."""
+    """The operand layouts written out element by element (test-side
+    restatement of what the header documents): bf16 hi/lo pairs of x [M, K]
+    as a uint16 array of the library's byte size. Up to 16 rows: fragment
+    order; above 16: the tensor-core operand order (128-byte rows of 8
+    features x 8 pieces, piece q of row col at position q ^ col)."""
     M, K = x.shape
     T = (M + 3) // 4
     nch = (K + 63) // 64
@@ -104,11 +109,19 @@ def _frag_reference(x):
     for m in range(M):
         for k in range(K):
             j, kk = divmod(k, 64)
-            c, h, e = kk // 16, (kk // 8) % 2, kk % 8
-            t, col = m // 4, 2 * (m % 4)
-            unit = ((j * T + t) * 2 + h) * 32 + 4 * col + c
-            out[unit * 8 + e] = hi16[m, k]
-            out[(unit + 4) * 8 + e] = lo16[m, k]
+            t = m // 4
+            if M <= 16:
+                c, h, e = kk // 16, (kk // 8) % 2, kk % 8
+                col = 2 * (m % 4)
+                unit = ((j * T + t) * 2 + h) * 32 + 4 * col + c
+                out[unit * 8 + e] = hi16[m, k]
+                out[(unit + 4) * 8 + e] = lo16[m, k]
+            else:
+                q, e = kk // 8, kk % 8
+                for half, src in ((0, hi16), (1, lo16)):
+                    col = 2 * (m % 4) + half
+                    byte = (j * T + t) * 1024 + col * 128 + ((q ^ col) << 4)
+                    out[byte // 2 + e] = src[m, k]
     return out
 
 

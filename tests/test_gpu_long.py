@@ -119,7 +119,7 @@ def test_attention_merge_beyond_one_round(pkg, name, shape, ctx, s_max):
 
 
 def test_batch8_ragged_long_contexts(pkg):
-    """Eight sequences, K = 8 (72 verify rows in five 16-row groups), the
+    """Eight sequences, K = 8 (72 verify rows: the tcgen05 GEMM), the
     longest at 3300 tokens: 52 chunks at head dim 128."""
     K, shape = 8, HD128_G7
     lens = [3300, 200, 1500, 40, 900, 3150, 12, 700]
@@ -136,7 +136,9 @@ def test_batch8_ragged_long_contexts(pkg):
     eng.draft(d_out, d_log)
     eng.verify(None, t_log)
     torch.cuda.synchronize()
-    assert torch.equal(d_log, t_log[:, :K])
+    # draft rows (mma.sync GEMM) vs verify rows (72 rows: tcgen05 GEMM)
+    rng = (t_log.max(dim=-1).values - t_log.min(dim=-1).values)[..., None]
+    assert bool(((d_log - t_log[:, :K]).abs() <= 1e-4 * rng[:, :K]).all())
     n_acc, _ = eng.accept_rollback()
     assert [int(n) for n in n_acc] == [K] * B
     lt, _ = eng.lengths()

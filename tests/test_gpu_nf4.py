@@ -115,10 +115,12 @@ def test_14b_shape_nf4_two_layers(pkg):
 ])
 def test_nf4_row_groups_ragged_batch(pkg, name, B, K, lens):
     """Sequences with prompts of different lengths whose verify forward has
-    more than 16 rows (tiny: 20 rows, two 16-row groups; 14B shape: 72 rows,
-    five groups), NF4 weights. Target = draft, so every guess is accepted and
-    each draft row (at most 16 rows per launch: the single-group kernels)
-    equals its verify row (the row-group kernels) bit for bit; every
+    more than 16 rows (tiny: 20 rows; 14B shape: 72 rows), NF4 weights: the
+    verify runs on the tcgen05 GEMM (each weight tile dequantised once into
+    bf16 level x scale), the draft steps (at most 16 rows) on the mma.sync
+    GEMM (bf16 levels, scale applied per chunk). Target = draft: each draft
+    row agrees with its verify row to one bf16 rounding of the weights;
+    accept lengths equal the brute-force prefix compare of the two; every
     sequence's verify logits are within the NF4 tolerance of the oracle."""
     shape = TINY_TARGET.with_(ffn=768) if name == "tiny" else QWEN14B.with_(layers=2)
     w = make_weights(shape, seed=51)
@@ -134,11 +136,18 @@ def test_nf4_row_groups_ragged_batch(pkg, name, B, K, lens):
     eng.draft(d_out, d_log)
     eng.verify(None, t_log)
     torch.cuda.synchronize()
-    assert torch.equal(d_log, t_log[:, :K])
+    rng = (t_log.max(dim=-1).values - t_log.min(dim=-1).values)[..., None]
+    assert bool(((d_log - t_log[:, :K]).abs() <= 2e-2 * rng[:, :K]).all())
+    t_arg = t_log.argmax(dim=-1).cpu()
     n_acc, _ = eng.accept_rollback()
-    assert [int(n) for n in n_acc] == [K] * B
+    d_h = d_out.cpu()
+    for b in range(B):
+        n = 0
+        while n < K and int(d_h[b, n]) == int(t_arg[b, n]):
+            n += 1
+        assert int(n_acc[b]) == n, b
     lt, _ = eng.lengths()
-    assert [int(x) for x in lt] == [n + K for n in lens]
+    assert [int(x) for x in lt] == [n + int(a) for n, a in zip(lens, n_acc)]
     eng.close()
     m = om.Model(shape, rw, rowwise=shape.hidden < 1024)
     worst = 0.0

@@ -120,12 +120,13 @@ def test_batch_invariance_target_as_its_own_draft(pkg, tiny):
 
 def test_batch8_ragged_rows_match_single_sequences(pkg, tiny):
     """Eight sequences whose prompts differ in length, K=8: every verify
-    forward has 72 token rows (five 16-row groups in each GEMM) and the first
-    draft step 16. Per sequence, the draft and verify logits equal those of
-    the same sequence run alone, bit for bit (a row's arithmetic does not
-    depend on the other rows or sequences); accept lengths, committed tokens
-    and cache lengths follow; the generated streams are the oracle's greedy
-    streams."""
+    forward has 72 token rows (the tcgen05 GEMM) and the first draft step 16
+    (the mma.sync GEMM). Per sequence, the draft logits equal those of the
+    same sequence run alone bit for bit (a row's arithmetic does not depend
+    on the other rows or sequences of a <= 16-row launch), the verify logits
+    agree with the single sequence's 9-row verify to float32 accumulation
+    error; accept lengths, committed tokens and cache lengths follow; the
+    generated streams are the oracle's greedy streams."""
     tw = tiny[0]
     K, B, V = 8, 8, TINY_TARGET.vocab
     lens = [20, 33, 47, 12, 60, 25, 8, 41]
@@ -151,7 +152,8 @@ def test_batch8_ragged_rows_match_single_sequences(pkg, tiny):
         torch.cuda.synchronize()
         one.close()
         assert torch.equal(d_log[b], d1[0]), b
-        assert torch.equal(t_log[b], t1[0]), b
+        rng = (t1[0].max(dim=-1).values - t1[0].min(dim=-1).values)[:, None]
+        assert bool(((t_log[b] - t1[0]).abs() <= 1e-4 * rng).all()), b
         assert int(n_acc[b]) == int(n1[0]) and list(committed[b]) == list(c1[0]), b
         assert int(lt[b]) == int(lt1[0]) == lens[b] + int(n_acc[b]), b
         assert int(ld[b]) == int(ld1[0]), b
@@ -219,15 +221,24 @@ def test_rounds_integer_state_and_rollback(pkg, tiny):
         seq += committed[0]
         lt, ld = eng.lengths()
         assert int(lt[0]) == len(seq) - 1 and int(ld[0]) == len(seq) - 2
-    # The caches below the lengths equal a fresh prefill of the committed prefix.
+    # The caches below the lengths equal a fresh prefill of the committed
+    # prefix: bit for bit where both wrote the entries through the same GEMM
+    # kernel, else to one bf16 rounding step (the fresh prefill's chunks of
+    # more than 16 rows run on the tcgen05 GEMM, the rounds on mma.sync).
     kv_t = eng.kv_view("target").clone()
     kv_d = eng.kv_view("draft").clone()
     C = len(seq)
     fresh = make_engine(pkg, tiny, K=K)
     fresh.prefill([seq])
     ft, fd = fresh.kv_view("target"), fresh.kv_view("draft")
-    assert torch.equal(kv_t[..., : C - 1, :], ft[..., : C - 1, :])
-    assert torch.equal(kv_d[..., : C - 2, :], fd[..., : C - 2, :])
+
+    def close(a, b):
+        a, b = a.float(), b.float()
+        return bool(((a - b).abs() <= 2.0 ** -7 * b.abs() + 1e-30).all())
+    P = len(prompt)
+    assert torch.equal(kv_t[..., : P - 1, :], ft[..., : P - 1, :])
+    assert close(kv_t[..., : C - 1, :], ft[..., : C - 1, :])
+    assert close(kv_d[..., : C - 2, :], fd[..., : C - 2, :])
     fresh.close()
     eng.close()
 
