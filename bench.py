@@ -508,6 +508,18 @@ def run_ours(args):
     hist = eng.accept_hist()[0]
     value = world * args.steps * N_NEW / (ms_max / 1e3)
 
+    # ---- prefill (time to first round): the 512-token prompt and the 2048-token context, both
+    # models, chunks of up to 80 rows (host wall clock around the synchronous call)
+    prefill = {}
+    for n, seed in ((PROMPT_LEN, 102), (VERIFY_CTX, 103)):
+        p = uniform_prompt(n, t_shape.vocab, seed=seed).numpy()
+        eng.prefill([p])                       # warm
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        eng.prefill([p])
+        dt = time.perf_counter() - t0
+        prefill[str(n)] = {"ms": round(1e3 * dt, 2), "tokens_per_s": round(n / dt, 1)}
+
     # ---- verify step and draft step at context 2048 (graph replays, events on the engine stream)
     eng.prefill([uniform_prompt(VERIFY_CTX, t_shape.vocab, seed=103).numpy()])
     v_ms, d_ms = [], []
@@ -618,6 +630,7 @@ def run_ours(args):
                            "frac_of_8TBs": round(d_bytes / (draft_ms / 1e3) / 8e12, 4)},
             "accept": {"mean_committed_per_round": round(mean_commit, 3), "hist": hist.tolist(),
                        "rounds": rounds_total},
+            "prefill": {"what": "both models over the prompt, chunks of up to 80 rows", **prefill},
             "clocks": clk.summary(),
         }
         if extra:

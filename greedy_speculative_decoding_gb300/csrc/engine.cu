@@ -431,7 +431,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   // More than 16 token rows: the projections run on the tcgen05 GEMM, whose
   // inputs the producers write in the tensor-core operand order (the LM head
   // keeps reading fragment order).
-  const bool tc = rs.M > kGroupRows;
+  const bool tc = rs.M >= umma_min_rows();
   auto gemm = [&](const GemmArgs& a, int epi) {
     return tc ? launch_umma(a, epi, s, e->pdl) : launch_gemm(a, epi, s, e->pdl);
   };
@@ -1234,7 +1234,7 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   int dev = 0, sms = 0;
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const bool tc = M > kGroupRows;   // more than 16 rows: the tcgen05 GEMM
+  const bool tc = M >= umma_min_rows();   // more than 16 rows: the tcgen05 GEMM
   const Plan p = make_plan((N + 127) / 128, K, 2 * sms, 1 << 30);
   const int groups = (M + kGroupRows - 1) / kGroupRows;
   if (p.nsplit > 1 && p.nblocks * p.nsplit * groups > kLinearTiles)

@@ -957,7 +957,7 @@ cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cuda
   const int T = (M + 3) / 4;
   const long units = (long)frag_bytes(K, T) / 16;
   k_to_frag<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(x, M, K, ld, T, reinterpret_cast<uint4*>(out), units,
-                                                            M > kGroupRows ? 1 : 0);
+                                                            M >= umma_min_rows() ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -28,6 +28,7 @@
 // apply the RMSNorm row factor and run the same epilogues as k_gemm, one
 // 16-row group at a time.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "gemm_epi.cuh"
@@ -218,6 +219,8 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     const uint32_t idesc = umma_idesc_bf16(128, N);
     for (int st = 0; st < nch; ++st) {
       const int s = st % S;
+      // Test hook for the error path (as in k_gemm): the first wait gives up at once.
+      if (st == 0 && a.expire_first_wait && !mbar_wait(&sm.full[s], 0, 0)) timed_out = true;
       if (!mbar_wait(&sm.full[s], (st / S) & 1, kUWaitIters)) timed_out = true;
       const int ds = st % kDeqStages;
       if (NF4 && !mbar_wait(&sm.afull[ds], (st / kDeqStages) & 1, kUWaitIters)) timed_out = true;
@@ -415,8 +418,20 @@ static cudaError_t launch_uf(const GemmArgs& a, int epi, cudaStream_t st, bool p
   }
 }
 
+// Token-row count from which the projections run on this kernel: 17 (above
+// one 16-row group of the mma.sync kernel), or SF_UMMA_MIN_ROWS from the
+// environment (1..81; read once per process), for comparing the two kernels.
+int umma_min_rows() {
+  static const int v = [] {
+    const char* e = getenv("SF_UMMA_MIN_ROWS");
+    const int n = e ? atoi(e) : kGroupRows + 1;
+    return n < 1 ? 1 : (n > kRows + 1 ? kRows + 1 : n);
+  }();
+  return v;
+}
+
 cudaError_t launch_umma(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
-  if (a.rs.M <= kGroupRows || a.rs.M > kRows) return cudaErrorInvalidValue;
+  if (a.rs.M < 1 || a.rs.M > kRows) return cudaErrorInvalidValue;
   if (a.cluster && a.nsplit > 8) return cudaErrorInvalidValue;
   if (a.stages < 2 || a.stages > kUMaxStages) return cudaErrorInvalidValue;
   if (umma_smem_bytes(a.rs.M, a.stages, a.nf4) > 227 * 1024) return cudaErrorInvalidValue;

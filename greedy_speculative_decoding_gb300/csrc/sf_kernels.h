@@ -117,6 +117,7 @@ cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
 // (umma_index), the weight maps have 64-row boxes, the K slices of a row
 // block are one cluster (at most 8) or use `part` / `counter`.
 cudaError_t launch_umma(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
+int umma_min_rows();
 cudaError_t umma_init();
 int umma_smem_bytes(int M, int stages, bool nf4);
 int umma_stages(int M, bool nf4);

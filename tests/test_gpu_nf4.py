@@ -83,9 +83,23 @@ def _check_model(pkg, shape, seed, prompt_len, s_max):
     eng.draft(d_out, d_log)
     eng.verify(None, t_log)
     torch.cuda.synchronize()
-    assert torch.equal(d_log, t_log[:K])
     n_acc, _ = eng.accept_rollback()
-    assert int(n_acc[0]) == K
+    if prompt_len <= 16:
+        # prompt and rounds on the mma.sync GEMM: draft rows equal verify rows
+        assert torch.equal(d_log, t_log[:K])
+        assert int(n_acc[0]) == K
+    else:
+        # prompt prefilled on the tcgen05 GEMM (weights dequantised as
+        # bf16(level x scale)), slot C-2 rewritten by mma.sync (bf16 levels,
+        # scale per chunk): rows agree to one bf16 rounding of the weights
+        rng = (t_log.max(dim=-1).values - t_log.min(dim=-1).values)[:, None]
+        assert bool(((d_log - t_log[:K]).abs() <= 2e-2 * rng[:K]).all())
+        t_arg = t_log.argmax(dim=-1).cpu().tolist()
+        d_h = d_out.cpu().tolist()
+        n = 0
+        while n < K and d_h[n] == t_arg[n]:
+            n += 1
+        assert int(n_acc[0]) == n
     eng.close()
     d = d_out.cpu().tolist()
     m = om.Model(shape, rw, rowwise=shape.hidden < 1024)

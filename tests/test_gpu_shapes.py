@@ -40,7 +40,7 @@ def test_05b_shape_self_draft(pkg):
     eng = pkg.SpecEngine(QWEN05B, w, QWEN05B, w, batch=1, K=K, s_max=4096)
     eng.kv_t.fill_(0xFF)
     eng.kv_d.fill_(0xFF)
-    prompt = uniform_prompt(20, QWEN05B.vocab, seed=101).tolist()
+    prompt = uniform_prompt(16, QWEN05B.vocab, seed=101).tolist()
     eng.prefill([prompt])
     d, d_log, t_log = _round(eng, QWEN05B.vocab)
     assert torch.equal(d_log, t_log[:K])
