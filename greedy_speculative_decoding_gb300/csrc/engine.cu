@@ -84,10 +84,15 @@ struct Model {
   const bf16* lm = nullptr;
   int lm_ld = 0;
   CUtensorMap lm_tm;
+  CUtensorMap lm_tmu;      // 64-row boxes: the LM head of forwards of more than 16 rows (tcgen05)
   bf16* kv = nullptr;
+  CUtensorMap kvmap;       // the whole cache as [rows][head_dim] for the attention kernel's TMA
+  int attn_R = 1;          // cache chunks per attention work item
+  int attn_TG = 1;         // query tiles per attention work item
+  int attn_stages = 1;     // key/value chunks in flight per attention CTA
   float2* rope = nullptr;
   Plan p_qkv, p_o, p_gu, p_d, p_lm;
-  Plan u_qkv, u_o, u_gu, u_d;   // tcgen05 GEMM plans (forwards of more than 16 rows)
+  Plan u_qkv, u_o, u_gu, u_d, u_lm;   // tcgen05 GEMM plans (forwards of more than 16 rows)
   int q_dim() const { return c.n_heads * c.head_dim; }
   int kv_dim() const { return c.n_kv_heads * c.head_dim; }
 };
@@ -318,6 +323,22 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     if (!check(md.lm, "lm_head", false)) return fail(SF_ERR_ARG, "lm_head pointer null or misaligned");
   }
   md.kv = kv;
+  {
+    const long rows = (long)c->layers * 2 * e->B * c->n_kv_heads * e->s_max;
+    const cudaError_t ce = make_kv_map(&md.kvmap, kv, rows, c->head_dim);
+    if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "KV cache tensor map: %s", cudaGetErrorString(ce));
+    // Attention work items of R chunks: one chunk each while the cache is
+    // small; up to 8 for a large batch of long caches, so the items fill the
+    // GPU a few times over and the merge reads a few partials per row. Fixed
+    // per model and engine: a row's arithmetic never depends on other rows.
+    // The same load decides whether an item carries every query tile of its
+    // KV head (each chunk read once, two chunks in flight) or one tile (more
+    // items for a small batch: the same work spread over more CTAs).
+    const long load = (long)e->B * c->n_kv_heads * (e->s_max / kKvChunk) / 2048;
+    md.attn_R = load >= 8 ? 8 : (load >= 4 ? 4 : (load >= 2 ? 2 : 1));
+    md.attn_TG = load >= 2 ? 4 : 1;
+    md.attn_stages = load >= 2 ? 2 : 1;
+  }
   const int H = c->hidden;
   const int QD = c->n_heads * c->head_dim, KVD = c->n_kv_heads * c->head_dim, F = c->ffn;
   for (int l = 0; l < c->layers; ++l) {
@@ -335,7 +356,8 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     }
   }
   {
-    const cudaError_t ce = make_weight_map(&md.lm_tm, md.lm, c->vocab, H, md.lm_ld);
+    cudaError_t ce = make_weight_map(&md.lm_tm, md.lm, c->vocab, H, md.lm_ld);
+    if (ce == cudaSuccess) ce = make_weight_map(&md.lm_tmu, md.lm, c->vocab, H, md.lm_ld, 64);
     if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "LM head tensor map: %s", cudaGetErrorString(ce));
   }
   // The K splits of a row block form one thread-block cluster. Matrices of
@@ -377,6 +399,9 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   md.u_o = uplan(nblocks_of(c, 1), (long)c->n_heads * c->head_dim);
   md.u_gu = uplan(nblocks_of(c, 2), H);
   md.u_d = uplan(nblocks_of(c, 1), c->ffn);
+  md.u_lm.nblocks = nblocks_of(c, 3);   // LM heads: no K split
+  md.u_lm.nsplit = 1;
+  md.u_lm.cps = (H + kChunk - 1) / kChunk;
   md.p_lm.nblocks = nblocks_of(c, 3);   // the persistent LM head: no K split
   md.p_lm.nsplit = 1;
   md.p_lm.cps = (H + kChunk - 1) / kChunk;
@@ -503,9 +528,14 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     CK(gemm(a, EPI_QKV));
     // attention
     AttnArgs t{};
+    t.kvmap = md.kvmap;
+    t.kv_brows = c.n_kv_heads * e->s_max;
+    t.kv_vrows = e->B * t.kv_brows;
+    t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
+    t.R = md.attn_R;
+    t.TG = md.attn_TG;
+    t.stages = md.attn_stages;
     t.q = e->q;
-    t.kc = kc;
-    t.vc = vc;
     t.part = e->apart;
     t.out = e->fo;
     t.nq = c.n_heads;
@@ -577,14 +607,14 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.ssq_out = e->ssq;
     a.frag_out = e->fx;   // the next layer's QKV input, or the LM head's
     a.frag_gain = l + 1 < c.layers ? md.L[l + 1].ln1 : md.norm;
-    a.frag_umma = tc && l + 1 < c.layers;   // the LM head reads fragment order
+    a.frag_umma = tc;   // the next layer's QKV or the LM head, same kernel family
     a.rs = traced(e, rs, "down");
     CK(gemm(a, EPI_RESID));
   }
   if (!lm) return SF_OK;
-  GemmArgs a = base_args(e, md, md.p_lm, rs);
+  GemmArgs a = base_args(e, md, tc ? md.u_lm : md.p_lm, rs);
   a.w[0] = md.lm;
-  a.tm[0] = md.lm_tm;
+  a.tm[0] = tc ? md.lm_tmu : md.lm_tm;
   a.seg_end[0] = c.vocab;
   a.ld[0] = md.lm_ld;
   a.nseg = 1;
@@ -603,9 +633,14 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   a.logits = to.logits;
   a.lg_stride = to.lg_stride;
   a.lg_off = to.lg_off;
-  a.stages = 5;
   a.rs = traced(e, rs, "lm_head");
-  CK(launch_lmhead(a, e->num_sms, s, e->pdl));
+  if (tc) {
+    a.stages = umma_stages(rs.M, false);
+    CK(launch_umma(a, EPI_ARGMAX, s, e->pdl));
+  } else {
+    a.stages = 5;
+    CK(launch_lmhead(a, e->num_sms, s, e->pdl));
+  }
   return SF_OK;
 }
 

@@ -146,5 +146,54 @@ __device__ void epi_store(const GemmArgs& a, const float* ys, int rb, int m0, in
   }
 }
 
+__device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// `finishers`: CTAs that run this epilogue in the launch (row blocks x row
+// groups); the last to arrive writes the tokens of all rows of the forward.
+__device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int m0, int M, int finishers, int* s_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int m = warp; m < M; m += kGemmThreads / 32) {
+    unsigned long long best = 0ull;
+    bool bad = false;
+    const int mb = (m0 + m) / a.rs.rps, mj = (m0 + m) - mb * a.rs.rps;
+    const int lg_row = mj >= a.tok_skip ? mb * a.lg_stride + a.lg_off + mj - a.tok_skip : -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = lane + 32 * j;
+      const int n = rb * kBlockRows + r;
+      if (n < a.N) {
+        const float v = ys[m * kBlockRows + r];
+        if (a.logits && lg_row >= 0) a.logits[(size_t)lg_row * a.N + n] = v;
+        bad |= !isfinite(v);
+        const unsigned long long k = argmax_key(v, n);
+        best = k > best ? k : best;
+      }
+    }
+    best = shfl_max_u64(best);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report_err(a.err, kErrNonfinite);
+    if (lane == 0) atomicMax(a.keys + m0 + m, best);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.done, 1) == finishers - 1);
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  if (threadIdx.x < a.rs.M) {
+    const int m = threadIdx.x;
+    const unsigned long long k = atomicExch(a.keys + m, 0ull);
+    const int b = m / a.rs.rps, j = m - b * a.rs.rps;
+    if (j >= a.tok_skip) a.tok_out[b * a.tok_stride + a.tok_off + j - a.tok_skip] = key_index(k);
+  }
+  if (threadIdx.x == 0) *a.done = 0;
+}
+
 }  // namespace
 }  // namespace sf

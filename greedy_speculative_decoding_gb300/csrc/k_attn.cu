@@ -15,6 +15,8 @@
 
 namespace sf {
 
+constexpr uint32_t kAttnWaitIters = 1u << 24;
+
 // ------------------------------------------------------------------ embedding
 // x[m][:] = E[tok_m][:] in fp32, the per-128-feature sums of squares the next
 // RMSNorm needs, and x * gain in fragment order (that RMSNorm's GEMM input).
@@ -67,38 +69,45 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uin
   lo = pack_bf16x2(__float2bfloat16_rn(x - __bfloat162float(hx)), __float2bfloat16_rn(y - __bfloat162float(hy)));
 }
 
-// One work item = (sequence b, KV head, 64-slot chunk c). Its keys and values
-// come into padded shared-memory rows with 16-byte asynchronous copies
-// (slots past the last row's position are zero-filled instead: a zero
-// probability times a stale NaN would still be NaN). The queries that read
-// this KV head (rows of the sequence x query heads of the group) go through
-// in tiles of 16, and all eight warps share each tile:
+// One work item = (sequence b, KV head, range r of R consecutive 64-slot
+// chunks, group of up to four 16-query tiles); the queries are all rows of the
+// sequence times the query heads that read this KV head. The chunks' keys and
+// values arrive by 2-D TMA (box 64 dims x 64 slots, 128-byte swizzle) into a
+// two-stage ring that runs across the CTA's items, so the next chunk is in
+// flight while this one is computed; every query tile of the group is
+// computed from one copy. Per tile, all eight warps work on each chunk:
 //   S = Q K^T   warp w computes the 8 keys 8w..8w+7 over the whole head
 //               dimension (mma.sync m16n8k16, Q as an fp32-accurate bf16
-//               hi+lo pair, the head dimension walked in an order that makes
-//               each key fragment one 8-byte shared load);
-//   softmax     row max and row sum combined across the warps through
-//               shared memory (sums in warp order);
+//               hi+lo pair);
+//   softmax     online over the range: row max and row sum combined across
+//               the warps through shared memory (sums in warp order), the
+//               running max and sum rescaled per chunk;
 //   O = P V     P (hi+lo) through shared memory, warp w producing output
-//               dimensions w*HD/8 .. (w+1)*HD/8 - 1 from all 64 keys.
-// The split is the same for every tile and every launch, so a row's result
-// does not depend on how many other rows the launch carries.
-template <int HD>
+//               dimensions w*HD/8 .. (w+1)*HD/8 - 1 from all 64 keys, the
+//               running output rescaled per chunk.
+// The range's unnormalised output, running max and sum go to scratch; the
+// merge kernel combines the ranges of every (row, head) in order. R is fixed
+// per model and engine and the ranges start at fixed multiples of R chunks,
+// so a row's result does not depend on how many other rows the launch carries.
+template <int HD, int kTG>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_constant__ AttnArgs a) {
-  constexpr int KP = HD * 2 + 32;   // key row pitch (bytes): 8-bank shift per row for the 8-byte fragment loads
-  constexpr int VP = HD * 2 + 16;   // value row pitch: 4-bank shift per row for ldmatrix
-  constexpr int KS = HD / 16;       // k-steps over the head dimension
-  constexpr int NTW = HD / 64;      // output n-tiles (8 dimensions each) per warp
-  constexpr int HP = HD + 16;       // query hi / lo row pitch (bf16): 8-bank shift per row
-  constexpr int PP = kKvChunk + 8;  // probability tile row pitch (bf16)
-  constexpr int kPieces = kKvChunk * HD / 8;   // 16-byte pieces of a chunk's keys (and of its values)
+  constexpr int kBox = kKvChunk * 128;          // one TMA box: 64 slots x 64 dims (8 KB)
+  constexpr int kHalf = HD / 64;                // boxes per chunk of keys (or values)
+  constexpr int kKV = kHalf * kBox;             // one chunk's keys (or values)
+  constexpr int kStage = 2 * kKV;
+  constexpr int KS = HD / 16;                   // k-steps over the head dimension
+  constexpr int NTW = HD / 64;                  // output n-tiles (8 dimensions each) per warp
+  constexpr int HP = HD + 16;                   // query hi / lo row pitch (bf16): 8-bank shift per row
+  constexpr int PP = kKvChunk + 8;              // probability tile row pitch (bf16)
   static_assert(kAttnThreads == 256 && kKvChunk == 64, "eight warps of eight keys");
-  extern __shared__ __align__(128) unsigned char attn_smem[];
-  unsigned char* ks = attn_smem;                                   // [64][KP]
-  unsigned char* vs = ks + kKvChunk * KP;                          // [64][VP]
-  bf16* sph = reinterpret_cast<bf16*>(vs + kKvChunk * VP);         // [16][PP] P hi
-  bf16* spl = sph + 16 * PP;                                       // [16][PP] P lo
+  extern __shared__ unsigned char attn_smem_raw[];
+  unsigned char* base = attn_smem_raw + ((1024 - (smem_u32(attn_smem_raw) & 1023)) & 1023);
+  bf16* sph = reinterpret_cast<bf16*>(base + a.stages * kStage); // [16][PP] P hi
+  bf16* spl = sph + 16 * PP;                                     // [16][PP] P lo
+  bf16* sq = spl + 16 * PP;                                      // [TG][2][16][HP] queries hi / lo
   __shared__ float red_mx[8][16], red_l[8][16];
+  __shared__ float m_run[kTG][16], l_run[kTG][16];
+  __shared__ __align__(8) uint64_t full[2];
 
   trace_mark(a.rs, 0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -107,227 +116,289 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
   const int rps = a.rs.rps;
   const int Mq = rps * group;
   const int ntiles = (Mq + 15) / 16;
-  bf16* sqh = spl + 16 * PP;                                       // [16][HP] queries of the tile, hi
-  bf16* sql = sqh + 16 * HP;                                       // [16][HP] queries of the tile, lo
+  constexpr int TG = kTG;   // query tiles per item (a.TG)
+  const int ntg = (ntiles + TG - 1) / TG;
+  const int R = a.R;
+  const int NS = a.stages;
 
   // The lengths were written by kernels that finished before the preceding
   // one started, so they (and the cache slots below this pass's first
   // position) can be read before waiting on the preceding kernel.
-  // Work item = (sequence b, KV head, chunk c, query tile qt); the tiles of
-  // one chunk are consecutive items (their CTAs share the chunk through L2).
   int total = 0;
   for (int b = 0; b < a.B; ++b) {
-    const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
-    total += a.nkv * (p_last / kKvChunk + 1) * ntiles;
+    const int nch = (a.rs.pos_base[b] + a.rs.pos_off + rps - 1) / kKvChunk + 1;
+    total += a.nkv * ((nch + R - 1) / R) * ntg;
   }
-  auto locate = [&](int item, int& b, int& kvh, int& c, int& qt) {
-    int rest = item, nch = 0;
-    for (b = 0; b < a.B; ++b) {
-      const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
-      nch = p_last / kKvChunk + 1;
-      if (rest < a.nkv * nch * ntiles) break;
-      rest -= a.nkv * nch * ntiles;
-    }
-    kvh = rest / (nch * ntiles);
-    rest -= kvh * nch * ntiles;
-    c = rest / ntiles;
-    qt = rest - c * ntiles;
+  struct Item {
+    int b, kvh, r, tg, c0, c1, p0, p_last;
   };
-  // Copy slots [0, nvalid) of the chunk; zero the rest of the tile.
-  auto issue = [&](int b, int kvh, int c, int nvalid) {
-    const size_t off = (((size_t)b * a.nkv + kvh) * a.s_max + (size_t)c * kKvChunk) * HD;
-    for (int i = tid; i < kPieces; i += kAttnThreads) {
-      const int r = i / (HD / 8), u = i - r * (HD / 8);
-      if (r < nvalid) {
-        cp_async16(ks + r * KP + 16 * u, a.kc + off + (size_t)r * HD + 8 * u);
-        cp_async16(vs + r * VP + 16 * u, a.vc + off + (size_t)r * HD + 8 * u);
-      } else {
-        *reinterpret_cast<uint4*>(ks + r * KP + 16 * u) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(vs + r * VP + 16 * u) = make_uint4(0, 0, 0, 0);
+  auto locate = [&](int item) {
+    Item it;
+    int rest = item;
+    for (it.b = 0; it.b < a.B; ++it.b) {
+      it.p0 = a.rs.pos_base[it.b] + a.rs.pos_off;
+      it.p_last = it.p0 + rps - 1;
+      const int n = a.nkv * ((it.p_last / kKvChunk + 1 + R - 1) / R) * ntg;
+      if (rest < n) break;
+      rest -= n;
+    }
+    const int nr = (it.p_last / kKvChunk + 1 + R - 1) / R;
+    it.kvh = rest / (nr * ntg);
+    rest -= it.kvh * nr * ntg;
+    it.r = rest / ntg;
+    it.tg = rest - it.r * ntg;
+    it.c0 = it.r * R;
+    it.c1 = min(it.c0 + R, it.p_last / kKvChunk + 1);
+    return it;
+  };
+  auto kv_row = [&](const Item& it, int c) { return a.kv_row0 + it.b * a.kv_brows + it.kvh * a.s_max + c * kKvChunk; };
+
+  // Producer (thread 0): a cursor over (item, chunk) steps of this CTA.
+  int is_item = blockIdx.x, is_c = 0, issued = 0;
+  Item is_it;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (is_item < total) {
+      is_it = locate(is_item);
+      is_c = is_it.c0;
+    }
+  }
+  auto issue_next = [&]() {   // thread 0: load the cursor's chunk into stage issued & 1, advance
+    if (is_item >= total) return;
+    const int s = issued % NS;
+    unsigned char* st = base + s * kStage;
+    fence_proxy_async();
+    mbar_expect_tx(&full[s], kStage);
+    const int row = kv_row(is_it, is_c);
+#pragma unroll
+    for (int h = 0; h < kHalf; ++h) {
+      tma_load_2d(st + h * kBox, &a.kvmap, 64 * h, row, &full[s], policy_evict_first());
+      tma_load_2d(st + kKV + h * kBox, &a.kvmap, 64 * h, row + a.kv_vrows, &full[s], policy_evict_first());
+    }
+    ++issued;
+    if (++is_c >= is_it.c1) {
+      is_item += gridDim.x;
+      if (is_item < total) {
+        is_it = locate(is_item);
+        is_c = is_it.c0;
       }
     }
-    cp_async_commit();
   };
-  bool issued = false;
-  if ((int)blockIdx.x < total) {
-    int b, kvh, c, qt;
-    locate(blockIdx.x, b, kvh, c, qt);
-    if ((c + 1) * kKvChunk <= a.rs.pos_base[b] + a.rs.pos_off) {   // no slot of this pass in the chunk
-      issue(b, kvh, c, kKvChunk);
-      issued = true;
-    }
-  }
+  __syncthreads();
+  // The first chunk, before the wait when it holds no slot of this pass.
+  if (tid == 0 && is_item < total && (is_c + 1) * kKvChunk <= is_it.p0) issue_next();
   pdl_wait();
   trace_mark(a.rs, 1);
   pdl_launch_next();
+  if (tid == 0 && issued == 0) issue_next();
 
-  // The item's 16 query rows -> shared memory as bf16 hi + lo pairs (rows
-  // past Mq are zero), all loads of a thread in flight at once.
-  auto stage_q = [&](int b, int kvh, int qt) {
-    constexpr int kBatch = 16 * (HD / 4) / kAttnThreads;
-    const int n4 = 16 * (HD / 4);
-    for (int i0 = 0; i0 < n4; i0 += kBatch * kAttnThreads) {
-      float4 v[kBatch];
-#pragma unroll
-      for (int e = 0; e < kBatch; ++e) {
-        const int i = i0 + tid + e * kAttnThreads;
-        const int qi = qt * 16 + i / (HD / 4), u = i % (HD / 4);
-        v[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < n4 && qi < Mq) {
+  int step = 0;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    const Item it = locate(item);
+    const int t0 = it.tg * TG, nt = min(TG, ntiles - t0);
+    // The item's query tiles -> shared memory as bf16 hi + lo pairs (rows
+    // past Mq are zero); the running max and sum start empty.
+    {
+      const int n4 = nt * 16 * (HD / 4);
+      for (int i = tid; i < n4; i += kAttnThreads) {
+        const int ti = i / (16 * (HD / 4)), rem = i - ti * (16 * (HD / 4));
+        const int qr = rem / (HD / 4), u = rem - qr * (HD / 4);
+        const int qi = (t0 + ti) * 16 + qr;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qi < Mq) {
           const int j = qi / group, hh = qi - j * group;
-          v[e] = *reinterpret_cast<const float4*>(a.q + ((size_t)(b * rps + j) * a.nq + kvh * group + hh) * HD + 4 * u);
+          v = *reinterpret_cast<const float4*>(a.q + ((size_t)(it.b * rps + j) * a.nq + it.kvh * group + hh) * HD + 4 * u);
         }
-      }
-#pragma unroll
-      for (int e = 0; e < kBatch; ++e) {
-        const int i = i0 + tid + e * kAttnThreads;
-        if (i >= n4) break;
-        const int qi = i / (HD / 4), u = i - qi * (HD / 4);   // row within the tile
         uint2 h, l;
-        split_bf16x2(v[e].x, v[e].y, h.x, l.x);
-        split_bf16x2(v[e].z, v[e].w, h.y, l.y);
-        *reinterpret_cast<uint2*>(sqh + qi * HP + 4 * u) = h;
-        *reinterpret_cast<uint2*>(sql + qi * HP + 4 * u) = l;
+        split_bf16x2(v.x, v.y, h.x, l.x);
+        split_bf16x2(v.z, v.w, h.y, l.y);
+        *reinterpret_cast<uint2*>(sq + ((2 * ti) * 16 + qr) * HP + 4 * u) = h;
+        *reinterpret_cast<uint2*>(sq + ((2 * ti + 1) * 16 + qr) * HP + 4 * u) = l;
+      }
+      if (tid < kTG * 16) {
+        m_run[tid >> 4][tid & 15] = -INFINITY;
+        l_run[tid >> 4][tid & 15] = 0.f;
       }
     }
-  };
-
-  for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    int b, kvh, c, qt;
-    locate(item, b, kvh, c, qt);
-    const int p0 = a.rs.pos_base[b] + a.rs.pos_off;
-    if (!issued) issue(b, kvh, c, min(kKvChunk, p0 + rps - c * kKvChunk));
-    issued = false;
-    stage_q(b, kvh, qt);
-    cp_async_wait_all();
+    float oacc[kTG][NTW][4];
+#pragma unroll
+    for (int ti = 0; ti < kTG; ++ti)
+#pragma unroll
+      for (int t2 = 0; t2 < NTW; ++t2) oacc[ti][t2][0] = oacc[ti][t2][1] = oacc[ti][t2][2] = oacc[ti][t2][3] = 0.f;
     __syncthreads();
 
-    {
-      const bf16* qht = sqh;
-      const bf16* qlt = sql;
-      // Rows g and g+8 of the tile: slots this row may see within the chunk.
-      int nk[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int qi = qt * 16 + g + 8 * r;
-        const int j = qi / group;
-        nk[r] = qi < Mq ? min(kKvChunk, p0 + j - c * kKvChunk + 1) : 0;
+    for (int c = it.c0; c < it.c1; ++c, ++step) {
+      const int s = step % NS;
+      // Two stages: the next step's chunk goes into the other one now; one
+      // stage: after this step has released it (end of the step).
+      if (tid == 0 && NS == 2) issue_next();
+      if (!mbar_wait(&full[s], (step / NS) & 1, kAttnWaitIters)) {
+        report_err(a.err, kErrWait);
+        mbar_wait(&full[s], (step / NS) & 1, kAttnWaitIters);
       }
-      // S for keys 8w .. 8w+7: four independent accumulation chains (hi / lo
-      // part of Q x even / odd k-step), added in a fixed order at the end.
-      float sa[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sa[i][0] = sa[i][1] = sa[i][2] = sa[i][3] = 0.f;
-      const unsigned char* krow = ks + (8 * warp + g) * KP + 8 * c4;
-#pragma unroll
-      for (int k = 0; k < KS; ++k) {
-        // Elements 16k + 4c4 .. +3 of rows g and g+8: (a0, a2) and (a1, a3).
-        const uint2 h0 = *reinterpret_cast<const uint2*>(qht + g * HP + 16 * k + 4 * c4);
-        const uint2 h1 = *reinterpret_cast<const uint2*>(qht + (g + 8) * HP + 16 * k + 4 * c4);
-        const uint2 l0 = *reinterpret_cast<const uint2*>(qlt + g * HP + 16 * k + 4 * c4);
-        const uint2 l1 = *reinterpret_cast<const uint2*>(qlt + (g + 8) * HP + 16 * k + 4 * c4);
-        const uint2 kb = *reinterpret_cast<const uint2*>(krow + 32 * k);
-        mma_bf16_16816(sa[k & 1], h0.x, h1.x, h0.y, h1.y, kb.x, kb.y);
-        mma_bf16_16816(sa[2 + (k & 1)], l0.x, l1.x, l0.y, l1.y, kb.x, kb.y);
-      }
-      float sacc[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
-      // sacc[e]: row g (e < 2) or g+8, key 8w + 2c4 + (e & 1).
-      float mx[2];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = e >> 1, key = 8 * warp + 2 * c4 + (e & 1);
-        sacc[e] = key < nk[r] ? sacc[e] * a.scale : -INFINITY;
+      const unsigned char* ks = base + s * kStage;
+      unsigned char* vs = base + s * kStage + kKV;
+      // Slots past the sequence's last row were not written by anyone this
+      // pass: zero their values (a zero probability times a stale NaN would
+      // still be NaN); their scores are masked below.
+      const int nvalid = min(kKvChunk, it.p_last - c * kKvChunk + 1);
+      if (nvalid < kKvChunk) {
+        for (int i = tid; i < (kKvChunk - nvalid) * 8 * kHalf; i += kAttnThreads) {
+          const int r = nvalid + i / (8 * kHalf), rem = i % (8 * kHalf);
+          *reinterpret_cast<uint4*>(vs + (rem >> 3) * kBox + r * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();   // ordered before the next copy into this stage; the first
+                               // tile's barrier orders it before the P V reads
       }
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        mx[r] = fmaxf(sacc[2 * r], sacc[2 * r + 1]);
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        if (c4 == 0) red_mx[warp][g + 8 * r] = mx[r];
-      }
-      __syncthreads();   // red_mx complete
+      for (int ti = 0; ti < kTG; ++ti) {
+        if (ti >= nt) break;
+        const bf16* qht = sq + (2 * ti) * 16 * HP;
+        const bf16* qlt = sq + (2 * ti + 1) * 16 * HP;
+        int nk[2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float m8 = red_mx[0][g + 8 * r];
+        for (int r = 0; r < 2; ++r) {
+          const int qi = (t0 + ti) * 16 + g + 8 * r;
+          nk[r] = qi < Mq ? min(kKvChunk, it.p0 + qi / group - c * kKvChunk + 1) : 0;
+        }
+        // S for keys 8w .. 8w+7: four independent chains (hi / lo part of Q
+        // x even / odd k-step), added in a fixed order at the end. Key row
+        // `key` of the swizzled tile: dims 8q .. 8q+7 at 16-byte piece q ^ (key & 7).
+        float sa[4][4];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m8 = fmaxf(m8, red_mx[w][g + 8 * r]);
-        mx[r] = m8;
-      }
-      float pe[4];
+        for (int i = 0; i < 4; ++i) sa[i][0] = sa[i][1] = sa[i][2] = sa[i][3] = 0.f;
+        const int key = 8 * warp + g;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = e >> 1, key = 8 * warp + 2 * c4 + (e & 1);
-        pe[e] = key < nk[r] ? expf(sacc[e] - mx[r]) : 0.f;
-      }
+        for (int k = 0; k < KS; ++k) {
+          const uint2 h0 = *reinterpret_cast<const uint2*>(qht + g * HP + 16 * k + 4 * c4);
+          const uint2 h1 = *reinterpret_cast<const uint2*>(qht + (g + 8) * HP + 16 * k + 4 * c4);
+          const uint2 l0 = *reinterpret_cast<const uint2*>(qlt + g * HP + 16 * k + 4 * c4);
+          const uint2 l1 = *reinterpret_cast<const uint2*>(qlt + (g + 8) * HP + 16 * k + 4 * c4);
+          const int q16 = 2 * (k & 3) + (c4 >> 1);
+          const uint2 kb = *reinterpret_cast<const uint2*>(ks + (k >> 2) * kBox + key * 128 +
+                                                           ((q16 ^ (key & 7)) << 4) + 8 * (c4 & 1));
+          mma_bf16_16816(sa[k & 1], h0.x, h1.x, h0.y, h1.y, kb.x, kb.y);
+          mma_bf16_16816(sa[2 + (k & 1)], l0.x, l1.x, l0.y, l1.y, kb.x, kb.y);
+        }
+        float sacc[4];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float l = pe[2 * r] + pe[2 * r + 1];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        if (c4 == 0) red_l[warp][g + 8 * r] = l;
-        uint32_t h, lo;
-        split_bf16x2(pe[2 * r], pe[2 * r + 1], h, lo);
-        *reinterpret_cast<uint32_t*>(sph + (g + 8 * r) * PP + 8 * warp + 2 * c4) = h;
-        *reinterpret_cast<uint32_t*>(spl + (g + 8 * r) * PP + 8 * warp + 2 * c4) = lo;
-      }
-      __syncthreads();
+        for (int e = 0; e < 4; ++e) {
+          const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
+          const float v = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+          sacc[e] = kk < nk[r] ? v * a.scale : -INFINITY;
+        }
+        float mx[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          mx[r] = fmaxf(sacc[2 * r], sacc[2 * r + 1]);
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+          if (c4 == 0) red_mx[warp][g + 8 * r] = mx[r];
+        }
+        __syncthreads();   // red_mx complete
+        float m_new[2], alpha[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float m8 = red_mx[0][g + 8 * r];
+#pragma unroll
+          for (int w = 1; w < 8; ++w) m8 = fmaxf(m8, red_mx[w][g + 8 * r]);
+          const float m_old = m_run[ti][g + 8 * r];
+          m_new[r] = fmaxf(m_old, m8);
+          alpha[r] = m_new[r] == -INFINITY ? 1.f : expf(m_old - m_new[r]);
+        }
+        float pe[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
+          pe[e] = kk < nk[r] ? expf(sacc[e] - m_new[r]) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float l = pe[2 * r] + pe[2 * r + 1];
+          l += __shfl_xor_sync(0xffffffffu, l, 1);
+          l += __shfl_xor_sync(0xffffffffu, l, 2);
+          if (c4 == 0) red_l[warp][g + 8 * r] = l;
+          uint32_t h, lo;
+          split_bf16x2(pe[2 * r], pe[2 * r + 1], h, lo);
+          *reinterpret_cast<uint32_t*>(sph + (g + 8 * r) * PP + 8 * warp + 2 * c4) = h;
+          *reinterpret_cast<uint32_t*>(spl + (g + 8 * r) * PP + 8 * warp + 2 * c4) = lo;
+        }
+        __syncthreads();   // P and red_l complete
 
-      // O = P V for this warp's output dimensions (P hi and P lo in two
-      // accumulation chains, added at the end).
-      float oh[NTW][4], ol[NTW][4];
+        // O = O * alpha + P V for this warp's output dimensions (P hi and P lo
+        // in two chains, added at the end). Value row `slot`, dims 8n .. 8n+7:
+        // 16-byte piece (n & 7) ^ (slot & 7) of box n >> 3.
+        float oh[NTW][4], ol[NTW][4];
 #pragma unroll
-      for (int t = 0; t < NTW; ++t)
+        for (int t2 = 0; t2 < NTW; ++t2)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) oh[t][e] = ol[t][e] = 0.f;
+          for (int e = 0; e < 4; ++e) oh[t2][e] = ol[t2][e] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < kKvChunk / 16; ++kk) {
-        uint32_t ph[4], pl[4];
-        const int k0 = 16 * kk + 2 * c4;
-        ph[0] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0);
-        ph[1] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0);
-        ph[2] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0 + 8);
-        ph[3] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0 + 8);
-        pl[0] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0);
-        pl[1] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0);
-        pl[2] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0 + 8);
-        pl[3] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0 + 8);
-        const unsigned char* vrow = vs + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * VP;
+        for (int kk = 0; kk < kKvChunk / 16; ++kk) {
+          uint32_t ph[4], pl[4];
+          const int k0 = 16 * kk + 2 * c4;
+          ph[0] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0);
+          ph[1] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0);
+          ph[2] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0 + 8);
+          ph[3] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0 + 8);
+          pl[0] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0);
+          pl[1] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0);
+          pl[2] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0 + 8);
+          pl[3] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0 + 8);
+          const int slot = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-        for (int t = 0; t < NTW; ++t) {
-          uint32_t b0, b1;
-          ldsm_x2_trans(b0, b1, vrow + 16 * (warp * NTW + t));
-          mma_bf16_16816(oh[t], ph[0], ph[1], ph[2], ph[3], b0, b1);
-          mma_bf16_16816(ol[t], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          for (int t2 = 0; t2 < NTW; ++t2) {
+            const int n = warp * NTW + t2;
+            uint32_t b0, b1;
+            ldsm_x2_trans(b0, b1, vs + (n >> 3) * kBox + slot * 128 + (((n & 7) ^ (slot & 7)) << 4));
+            mma_bf16_16816(oh[t2], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_bf16_16816(ol[t2], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          }
         }
+#pragma unroll
+        for (int t2 = 0; t2 < NTW; ++t2)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oacc[ti][t2][e] = oacc[ti][t2][e] * alpha[e >> 1] + (oh[t2][e] + ol[t2][e]);
+        if (warp == 0 && c4 == 0) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float l = red_l[0][g + 8 * r];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) l += red_l[w][g + 8 * r];
+            l_run[ti][g + 8 * r] = l_run[ti][g + 8 * r] * alpha[r] + l;
+            m_run[ti][g + 8 * r] = m_new[r];
+          }
+        }
+        __syncthreads();   // P, red_* and the stage free; running max / sum updated
       }
-      float oacc[NTW][4];
+      if (tid == 0 && NS == 1) issue_next();
+    }
+
+    // The range's partial result of every row that sees a slot of it.
 #pragma unroll
-      for (int t = 0; t < NTW; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[t][e] = oh[t][e] + ol[t][e];
+    for (int ti = 0; ti < kTG; ++ti) {
+      if (ti >= nt) break;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        if (nk[r] <= 0) continue;
-        const int qi = qt * 16 + g + 8 * r;
+        const int qi = (t0 + ti) * 16 + g + 8 * r;
+        if (qi >= Mq) continue;
         const int j = qi / group, hh = qi - j * group;
-        const int m = b * rps + j, h = kvh * group + hh;
-        float* dst = a.part + (((size_t)m * a.nq + h) * a.n_kv_chunks + c) * (HD + 2);
+        if (it.p0 + j < it.c0 * kKvChunk) continue;
+        const int m = it.b * rps + j, h = it.kvh * group + hh;
+        float* dst = a.part + (((size_t)m * a.nq + h) * a.n_kv_chunks + it.r) * (HD + 2);
 #pragma unroll
-        for (int t = 0; t < NTW; ++t)
-          *reinterpret_cast<float2*>(dst + 8 * (warp * NTW + t) + 2 * c4) =
-              make_float2(oacc[t][2 * r], oacc[t][2 * r + 1]);
+        for (int t2 = 0; t2 < NTW; ++t2)
+          *reinterpret_cast<float2*>(dst + 8 * (warp * NTW + t2) + 2 * c4) =
+              make_float2(oacc[ti][t2][2 * r], oacc[ti][t2][2 * r + 1]);
         if (warp == 0 && c4 == 0) {
-          float l = red_l[0][g + 8 * r];
-#pragma unroll
-          for (int w = 1; w < 8; ++w) l += red_l[w][g + 8 * r];
-          dst[HD] = mx[r];
-          dst[HD + 1] = l;
+          dst[HD] = m_run[ti][g + 8 * r];
+          dst[HD + 1] = l_run[ti][g + 8 * r];
         }
       }
-      __syncthreads();   // P and red_* are free again
     }
+    __syncthreads();   // the query tiles and running state are reused by the next item
   }
 }
 
@@ -342,28 +413,36 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
   trace_mark(rs1, 1);
   pdl_launch_next();
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
-  const int nch = row_pos(a.rs, m) / kKvChunk + 1;
-  const float v = merge_row_head(a.part, a.nq, a.hd, a.n_kv_chunks, m, h, nch, sm);
+  const int nparts = (row_pos(a.rs, m) / kKvChunk) / a.R + 1;   // ranges of R chunks the row sees
+  const float v = merge_row_head(a.part, a.nq, a.hd, a.n_kv_chunks, m, h, nparts, sm);
   if ((int)threadIdx.x < a.hd) act_store(a.out, m, h * a.hd + threadIdx.x, (a.rs.M + 3) / 4, v, a.umma);
 }
 
-// Dynamic shared memory of the chunk kernel: keys, values, P hi + lo, and
-// the item's query rows (padded to whole tiles of 16).
-static int attn_smem_bytes(int hd) {
-  return kKvChunk * (hd * 2 + 32) + kKvChunk * (hd * 2 + 16) + 2 * 16 * (kKvChunk + 8) * 2 + 2 * 16 * (hd + 16) * 2;
+// Dynamic shared memory of the chunk kernel: `stages` stages of keys + values
+// (1024-byte aligned for the swizzled TMA boxes), P hi + lo, and TG query
+// tiles (hi + lo).
+static int attn_smem_bytes(int hd, int stages, int tg) {
+  return 1024 + stages * 2 * kKvChunk * hd * 2 + 2 * 16 * (kKvChunk + 8) * 2 + tg * 2 * 16 * (hd + 16) * 2;
 }
 
 // Dynamic shared-memory limits of the chunk kernels and the largest
 // shared-memory carve-out for every kernel of the chain.
 cudaError_t attn_init() {
-  cudaError_t e = cudaFuncSetAttribute(k_attn_chunks<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       attn_smem_bytes(128));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_attn_chunks<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(64));
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_attn_chunks<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn_smem_bytes(128, 2, 4))) ||
+      (e = cudaFuncSetAttribute(k_attn_chunks<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn_smem_bytes(128, 2, 1))) ||
+      (e = cudaFuncSetAttribute(k_attn_chunks<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn_smem_bytes(64, 2, 4))) ||
+      (e = cudaFuncSetAttribute(k_attn_chunks<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn_smem_bytes(64, 2, 1))))
+    return e;
   // Largest shared-memory carve-out for every kernel of the chain (see gemm_init).
-  const void* fns[] = {reinterpret_cast<const void*>(k_attn_chunks<128>),
-                       reinterpret_cast<const void*>(k_attn_chunks<64>),
+  const void* fns[] = {reinterpret_cast<const void*>(k_attn_chunks<128, 4>),
+                       reinterpret_cast<const void*>(k_attn_chunks<128, 1>),
+                       reinterpret_cast<const void*>(k_attn_chunks<64, 4>),
+                       reinterpret_cast<const void*>(k_attn_chunks<64, 1>),
                        reinterpret_cast<const void*>(k_attn_merge), reinterpret_cast<const void*>(k_embed)};
   for (const void* f : fns)
     if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -378,17 +457,20 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   // Enough CTAs for the largest item count this launch can see (the count
-  // itself lives on the device): B * nkv * chunks of the whole cache, capped.
-  const int max_items = a.B * a.nkv * a.n_kv_chunks * ((a.rs.rps * (a.nq / a.nkv) + 15) / 16);
+  // itself lives on the device): B * nkv * ranges of the whole cache, capped.
+  const int ntiles = (a.rs.rps * (a.nq / a.nkv) + 15) / 16;
+  const int max_items = a.B * a.nkv * ((a.n_kv_chunks + a.R - 1) / a.R) * ((ntiles + a.TG - 1) / a.TG);
+  if (a.TG < 1 || a.TG > 4 || a.stages < 1 || a.stages > 2 || a.R < 1) return cudaErrorInvalidValue;
   cfg.gridDim = dim3(max(1, min(max_items, 2 * num_sms)));
   cfg.blockDim = dim3(kAttnThreads);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  cfg.dynamicSmemBytes = attn_smem_bytes(a.hd);
-  if (a.hd == 128) e = cudaLaunchKernelEx(&cfg, k_attn_chunks<128>, a);
-  else if (a.hd == 64) e = cudaLaunchKernelEx(&cfg, k_attn_chunks<64>, a);
+  cfg.dynamicSmemBytes = attn_smem_bytes(a.hd, a.stages, a.TG);
+  if (a.TG != 1 && a.TG != 4) return cudaErrorInvalidValue;
+  if (a.hd == 128) e = a.TG == 4 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 4>, a) : cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 1>, a);
+  else if (a.hd == 64) e = a.TG == 4 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 4>, a) : cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 1>, a);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};

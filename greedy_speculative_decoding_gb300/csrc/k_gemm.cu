@@ -110,54 +110,6 @@ __device__ __forceinline__ void mma_chunk(float (&acc)[T][4], const uint4 (&w)[4
   }
 }
 
-__device__ __forceinline__ unsigned long long shfl_max_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
-}
-
-// `finishers`: CTAs that run this epilogue in the launch (row blocks x row
-// groups); the last to arrive writes the tokens of all rows of the forward.
-__device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int m0, int M, int finishers, int* s_flag) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int m = warp; m < M; m += kGemmThreads / 32) {
-    unsigned long long best = 0ull;
-    bool bad = false;
-    const int mb = (m0 + m) / a.rs.rps, mj = (m0 + m) - mb * a.rs.rps;
-    const int lg_row = mj >= a.tok_skip ? mb * a.lg_stride + a.lg_off + mj - a.tok_skip : -1;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = lane + 32 * j;
-      const int n = rb * kBlockRows + r;
-      if (n < a.N) {
-        const float v = ys[m * kBlockRows + r];
-        if (a.logits && lg_row >= 0) a.logits[(size_t)lg_row * a.N + n] = v;
-        bad |= !isfinite(v);
-        const unsigned long long k = argmax_key(v, n);
-        best = k > best ? k : best;
-      }
-    }
-    best = shfl_max_u64(best);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) report_err(a.err, kErrNonfinite);
-    if (lane == 0) atomicMax(a.keys + m0 + m, best);
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.done, 1) == finishers - 1);
-  __syncthreads();
-  if (!*s_flag) return;
-  __threadfence();
-  if (threadIdx.x < a.rs.M) {
-    const int m = threadIdx.x;
-    const unsigned long long k = atomicExch(a.keys + m, 0ull);
-    const int b = m / a.rs.rps, j = m - b * a.rs.rps;
-    if (j >= a.tok_skip) a.tok_out[b * a.tok_stride + a.tok_off + j - a.tok_skip] = key_index(k);
-  }
-  if (threadIdx.x == 0) *a.done = 0;
-}
 
 }  // namespace
 
@@ -770,6 +722,11 @@ cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, in
 
 int nf4_scale_ld(int K) { return ((K / 64 + 7) / 8) * 8; }
 
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, long rows, int hd) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, hd, (uint64_t)rows, (uint64_t)hd * 2, 64, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 cudaError_t make_nf4_maps(CUtensorMap* codes_map, CUtensorMap* scale_map, const void* codes, const void* scales,
                           int rows, int K, int box_rows) {
   cudaError_t e = encode_2d(codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K / 2, rows, K / 2, 128, box_rows,
@@ -920,13 +877,13 @@ __global__ void k_to_frag(const float* x, int M, int K, int ld, int T, uint4* ou
   const long u = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
   int m, k0, lo;
-  if (umma) {
-    const int pos = (int)(u & 7), col = (int)((u >> 3) & 7);
+  if (umma) {   // T counts 8-token tiles here
+    const int pos = (int)(u & 7), row = (int)((u >> 3) & 7);
     const long r = u >> 6;
     const int t = (int)(r % T), j = (int)(r / T);
-    m = 4 * t + (col >> 1);
-    lo = col & 1;
-    k0 = 64 * j + 8 * (pos ^ col);
+    m = 8 * t + row;
+    lo = 0;
+    k0 = 64 * j + 8 * (pos ^ row);
   } else {
     const int lane = (int)(u & 31);
     const int h = (int)((u >> 5) & 1);
@@ -954,10 +911,11 @@ __global__ void k_to_frag(const float* x, int M, int K, int ld, int T, uint4* ou
 }
 
 cudaError_t launch_to_frag(const float* x, int M, int K, int ld, bf16* out, cudaStream_t st) {
-  const int T = (M + 3) / 4;
+  const int umma = M >= umma_min_rows() ? 1 : 0;
+  const int T = umma ? (M + 7) / 8 : (M + 3) / 4;
   const long units = (long)frag_bytes(K, T) / 16;
   k_to_frag<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(x, M, K, ld, T, reinterpret_cast<uint4*>(out), units,
-                                                            M >= umma_min_rows() ? 1 : 0);
+                                                            umma);
   return cudaGetLastError();
 }
 

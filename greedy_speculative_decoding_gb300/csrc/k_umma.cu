@@ -6,9 +6,9 @@
 // The mma.sync kernel (k_gemm.cu) covers at most 16 token rows per CTA, so a
 // 72-row verify ran as five row groups that each streamed (from L2) and, for
 // NF4 weights, dequantised every weight tile again. Here the whole token
-// block is the N side of one MMA: M = 128 weight rows, N = 8 columns per
-// token tile (hi and lo bf16 halves of four tokens), accumulated in tensor
-// memory, so every weight tile is read and dequantised once.
+// block is the N side of one MMA: M = 128 weight rows, N = one column per
+// token (bf16 activations; rounded up to a multiple of 16), accumulated in
+// tensor memory, so every weight tile is read and dequantised once.
 //
 // Warp roles, 256 threads:
 //   thread 0      producer: weight tiles by TMA (two 64-row boxes, 128-byte
@@ -21,8 +21,8 @@
 //   warps 4-7     NF4 only: dequantise each chunk's codes into a bf16 weight
 //                 tile (level x block scale) in the MMA's layout;
 //   warps 4-7     afterwards: read the accumulator (tcgen05.ld, one weight row
-//                 per thread), add each token's hi and lo columns, and write
-//                 the CTA's tile ys[m][128] in shared memory.
+//                 per thread, one column per token) and write the CTA's tile
+//                 ys[m][128] in shared memory.
 // Then all 256 threads sum the K slices (thread-block cluster, rank 0 reads
 // the other ranks' tiles; or global partial tiles and an arrival counter),
 // apply the RMSNorm row factor and run the same epilogues as k_gemm, one
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int M = a.rs.M;
-  const int T = (M + 3) / 4;              // token tiles of the operand layout
+  const int T = (M + 7) / 8;              // 8-token tiles of the operand layout
+  const int T4 = (M + 3) / 4;             // the fragment layout's tile count (epilogue stores)
   const int Tp = tiles_padded(T);         // MMA N = 8 * Tp (a multiple of 16)
   const int N = 8 * Tp;
   const int ncols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
@@ -131,10 +132,10 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     }
     for (int s = 0; s < kCodeStages; ++s) {
       mbar_init(&sm.cfull[s], 1);
-      mbar_init(&sm.cempty[s], 128);
+      mbar_init(&sm.cempty[s], 4);   // one arrival per dequantising warp
     }
     for (int s = 0; s < kDeqStages; ++s) {
-      mbar_init(&sm.afull[s], 128);
+      mbar_init(&sm.afull[s], 4);
       mbar_init(&sm.aempty[s], 1);
     }
     mbar_init(&sm.acc, 1);
@@ -261,9 +262,12 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
         }
         *reinterpret_cast<uint4*>(drow + ((c ^ sw) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
       }
-      fence_proxy_async();
-      mbar_arrive(&sm.afull[ds]);
-      if (sub == 3 || st == nch - 1) mbar_arrive(&sm.cempty[cs]);
+      fence_proxy_async();   // this thread's tile writes before the MMA's async-proxy reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.afull[ds]);
+        if (sub == 3 || st == nch - 1) mbar_arrive(&sm.cempty[cs]);
+      }
     }
   }
 
@@ -281,9 +285,9 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
       tmem_ld16(taddr + 16 * c16, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int m = 8 * c16 + i;
-        if (m < M) ys[m * kBlockRows + row] = __uint_as_float(v[2 * i]) + __uint_as_float(v[2 * i + 1]);
+      for (int i = 0; i < 16; ++i) {
+        const int m = 16 * c16 + i;
+        if (m < M) ys[m * kBlockRows + row] = __uint_as_float(v[i]);
       }
     }
   }
@@ -305,24 +309,62 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     }
   __syncthreads();
 
-  // ---- sum the K slices in slice order, scale rows by 1 / rms
+  // ---- sum the K slices in slice order, scale rows by 1 / rms, epilogue
   const int nel = M * kBlockRows;
+  const int G = (M + kGroupRows - 1) / kGroupRows;
+  auto epilogue = [&](int m0) {   // one 16-row group (the k_gemm epilogues)
+    const int Mg = min(kGroupRows, M - m0);
+    float* yg = ys + m0 * kBlockRows;
+    EpiPre<4> pre_g;
+    epi_prefetch<4, EPI>(a, rb, m0, Mg, pre_g, sm.pos + m0);
+    if (EPI == EPI_RESID) epi_resid<4>(a, yg, rb, m0, Mg, T4, pre_g);
+    else if (EPI == EPI_QKV) epi_qkv<4>(a, yg, rb, m0, Mg, pre_g, sm.pos + m0);
+    else if (EPI == EPI_SWIGLU) epi_swiglu(a, yg, rb, m0, Mg, T4);
+    else if (EPI == EPI_ARGMAX) epi_argmax(a, yg, rb, m0, Mg, a.nblocks * G, &sm.flag);   // every (block, group) once
+    else epi_store(a, yg, rb, m0, Mg);
+  };
   if (a.nsplit > 1 && a.cluster) {
-    cluster_sync();   // every rank's tile is complete
-    const uint32_t rank = cluster_rank();
-    if (rank != 0) {
-      cluster_sync();   // rank 0 has read it
-      return;
-    }
-    const uint32_t ys_s = smem_u32(ys);
-    for (int i = tid; i < nel; i += kUThreads) {
-      float v = ys[i];
-      for (int r = 1; r < a.nsplit; ++r) v += ld_dsmem(dsmem_addr(ys_s + 4 * i, r));
-      ys[i] = a.ssq ? v * sm.rinv[i / kBlockRows] : v;
-    }
+    // The K slices of this row block are the CTAs of one cluster. The sum is
+    // spread over the ranks: rank r adds 16-row groups r, r + nsplit, ...
+    // from every rank's tile (ranks in order, 16-byte remote loads all in
+    // flight together), writes them into its own tile and runs their
+    // epilogue; a last barrier keeps every tile alive until all have read.
     cluster_sync();
-  } else if (a.nsplit > 1) {
-    const int G = (M + kGroupRows - 1) / kGroupRows;
+    const uint32_t rank = cluster_rank();
+    const uint32_t ys_s = smem_u32(ys);
+    for (int g = (int)rank; g < G; g += a.nsplit) {
+      const int m0 = g * kGroupRows, Mg = min(kGroupRows, M - m0);
+      for (int i = tid; i < Mg * (kBlockRows / 4); i += kUThreads) {
+        const int e = m0 * (kBlockRows / 4) + i;   // float4 index in the tile
+        float4 v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < a.nsplit) v[r] = ld_dsmem_v4(dsmem_addr(ys_s + 16 * e, r));
+        float4 acc = v[0];
+#pragma unroll
+        for (int r = 1; r < 8; ++r)
+          if (r < a.nsplit) {
+            acc.x += v[r].x;
+            acc.y += v[r].y;
+            acc.z += v[r].z;
+            acc.w += v[r].w;
+          }
+        if (a.ssq) {
+          const float f = sm.rinv[(4 * e) / kBlockRows];
+          acc.x *= f;
+          acc.y *= f;
+          acc.z *= f;
+          acc.w *= f;
+        }
+        reinterpret_cast<float4*>(ys)[e] = acc;
+      }
+    }
+    __syncthreads();
+    for (int g = (int)rank; g < G; g += a.nsplit) epilogue(g * kGroupRows);
+    cluster_sync();
+    return;
+  }
+  if (a.nsplit > 1) {
     for (int i = tid; i < nel; i += kUThreads) {
       const int m = i / kBlockRows, g = m / kGroupRows;
       __stcg(a.part + (((size_t)(rb * G + g) * a.nsplit + sp) * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
@@ -348,23 +390,12 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     for (int i = tid; i < nel; i += kUThreads) ys[i] *= sm.rinv[i / kBlockRows];
   }
   __syncthreads();
-
-  // ---- epilogue, one 16-row group at a time (the k_gemm epilogues)
-  for (int m0 = 0; m0 < M; m0 += kGroupRows) {
-    const int Mg = min(kGroupRows, M - m0);
-    float* yg = ys + m0 * kBlockRows;
-    EpiPre<4> pre_g;
-    epi_prefetch<4, EPI>(a, rb, m0, Mg, pre_g, sm.pos + m0);
-    if (EPI == EPI_RESID) epi_resid<4>(a, yg, rb, m0, Mg, T, pre_g);
-    else if (EPI == EPI_QKV) epi_qkv<4>(a, yg, rb, m0, Mg, pre_g, sm.pos + m0);
-    else if (EPI == EPI_SWIGLU) epi_swiglu(a, yg, rb, m0, Mg, T);
-    else epi_store(a, yg, rb, m0, Mg);
-  }
+  for (int m0 = 0; m0 < M; m0 += kGroupRows) epilogue(m0);
 }
 
 // Dynamic shared memory of a launch (plus 1 KB for the 1024-byte alignment).
 int umma_smem_bytes(int M, int stages, bool nf4) {
-  const int Tp = ((M + 3) / 4 + 1) & ~1;
+  const int Tp = ((M + 7) / 8 + 1) & ~1;
   const int ring = nf4 ? kCodeStages * kCodeStage + kDeqStages * kATileBytes + stages * Tp * 1024
                        : stages * (kATileBytes + Tp * 1024);
   return 1024 + std::max(ring, M * kBlockRows * 4);
@@ -414,6 +445,7 @@ static cudaError_t launch_uf(const GemmArgs& a, int epi, cudaStream_t st, bool p
     case EPI_RESID: return launch_ut<EPI_RESID, NF4>(a, st, pdl);
     case EPI_SWIGLU: return launch_ut<EPI_SWIGLU, NF4>(a, st, pdl);
     case EPI_STORE: return launch_ut<EPI_STORE, NF4>(a, st, pdl);
+    case EPI_ARGMAX: return NF4 ? cudaErrorInvalidValue : launch_ut<EPI_ARGMAX, false>(a, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -454,6 +486,7 @@ static cudaError_t uinit_t() {
   cudaError_t e;
   if ((e = uinit_one<EPI_QKV, NF4>()) || (e = uinit_one<EPI_RESID, NF4>()) || (e = uinit_one<EPI_SWIGLU, NF4>()))
     return e;
+  if (!NF4 && (e = uinit_one<EPI_ARGMAX, false>())) return e;
   return uinit_one<EPI_STORE, NF4>();
 }
 

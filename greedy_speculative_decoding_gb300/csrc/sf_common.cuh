@@ -169,6 +169,14 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_smem, uint32_t ran
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
   return r;
 }
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -251,32 +259,32 @@ __device__ __forceinline__ size_t frag_index(int m, int k, int T) {
 
 // ------------------------------------------------ tensor-core operand order
 // Forwards of more than 16 token rows run their projections on the tcgen05
-// tensor cores, whose B operand is the canonical K-major tile with 128-byte
-// swizzle: for 64-feature chunk j and token tile t (tokens 4t .. 4t+3) one
-// 1024-byte block at byte (j * T + t) * 1024 holds 8 operand rows of 128
-// bytes, row col = 2 * (m % 4) + {0: hi, 1: lo}; the 16-byte piece with
-// features 8q .. 8q+7 of the chunk sits at position q ^ col of its row. A
-// chunk of all T tiles is therefore one contiguous T * 1024-byte block that a
-// single bulk copy brings into shared memory ready for the MMA.
-__device__ __forceinline__ size_t umma_index(int m, int k, int T, int lo) {
+// tensor cores, with the activations as plain bf16 (one operand row per
+// token) in the MMA's canonical K-major B tile with 128-byte swizzle: for
+// 64-feature chunk j and token tile t (tokens 8t .. 8t+7) one 1024-byte
+// block at byte (j * T8 + t) * 1024, T8 = ceil(M / 8), holds 8 rows of 128
+// bytes, row m % 8; the 16-byte piece with features 8q .. 8q+7 of the chunk
+// sits at position q ^ (m % 8) of its row. A chunk of all T8 tiles is one
+// contiguous T8 * 1024-byte block that a single bulk copy brings into shared
+// memory ready for the MMA.
+__device__ __forceinline__ size_t umma_index(int m, int k, int T8) {
   const int j = k >> 6, kk = k & 63;
-  const int t = m >> 2, col = 2 * (m & 3) + lo;
+  const int t = m >> 3, row = m & 7;
   const int q = kk >> 3, e = kk & 7;
-  return (((size_t)j * T + t) * 1024 + col * 128 + ((q ^ col) << 4)) / 2 + e;
+  return (((size_t)j * T8 + t) * 1024 + row * 128 + ((q ^ row) << 4)) / 2 + e;
 }
 
-// Store one activation as a bf16 hi/lo pair in the order its consumer reads:
-// fragment order (mma.sync GEMMs) or the tensor-core operand order.
+// Store one activation in the order its consumer reads: fragment order
+// (mma.sync GEMMs: a bf16 hi/lo pair) or the tensor-core operand order (bf16).
+// T = ceil(M / 4), the fragment layout's tile count.
 __device__ __forceinline__ void act_store(bf16* f, int m, int k, int T, float v, int umma) {
   const bf16 hi = __float2bfloat16_rn(v);
-  const bf16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
   if (umma) {
-    f[umma_index(m, k, T, 0)] = hi;
-    f[umma_index(m, k, T, 1)] = lo;
+    f[umma_index(m, k, (T + 1) >> 1)] = hi;
   } else {
     const size_t i = frag_index(m, k, T);
     f[i] = hi;
-    f[i + 32] = lo;
+    f[i + 32] = __float2bfloat16_rn(v - __bfloat162float(hi));
   }
 }
 

@@ -141,10 +141,17 @@ struct EmbedArgs {
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl);
 
 struct AttnArgs {
+  // The model's whole KV cache as a 2-D tensor of head_dim-wide bf16 rows
+  // (box 64 x 64, 128-byte swizzle): the keys of (sequence b, KV head h,
+  // slot p) of this layer are row kv_row0 + b * kv_brows + h * s_max + p, the
+  // values kv_vrows rows further.
+  CUtensorMap kvmap;
+  int kv_row0, kv_brows, kv_vrows;
+  int R;                   // cache chunks per work item (one partial result per R chunks)
+  int TG;                  // 16-query tiles per work item (1..4)
+  int stages;              // key/value chunks in flight per CTA (1 or 2)
   const float* q;          // [M][nq*hd], RoPE applied
-  const bf16* kc;          // layer key cache [B][nkv][s_max][hd]
-  const bf16* vc;
-  float* part;             // [M*nq][n_kv_chunks][hd + 2]
+  float* part;             // [M*nq][n_kv_chunks][hd + 2]: partial results per R-chunk range
   bf16* out;               // attention output [M][nq*hd] in fragment order
   int umma;                // out in the tensor-core operand order instead
   int nq, nkv, hd, s_max, B, n_kv_chunks;
@@ -154,6 +161,8 @@ struct AttnArgs {
   RowSet rs;
 };
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl);
+// Tensor map of a KV cache [rows][hd] bf16 (rows = layers * 2 * batch * n_kv_heads * s_max).
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, long rows, int hd);
 // Shared-memory limits and carve-out of the attention kernels (current device).
 cudaError_t attn_init();
 

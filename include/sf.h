@@ -280,15 +280,23 @@ SF_API sf_status sf_linear(const void* d_w, int32_t N, int32_t K, int32_t ld, co
                            float* d_y, void* d_workspace, void* cuda_stream);
 
 /*
- * The two halves of sf_linear. Every projection reads its token rows as
- * bf16 pairs (hi = bf16(v), lo = bf16(v - hi), about 16 mantissa bits of the
- * fp32 value) in the order the GEMM's MMA lanes consume them ("fragment
- * order"): with T = ceil(M / 4) token tiles, the 16-byte unit
- * ((j * T + t) * 2 + h) * 32 + l holds, for 64-feature chunk j, tile t, half h
- * and lane l = 4 * col + c, the 8 features 64j + 16c + 8h + 0..7 of token
- * 4t + col / 2, hi parts for even col and lo parts for odd col. Features past
- * K and tokens past M are zero.
- *   sf_frag_bytes(K, M): size of that copy (0 if invalid).
+ * The two halves of sf_linear. Every projection reads its token rows in the
+ * order its GEMM kernel consumes them.
+ * Up to 16 rows ("fragment order", the mma.sync kernel): bf16 pairs (hi =
+ * bf16(v), lo = bf16(v - hi), about 16 mantissa bits of the fp32 value) in
+ * the order the MMA lanes read their B operand: with T = ceil(M / 4) token
+ * tiles, the 16-byte unit ((j * T + t) * 2 + h) * 32 + l holds, for 64-feature
+ * chunk j, tile t, half h and lane l = 4 * col + c, the 8 features
+ * 64j + 16c + 8h + 0..7 of token 4t + col / 2, hi parts for even col and lo
+ * parts for odd col.
+ * More than 16 rows (the tcgen05 kernel; the threshold is 17 unless
+ * SF_UMMA_MIN_ROWS says otherwise): bf16(v) in the tensor-core B tile with
+ * 128-byte swizzle: with T8 = ceil(M / 8), the 1024-byte block at byte
+ * (j * T8 + t) * 1024 holds tokens 8t .. 8t+7 of chunk j, one 128-byte row
+ * per token (row m % 8), its 16-byte piece q (features 64j + 8q .. +7) at
+ * position q ^ (m % 8) of the row.
+ * Features past K and tokens past M are zero.
+ *   sf_frag_bytes(K, M): size of the copy to allocate (0 if invalid).
  *   sf_to_frag: x (device fp32 [M, ld], features 0..K-1) -> d_frag (device,
  *     16-byte aligned, sf_frag_bytes(K, M) bytes), enqueued on cuda_stream.
  *   sf_linear_frag: sf_linear reading the copy instead of x (same W, y and

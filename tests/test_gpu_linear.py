@@ -4,10 +4,19 @@ chunks with ragged tails, every row count 1..16 (the mma.sync kernel), row
 counts above 16 (the tcgen05 kernel: all rows in one tensor-memory
 accumulator), and K splits across CTAs.
 
-Error bound: the activation is carried as a bf16 pair (hi + lo, about 16
-mantissa bits) and products are summed in fp32, so |y - y_ref| stays within
-a small multiple of 2^-16 * sum_k |x_k w_nk|; the test allows 1e-4 of that sum.
+Error bound: up to 16 rows the activation is carried as a bf16 pair (hi +
+lo, about 16 mantissa bits) and products are summed in fp32, so |y - y_ref|
+stays within a small multiple of 2^-16 * sum_k |x_k w_nk|; the test allows
+1e-4 of that sum. Above 16 rows the tensor-core kernel takes the activation
+as one bf16 (relative rounding <= 2^-9 per element), so the bound is 2^-8 of
+the same sum.
 """
+
+TOL_SYNC, TOL_TC = 1e-4, 2.0 ** -8
+
+
+def tol(M):
+    return TOL_TC if M > 16 else TOL_SYNC
 
 import pytest
 import torch
@@ -35,7 +44,7 @@ def _check(pkg, N, K, M, ld=None, seed=0):
     ref = xd @ wd.t()
     bound = xd.abs() @ wd.abs().t()
     err = (y.double() - ref).abs()
-    assert bool((err <= 1e-4 * bound + 1e-30).all()), float((err / bound).max())
+    assert bool((err <= tol(M) * bound + 1e-30).all()), float((err / bound).max())
     return float((err / bound).max())
 
 
@@ -77,7 +86,8 @@ def test_tensor_core_rows(pkg, N, K, M):
     """Above 16 rows the tcgen05 kernel takes every row in one accumulator.
     Its results are deterministic, a row's bits do not depend on how many
     other rows (above 16) share the launch, and they agree with the 16-row
-    mma.sync launches of the same rows to float32 accumulation error."""
+    mma.sync launches of the same rows within the bf16 rounding of the
+    activations."""
     g = torch.Generator(device="cuda").manual_seed(N + K + M)
     w = (torch.randn(N, K, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
     x = torch.randn(M, K, generator=g, device="cuda")
@@ -87,20 +97,21 @@ def test_tensor_core_rows(pkg, N, K, M):
     wd, xd = w.double(), x.double()
     bound = xd.abs() @ wd.abs().t()
     err = (y.double() - xd @ wd.t()).abs()
-    assert bool((err <= 1e-4 * bound + 1e-30).all())
+    assert bool((err <= TOL_TC * bound + 1e-30).all())
     for m0 in range(0, M, 16):
         part = pkg.linear(w, x[m0:m0 + 16].contiguous())
-        assert bool(((part.double() - y[m0:m0 + 16].double()).abs() <= 1e-5 * bound[m0:m0 + 16] + 1e-30).all()), m0
+        assert bool(((part.double() - y[m0:m0 + 16].double()).abs() <= TOL_TC * bound[m0:m0 + 16] + 1e-30).all()), m0
 
 
 def _frag_reference(x):
     """The operand layouts written out element by element (test-side
-    restatement of what the header documents): bf16 hi/lo pairs of x [M, K]
-    as a uint16 array of the library's byte size. Up to 16 rows: fragment
-    order; above 16: the tensor-core operand order (128-byte rows of 8
-    features x 8 pieces, piece q of row col at position q ^ col)."""
+    restatement of what the header documents), as a uint16 array. Up to 16
+    rows: fragment order, bf16 hi/lo pairs of x [M, K]; above 16: the
+    tensor-core operand order, bf16 x in 128-byte rows of one token (8
+    tokens per 1024-byte tile), piece q (features 8q..8q+7 of a chunk) of row
+    m % 8 at position q ^ (m % 8)."""
     M, K = x.shape
-    T = (M + 3) // 4
+    T = (M + 3) // 4 if M <= 16 else (M + 7) // 8
     nch = (K + 63) // 64
     out = torch.zeros(nch * T * 2 * 32 * 8, dtype=torch.int16)
     hi = x.to(torch.bfloat16)
@@ -117,11 +128,9 @@ def _frag_reference(x):
                 out[unit * 8 + e] = hi16[m, k]
                 out[(unit + 4) * 8 + e] = lo16[m, k]
             else:
-                q, e = kk // 8, kk % 8
-                for half, src in ((0, hi16), (1, lo16)):
-                    col = 2 * (m % 4) + half
-                    byte = (j * T + t) * 1024 + col * 128 + ((q ^ col) << 4)
-                    out[byte // 2 + e] = src[m, k]
+                q, e, row = kk // 8, kk % 8, m % 8
+                byte = (j * T + m // 8) * 1024 + row * 128 + ((q ^ row) << 4)
+                out[byte // 2 + e] = hi16[m, k]
     return out
 
 
@@ -132,8 +141,8 @@ def test_to_frag_layout(pkg, M, K):
     xf = pkg.to_frag(x)
     torch.cuda.synchronize()
     ref = _frag_reference(x.cpu())
-    assert xf.numel() == 2 * ref.numel()
-    assert torch.equal(xf.cpu().view(torch.int16), ref)
+    assert xf.numel() >= 2 * ref.numel()
+    assert torch.equal(xf.cpu().view(torch.int16)[:ref.numel()], ref)
 
 
 @pytest.mark.parametrize("N,K,M", [(37888, 3584, 9), (1000, 904, 3), (129, 72, 16), (5, 8, 1), (1000, 904, 72)])

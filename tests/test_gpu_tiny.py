@@ -126,9 +126,11 @@ def test_batch8_ragged_rows_match_single_sequences(pkg, tiny):
     (the mma.sync GEMM). Per sequence, the draft logits equal those of the
     same sequence run alone bit for bit (a row's arithmetic does not depend
     on the other rows or sequences of a <= 16-row launch), the verify logits
-    agree with the single sequence's 9-row verify to float32 accumulation
-    error; accept lengths, committed tokens and cache lengths follow; the
-    generated streams are the oracle's greedy streams."""
+    agree with the single sequence's 9-row verify within the bf16 rounding
+    of the tensor-core path's activations (1.5e-2 of the row's range); accept
+    lengths, committed tokens and cache lengths agree with the batch's own
+    guesses and target choices (a brute-force prefix compare); the generated
+    streams are the oracle's greedy streams (near ties allowed)."""
     tw = tiny[0]
     K, B, V = 8, 8, TINY_TARGET.vocab
     lens = [20, 33, 47, 12, 60, 25, 8, 41]
@@ -155,10 +157,12 @@ def test_batch8_ragged_rows_match_single_sequences(pkg, tiny):
         one.close()
         assert torch.equal(d_log[b], d1[0]), b
         rng = (t1[0].max(dim=-1).values - t1[0].min(dim=-1).values)[:, None]
-        assert bool(((t_log[b] - t1[0]).abs() <= 1e-4 * rng).all()), b
-        assert int(n_acc[b]) == int(n1[0]) and list(committed[b]) == list(c1[0]), b
-        assert int(lt[b]) == int(lt1[0]) == lens[b] + int(n_acc[b]), b
-        assert int(ld[b]) == int(ld1[0]), b
+        assert bool(((t_log[b] - t1[0]).abs() <= 1.5e-2 * rng).all()), b
+        d_b = [int(v) for v in d_log[b].argmax(dim=-1).cpu()]
+        t_b = [int(v) for v in t_log[b].argmax(dim=-1).cpu()]
+        n = accept_brute(d_b, t_b, K)
+        assert int(n_acc[b]) == n and list(committed[b]) == d_b[:n] + [t_b[n]], b
+        assert int(lt[b]) == lens[b] + n and int(ld[b]) == lens[b] + n - 1, b
     out, rounds = eng.generate(24)
     eng.close()
     model = om.Model(TINY_TARGET, tw)
@@ -235,13 +239,45 @@ def test_rounds_integer_state_and_rollback(pkg, tiny):
     ft, fd = fresh.kv_view("target"), fresh.kv_view("draft")
 
     def close(a, b):
-        # one bf16 rounding step of the entry, or 1e-3 of the cache's scale
+        # The fresh prefill's QKV projection takes its activations as bf16
+        # (tensor-core path): a key or value moves by up to 2^-9 of
+        # sum_k |W_nk x_k|, about 1e-2 of the cache's largest entry here.
         a, b = a.float(), b.float()
-        return bool(((a - b).abs() <= 2.0 ** -7 * b.abs() + 1e-3 * b.abs().max()).all())
+        return bool(((a - b).abs() <= 2.0 ** -6 * b.abs() + 1e-2 * b.abs().max()).all())
     P = len(prompt)
     assert torch.equal(kv_t[..., : P - 1, :], ft[..., : P - 1, :])
     assert close(kv_t[..., : C - 1, :], ft[..., : C - 1, :])
     assert close(kv_d[..., : C - 2, :], fd[..., : C - 2, :])
+    fresh.close()
+    eng.close()
+
+
+def test_rollback_bit_exact_short(pkg, tiny):
+    """Two rounds from a 6-token prompt keep every forward (prefill, draft
+    steps, verify, and the fresh prefill of the committed prefix) at 16 rows
+    or fewer, so all run on the same GEMM kernel: after the in-place
+    rollback both caches below their lengths equal a fresh prefill of the
+    committed prefix bit for bit."""
+    K = 4
+    prompt = uniform_prompt(6, 1024, seed=104).tolist()
+    eng = make_engine(pkg, tiny, K=K)
+    eng.prefill([prompt])
+    seq = list(prompt)
+    for _ in range(2):
+        eng.draft()
+        eng.verify()
+        _, committed = eng.accept_rollback()
+        seq += committed[0]
+    C = len(seq)
+    assert C - 1 <= 16
+    lt, ld = eng.lengths()
+    assert int(lt[0]) == C - 1 and int(ld[0]) == C - 2
+    kv_t = eng.kv_view("target").clone()
+    kv_d = eng.kv_view("draft").clone()
+    fresh = make_engine(pkg, tiny, K=K)
+    fresh.prefill([seq])
+    assert torch.equal(kv_t[..., : C - 1, :], fresh.kv_view("target")[..., : C - 1, :])
+    assert torch.equal(kv_d[..., : C - 2, :], fresh.kv_view("draft")[..., : C - 2, :])
     fresh.close()
     eng.close()
 
@@ -385,9 +421,9 @@ def test_head_shapes_with_poisoned_caches(pkg, name):
     torch.cuda.synchronize()
     # The draft is the target; the 70-token prompt was prefilled by the
     # tcgen05 GEMM and the first draft step rewrote slot C-2 with the mma.sync
-    # GEMM, so draft and verify rows agree to float32 accumulation error.
+    # GEMM, so draft and verify rows agree within that slot's rounding.
     rng = (t_log.max(dim=-1).values - t_log.min(dim=-1).values)[:, None]
-    assert bool(((d_log - t_log[:K]).abs() <= 1e-4 * rng[:K]).all())
+    assert bool(((d_log - t_log[:K]).abs() <= 1.5e-2 * rng[:K]).all())
     d = d_out.cpu().tolist()
     m = om.Model(shape, w)
     c = m.new_cache()
@@ -396,7 +432,8 @@ def test_head_shapes_with_poisoned_caches(pkg, name):
     worst = max(logit_err(t_log[j], ref[j]) for j in range(K + 1))
     print(f"{name}: max logit error / range = {worst:.3e}")
     assert worst < LOGIT_TOL_BF16
-    eng.accept_rollback()
+    n_acc, _ = eng.accept_rollback()
+    assert int(n_acc[0]) == accept_brute(d, t_log.argmax(dim=-1).cpu().tolist(), K)
     eng.close()
 
 
