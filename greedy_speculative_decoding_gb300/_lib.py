@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libsf.so")
 
 SF_OK, SF_ERR_ARG, SF_ERR_CAPACITY, SF_ERR_CUDA, SF_ERR_NONFINITE, SF_ERR_STATE, SF_ERR_UNSUPPORTED, \
     SF_ERR_DEVICE = range(8)
-SF_WDTYPE_BF16, SF_WDTYPE_NF4 = 0, 1
+SF_WDTYPE_BF16, SF_WDTYPE_NF4, SF_WDTYPE_F32 = 0, 1, 2
 SF_DRAFT_NEURAL, SF_DRAFT_NGRAM, SF_DRAFT_NONE = 0, 1, 2
 SF_MAX_ROWS = 80
 

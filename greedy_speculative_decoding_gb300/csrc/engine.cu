@@ -45,6 +45,7 @@ sf_status fail(sf_status s, const char* fmt, ...) {
 
 struct Plan {
   int nblocks = 0, nsplit = 1, cps = 1;
+  int cluster = 1;   // the K slices of a row block form one cluster (else: global partial tiles)
 };
 
 // Split K only when the row blocks alone cannot fill the GPU; the split
@@ -72,16 +73,16 @@ struct LayerW {
   CUtensorMap tmsu[7];
   const void* w[7] = {};
   const void* sc[7] = {};  // NF4 block scales
-  const bf16 *ln1 = nullptr, *ln2 = nullptr, *bq = nullptr, *bk = nullptr, *bv = nullptr;
+  const void *ln1 = nullptr, *ln2 = nullptr, *bq = nullptr, *bk = nullptr, *bv = nullptr;   // bf16 or fp32
 };
 
 struct Model {
   sf_model_cfg c{};
-  const bf16* embed = nullptr;
+  const void* embed = nullptr;   // bf16, or fp32 (SF_WDTYPE_F32)
   int embed_ld = 0;
   std::vector<LayerW> L;
-  const bf16* norm = nullptr;
-  const bf16* lm = nullptr;
+  const void* norm = nullptr;
+  const void* lm = nullptr;
   int lm_ld = 0;
   CUtensorMap lm_tm;
   CUtensorMap lm_tmu;      // 64-row boxes: the LM head of forwards of more than 16 rows (tcgen05)
@@ -104,6 +105,8 @@ constexpr size_t kLinearPartBytes = (size_t)kLinearTiles * kGroupRows * kBlockRo
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+constexpr int kMaxSms = 256;   // bound on the SM count for workspace sizing
+
 bool cfg_ok(const sf_model_cfg* c, std::string* why) {
   auto bad = [&](const char* m) {
     *why = m;
@@ -119,7 +122,8 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
   if ((c->n_heads * c->head_dim) % 128 || (c->n_kv_heads * c->head_dim) % 128)
     return bad("n_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
   if (c->ffn % 8) return bad("ffn must be a multiple of 8");
-  if (c->wdtype != SF_WDTYPE_BF16 && c->wdtype != SF_WDTYPE_NF4) return bad("unknown wdtype");
+  if (c->wdtype != SF_WDTYPE_BF16 && c->wdtype != SF_WDTYPE_NF4 && c->wdtype != SF_WDTYPE_F32)
+    return bad("unknown wdtype");
   if (c->wdtype == SF_WDTYPE_NF4 && c->ffn % 64) return bad("NF4 weights need ffn to be a multiple of 64");
   const int eld = c->embed_ld ? c->embed_ld : c->hidden;
   if (eld < c->hidden || eld % 8) return bad("embed_ld must be >= hidden and a multiple of 8");
@@ -128,7 +132,7 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
 }
 
 struct Layout {
-  size_t x, ssq, q, apart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, total;
+  size_t x, ssq, q, apart, upart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, total;
   int n_kv_chunks, max_blocks;
 };
 
@@ -207,6 +211,9 @@ Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, i
   L.ssq = take((size_t)(H / 128) * kRows * 4);
   L.q = take((size_t)kRows * QD * 4);
   L.apart = take((size_t)kRows * NQ * L.n_kv_chunks * (HD + 2) * 4);
+  // tcgen05 GEMM partial tiles when its K slices cannot all be clusters: at
+  // most two CTAs per SM, each with up to SF_MAX_ROWS x 128 floats.
+  L.upart = take((size_t)2 * kMaxSms * kRows * kBlockRows * 4);
   L.counters = take((size_t)L.max_blocks * kMaxGroups * 4);
   L.keys = take((size_t)kRows * 8);
   L.done = take(4);
@@ -250,6 +257,7 @@ struct sf_engine {
   int B = 0, K = 0, s_max = 0, num_sms = 0, slots = 0;
   cudaStream_t user = nullptr, cap = nullptr;
   unsigned char* ws = nullptr;
+  float* upart = nullptr;   // tcgen05 GEMM partial tiles (non-cluster K split)
   Layout lay{};
   StateOff so{};
   bf16 *fx = nullptr, *fh = nullptr, *fo = nullptr, *fa = nullptr;
@@ -282,7 +290,7 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
   };
   int i = 0;
-  md.embed = static_cast<const bf16*>(w[i++]);
+  md.embed = w[i++];
   if (!check(md.embed, "embed", false)) return fail(SF_ERR_ARG, "embed pointer null or not 16-byte aligned");
   md.embed_ld = c->embed_ld ? c->embed_ld : c->hidden;
   md.L.resize(c->layers);
@@ -294,15 +302,15 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
       lw.w[k] = w[i++];
       if (nf4) lw.sc[k] = w[i++];
     };
-    lw.ln1 = static_cast<const bf16*>(w[i++]);
+    lw.ln1 = w[i++];
     lin(W_Q);
     lin(W_K);
     lin(W_V);
-    lw.bq = static_cast<const bf16*>(w[i++]);
-    lw.bk = static_cast<const bf16*>(w[i++]);
-    lw.bv = static_cast<const bf16*>(w[i++]);
+    lw.bq = w[i++];
+    lw.bk = w[i++];
+    lw.bv = w[i++];
     lin(W_O);
-    lw.ln2 = static_cast<const bf16*>(w[i++]);
+    lw.ln2 = w[i++];
     lin(W_G);
     lin(W_U);
     lin(W_D);
@@ -312,13 +320,13 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     if (c->qkv_bias) ok = ok && check(lw.bq, "bq", false) && check(lw.bk, "bk", false) && check(lw.bv, "bv", false);
     if (!ok) return fail(SF_ERR_ARG, "layer %d: a weight pointer is null or not 16-byte aligned", l);
   }
-  md.norm = static_cast<const bf16*>(w[i++]);
+  md.norm = w[i++];
   if (!check(md.norm, "norm", false)) return fail(SF_ERR_ARG, "final norm pointer null or misaligned");
   if (c->tied) {
     md.lm = md.embed;
     md.lm_ld = md.embed_ld;
   } else {
-    md.lm = static_cast<const bf16*>(w[i++]);
+    md.lm = w[i++];
     md.lm_ld = c->hidden;
     if (!check(md.lm, "lm_head", false)) return fail(SF_ERR_ARG, "lm_head pointer null or misaligned");
   }
@@ -341,7 +349,8 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   }
   const int H = c->hidden;
   const int QD = c->n_heads * c->head_dim, KVD = c->n_kv_heads * c->head_dim, F = c->ffn;
-  for (int l = 0; l < c->layers; ++l) {
+  const bool f32 = c->wdtype == SF_WDTYPE_F32;   // plain pointers, no tensor maps
+  for (int l = 0; l < c->layers && !f32; ++l) {
     LayerW& lw = md.L[l];
     const int rows[7] = {QD, KVD, KVD, H, F, F, H};
     const int ks[7] = {H, H, H, QD, H, H, F};
@@ -355,7 +364,7 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
         return fail(SF_ERR_CUDA, "layer %d weight %d: tensor map: %s", l, k, cudaGetErrorString(ce));
     }
   }
-  {
+  if (!f32) {
     cudaError_t ce = make_weight_map(&md.lm_tm, md.lm, c->vocab, H, md.lm_ld);
     if (ce == cudaSuccess) ce = make_weight_map(&md.lm_tmu, md.lm, c->vocab, H, md.lm_ld, 64);
     if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "LM head tensor map: %s", cudaGetErrorString(ce));
@@ -373,6 +382,17 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   auto plan = [&](int nblocks, long rows, long k) {
     const bool big = rows * k * (nf4 ? 1 : 2) >= (24l << 20);
     const int slots = big ? 2 * e->num_sms : e->num_sms;
+    // Matrices of 64 MB and more whose row blocks fill less than a third of
+    // the CTA slots take more than 8 K slices, summed through global partial
+    // tiles (the last CTA of a row block adds them in order): bandwidth over
+    // the cluster reduction's lower latency.
+    if (rows * k * (nf4 ? 1 : 2) >= (64l << 20) && slots / nblocks > 8) {
+      Plan p = make_plan(nblocks, (int)k, slots, 16, al);
+      if (p.nsplit > 8) {
+        p.cluster = 0;
+        return p;
+      }
+    }
     Plan p = make_plan(nblocks, (int)k, slots, big ? 8 : kMaxClusterSplit, al);
     while (p.nsplit > 1) {
       const int stages = pick_stages(p.nblocks * p.nsplit, p.cps, e->num_sms, nf4);
@@ -386,13 +406,14 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   md.p_o = plan(nblocks_of(c, 1), H, (long)c->n_heads * c->head_dim);
   md.p_gu = plan(nblocks_of(c, 2), 2l * c->ffn, H);
   md.p_d = plan(nblocks_of(c, 1), H, c->ffn);
-  // tcgen05 GEMM: two CTAs per SM whatever the row count, K slices in
-  // clusters of at most 8 that fit with a fifth of the cluster slots to spare.
+  // tcgen05 GEMM: two CTAs per SM whatever the row count, up to 8 K slices;
+  // the slices of a row block form a cluster when all clusters fit on the GPU
+  // at once, else they add their tiles through global memory (the cluster
+  // placement of this footprint allows far fewer than two CTAs per SM).
   auto uplan = [&](int nblocks, long k) {
     const int stages = umma_stages(kRows, nf4);
     Plan p = make_plan(nblocks, (int)k, 2 * e->num_sms, 8, al);
-    while (p.nsplit > 1 && 5 * p.nblocks > 4 * umma_max_clusters(p.nsplit, kRows, stages, nf4))
-      p = make_plan(nblocks, (int)k, 2 * e->num_sms, p.nsplit - 1, al);
+    if (p.nsplit > 1 && p.nblocks > umma_max_clusters(p.nsplit, kRows, stages, nf4)) p.cluster = 0;
     return p;
   };
   md.u_qkv = uplan(nblocks_of(c, 0), H);
@@ -417,6 +438,7 @@ GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& r
   a.counter = e->counters;
   a.cluster = 1;   // the K slices of a row block are one cluster
   a.err = e->st.err;
+  a.wf32 = md.c.wdtype == SF_WDTYPE_F32 ? 1 : 0;
   a.expire_first_wait = e->expire_waits ? 1 : 0;
   a.rs = rs;
   a.eps = md.c.rms_eps;
@@ -456,8 +478,10 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   // More than 16 token rows: the projections run on the tcgen05 GEMM, whose
   // inputs the producers write in the tensor-core operand order (the LM head
   // keeps reading fragment order).
-  const bool tc = rs.M >= umma_min_rows();
+  const bool f32 = c.wdtype == SF_WDTYPE_F32;   // fp32 weights: the plain fp32 kernel, fragment order
+  const bool tc = !f32 && rs.M >= umma_min_rows();
   auto gemm = [&](const GemmArgs& a, int epi) {
+    if (f32) return launch_gemm_f32(a, epi, s, e->pdl);
     return tc ? launch_umma(a, epi, s, e->pdl) : launch_gemm(a, epi, s, e->pdl);
   };
   auto maps = [&](GemmArgs& a, const LayerW& lw, int slot, int w) {
@@ -466,6 +490,10 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   };
   auto stages = [&](const GemmArgs& a) {
     return tc ? umma_stages(rs.M, nf4) : pick_stages(a.nblocks * a.nsplit, a.cps, e->num_sms, nf4);
+  };
+  auto uplan_args = [&](GemmArgs& a, const Plan& p) {   // cluster or global K-slice sums
+    a.cluster = p.cluster;
+    a.part = e->upart;
   };
   EmbedArgs ea{};
   ea.E = md.embed;
@@ -477,6 +505,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.ssq = e->ssq;
   ea.frag = e->fx;
   ea.gain = md.L[0].ln1;
+  ea.f32 = f32;
   ea.umma = tc;
   ea.rs = traced(e, rs, "embed");
   CK(launch_embed(ea, s, e->pdl));
@@ -500,6 +529,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     maps(a, lw, 2, W_V);
     a.nf4 = nf4;
     a.stages = stages(a);
+    uplan_args(a, tc ? md.u_qkv : md.p_qkv);
     a.bias[0] = lw.bq;
     a.bias[1] = lw.bk;
     a.bias[2] = lw.bv;
@@ -556,6 +586,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     maps(a, lw, 0, W_O);
     a.nf4 = nf4;
     a.stages = stages(a);
+    uplan_args(a, tc ? md.u_o : md.p_o);
     a.seg_end[0] = H;
     a.ld[0] = QD;
     a.nseg = 1;
@@ -578,6 +609,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     maps(a, lw, 1, W_U);
     a.nf4 = nf4;
     a.stages = stages(a);
+    uplan_args(a, tc ? md.u_gu : md.p_gu);
     a.ld[0] = a.ld[1] = H;
     a.nseg = 2;
     a.N = c.ffn;
@@ -596,6 +628,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     maps(a, lw, 0, W_D);
     a.nf4 = nf4;
     a.stages = stages(a);
+    uplan_args(a, tc ? md.u_d : md.p_d);
     a.seg_end[0] = H;
     a.ld[0] = c.ffn;
     a.nseg = 1;
@@ -634,7 +667,9 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   a.lg_stride = to.lg_stride;
   a.lg_off = to.lg_off;
   a.rs = traced(e, rs, "lm_head");
-  if (tc) {
+  if (f32) {
+    CK(launch_gemm_f32(a, EPI_ARGMAX, s, e->pdl));
+  } else if (tc) {
     a.stages = umma_stages(rs.M, false);
     CK(launch_umma(a, EPI_ARGMAX, s, e->pdl));
   } else {
@@ -825,6 +860,7 @@ extern "C" {
 
 int32_t sf_weight_count(const sf_model_cfg* cfg) {
   if (!cfg || cfg->layers < 1) return -1;
+  if (cfg->wdtype < SF_WDTYPE_BF16 || cfg->wdtype > SF_WDTYPE_F32) return -1;
   const int per_layer = cfg->wdtype == SF_WDTYPE_NF4 ? 12 + 7 : 12;
   return 1 + cfg->layers * per_layer + 1 + (cfg->tied ? 0 : 1);
 }
@@ -929,6 +965,7 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->fo = reinterpret_cast<bf16*>(ws + e->lay.fo);
   e->fa = reinterpret_cast<bf16*>(ws + e->lay.fa);
   e->apart = reinterpret_cast<float*>(ws + e->lay.apart);
+  e->upart = reinterpret_cast<float*>(ws + e->lay.upart);
   e->counters = reinterpret_cast<int*>(ws + e->lay.counters);
   e->keys = reinterpret_cast<unsigned long long*>(ws + e->lay.keys);
   e->done = reinterpret_cast<int*>(ws + e->lay.done);
@@ -1270,7 +1307,7 @@ sf_status sf_linear_frag(const void* d_w, int32_t N, int32_t K, int32_t ld, cons
   CK(cudaGetDevice(&dev));
   CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const bool tc = M >= umma_min_rows();   // more than 16 rows: the tcgen05 GEMM
-  const Plan p = make_plan((N + 127) / 128, K, 2 * sms, 1 << 30);
+  const Plan p = make_plan((N + 127) / 128, K, 2 * sms, tc ? 16 : 1 << 30);
   const int groups = (M + kGroupRows - 1) / kGroupRows;
   if (p.nsplit > 1 && p.nblocks * p.nsplit * groups > kLinearTiles)
     return fail(SF_ERR_UNSUPPORTED, "plan too large");

@@ -29,14 +29,14 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, 
       const int i = threadIdx.x + e * kGemmThreads;
       const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
       pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)(m0 + m) * a.out_ld + n] : 0.f;
-      pre.v1[e] = (a.frag_gain && n < a.N) ? __bfloat162float(a.frag_gain[n]) : 0.f;
+      pre.v1[e] = (a.frag_gain && n < a.N) ? ldw(a.frag_gain, n, a.wf32) : 0.f;
     }
   } else if (EPI == EPI_QKV) {
     const int half = a.hd >> 1;
     const int n0 = rb * kBlockRows;
     const int s = n0 < a.seg_end[0] ? 0 : (n0 < a.seg_end[1] ? 1 : 2);   // one segment per block
     const int seg0 = s ? a.seg_end[s - 1] : 0;
-    const bf16* bias = a.bias[s];
+    const void* bias = a.bias[s];
 #pragma unroll
     for (int e = 0; e < kE; ++e) {
       const int i = threadIdx.x + e * kGemmThreads;
@@ -46,9 +46,9 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, 
       pre.v0[e] = pre.v1[e] = 0.f;
       pre.cs[e] = make_float2(1.f, 0.f);
       if (m < M && n0 + r < a.N) {
-        if (bias) pre.v0[e] = __bfloat162float(bias[local]);
+        if (bias) pre.v0[e] = ldw(bias, local, a.wf32);
         if (s < 2 && d < half) {
-          if (bias) pre.v1[e] = __bfloat162float(bias[local + half]);
+          if (bias) pre.v1[e] = ldw(bias, local + half, a.wf32);
           pre.cs[e] = a.rope[(size_t)pos[m] * half + d];
         }
       }

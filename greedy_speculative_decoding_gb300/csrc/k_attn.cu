@@ -34,9 +34,9 @@ __global__ void __launch_bounds__(128) k_embed(const __grid_constant__ EmbedArgs
     tok = 0;
   }
   const int n = blk * 128 + i;
-  const float v = __bfloat162float(a.E[(size_t)tok * a.ld + n]);
+  const float v = ldw(a.E, (size_t)tok * a.ld + n, a.f32);
   a.x[(size_t)m * a.H + n] = v;
-  act_store(a.frag, m, n, (a.rs.M + 3) / 4, v * __bfloat162float(a.gain[n]), a.umma);
+  act_store(a.frag, m, n, (a.rs.M + 3) / 4, v * ldw(a.gain, n, a.f32), a.umma);
   const float s = warp_sum(v * v);
   if ((i & 31) == 0) part[i >> 5] = s;
   __syncthreads();

@@ -828,6 +828,7 @@ static cudaError_t gemm_init_all() {
       (e = init_t<3, true>()) || (e = init_t<4, true>()) || (e = init_t<4, false, true>()) ||
       (e = init_t<4, true, true>()))
     return e;
+  if ((e = f32_init()) != cudaSuccess) return e;
   return umma_init();
 }
 

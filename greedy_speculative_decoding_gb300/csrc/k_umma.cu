@@ -377,13 +377,39 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     __syncthreads();
     if (!sm.flag) return;
     __threadfence();
-    for (int i = tid; i < nel; i += kUThreads) {
-      const int m = i / kBlockRows, g = m / kGroupRows;
-      const float* src = a.part + ((size_t)(rb * G + g) * a.nsplit * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
-                         (i - m * kBlockRows);
-      float v = 0.f;
-      for (int p = 0; p < a.nsplit; ++p) v += __ldcg(src + (size_t)p * kGroupRows * kBlockRows);
-      ys[i] = a.ssq ? v * sm.rinv[m] : v;
+    // The last CTA of the row block adds the slices in order, 16-byte loads
+    // of every slice for two positions in flight at once.
+    const int n4 = nel / 4;
+    for (int i0 = tid; i0 < n4; i0 += 2 * kUThreads) {
+      float4 v[2][16];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u * kUThreads;
+        if (i >= n4) break;
+        const int m = (4 * i) / kBlockRows, g = m / kGroupRows;
+        const float4* src = reinterpret_cast<const float4*>(
+            a.part + ((size_t)(rb * G + g) * a.nsplit * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
+            (4 * i - m * kBlockRows));
+#pragma unroll
+        for (int p = 0; p < 16; ++p)
+          if (p < a.nsplit) v[u][p] = __ldcg(src + (size_t)p * (kGroupRows * kBlockRows / 4));
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u * kUThreads;
+        if (i >= n4) break;
+        float4 acc = v[u][0];
+#pragma unroll
+        for (int p = 1; p < 16; ++p)
+          if (p < a.nsplit) {
+            acc.x += v[u][p].x;
+            acc.y += v[u][p].y;
+            acc.z += v[u][p].z;
+            acc.w += v[u][p].w;
+          }
+        const float f = a.ssq ? sm.rinv[(4 * i) / kBlockRows] : 1.f;
+        reinterpret_cast<float4*>(ys)[i] = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+      }
     }
     if (tid == 0) a.counter[rb * G] = 0;
   } else if (a.ssq) {
@@ -464,7 +490,7 @@ int umma_min_rows() {
 
 cudaError_t launch_umma(const GemmArgs& a, int epi, cudaStream_t st, bool pdl) {
   if (a.rs.M < 1 || a.rs.M > kRows) return cudaErrorInvalidValue;
-  if (a.cluster && a.nsplit > 8) return cudaErrorInvalidValue;
+  if (a.nsplit > (a.cluster ? 8 : 16)) return cudaErrorInvalidValue;
   if (a.stages < 2 || a.stages > kUMaxStages) return cudaErrorInvalidValue;
   if (umma_smem_bytes(a.rs.M, a.stages, a.nf4) > 227 * 1024) return cudaErrorInvalidValue;
   if (a.nf4 && (a.K % 64 || (a.nsplit > 1 && a.cps % 4))) return cudaErrorInvalidValue;

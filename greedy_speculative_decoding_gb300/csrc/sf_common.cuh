@@ -57,6 +57,11 @@ __device__ __forceinline__ void trace_mark(const RowSet& rs, int k) {
   }
 }
 
+// One weight-side scalar (gain, bias, embedding entry): bf16, or fp32.
+__device__ __forceinline__ float ldw(const void* p, size_t i, int f32) {
+  return f32 ? static_cast<const float*>(p)[i] : __bfloat162float(static_cast<const bf16*>(p)[i]);
+}
+
 // Set an error bit in the caller's status word; launches made outside an
 // engine (sf_linear) carry no status word and report nothing.
 __device__ __forceinline__ void report_err(int* err, int bit) {

@@ -16,7 +16,7 @@ struct GemmArgs {
                               // (NF4: codes {K/2 bytes, rows}, box {128, 16}, 128-byte swizzle)
   CUtensorMap tms[3];         // NF4 block scales per segment: {K/64, rows}, box {8, 16}
   const void* w[3];           // row segments (QKV: q, k, v; SWIGLU: gate, up)
-  const bf16* bias[3];
+  const void* bias[3];        // bf16, or fp32 when wf32
   int seg_end[3];             // cumulative row ends of the segments
   int ld[3];                  // row stride in elements (bf16) / codes (NF4)
   int nseg;
@@ -39,7 +39,7 @@ struct GemmArgs {
   // Fragment-ordered copy of the epilogue's result for the next GEMM: RESID
   // writes x * frag_gain (the next RMSNorm's input), SWIGLU the activation.
   bf16* frag_out;
-  const bf16* frag_gain;
+  const void* frag_gain;      // bf16, or fp32 when wf32
   int frag_umma;              // frag_out in the tensor-core operand order (umma_index) instead of fragment order
   // split-K scratch without clusters: partial tiles [row block x row group][split][16][128]
   // and one arrival counter per (row block, row group)
@@ -60,6 +60,7 @@ struct GemmArgs {
   float* logits;              // ARGMAX: optional fp32 rows, row (b*lg_stride + lg_off + j - tok_skip)
   int lg_stride, lg_off;
   int* err;                   // status word (kErr* bits), or null
+  int wf32;                   // gains and biases are fp32 (SF_WDTYPE_F32 models)
   int expire_first_wait;      // test hook: the first weight-tile wait reports an expiry
   RowSet rs;
 };
@@ -126,15 +127,21 @@ cudaError_t set_umma_nf4_levels(const float levels[16]);
 // The LM head with its argmax as a persistent kernel (one K slice, at most
 // two CTAs per SM walking the row blocks); same arguments as EPI_ARGMAX.
 cudaError_t launch_lmhead(const GemmArgs& a, int num_sms, cudaStream_t st, bool pdl);
+// The projections of SF_WDTYPE_F32 models (k_f32.cu): fp32 weights (plain
+// pointers, row stride ld), one CTA per 128 output rows, any row count up to
+// SF_MAX_ROWS, inputs in fragment order, the same epilogues.
+cudaError_t launch_gemm_f32(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
+cudaError_t f32_init();
 
 struct EmbedArgs {
-  const bf16* E;
+  const void* E;   // bf16, or fp32 when f32
   int ld, H, vocab;
   int* err;
   float* x;      // [M][H]
   float* ssq;    // [H/128][kRows]
   bf16* frag;    // x * gain in fragment order (the first RMSNorm's input)
-  const bf16* gain;
+  const void* gain;
+  int f32;       // embedding and gain in fp32
   int umma;      // frag in the tensor-core operand order instead
   RowSet rs;
 };

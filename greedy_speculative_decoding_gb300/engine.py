@@ -45,8 +45,22 @@ def is_nf4(weights: dict) -> bool:
     return any(k.endswith(".scales") for k in weights)
 
 
+def is_f32(weights: dict) -> bool:
+    e = weights.get("embed")
+    return e is not None and e.dtype == torch.float32
+
+
+def wdtype_of(weights: dict) -> int:
+    """SF_WDTYPE_* of a weight dict: NF4 when block scales are present, fp32
+    when the tensors are float32, else bf16."""
+    if is_nf4(weights):
+        return L.SF_WDTYPE_NF4
+    return L.SF_WDTYPE_F32 if is_f32(weights) else L.SF_WDTYPE_BF16
+
+
 def _ptr_array(shape, weights: dict):
     nf4 = is_nf4(weights)
+    f32 = is_f32(weights)
     names = weight_order(shape, nf4)
     arr = (ctypes.c_void_p * len(names))()
     keep = []
@@ -55,7 +69,7 @@ def _ptr_array(shape, weights: dict):
         if t is None:
             arr[i] = None
             continue
-        want = torch.bfloat16
+        want = torch.float32 if f32 else torch.bfloat16
         if nf4 and n.split(".")[-1] in LINEAR:
             want = torch.uint8
         elif n.endswith(".scales"):
@@ -84,7 +98,8 @@ class SpecEngine:
     draft model (without one, prompt lookup drafts).
 
     Weight dicts map the canonical names (embed, layers.i.*, norm, lm_head)
-    to bf16 CUDA tensors that must outlive the engine.
+    to CUDA tensors that must outlive the engine: bf16, fp32 (every tensor),
+    or bf16 with NF4 codes + scales for the linear maps.
     """
 
     def __init__(self, target_shape, target_w: dict, draft_shape=None, draft_w=None, batch: int = 1,
@@ -92,10 +107,10 @@ class SpecEngine:
         self.lib = L.load()
         self.B, self.K, self.s_max = batch, K, s_max
         self.target_shape, self.draft_shape = target_shape, draft_shape
-        self.tc = model_cfg(target_shape, L.SF_WDTYPE_NF4 if is_nf4(target_w) else L.SF_WDTYPE_BF16)
+        self.tc = model_cfg(target_shape, wdtype_of(target_w))
         self.dc = None
         if draft_shape is not None:
-            self.dc = model_cfg(draft_shape, L.SF_WDTYPE_NF4 if is_nf4(draft_w) else L.SF_WDTYPE_BF16)
+            self.dc = model_cfg(draft_shape, wdtype_of(draft_w))
         pdc = ctypes.byref(self.dc) if self.dc is not None else None
         ws = self.lib.sf_workspace_bytes(ctypes.byref(self.tc), pdc, batch, K, s_max)
         if ws == 0:

@@ -78,7 +78,10 @@ typedef enum {
   SF_ERR_DEVICE = 7        /* a kernel reported a bounded wait that expired */
 } sf_status;
 
-enum { SF_WDTYPE_BF16 = 0, SF_WDTYPE_NF4 = 1 };
+/* Weight types: bf16; NF4 for the 7 linear maps of every layer (embedding,
+ * norms, biases and LM head stay bf16); or fp32 for every tensor (the
+ * single-precision correctness workload; plain fp32 arithmetic, not a fast path). */
+enum { SF_WDTYPE_BF16 = 0, SF_WDTYPE_NF4 = 1, SF_WDTYPE_F32 = 2 };
 /* Drafters: the draft model, prompt lookup, or none (each round then commits
  * only the target's own next token: plain greedy decoding, the baseline the
  * speculative rounds are measured against). */
@@ -92,12 +95,12 @@ typedef struct {
   int32_t embed_ld;   /* row stride of the embedding in elements; 0 = hidden */
   float rope_theta;   /* RoPE base */
   float rms_eps;      /* RMSNorm epsilon */
-  int32_t wdtype;     /* SF_WDTYPE_BF16, or SF_WDTYPE_NF4 for the 7 linear
-                         maps of every layer (embedding, norms, LM head stay bf16) */
+  int32_t wdtype;     /* SF_WDTYPE_BF16, SF_WDTYPE_NF4 or SF_WDTYPE_F32 */
 } sf_model_cfg;
 
 /*
- * Weight pointers (device, row-major [out, in], bf16 unless stated), in this
+ * Weight pointers (device, row-major [out, in], bf16 unless stated; every
+ * tensor fp32 with SF_WDTYPE_F32), in this
  * order: embed [vocab, hidden] (row stride embed_ld); per layer: ln1 [hidden],
  * wq [n_heads*head_dim, hidden], wk, wv [n_kv_heads*head_dim, hidden],
  * bq, bk, bv (NULL when qkv_bias == 0), wo [hidden, n_heads*head_dim],
