@@ -443,14 +443,15 @@ def run_trace(args):
 # ---------------------------------------------------------------------------- ours
 def run_gemm_only(args):
     """Small case for kernel profiling: the 7B gate+up matrix (271 MB, above
-    L2) streamed by sf_linear with 9 rows, a few launches."""
+    L2) streamed by sf_linear with --gemm-rows token rows (default 9: the
+    mma.sync kernel; above 16: the tcgen05 kernel), a few launches."""
     import torch
     torch.cuda.set_device(0)
     import __graft_entry__ as g
     g.build()
     import greedy_speculative_decoding_gb300 as pkg
     t_shape, _ = _shapes()
-    N, K, M = 2 * t_shape.ffn, t_shape.hidden, K_GUESS + 1
+    N, K, M = 2 * t_shape.ffn, t_shape.hidden, args.gemm_rows
     gen = torch.Generator(device="cuda").manual_seed(0)
     w = (torch.randn(N, K, generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
     x = torch.randn(M, K, generator=gen, device="cuda")
@@ -461,6 +462,37 @@ def run_gemm_only(args):
         pkg.linear_frag(w, xf, M, y, ws)
     torch.cuda.synchronize()
     print(json.dumps({"gemm_only": True, "N": N, "K": K, "M": M}))
+
+
+def run_nf4_b8_small(args):
+    """Small case for kernel profiling of the batch-8 NF4 verify: the 14B
+    shape with 2 layers and a 32000-token vocabulary (about 2.5 GB on the
+    device), NF4 linear maps, 8 sequences prefilled to the batch-8
+    workload's contexts, prompt-lookup rounds (72-row verify forwards); the
+    last two rounds run inside the NVTX range "round"."""
+    import numpy as np
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as pkg
+    from synth import QWEN14B, make_weights, uniform_prompt
+    shape = QWEN14B.with_(layers=2, vocab=32000)
+    w = pkg.quantize_model_nf4(shape, make_weights(shape, seed=0, device="cuda"))
+    B = 8
+    ctx = np.random.default_rng(300).integers(1024, 8193, size=B)
+    prompts = [uniform_prompt(int(n), shape.vocab, seed=310 + b).numpy() for b, n in enumerate(ctx)]
+    eng = pkg.SpecEngine(shape, w, batch=B, K=K_GUESS, s_max=NF4_B8_SMAX)
+    eng.prefill(prompts)
+    eng.step()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        torch.cuda.nvtx.range_push("round")
+        eng.step()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    eng.close()
+    print(json.dumps({"nf4_b8_small": True, "contexts": [int(n) for n in ctx]}))
 
 
 def run_ours(args):
@@ -560,7 +592,22 @@ def run_ours(args):
     gemm_ms = g0.elapsed_time(g1) / reps
     gemm_bytes = N * K * 2 + M * K * 4 + M * N * 4
     gemm_gbs = gemm_bytes / (gemm_ms / 1e3) / 1e9
-    del wg
+    # The tcgen05 (TMEM-accumulator) GEMM on the same matrix at 72 token rows,
+    # the batch-8 verify's row count: same timing method.
+    M72 = 72
+    x72 = torch.randn(M72, K, device="cuda")
+    y72 = torch.empty(M72, N, device="cuda")
+    xf72 = pkg.to_frag(x72)
+    for _ in range(3):
+        pkg.linear_frag(wg, xf72, M72, y72, ws)
+    g0.record(cur)
+    for _ in range(reps):
+        pkg.linear_frag(wg, xf72, M72, y72, ws)
+    g1.record(cur)
+    torch.cuda.synchronize()
+    tc_ms = g0.elapsed_time(g1) / reps
+    tc_bytes = N * K * 2 + M72 * K * 4 + M72 * N * 4
+    del wg, x72, y72, xf72
 
     # ---- end to end through the C ABI with host buffers (prefill from pinned host memory)
     pinned = torch.from_numpy(prompt.astype(np.int32)).pin_memory()
@@ -620,6 +667,11 @@ def run_ours(args):
                          "bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gemm_gbs / peak, 4), "traffic": _gemm_traffic(), "peak_source": peak_src,
                          "algorithmic_bytes": gemm_bytes, "ms_per_launch": round(gemm_ms, 4)},
+            "tc_gemm_72rows": {"kernel": "k_umma (tcgen05, TMEM accumulator), 7B gate+up [37888 x 3584] bf16, "
+                                         "72 token rows", "ms_per_launch": round(tc_ms, 4),
+                               "gbs": round(tc_bytes / (tc_ms / 1e3) / 1e9, 1),
+                               "frac_of_measured_peak": round(tc_bytes / (tc_ms / 1e3) / 1e9 / peak, 4),
+                               "tflops": round(2 * N * K * M72 / (tc_ms / 1e3) / 1e12, 1)},
             "verify_step": {"ms": round(verify_ms, 4), "bytes": v_bytes, "ctx": VERIFY_CTX,
                             "gbs": round(v_bytes / (verify_ms / 1e3) / 1e9, 1),
                             "frac_of_measured_peak": round(v_bytes / (verify_ms / 1e3) / 1e9 / peak, 4),
@@ -779,11 +831,16 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--tokens", type=int, default=N_NEW, help="new tokens per step (profiling runs use fewer)")
     ap.add_argument("--gemm-only", action="store_true", help="small case for kernel profiling")
+    ap.add_argument("--gemm-rows", type=int, default=K_GUESS + 1, help="token rows of --gemm-only")
+    ap.add_argument("--nf4-b8-small", action="store_true", help="small case: 2-layer 14B-shape NF4 batch-8 rounds")
     ap.add_argument("--trace", action="store_true", help="launch timeline of a round (needs SF_TRACE=1)")
     args = ap.parse_args()
     globals()["N_NEW"] = args.tokens
     if args.gemm_only:
         run_gemm_only(args)
+        return
+    if args.nf4_b8_small:
+        run_nf4_b8_small(args)
         return
     if args.trace:
         run_trace(args)

@@ -18,8 +18,11 @@
 //                 the MMA reads: umma_index in sf_common.cuh);
 //   thread 32     MMA issuer: four tcgen05.mma (K = 16 each) per chunk,
 //                 tcgen05.commit to the stage's "empty" barrier;
-//   warps 4-7     NF4 only: dequantise each chunk's codes into a bf16 weight
-//                 tile (level x block scale) in the MMA's layout;
+//   warps 4-7     NF4 only: dequantise each chunk's codes (thread r = weight
+//                 row r: one lookup of a per-lane table of bf16 level pairs
+//                 and one bf16x2 multiply by the block scale per two codes)
+//                 and write the bf16 tile straight into tensor memory
+//                 (tcgen05.st), four chunks deep; the MMA reads A from there;
 //   warps 4-7     afterwards: read the accumulator (tcgen05.ld, one weight row
 //                 per thread, one column per token) and write the CTA's tile
 //                 ys[m][128] in shared memory.
@@ -45,7 +48,10 @@ constexpr int kATileBytes = 128 * 128;      // 128 weight rows x 64 k bf16 (also
 constexpr int kUScaleBytes = 128 * 16;      // NF4: 128 rows x 8 fp16 block scales
 constexpr int kCodeStage = kATileBytes + kUScaleBytes;
 constexpr int kCodeStages = 2;
-constexpr int kDeqStages = 2;
+constexpr int kDeqStages = 4;               // NF4: dequantised chunks in tensor memory
+constexpr int kLutBytes = 256 * 32 * 4;     // NF4: byte -> bf16 level pair, one copy per lane
+constexpr int kAccCols = 128;               // tensor-memory columns of the accumulator (N <= 128)
+constexpr int kNf4Cols = 256;               // NF4: accumulator + kDeqStages x 32 columns of A
 
 __constant__ float c_levels[16];
 
@@ -58,7 +64,6 @@ struct USmem {
   int flag;
   int pos[kRows];
   float rinv[kRows];
-  float levels[16];   // NF4 levels: 16 words in 16 banks, so lookups never conflict
 };
 
 __device__ __forceinline__ int tiles_padded(int T) { return (T + 1) & ~1; }
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
   const int T4 = (M + 3) / 4;             // the fragment layout's tile count (epilogue stores)
   const int Tp = tiles_padded(T);         // MMA N = 8 * Tp (a multiple of 16)
   const int N = 8 * Tp;
-  const int ncols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+  const int ncols = NF4 ? kNf4Cols : (N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256)));
   const int S = a.stages;
   const int rb = blockIdx.x / a.nsplit, sp = blockIdx.x - rb * a.nsplit;
   const int nch_total = (a.K + kChunk - 1) / kChunk;
@@ -106,16 +111,15 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
   const uint32_t btile = (uint32_t)T * 1024;   // bytes of one chunk's token operand
 
   // Shared memory: bf16: S stages of [weights 16 KB | tokens Tp KB];
-  // NF4: 2 code stages [codes 16 KB | scales 2 KB], 2 dequantised weight
-  // tiles of 16 KB, S token stages of Tp KB. The result tile ys aliases it.
+  // NF4: 2 code stages [codes 16 KB | scales 2 KB], the level-pair table
+  // (32 KB), S token stages of Tp KB. The result tile ys aliases it.
   const int bstage = Tp * 1024;
   auto wtile = [&](int s) -> unsigned char* { return base + (size_t)s * (kATileBytes + bstage); };
   auto btile_p = [&](int s) -> unsigned char* {
-    return NF4 ? base + kCodeStages * kCodeStage + kDeqStages * kATileBytes + (size_t)s * bstage
-               : wtile(s) + kATileBytes;
+    return NF4 ? base + kCodeStages * kCodeStage + kLutBytes + (size_t)s * bstage : wtile(s) + kATileBytes;
   };
   auto ctile = [&](int s) -> unsigned char* { return base + (size_t)s * kCodeStage; };
-  auto dtile = [&](int s) -> unsigned char* { return base + kCodeStages * kCodeStage + (size_t)s * kATileBytes; };
+  uint32_t* lut = reinterpret_cast<uint32_t*>(base + kCodeStages * kCodeStage);   // [256][32]
   float* ys = reinterpret_cast<float*>(base);
 
   int seg_lo, row_lo, seg_hi, row_hi;
@@ -150,7 +154,13 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
   // Token positions (QKV epilogue), read before the wait: lengths are never
   // written by the kernel that directly precedes a projection.
   if (EPI == EPI_QKV && tid < M) sm.pos[tid] = row_pos(a.rs, tid);
-  if (NF4 && tid < 16) sm.levels[tid] = c_levels[tid];
+  if (NF4) {
+    // Entry b of lane l at 32 b + l: every lookup of a warp hits its own bank.
+    for (int i = tid; i < 256 * 32; i += kUThreads) {
+      const int b = i >> 5;
+      lut[i] = pack_bf16x2(__float2bfloat16_rn(c_levels[b & 15]), __float2bfloat16_rn(c_levels[b >> 4]));
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -226,43 +236,53 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
       const int ds = st % kDeqStages;
       if (NF4 && !mbar_wait(&sm.afull[ds], (st / kDeqStages) & 1, kUWaitIters)) timed_out = true;
       tc_fence_after();
-      const uint32_t aw = smem_u32(NF4 ? dtile(ds) : wtile(s));
       const uint32_t bw = smem_u32(btile_p(s));
+      if (NF4) {
+        const uint32_t at = tmem + kAccCols + 32 * ds;   // A: 64 k = 32 columns per chunk
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem, sw128_desc(aw + 32 * kk), sw128_desc(bw + 32 * kk), idesc, (st | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tmem, at + 8 * kk, sw128_desc(bw + 32 * kk), idesc, (st | kk) != 0);
+      } else {
+        const uint32_t aw = smem_u32(wtile(s));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem, sw128_desc(aw + 32 * kk), sw128_desc(bw + 32 * kk), idesc, (st | kk) != 0);
+      }
       umma_commit(&sm.empty[s]);
       if (NF4) umma_commit(&sm.aempty[ds]);
     }
     umma_commit(&sm.acc);
   } else if (NF4 && warp >= 4) {
-    // ---- dequantisers: thread r owns weight row r of the tile
+    // ---- dequantisers: thread r owns weight row r = tensor-memory lane r
     const int r = tid - 128;
     const int sw = r & 7;
-    const float* lv = sm.levels;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
     for (int st = 0; st < nch; ++st) {
       const int q = st >> 2, sub = st & 3, cs = q % kCodeStages, ds = st % kDeqStages;
       if (sub == 0 && !mbar_wait(&sm.cfull[cs], (q / kCodeStages) & 1, kUWaitIters)) timed_out = true;
       if (!mbar_wait(&sm.aempty[ds], ((st / kDeqStages) + 1) & 1, kUWaitIters)) timed_out = true;
+      tc_fence_after();
       const unsigned char* crow = ctile(cs) + (r >> 3) * 1024 + sw * 128;
       const uint4 b0 = *reinterpret_cast<const uint4*>(crow + (((2 * sub) ^ sw) << 4));
       const uint4 b1 = *reinterpret_cast<const uint4*>(crow + (((2 * sub + 1) ^ sw) << 4));
       const __half* sc = reinterpret_cast<const __half*>(ctile(cs) + kATileBytes) + r * 8;
-      const float scale = __half2float(sc[(c0 + st) & 7]);
-      const uint32_t cw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-      unsigned char* drow = dtile(ds) + (r >> 3) * 1024 + sw * 128;
+      const bf16 sb = __float2bfloat16_rn(__half2float(sc[(c0 + st) & 7]));
+      const uint32_t scale2 = pack_bf16x2(sb, sb);
+      // Column j of the chunk: elements 2j (low nibble of code byte j) and
+      // 2j + 1; written in two halves of 16 columns.
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {   // 8 weights per 16-byte piece: code word c
-        const uint32_t w = cw[c];
-        uint32_t p[4];
+      for (int h = 0; h < 2; ++h) {
+        const uint4 bw = h ? b1 : b0;
+        const uint32_t cw[4] = {bw.x, bw.y, bw.z, bw.w};
+        uint32_t a[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t byte = (w >> (8 * e)) & 255u;
-          p[e] = pack_bf16x2(__float2bfloat16_rn(lv[byte & 15] * scale), __float2bfloat16_rn(lv[byte >> 4] * scale));
-        }
-        *reinterpret_cast<uint4*>(drow + ((c ^ sw) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a[4 * c + e] = bf16x2_mul(lut[(((cw[c] >> (8 * e)) & 255u) << 5) + lane], scale2);
+        tmem_st16(lane_addr + kAccCols + 32 * ds + 16 * h, a);
       }
-      fence_proxy_async();   // this thread's tile writes before the MMA's async-proxy reads
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sm.afull[ds]);
@@ -378,38 +398,30 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     if (!sm.flag) return;
     __threadfence();
     // The last CTA of the row block adds the slices in order, 16-byte loads
-    // of every slice for two positions in flight at once.
+    // of up to eight slices in flight at once.
     const int n4 = nel / 4;
-    for (int i0 = tid; i0 < n4; i0 += 2 * kUThreads) {
-      float4 v[2][16];
+    for (int i = tid; i < n4; i += kUThreads) {
+      const int m = (4 * i) / kBlockRows, g = m / kGroupRows;
+      const float4* src = reinterpret_cast<const float4*>(
+          a.part + ((size_t)(rb * G + g) * a.nsplit * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
+          (4 * i - m * kBlockRows));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p0 = 0; p0 < a.nsplit; p0 += 8) {
+        float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u * kUThreads;
-        if (i >= n4) break;
-        const int m = (4 * i) / kBlockRows, g = m / kGroupRows;
-        const float4* src = reinterpret_cast<const float4*>(
-            a.part + ((size_t)(rb * G + g) * a.nsplit * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
-            (4 * i - m * kBlockRows));
+        for (int p = 0; p < 8; ++p)
+          if (p0 + p < a.nsplit) v[p] = __ldcg(src + (size_t)(p0 + p) * (kGroupRows * kBlockRows / 4));
 #pragma unroll
-        for (int p = 0; p < 16; ++p)
-          if (p < a.nsplit) v[u][p] = __ldcg(src + (size_t)p * (kGroupRows * kBlockRows / 4));
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u * kUThreads;
-        if (i >= n4) break;
-        float4 acc = v[u][0];
-#pragma unroll
-        for (int p = 1; p < 16; ++p)
-          if (p < a.nsplit) {
-            acc.x += v[u][p].x;
-            acc.y += v[u][p].y;
-            acc.z += v[u][p].z;
-            acc.w += v[u][p].w;
+        for (int p = 0; p < 8; ++p)
+          if (p0 + p < a.nsplit) {
+            acc.x += v[p].x;
+            acc.y += v[p].y;
+            acc.z += v[p].z;
+            acc.w += v[p].w;
           }
-        const float f = a.ssq ? sm.rinv[(4 * i) / kBlockRows] : 1.f;
-        reinterpret_cast<float4*>(ys)[i] = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
       }
+      const float f = a.ssq ? sm.rinv[m] : 1.f;
+      reinterpret_cast<float4*>(ys)[i] = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
     }
     if (tid == 0) a.counter[rb * G] = 0;
   } else if (a.ssq) {
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
 // Dynamic shared memory of a launch (plus 1 KB for the 1024-byte alignment).
 int umma_smem_bytes(int M, int stages, bool nf4) {
   const int Tp = ((M + 7) / 8 + 1) & ~1;
-  const int ring = nf4 ? kCodeStages * kCodeStage + kDeqStages * kATileBytes + stages * Tp * 1024
+  const int ring = nf4 ? kCodeStages * kCodeStage + kLutBytes + stages * Tp * 1024
                        : stages * (kATileBytes + Tp * 1024);
   return 1024 + std::max(ring, M * kBlockRows * 4);
 }
