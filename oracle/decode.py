@@ -74,14 +74,64 @@ def ngram_propose(ctx, max_guess: int = 4, min_n: int = 2, max_n: int = 4):
     return []
 
 
+def ngram_candidates(ctx, n_cand: int, max_guess: int = 4, min_n: int = 2, max_n: int = 4):
+    """Several prompt-lookup guesses at once (the Sangama page's "Next":
+    better guesses; here several earlier occurrences verified together).
+
+    Readings where the page is silent: the occurrences are visited in the
+    order ngram_propose ranks them (longest suffix length n first, max_n down
+    to min_n; for each n the rightmost earlier start j < len(ctx) - n first,
+    leftward); each gives the up to ``max_guess`` tokens that followed it,
+    cut at the end of the context; an empty guess or one equal to a guess
+    already taken is skipped; at most ``n_cand`` guesses. The first guess is
+    ngram_propose's.
+    """
+    ctx = [int(t) for t in ctx]
+    T = len(ctx)
+    out = []
+    for n in range(max_n, min_n - 1, -1):
+        if n > T - 1:
+            continue
+        suffix = ctx[T - n:]
+        for j in range(T - n - 1, -1, -1):
+            if ctx[j:j + n] == suffix:
+                g = ctx[j + n: min(j + n + max_guess, T)]
+                if g and g not in out:
+                    out.append(g)
+                    if len(out) == n_cand:
+                        return out
+    return out
+
+
+def tree_accept(guesses, choices):
+    """Acceptance over several guesses verified in one pass. ``guesses[c]``
+    is candidate c's token list; ``choices[c][j]`` is the target's own choice
+    after the pending token and guesses[c][:j] (choices[c][0] is the same
+    for every c: the choice after the pending token). Candidate c accepts
+    n_c = accept_length(guesses[c], choices[c]); the candidate with the
+    largest n_c is taken, the lowest index on ties (reading). Returns
+    (c, n, committed = guesses[c][:n] + [choices[c][n]])."""
+    best_c, best_n = 0, -1
+    for c, (g, t) in enumerate(zip(guesses, choices)):
+        n = accept_length(g, t, len(g))
+        if n > best_n:
+            best_c, best_n = c, n
+    g, t = guesses[best_c], choices[best_c]
+    return best_c, best_n, list(g[:best_n]) + [t[best_n]]
+
+
 def spec_decode(target: Model, draft, prompt, K: int, n_new: int, drafter: str = "neural",
-                min_n: int = 2, max_n: int = 4):
+                min_n: int = 2, max_n: int = 4, n_cand: int = 1):
     """Greedy speculative decoding of n_new tokens after ``prompt``.
 
     drafter == "neural": ``draft`` is a Model proposing K tokens by its own
     greedy decoding. drafter == "ngram": ``draft`` is unused; up to K tokens
     come from ngram_propose over the committed sequence (unfilled guess slots
-    hold token 0 and never count as accepted).
+    hold token 0 and never count as accepted). drafter == "tree": up to
+    ``n_cand`` guesses of up to K // n_cand tokens from ngram_candidates, each
+    scored by the target on its own (the pending token and the guess from the
+    committed state), the best taken by tree_accept; no guess: the target's
+    own next token.
 
     Returns dict(tokens=[n_new generated tokens], rounds=[(n_accepted,
     committed_tokens, proposals, target_choices), ...]).
@@ -121,6 +171,19 @@ def spec_decode(target: Model, draft, prompt, K: int, n_new: int, drafter: str =
                 guesses.append(g)
                 feed = [g]
             limit = K
+        elif drafter == "tree":
+            cands = ngram_candidates(seq, n_cand, K // n_cand, min_n, max_n) or [[]]
+            choices = []
+            for g in cands:
+                lg = target.forward([seq[-1]] + g, tcache)
+                choices.append([first_argmax(lg[i]) for i in range(len(g) + 1)])
+                tcache.truncate(C - 1)            # each guess is scored from the committed state
+            c, n, committed = tree_accept(cands, choices)
+            # Keys and values of the pending token and the accepted guesses.
+            target.forward([seq[-1]] + cands[c][:n], tcache, logit_rows=[])
+            seq += committed
+            rounds.append((n, committed, cands, choices))
+            continue
         else:
             prop = ngram_propose(seq, K, min_n, max_n)
             limit = len(prop)

@@ -172,3 +172,71 @@ def test_planted_prompts_give_every_accept_length():
         assert len(prop) == 4
         assert od.accept_length(prop, g + [-1] * (5 - len(g)), 4) == j
         assert g == od.greedy(m, P, j + 1)
+
+
+def _candidates_by_sorting(ctx, n_cand, max_guess, min_n, max_n):
+    """The multi-candidate reading restated another way: every (n, j) match
+    sorted by longest n, then rightmost j; duplicates and empty guesses
+    dropped; the first n_cand kept."""
+    T = len(ctx)
+    matches = [(n, j) for n in range(min_n, max_n + 1) if n <= T - 1
+               for j in range(0, T - n) if ctx[j:j + n] == ctx[T - n:]]
+    matches.sort(key=lambda nj: (-nj[0], -nj[1]))
+    out = []
+    for n, j in matches:
+        g = ctx[j + n: min(j + n + max_guess, T)]
+        if g and g not in out:
+            out.append(g)
+    return out[:n_cand]
+
+
+def test_ngram_candidates_brute_force():
+    rng = random.Random(11)
+    for trial in range(400):
+        T = rng.randint(1, 24)
+        ctx = [rng.randint(0, 3) for _ in range(T)]
+        for n_cand in (1, 2, 3, 4):
+            for mg in (1, 3, 4):
+                got = od.ngram_candidates(ctx, n_cand, mg, 2, 4)
+                assert got == _candidates_by_sorting(ctx, n_cand, mg, 2, 4), (ctx, n_cand, mg)
+                first = od.ngram_propose(ctx, mg, 2, 4)
+                assert (got[:1] == [first]) if first else got == []
+
+
+def test_tree_accept_cases():
+    # candidate 1 agrees further than candidate 0
+    assert od.tree_accept([[5, 6], [7, 8, 9]], [[5, 0, 0], [7, 8, 1, 2]]) == (1, 2, [7, 8, 1])
+    # ties go to the lowest index; nothing agrees: the target's own token
+    assert od.tree_accept([[3], [4]], [[9, 0], [9, 0]]) == (0, 0, [9])
+    # a full agreement takes the bonus token after the last guess
+    assert od.tree_accept([[1, 2]], [[1, 2, 3]]) == (0, 2, [1, 2, 3])
+    # an empty guess list: plain greedy
+    assert od.tree_accept([[]], [[42]]) == (0, 0, [42])
+
+
+def test_tree_accept_brute_force():
+    rng = random.Random(5)
+    for _ in range(500):
+        C = rng.randint(1, 4)
+        gs = [[rng.randint(0, 2) for _ in range(rng.randint(0, 4))] for _ in range(C)]
+        t0 = rng.randint(0, 2)
+        ts = [[t0] + [rng.randint(0, 2) for _ in range(len(g))] for g in gs]
+        c, n, com = od.tree_accept(gs, ts)
+        ns = [max(m for m in range(len(g) + 1) if all(g[i] == t[i] for i in range(m))) for g, t in zip(gs, ts)]
+        assert n == max(ns) and c == ns.index(max(ns))
+        assert com == gs[c][:n] + [ts[c][n]]
+
+
+@pytest.mark.parametrize("n_cand,K", [(1, 4), (2, 8), (3, 6)])
+def test_tree_spec_decode_equals_greedy(n_cand, K):
+    """Speculation with several guesses per round never changes the output."""
+    from synth import ngram_prompt
+    m = om.Model(TINY_TARGET, make_weights(TINY_TARGET, seed=0))
+    for seed in (200, 201):
+        prompt, _ = ngram_prompt(64, 0.8, TINY_TARGET.vocab, seed=seed, base_len=32, seg_lo=6, seg_hi=12)
+        prompt = prompt.tolist()
+        r = od.spec_decode(m, None, prompt, K, 24, drafter="tree", n_cand=n_cand)
+        assert r["tokens"] == od.greedy(m, prompt, 24)
+        for n, committed, cands, choices in r["rounds"]:
+            assert len(cands) <= n_cand and all(len(g) <= K // n_cand for g in cands)
+            assert committed[:n] == cands[[len(g) >= n and g[:n] == committed[:n] for g in cands].index(True)][:n]
