@@ -37,15 +37,24 @@ S_MAX = 4096
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
 # the roofline kernel from one ncu capture, valid only for the k_gemm.cu
 # source it was taken on (sha256 prefix); reported as null otherwise.
-GEMM_TRAFFIC = {"sha": "0df81db18173a363", "bytes": 274944768}
+GEMM_TRAFFIC = {"sha": "a5765817d67654f2", "bytes": 274869504}
+# Sources the k_gemm kernel is compiled from; the stored traffic applies only
+# to the exact sources it was captured with.
+GEMM_SOURCES = ("k_gemm.cu", "gemm_epi.cuh", "sf_common.cuh", "sf_kernels.h")
+
+
+def _gemm_sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "greedy_speculative_decoding_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _gemm_traffic():
-    import hashlib
-    src = os.path.join(ROOT, "greedy_speculative_decoding_gb300", "csrc", "k_gemm.cu")
     try:
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        sha = _gemm_sources_sha()
     except OSError:
         return None
     return GEMM_TRAFFIC["bytes"] if sha == GEMM_TRAFFIC["sha"] else None
@@ -206,7 +215,8 @@ def extra_workloads(pkg, tw, peak):
     """The other workloads of the suite, each bounded to a few seconds:
     the 0.5B-shape draft decode step at context 512 (standalone, vocabulary
     151936), sigma-perturbed target copies as drafts, prompt-lookup drafting
-    on repetitive prompts, and the 14B-shape NF4 target at batch 1."""
+    on repetitive prompts (one guess, and several verified side by side),
+    and the 14B-shape NF4 target at batch 1."""
     import torch
     from synth import (QWEN05B, QWEN14B, QWEN7B, make_weights, ngram_prompt, perturbed_copy,
                        repeated_fraction, shared_embedding_draft, uniform_prompt)
@@ -265,6 +275,23 @@ def extra_workloads(pkg, tw, peak):
             en.close()
         except Exception as ex:
             out[f"ngram_r{r}"] = {"error": repr(ex)[:200]}
+    torch.cuda.empty_cache()
+    # Several prompt-lookup guesses per round (K = 8 verify rows after the
+    # pending token): one guess of 8, two of 4, four of 2, on the r = 0.8 prompt.
+    try:
+        p, mask = ngram_prompt(1024, 0.8, QWEN7B.vocab, seed=208)
+        for n_cand in (1, 2, 4):
+            en = pkg.SpecEngine(QWEN7B, tw, batch=1, K=8, s_max=S_MAX)
+            en.set_drafter(pkg.SF_DRAFT_TREE, 2, 4)
+            en.set_tree_candidates(n_cand)
+            en.prefill([p.numpy()])
+            rate, mean_c = _gen_rate(en)
+            out[f"ngram_tree_r0.8_c{n_cand}"] = {"tokens_per_s": round(rate, 2),
+                                                 "mean_committed_per_round": round(mean_c, 3),
+                                                 "candidates": n_cand, "guesses_each": 8 // n_cand}
+            en.close()
+    except Exception as ex:
+        out["ngram_tree_r0.8"] = {"error": repr(ex)[:200]}
     torch.cuda.empty_cache()
     # Plain greedy decoding of the same target (no drafter: each round verifies
     # the pending token and commits the target's own choice), the baseline the

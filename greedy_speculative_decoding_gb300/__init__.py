@@ -14,11 +14,11 @@ there is no fallback path.
 """
 
 from . import _lib
-from ._lib import (SF_DRAFT_NEURAL, SF_DRAFT_NGRAM, SF_DRAFT_NONE, SF_MAX_ROWS, SFError, load)
+from ._lib import (SF_DRAFT_NEURAL, SF_DRAFT_NGRAM, SF_DRAFT_NONE, SF_DRAFT_TREE, SF_MAX_ROWS, SFError, load)
 from .engine import (SpecEngine, linear, linear_frag, model_cfg, nf4_quantize, nf4_scale_ld, quantize_model_nf4,
                      to_frag, weight_order)
 
 __all__ = ["SpecEngine", "SFError", "linear", "linear_frag", "to_frag", "model_cfg", "weight_order",
            "nf4_quantize", "nf4_scale_ld",
            "quantize_model_nf4", "SF_DRAFT_NEURAL",
-           "SF_DRAFT_NGRAM", "SF_DRAFT_NONE", "SF_MAX_ROWS"]
+           "SF_DRAFT_NGRAM", "SF_DRAFT_NONE", "SF_DRAFT_TREE", "SF_MAX_ROWS"]

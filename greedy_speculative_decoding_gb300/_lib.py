@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_HERE, "libsf.so")
 SF_OK, SF_ERR_ARG, SF_ERR_CAPACITY, SF_ERR_CUDA, SF_ERR_NONFINITE, SF_ERR_STATE, SF_ERR_UNSUPPORTED, \
     SF_ERR_DEVICE = range(8)
 SF_WDTYPE_BF16, SF_WDTYPE_NF4, SF_WDTYPE_F32 = 0, 1, 2
-SF_DRAFT_NEURAL, SF_DRAFT_NGRAM, SF_DRAFT_NONE = 0, 1, 2
+SF_DRAFT_NEURAL, SF_DRAFT_NGRAM, SF_DRAFT_NONE, SF_DRAFT_TREE = 0, 1, 2, 3
 SF_MAX_ROWS = 80
 
 EXPORTS = (
@@ -23,6 +23,7 @@ EXPORTS = (
     "sf_set_drafter", "sf_get_lengths", "sf_get_accept_hist", "sf_status_str", "sf_last_error",
     "sf_destroy", "sf_nf4_quantize", "sf_linear_workspace_bytes", "sf_linear", "sf_linear_noalloc",
     "sf_trace", "sf_trace_label", "sf_frag_bytes", "sf_to_frag", "sf_linear_frag", "sf_round_launches",
+    "sf_tree_draft", "sf_set_tree_candidates", "sf_tree_winner",
 )
 
 
@@ -85,6 +86,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sf_linear_frag": (ST, [P, I32, I32, I32, P, I32, P, P, P]),
         "sf_trace_label": (ctypes.c_char_p, [P, I32]),
         "sf_round_launches": (ctypes.c_int64, [P]),
+        "sf_tree_draft": (ST, [P, I32, I32, I32, P, P]),
+        "sf_set_tree_candidates": (ST, [P, I32]),
+        "sf_tree_winner": (ST, [P, PI32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -88,6 +88,7 @@ struct Model {
   CUtensorMap lm_tmu;      // 64-row boxes: the LM head of forwards of more than 16 rows (tcgen05)
   bf16* kv = nullptr;
   CUtensorMap kvmap;       // the whole cache as [rows][head_dim] for the attention kernel's TMA
+  CUtensorMap kvmap8;      // the same with 8-slot boxes
   int attn_R = 1;          // cache chunks per attention work item
   int attn_TG = 1;         // query tiles per attention work item
   int attn_stages = 1;     // key/value chunks in flight per attention CTA
@@ -149,8 +150,8 @@ int nblocks_of(const sf_model_cfg* c, int which) {
 // acc_hist, then the report block (ncommit, nacc, commit, total, err) that
 // one copy brings back to the host.
 struct StateOff {
-  size_t len_t, len_d, vtok, ttok, dtok0, nprop, hist, prompt_len, acc_hist, loop_target, report, ncommit, nacc,
-      commit, total, err, rounds, n_ints, report_ints;
+  size_t len_t, len_d, vtok, ttok, dtok0, nprop, hist, prompt_len, acc_hist, loop_target, clen, report, ncommit,
+      nacc, commit, total, err, rounds, tree_c, n_ints, report_ints;
 };
 
 StateOff state_offsets(int B, int K, int s_max) {
@@ -172,6 +173,7 @@ StateOff state_offsets(int B, int K, int s_max) {
   o.prompt_len = take(B);
   o.acc_hist = take(B * K1);
   o.loop_target = take(1);
+  o.clen = take(B * K);
   o.report = p;
   o.ncommit = p;
   p += B;
@@ -185,6 +187,8 @@ StateOff state_offsets(int B, int K, int s_max) {
   p += 1;
   o.rounds = p;
   p += 1;
+  o.tree_c = p;
+  p += B;
   o.report_ints = p - o.report;
   o.n_ints = p;
   return o;
@@ -266,12 +270,15 @@ struct sf_engine {
   unsigned long long* keys = nullptr;
   SpecState st{};
   int* pin = nullptr;   // pinned host copy of the report block
-  cudaGraphExec_t graph[3] = {nullptr, nullptr, nullptr};   // whole round, per drafter (SF_DRAFT_*)
-  size_t graph_kernels[3] = {0, 0, 0};                      // kernel launches in each round graph
-  cudaGraphExec_t loop[3] = {nullptr, nullptr, nullptr};    // sf_generate: rounds in a device-side WHILE loop
+  cudaGraphExec_t graph[4] = {};   // whole round, per drafter (SF_DRAFT_*)
+  size_t graph_kernels[4] = {};    // kernel launches in each round graph
+  cudaGraphExec_t loop[4] = {};    // sf_generate: rounds in a device-side WHILE loop
   bool host_loop = false;   // SF_HOST_LOOP=1: sf_generate replays the round graph from the host instead
-  cudaGraphExec_t g_draft = nullptr, g_verify = nullptr;
+  cudaGraphExec_t g_draft = nullptr, g_verify = nullptr, g_verify_tree = nullptr;
+  int g_verify_tree_g = 0;   // guesses per candidate g_verify_tree was captured with
   int drafter = SF_DRAFT_NEURAL, ng_min = 2, ng_max = 4;
+  int tree_n = 1;            // SF_DRAFT_TREE: candidates per round (g = K / tree_n guesses each)
+  int drafted_tree_n = 1;    // candidates of the last sf_tree_draft
   std::vector<int> C;   // committed tokens per sequence (host mirror)
   std::vector<int> P;   // prompt length per sequence
   int phase = 0;        // 0: no prompt, 1: ready, 2: drafted, 3: verified
@@ -333,7 +340,8 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
   md.kv = kv;
   {
     const long rows = (long)c->layers * 2 * e->B * c->n_kv_heads * e->s_max;
-    const cudaError_t ce = make_kv_map(&md.kvmap, kv, rows, c->head_dim);
+    cudaError_t ce = make_kv_map(&md.kvmap, kv, rows, c->head_dim);
+    if (ce == cudaSuccess) ce = make_kv_map(&md.kvmap8, kv, rows, c->head_dim, 8);
     if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "KV cache tensor map: %s", cudaGetErrorString(ce));
     // Attention work items of R chunks: one chunk each while the cache is
     // small; up to 8 for a large batch of long caches, so the items fill the
@@ -559,6 +567,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     // attention
     AttnArgs t{};
     t.kvmap = md.kvmap;
+    t.kvmap8 = md.kvmap8;
     t.kv_brows = c.n_kv_heads * e->s_max;
     t.kv_vrows = e->B * t.kv_brows;
     t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
@@ -709,9 +718,11 @@ sf_status enqueue_draft(sf_engine* e, float* logits, cudaStream_t s) {
   return SF_OK;
 }
 
-sf_status enqueue_verify(sf_engine* e, float* logits, cudaStream_t s) {
+// tree_g > 0: the rows are candidate guesses of tree_g tokens each (see RowSet).
+sf_status enqueue_verify(sf_engine* e, float* logits, cudaStream_t s, int tree_g = 0) {
   const int K1 = e->K + 1;
   RowSet rs{e->st.vtok, K1, 0, K1, e->B * K1, e->st.len_t, 0};
+  rs.tree_g = tree_g;
   TokOut to;
   to.tok = e->st.ttok;
   to.stride = K1;
@@ -723,12 +734,33 @@ sf_status enqueue_verify(sf_engine* e, float* logits, cudaStream_t s) {
   return forward(e, e->tgt, rs, true, to, s);
 }
 
+// Acceptance over the candidates, then the winner's cache entries move down
+// to the committed slots.
+sf_status enqueue_tree_accept(sf_engine* e, int n_cand, cudaStream_t s, bool pdl) {
+  const int g = e->K / n_cand;
+  CK(launch_accept_tree(e->st, n_cand, g, s, pdl));
+  const sf_model_cfg& c = e->tgt.c;
+  CK(launch_tree_compact(e->st, e->tgt.kv, c.layers, c.n_kv_heads, c.head_dim, g, s, pdl));
+  return SF_OK;
+}
+
+// One round with several prompt-lookup guesses verified side by side.
+sf_status enqueue_tree_round(sf_engine* e, int n_cand, int min_n, int max_n, cudaStream_t s) {
+  const int g = e->K / n_cand;
+  CK(launch_ngram_tree(e->st, n_cand, g, min_n, max_n, nullptr, nullptr, s, e->pdl));
+  sf_status r = enqueue_verify(e, nullptr, s, g);
+  if (r != SF_OK) return r;
+  return enqueue_tree_accept(e, n_cand, s, e->pdl);
+}
+
 sf_status enqueue_round(sf_engine* e, int mode, cudaStream_t s) {
   sf_status r;
   if (mode == SF_DRAFT_NEURAL) {
     if ((r = enqueue_draft(e, nullptr, s)) != SF_OK) return r;
   } else if (mode == SF_DRAFT_NGRAM) {
     CK(launch_ngram(e->st, e->K, e->ng_min, e->ng_max, nullptr, nullptr, s, e->pdl));
+  } else if (mode == SF_DRAFT_TREE) {
+    return enqueue_tree_round(e, e->tree_n, e->ng_min, e->ng_max, s);
   } else {
     // No drafter: the lookup kernel with an empty range of n proposes nothing,
     // so the round commits the target's own next token (plain greedy decoding).
@@ -739,11 +771,15 @@ sf_status enqueue_round(sf_engine* e, int mode, cudaStream_t s) {
   return SF_OK;
 }
 
-enum { CAP_ROUND_NEURAL = 0, CAP_ROUND_NGRAM = 1, CAP_ROUND_NONE = 2, CAP_DRAFT = 3, CAP_VERIFY = 4 };
+enum {
+  CAP_ROUND_NEURAL = 0, CAP_ROUND_NGRAM = 1, CAP_ROUND_NONE = 2, CAP_ROUND_TREE = 3,
+  CAP_DRAFT = 4, CAP_VERIFY = 5, CAP_VERIFY_TREE = 6
+};
 
 cudaGraphExec_t* graph_slot(sf_engine* e, int what) {
   if (what == CAP_DRAFT) return &e->g_draft;
   if (what == CAP_VERIFY) return &e->g_verify;
+  if (what == CAP_VERIFY_TREE) return &e->g_verify_tree;
   return &e->graph[what];
 }
 
@@ -756,6 +792,7 @@ sf_status build_graph(sf_engine* e, int what) {
   sf_status r;
   if (what == CAP_DRAFT) r = enqueue_draft(e, nullptr, e->cap);
   else if (what == CAP_VERIFY) r = enqueue_verify(e, nullptr, e->cap);
+  else if (what == CAP_VERIFY_TREE) r = enqueue_verify(e, nullptr, e->cap, e->K / e->drafted_tree_n);
   else r = enqueue_round(e, what, e->cap);
   cudaGraph_t g = nullptr;
   cudaError_t ce = cudaStreamEndCapture(e->cap, &g);
@@ -764,12 +801,13 @@ sf_status build_graph(sf_engine* e, int what) {
     return r;
   }
   if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(ce));
-  if (what == CAP_ROUND_NEURAL || what == CAP_ROUND_NGRAM || what == CAP_ROUND_NONE) {
+  if (what <= CAP_ROUND_TREE) {
     size_t n = 0;
     if (cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess) e->graph_kernels[what] = n;
   }
   ce = cudaGraphInstantiate(slot, g, 0);
   cudaGraphDestroy(g);
+  if (what == CAP_VERIFY_TREE && ce == cudaSuccess) e->g_verify_tree_g = e->K / e->drafted_tree_n;
   if (ce != cudaSuccess) return fail(SF_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(ce));
   return SF_OK;
 }
@@ -923,6 +961,7 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->user = static_cast<cudaStream_t>(cuda_stream);
   e->has_dft = dft != nullptr;
   e->drafter = dft ? SF_DRAFT_NEURAL : SF_DRAFT_NGRAM;
+  e->tree_n = K >= 2 ? 2 : 1;
   // SF_PDL=0 in the environment launches the kernels without programmatic
   // dependent launch (for comparing the two; results are identical).
   if (const char* v = getenv("SF_PDL")) e->pdl = v[0] != '0';
@@ -991,6 +1030,8 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   st.err = S + e->so.err;
   st.loop_target = S + e->so.loop_target;
   st.rounds = S + e->so.rounds;
+  st.clen = S + e->so.clen;
+  st.tree_c = S + e->so.tree_c;
   st.B = batch;
   st.K = K;
   st.s_max = s_max;
@@ -1028,6 +1069,7 @@ void sf_destroy(sf_handle h) {
     if (g) cudaGraphExecDestroy(g);
   if (h->g_draft) cudaGraphExecDestroy(h->g_draft);
   if (h->g_verify) cudaGraphExecDestroy(h->g_verify);
+  if (h->g_verify_tree) cudaGraphExecDestroy(h->g_verify_tree);
   if (h->cap) cudaStreamDestroy(h->cap);
   if (h->pin) cudaFreeHost(h->pin);
   delete h;
@@ -1095,26 +1137,43 @@ sf_status sf_reset(sf_handle h) {
   return SF_OK;
 }
 
+// Drop the round graphs of drafter `mode` (their launches carry its settings).
+static void drop_round_graphs(sf_handle h, int mode) {
+  if (h->graph[mode]) {
+    cudaGraphExecDestroy(h->graph[mode]);
+    h->graph[mode] = nullptr;
+  }
+  if (h->loop[mode]) {
+    cudaGraphExecDestroy(h->loop[mode]);
+    h->loop[mode] = nullptr;
+  }
+  h->graph_kernels[mode] = 0;
+}
+
 sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n) {
   if (!h) return fail(SF_ERR_ARG, "null handle");
-  if (mode != SF_DRAFT_NEURAL && mode != SF_DRAFT_NGRAM && mode != SF_DRAFT_NONE)
+  if (mode != SF_DRAFT_NEURAL && mode != SF_DRAFT_NGRAM && mode != SF_DRAFT_NONE && mode != SF_DRAFT_TREE)
     return fail(SF_ERR_ARG, "unknown drafter");
   if (mode == SF_DRAFT_NEURAL && !h->has_dft) return fail(SF_ERR_STATE, "no draft model");
-  if (mode == SF_DRAFT_NGRAM && (min_n < 1 || max_n < min_n || max_n > 64))
-    return fail(SF_ERR_ARG, "need 1 <= min_n <= max_n <= 64");
-  if (mode == SF_DRAFT_NGRAM && (min_n != h->ng_min || max_n != h->ng_max)) {
-    if (h->graph[SF_DRAFT_NGRAM]) {
-      cudaGraphExecDestroy(h->graph[SF_DRAFT_NGRAM]);
-      h->graph[SF_DRAFT_NGRAM] = nullptr;
-    }
-    if (h->loop[SF_DRAFT_NGRAM]) {
-      cudaGraphExecDestroy(h->loop[SF_DRAFT_NGRAM]);
-      h->loop[SF_DRAFT_NGRAM] = nullptr;
-    }
+  const bool lookup = mode == SF_DRAFT_NGRAM || mode == SF_DRAFT_TREE;
+  if (lookup && (min_n < 1 || max_n < min_n || max_n > 64)) return fail(SF_ERR_ARG, "need 1 <= min_n <= max_n <= 64");
+  if (lookup && (min_n != h->ng_min || max_n != h->ng_max)) {
+    drop_round_graphs(h, SF_DRAFT_NGRAM);
+    drop_round_graphs(h, SF_DRAFT_TREE);
     h->ng_min = min_n;
     h->ng_max = max_n;
   }
   h->drafter = mode;
+  return SF_OK;
+}
+
+sf_status sf_set_tree_candidates(sf_handle h, int32_t n_cand) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (n_cand < 1 || n_cand > h->K) return fail(SF_ERR_ARG, "need 1 <= n_cand <= K");
+  if (n_cand != h->tree_n) {
+    drop_round_graphs(h, SF_DRAFT_TREE);
+    h->tree_n = n_cand;
+  }
   return SF_OK;
 }
 
@@ -1150,14 +1209,35 @@ sf_status sf_ngram_draft(sf_handle h, int32_t max_guess, int32_t min_n, int32_t 
   return SF_OK;
 }
 
+sf_status sf_tree_draft(sf_handle h, int32_t n_cand, int32_t min_n, int32_t max_n, int32_t* d_prop,
+                        int32_t* d_len) {
+  if (!h) return fail(SF_ERR_ARG, "null handle");
+  if (h->phase != 1) return fail(SF_ERR_STATE, "sf_tree_draft needs a prefilled engine between rounds");
+  if (n_cand < 1 || n_cand > h->K || min_n < 1 || max_n < min_n || max_n > 64)
+    return fail(SF_ERR_ARG, "need 1 <= n_cand <= K and 1 <= min_n <= max_n <= 64");
+  if (max_committed(h) + h->K + 1 > h->s_max) return fail(SF_ERR_CAPACITY, "round would exceed s_max");
+  CK(launch_ngram_tree(h->st, n_cand, h->K / n_cand, min_n, max_n, d_prop, d_len, h->user, false));
+  h->phase = 2;
+  h->drafted_mode = SF_DRAFT_TREE;
+  h->drafted_tree_n = n_cand;
+  return SF_OK;
+}
+
 sf_status sf_verify(sf_handle h, int32_t* d_tgt_argmax, float* d_logits) {
   if (!h) return fail(SF_ERR_ARG, "null handle");
   if (h->phase != 2) return fail(SF_ERR_STATE, "sf_verify needs a draft first");
   sf_status r;
+  const bool tree = h->drafted_mode == SF_DRAFT_TREE;
+  const int tree_g = tree ? h->K / h->drafted_tree_n : 0;
   if (!d_tgt_argmax && !d_logits) {
-    if ((r = build_graph(h, CAP_VERIFY)) != SF_OK) return r;
-    CK(cudaGraphLaunch(h->g_verify, h->user));
-  } else if ((r = enqueue_verify(h, d_logits, h->user)) != SF_OK) {
+    const int what = tree ? CAP_VERIFY_TREE : CAP_VERIFY;
+    if (tree && h->g_verify_tree && h->g_verify_tree_g != tree_g) {
+      cudaGraphExecDestroy(h->g_verify_tree);
+      h->g_verify_tree = nullptr;
+    }
+    if ((r = build_graph(h, what)) != SF_OK) return r;
+    CK(cudaGraphLaunch(*graph_slot(h, what), h->user));
+  } else if ((r = enqueue_verify(h, d_logits, h->user, tree_g)) != SF_OK) {
     return r;
   }
   if (d_tgt_argmax)
@@ -1181,7 +1261,12 @@ static void copy_out(sf_handle h, int32_t* h_n_accepted, int32_t* h_committed, i
 sf_status sf_accept_rollback(sf_handle h, int32_t* h_n_accepted, int32_t* h_committed, int32_t* h_n_committed) {
   if (!h) return fail(SF_ERR_ARG, "null handle");
   if (h->phase != 3) return fail(SF_ERR_STATE, "sf_accept_rollback needs a verify first");
-  CK(launch_accept(h->st, h->drafted_mode, h->user, false));
+  if (h->drafted_mode == SF_DRAFT_TREE) {
+    const sf_status ta = enqueue_tree_accept(h, h->drafted_tree_n, h->user, false);
+    if (ta != SF_OK) return ta;
+  } else {
+    CK(launch_accept(h->st, h->drafted_mode, h->user, false));
+  }
   h->phase = 1;
   if (h->drafted_mode != SF_DRAFT_NEURAL && h->has_dft) h->draft_stale = true;
   sf_status r = sync_report(h);
@@ -1271,6 +1356,13 @@ sf_status sf_get_lengths(sf_handle h, int32_t* h_len_t, int32_t* h_len_d) {
 sf_status sf_get_accept_hist(sf_handle h, int32_t* h_hist) {
   if (!h || !h_hist) return fail(SF_ERR_ARG, "null argument");
   CK(cudaMemcpyAsync(h_hist, h->st.acc_hist, h->B * (h->K + 1) * sizeof(int), cudaMemcpyDeviceToHost, h->user));
+  CK(cudaStreamSynchronize(h->user));
+  return SF_OK;
+}
+
+sf_status sf_tree_winner(sf_handle h, int32_t* h_c) {
+  if (!h || !h_c) return fail(SF_ERR_ARG, "null argument");
+  CK(cudaMemcpyAsync(h_c, h->st.tree_c, h->B * sizeof(int), cudaMemcpyDeviceToHost, h->user));
   CK(cudaStreamSynchronize(h->user));
   return SF_OK;
 }

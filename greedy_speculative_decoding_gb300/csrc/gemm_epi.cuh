@@ -18,7 +18,9 @@ struct EpiPre {
   float2 cs[kE];
 };
 
-// Rows m < M of the CTA are token rows m0 + m of the forward.
+// Rows m < M of the CTA are token rows m0 + m of the forward; pos[m] is the
+// cache slot of row m0 + m (its RoPE position differs for the rows of a
+// multi-candidate verify).
 template <int T, int EPI>
 __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, int M, EpiPre<T>& pre,
                                              const int* pos) {
@@ -49,7 +51,7 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, 
         if (bias) pre.v0[e] = ldw(bias, local, a.wf32);
         if (s < 2 && d < half) {
           if (bias) pre.v1[e] = ldw(bias, local + half, a.wf32);
-          pre.cs[e] = a.rope[(size_t)pos[m] * half + d];
+          pre.cs[e] = a.rope[(size_t)(pos[m] - tree_gap(a.rs, (m0 + m) % a.rs.rps)) * half + d];
         }
       }
     }

@@ -165,17 +165,31 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
       is_c = is_it.c0;
     }
   }
-  auto issue_next = [&]() {   // thread 0: load the cursor's chunk into stage issued & 1, advance
+  auto issue_next = [&]() {   // thread 0: load the cursor's chunk into stage issued % NS, advance
     if (is_item >= total) return;
     const int s = issued % NS;
     unsigned char* st = base + s * kStage;
     fence_proxy_async();
-    mbar_expect_tx(&full[s], kStage);
     const int row = kv_row(is_it, is_c);
+    // Slots past the sequence's last row hold nothing of this pass: a partly
+    // filled last chunk loads only the 8-slot boxes that hold valid slots.
+    const int nvalid = min(kKvChunk, is_it.p_last - is_c * kKvChunk + 1);
+    if (nvalid < kKvChunk) {
+      const int nb = (nvalid + 7) / 8;
+      mbar_expect_tx(&full[s], 2 * kHalf * nb * 8 * 128);
+      for (int h = 0; h < kHalf; ++h)
+        for (int i = 0; i < nb; ++i) {
+          tma_load_2d(st + h * kBox + i * 1024, &a.kvmap8, 64 * h, row + 8 * i, &full[s], policy_evict_first());
+          tma_load_2d(st + kKV + h * kBox + i * 1024, &a.kvmap8, 64 * h, row + a.kv_vrows + 8 * i, &full[s],
+                      policy_evict_first());
+        }
+    } else {
+      mbar_expect_tx(&full[s], kStage);
 #pragma unroll
-    for (int h = 0; h < kHalf; ++h) {
-      tma_load_2d(st + h * kBox, &a.kvmap, 64 * h, row, &full[s], policy_evict_first());
-      tma_load_2d(st + kKV + h * kBox, &a.kvmap, 64 * h, row + a.kv_vrows, &full[s], policy_evict_first());
+      for (int h = 0; h < kHalf; ++h) {
+        tma_load_2d(st + h * kBox, &a.kvmap, 64 * h, row, &full[s], policy_evict_first());
+        tma_load_2d(st + kKV + h * kBox, &a.kvmap, 64 * h, row + a.kv_vrows, &full[s], policy_evict_first());
+      }
     }
     ++issued;
     if (++is_c >= is_it.c1) {
@@ -257,11 +271,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
         if (ti >= nt) break;
         const bf16* qht = sq + (2 * ti) * 16 * HP;
         const bf16* qlt = sq + (2 * ti + 1) * 16 * HP;
-        int nk[2];
+        // Row j sees the chunk's keys below nk, except [gl, gh): in a
+        // multi-candidate verify, the slots of the candidates before its own.
+        int nk[2], gl[2], gh[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int qi = (t0 + ti) * 16 + g + 8 * r;
-          nk[r] = qi < Mq ? min(kKvChunk, it.p0 + qi / group - c * kKvChunk + 1) : 0;
+          const int j = qi / group;
+          nk[r] = qi < Mq ? min(kKvChunk, it.p0 + j - c * kKvChunk + 1) : 0;
+          gl[r] = it.p0 + 1 - c * kKvChunk;
+          gh[r] = gl[r] + tree_gap(a.rs, j);
         }
         // S for keys 8w .. 8w+7: four independent chains (hi / lo part of Q
         // x even / odd k-step), added in a fixed order at the end. Key row
@@ -287,7 +306,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
         for (int e = 0; e < 4; ++e) {
           const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
           const float v = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
-          sacc[e] = kk < nk[r] ? v * a.scale : -INFINITY;
+          sacc[e] = (kk < nk[r] && (kk < gl[r] || kk >= gh[r])) ? v * a.scale : -INFINITY;
         }
         float mx[2];
 #pragma unroll
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
-          pe[e] = kk < nk[r] ? expf(sacc[e] - m_new[r]) : 0.f;
+          pe[e] = sacc[e] != -INFINITY ? expf(sacc[e] - m_new[r]) : 0.f;
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -413,7 +432,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
   trace_mark(rs1, 1);
   pdl_launch_next();
   const int m = blockIdx.x / a.nq, h = blockIdx.x - m * a.nq;
-  const int nparts = (row_pos(a.rs, m) / kKvChunk) / a.R + 1;   // ranges of R chunks the row sees
+  const int nparts = (row_slot(a.rs, m) / kKvChunk) / a.R + 1;   // ranges of R chunks the row sees
   const float v = merge_row_head(a.part, a.nq, a.hd, a.n_kv_chunks, m, h, nparts, sm);
   if ((int)threadIdx.x < a.hd) act_store(a.out, m, h * a.hd + threadIdx.x, (a.rs.M + 3) / 4, v, a.umma);
 }

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kGemmThreads) k_gemm_f32(const __grid_constant
   const int rows_seg = a.seg_end[seg] - (seg ? a.seg_end[seg - 1] : 0);
   const bool row_ok = EPI == EPI_SWIGLU ? wrow < a.N : wrow < rows_seg && rb * kBlockRows + r < a.N;
   const float* W = static_cast<const float*>(a.w[seg]) + (size_t)wrow * a.ld[seg];
-  if (EPI == EPI_QKV && tid < M) s_pos[tid] = row_pos(a.rs, tid);
+  if (EPI == EPI_QKV && tid < M) s_pos[tid] = row_slot(a.rs, tid);
   pdl_wait();
   trace_mark(a.rs, 1);
   pdl_launch_next();

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, (T <= 3 || (!NF4 && EPI != EPI_Q
   // the sequence lengths are written only by the acceptance and reset
   // kernels and by host copies, never by the kernel that directly precedes a
   // projection (the only one that can still be running at this point).
-  if (EPI == EPI_QKV && tid < M) s_pos[tid] = row_pos(a.rs, m0 + tid);
+  if (EPI == EPI_QKV && tid < M) s_pos[tid] = row_slot(a.rs, m0 + tid);
   if (a.push) {
     // Rank 0's landing barrier expects every other rank's tile; the cluster
     // barrier that starts here (and is waited on only after the main loop)
@@ -722,8 +722,8 @@ cudaError_t make_weight_map(CUtensorMap* map, const void* w, int rows, int K, in
 
 int nf4_scale_ld(int K) { return ((K / 64 + 7) / 8) * 8; }
 
-cudaError_t make_kv_map(CUtensorMap* map, const void* kv, long rows, int hd) {
-  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, hd, (uint64_t)rows, (uint64_t)hd * 2, 64, 64,
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, long rows, int hd, int box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, hd, (uint64_t)rows, (uint64_t)hd * 2, 64, box_rows,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 

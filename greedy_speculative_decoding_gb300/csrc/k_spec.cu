@@ -1,5 +1,6 @@
 // Integer kernels of the speculative round: accept + in-place rollback,
-// prompt-lookup (n-gram) drafting, state reset; and the NF4 codebook and
+// prompt-lookup (n-gram) drafting with one guess or several (with their
+// acceptance and cache compaction), state reset; and the NF4 codebook and
 // quantiser used to prepare 4-bit weights.
 #include <cmath>
 
@@ -129,6 +130,194 @@ cudaError_t launch_ngram(const SpecState& s, int max_guess, int min_n, int max_n
   cfg.attrs = &attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, k_ngram, s, max_guess, min_n, max_n, d_prop, d_count);
+}
+
+// ---------------------------------------------------------------- several guesses
+// Multi-candidate prompt lookup, one CTA per sequence. The earlier
+// occurrences of the context's last n tokens are visited in k_ngram's order
+// (n from max_n down to min_n; for each n the rightmost start first); each
+// gives the up to g tokens that followed it, cut at the end of the context,
+// and is kept unless it equals a guess already kept; at most n_cand. Every
+// step tests 256 starts at once; warp 0 walks that step's matches in visit
+// order and keeps the new ones. Candidate c's guess fills verify rows
+// 1 + c * g .. c * g + g (unused rows: token 0).
+constexpr int kTreeThreads = 256;
+
+__global__ void __launch_bounds__(kTreeThreads) k_ngram_tree(const __grid_constant__ SpecState s, int n_cand,
+                                                             int g, int min_n, int max_n, int* d_prop,
+                                                             int* d_len) {
+  pdl_wait();
+  pdl_launch_next();
+  __shared__ int kept_at[32], kept_len[32];
+  __shared__ unsigned ballot[kTreeThreads / 32];
+  __shared__ int nkept;
+  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = s.len_t[b] + 1;
+  const int* ctx = s.hist + (size_t)b * s.s_max;
+  if (tid == 0) nkept = 0;
+  __syncthreads();
+  for (int n = max_n; n >= min_n; --n) {
+    if (n > C - 1) continue;
+    for (int top = C - n - 1; top >= 0 && nkept < n_cand; top -= kTreeThreads) {
+      const int j = top - tid;
+      bool eq = j >= 0;
+      for (int i = 0; i < n && eq; ++i) eq = ctx[j + i] == ctx[C - n + i];
+      const unsigned bal = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) ballot[warp] = bal;
+      if (!__syncthreads_or(eq)) continue;
+      if (warp == 0) {
+        // Lower thread = larger start = earlier in visit order.
+        for (int w = 0; w < kTreeThreads / 32 && nkept < n_cand; ++w) {
+          unsigned m = ballot[w];
+          while (m && nkept < n_cand) {
+            const int t = __ffs(m) - 1;
+            m &= m - 1;
+            const int at = top - (32 * w + t) + n, len = min(g, C - at);
+            // Lane k < nkept compares this guess with kept guess k.
+            bool dup = false;
+            if (lane < nkept && kept_len[lane] == len) {
+              dup = true;
+              for (int i = 0; i < len && dup; ++i) dup = ctx[kept_at[lane] + i] == ctx[at + i];
+            }
+            if (!__any_sync(0xffffffffu, dup)) {
+              if (lane == 0) {
+                kept_at[nkept] = at;
+                kept_len[nkept] = len;
+                nkept = nkept + 1;
+              }
+            }
+            __syncwarp();
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  const int K1 = s.K + 1;
+  for (int r = tid; r < s.K; r += kTreeThreads) {
+    const int c = r / g, i = r - c * g;
+    const int tok = (c < nkept && i < kept_len[c]) ? ctx[kept_at[c] + i] : 0;
+    s.vtok[b * K1 + 1 + r] = tok;
+    if (d_prop && c < n_cand) d_prop[(b * n_cand + c) * g + i] = tok;
+  }
+  for (int c = tid; c < s.K; c += kTreeThreads) {
+    const int len = c < nkept ? kept_len[c] : 0;
+    s.clen[b * s.K + c] = len;
+    if (d_len && c < n_cand) d_len[b * n_cand + c] = len;
+  }
+  if (tid == 0) s.nprop[b] = nkept;
+}
+
+cudaError_t launch_ngram_tree(const SpecState& s, int n_cand, int g, int min_n, int max_n, int* d_prop,
+                              int* d_len, cudaStream_t st, bool pdl) {
+  if (n_cand < 1 || g < 1 || n_cand * g > s.K || n_cand > 32) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr = pdl_attr();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.B);
+  cfg.blockDim = dim3(kTreeThreads);
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_ngram_tree, s, n_cand, g, min_n, max_n, d_prop, d_len);
+}
+
+// Acceptance over the candidates, one warp per sequence. Lane c counts the
+// leading tokens of candidate c that equal the target's choices along that
+// candidate's own rows: the choice after the pending token is row 0's, the
+// choice after guess tokens 0..i-1 of candidate c is row c * g + i's. The
+// longest count wins, the lowest candidate on ties; its accepted tokens and
+// the choice after them are committed, as in k_accept.
+__global__ void k_accept_tree(const __grid_constant__ SpecState s, int n_cand, int g) {
+  pdl_wait();
+  pdl_launch_next();
+  const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (b >= s.B) return;
+  const int K1 = s.K + 1;
+  const int* vt = s.vtok + b * K1;
+  const int* tt = s.ttok + b * K1;
+  int key = -1;
+  if (lane < n_cand) {
+    const int len = s.clen[b * s.K + lane];
+    int n = 0;
+    while (n < len && vt[1 + lane * g + n] == tt[n == 0 ? 0 : lane * g + n]) ++n;
+    key = n * 32 + (31 - lane);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+  const int n = key >> 5, c = 31 - (key & 31);
+  const int C = s.len_t[b] + 1;
+  const int last = tt[n == 0 ? 0 : c * g + n];
+  int tok = 0;
+  if (lane <= n) tok = lane < n ? vt[1 + c * g + lane] : last;
+  const int before_last = n > 0 ? vt[c * g + n] : vt[0];
+  __syncwarp();
+  if (lane <= n) {
+    s.commit[b * K1 + lane] = tok;
+    if (C + lane < s.s_max) s.hist[(size_t)b * s.s_max + C + lane] = tok;
+  }
+  if (lane == 0) {
+    const int Cn = C + n + 1;
+    s.len_t[b] = Cn - 1;
+    s.len_d[b] = Cn - 2;
+    s.ncommit[b] = n + 1;
+    s.nacc[b] = n;
+    s.tree_c[b] = c;
+    s.total[b] += n + 1;
+    s.acc_hist[b * K1 + n] += 1;
+    s.dtok0[2 * b] = before_last;
+    s.dtok0[2 * b + 1] = last;
+    s.vtok[b * K1] = last;
+    if (Cn + s.K + 1 > s.s_max) atomicOr(s.err, kErrCapacity);
+  }
+}
+
+cudaError_t launch_accept_tree(const SpecState& s, int n_cand, int g, cudaStream_t st, bool pdl) {
+  if (n_cand < 1 || g < 1 || n_cand * g > s.K || n_cand > 32) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr = pdl_attr();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32 * s.B);
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_accept_tree, s, n_cand, g);
+}
+
+// The verify pass wrote candidate c's guess i into slot C + c * g + i; the
+// accepted ones belong in slots C + i. One CTA per (layer, sequence) moves
+// the n accepted keys and values of every KV head, 16 bytes per thread step.
+// Source and destination never overlap (n <= g <= c * g for c >= 1).
+__global__ void k_tree_compact(const __grid_constant__ SpecState s, bf16* kv, int nkv, int hd, int g) {
+  pdl_wait();
+  pdl_launch_next();
+  const int l = blockIdx.x, b = blockIdx.y;
+  const int c = s.tree_c[b], n = s.nacc[b];
+  if (c == 0 || n == 0) return;
+  const int C = s.len_t[b] - n;
+  const int units = hd / 8;   // 16-byte pieces of one cache row
+  const int per_head = n * units;
+  for (int i = threadIdx.x; i < 2 * nkv * per_head; i += blockDim.x) {
+    const int kvsel = i / (nkv * per_head);
+    const int rest = i - kvsel * nkv * per_head;
+    const int h = rest / per_head, rr = rest - h * per_head;
+    const int row = rr / units, u = rr - row * units;
+    bf16* base = kv + ((((size_t)l * 2 + kvsel) * s.B + b) * nkv + h) * (size_t)s.s_max * hd;
+    const uint4 v = *reinterpret_cast<const uint4*>(base + (size_t)(C + c * g + row) * hd + 8 * u);
+    *reinterpret_cast<uint4*>(base + (size_t)(C + row) * hd + 8 * u) = v;
+  }
+}
+
+cudaError_t launch_tree_compact(const SpecState& s, bf16* kv, int layers, int nkv, int hd, int g, cudaStream_t st,
+                                bool pdl) {
+  if (hd % 8 || g < 1) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr = pdl_attr();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(layers, s.B);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_tree_compact, s, kv, nkv, hd, g);
 }
 
 // ---------------------------------------------------------------- device loop

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
   fence_proxy_async();
   // Token positions (QKV epilogue), read before the wait: lengths are never
   // written by the kernel that directly precedes a projection.
-  if (EPI == EPI_QKV && tid < M) sm.pos[tid] = row_pos(a.rs, tid);
+  if (EPI == EPI_QKV && tid < M) sm.pos[tid] = row_slot(a.rs, tid);
   if (NF4) {
     // Entry b of lane l at 32 b + l: every lookup of a warp hits its own bank.
     for (int i = tid; i < 256 * 32; i += kUThreads) {

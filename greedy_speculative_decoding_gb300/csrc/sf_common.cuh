@@ -33,8 +33,12 @@ constexpr int kErrNonfinite = 1;
 constexpr int kErrWait = 2;
 constexpr int kErrCapacity = 4;
 
-// Rows of one forward: row m belongs to sequence m / rps and sits at
-// position pos_base[m / rps] + pos_off + m % rps.
+// Rows of one forward: row m belongs to sequence m / rps and sits in cache
+// slot pos_base[m / rps] + pos_off + m % rps. That slot is also its sequence
+// position, except in a verify pass over several candidate guesses
+// (tree_g = g > 0): there row j >= 1 of a sequence is guess (j - 1) % g of
+// candidate (j - 1) / g, at position p0 + 1 + (j - 1) % g (p0: row 0's slot),
+// and it sees the slots up to p0 and its own candidate's slots up to itself.
 struct RowSet {
   const int* tok;      // token of row m: tok[b * tok_stride + tok_off + j]
   int tok_stride, tok_off;
@@ -44,6 +48,7 @@ struct RowSet {
   int pos_off;
   unsigned long long* trace;   // optional launch timeline: [2 * trace_id + {0: entry, 1: producer done}]
   int trace_id;
+  int tree_g;          // guesses per candidate of a multi-candidate verify pass; 0: one chain
 };
 
 // Launch timeline for profiling: CTA 0 stamps the global timer when the
@@ -68,8 +73,16 @@ __device__ __forceinline__ void report_err(int* err, int bit) {
   if (err) atomicOr(err, bit);
 }
 
-__device__ __forceinline__ int row_pos(const RowSet& rs, int m) {
+__device__ __forceinline__ int row_slot(const RowSet& rs, int m) {
   return rs.pos_base[m / rs.rps] + rs.pos_off + m % rs.rps;
+}
+// Slots between row 0 and row j's own candidate: (j - 1) / g * g of them.
+__device__ __forceinline__ int tree_gap(const RowSet& rs, int j) {
+  return (rs.tree_g > 0 && j > 0) ? (j - 1) / rs.tree_g * rs.tree_g : 0;
+}
+// Sequence position of row m (its RoPE angle).
+__device__ __forceinline__ int row_pos(const RowSet& rs, int m) {
+  return row_slot(rs, m) - tree_gap(rs, m % rs.rps);
 }
 
 // ---------------------------------------------------------------- PTX helpers

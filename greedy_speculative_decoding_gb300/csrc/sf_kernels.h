@@ -153,6 +153,7 @@ struct AttnArgs {
   // slot p) of this layer are row kv_row0 + b * kv_brows + h * s_max + p, the
   // values kv_vrows rows further.
   CUtensorMap kvmap;
+  CUtensorMap kvmap8;      // the same with 8-slot boxes: a sequence's partly filled last chunk
   int kv_row0, kv_brows, kv_vrows;
   int R;                   // cache chunks per work item (one partial result per R chunks)
   int TG;                  // 16-query tiles per work item (1..4)
@@ -169,7 +170,7 @@ struct AttnArgs {
 };
 cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bool pdl);
 // Tensor map of a KV cache [rows][hd] bf16 (rows = layers * 2 * batch * n_kv_heads * s_max).
-cudaError_t make_kv_map(CUtensorMap* map, const void* kv, long rows, int hd);
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, long rows, int hd, int box_rows = 64);
 // Shared-memory limits and carve-out of the attention kernels (current device).
 cudaError_t attn_init();
 
@@ -193,6 +194,8 @@ struct SpecState {
   int* err;
   int* loop_target; // device-resident loop: new tokens per sequence to reach
   int* rounds;      // device-resident loop: rounds run by the current sf_generate
+  int* clen;        // [B][K] multi-candidate draft: tokens of each candidate guess (0: none)
+  int* tree_c;      // [B] multi-candidate draft: the candidate the last round took
   int B, K, s_max;
 };
 
@@ -203,6 +206,16 @@ cudaError_t launch_accept(const SpecState& s, int mode, cudaStream_t st, bool pd
 cudaError_t launch_ngram(const SpecState& s, int max_guess, int min_n, int max_n, int* d_prop,
                          int* d_count, cudaStream_t st, bool pdl);
 cudaError_t launch_reset(const SpecState& s, cudaStream_t st);
+// Multi-candidate prompt lookup: up to n_cand guesses of up to g tokens
+// (g * n_cand <= K) into the verify rows; its acceptance over the candidates
+// (the longest accepted prefix wins, the lowest candidate on ties); and the
+// move of the winner's cache entries down to the committed slots of every
+// layer (kv: one model's cache, [layers][2][B][nkv][s_max][hd] bf16).
+cudaError_t launch_ngram_tree(const SpecState& s, int n_cand, int g, int min_n, int max_n, int* d_prop,
+                              int* d_len, cudaStream_t st, bool pdl);
+cudaError_t launch_accept_tree(const SpecState& s, int n_cand, int g, cudaStream_t st, bool pdl);
+cudaError_t launch_tree_compact(const SpecState& s, bf16* kv, int layers, int nkv, int hd, int g, cudaStream_t st,
+                                bool pdl);
 // Device-resident round loop: set the target and clear the round count
 // (before the loop graph), and the control kernel at the end of every round
 // that decides whether the loop runs another round.

@@ -170,6 +170,24 @@ class SpecEngine:
                                         None if prop is None else prop.data_ptr(),
                                         None if count is None else count.data_ptr()))
 
+    def tree_draft(self, n_cand: int, min_n: int = 2, max_n: int = 4, prop: torch.Tensor = None,
+                   lens: torch.Tensor = None):
+        """Up to n_cand prompt-lookup guesses of K // n_cand tokens, verified
+        side by side by the next verify; prop int32 [batch][n_cand][K // n_cand],
+        lens int32 [batch][n_cand] (optional device outputs)."""
+        L.check(self.lib.sf_tree_draft(self.h, n_cand, min_n, max_n,
+                                       None if prop is None else prop.data_ptr(),
+                                       None if lens is None else lens.data_ptr()))
+
+    def set_tree_candidates(self, n_cand: int):
+        L.check(self.lib.sf_set_tree_candidates(self.h, n_cand))
+
+    def tree_winner(self):
+        """The candidate each sequence's last multi-candidate round took."""
+        c = np.zeros(self.B, np.int32)
+        L.check(self.lib.sf_tree_winner(self.h, _i32(c)))
+        return c
+
     def verify(self, argmax: torch.Tensor = None, logits: torch.Tensor = None):
         L.check(self.lib.sf_verify(self.h, None if argmax is None else argmax.data_ptr(),
                                    None if logits is None else logits.data_ptr()))

@@ -82,10 +82,11 @@ typedef enum {
  * norms, biases and LM head stay bf16); or fp32 for every tensor (the
  * single-precision correctness workload; plain fp32 arithmetic, not a fast path). */
 enum { SF_WDTYPE_BF16 = 0, SF_WDTYPE_NF4 = 1, SF_WDTYPE_F32 = 2 };
-/* Drafters: the draft model, prompt lookup, or none (each round then commits
+/* Drafters: the draft model, prompt lookup, none (each round then commits
  * only the target's own next token: plain greedy decoding, the baseline the
- * speculative rounds are measured against). */
-enum { SF_DRAFT_NEURAL = 0, SF_DRAFT_NGRAM = 1, SF_DRAFT_NONE = 2 };
+ * speculative rounds are measured against), or prompt lookup with several
+ * guesses verified side by side in one target pass (sf_tree_draft). */
+enum { SF_DRAFT_NEURAL = 0, SF_DRAFT_NGRAM = 1, SF_DRAFT_NONE = 2, SF_DRAFT_TREE = 3 };
 
 /* Decoder shape (Qwen2-style: GQA attention with RoPE, RMSNorm, SwiGLU MLP). */
 typedef struct {
@@ -181,6 +182,26 @@ SF_API sf_status sf_ngram_draft(sf_handle h, int32_t max_guess, int32_t min_n, i
                          int32_t* d_prop, int32_t* d_count);
 
 /*
+ * Several prompt-lookup guesses per round (the Sangama page, "Next": better
+ * guesses for the look-back drafter; here several earlier occurrences are
+ * checked by the target together instead of only the most recent one). The
+ * earlier occurrences of the last n committed tokens are taken in
+ * sf_ngram_draft's order (n from max_n down to min_n, rightmost first); each
+ * gives up to g = K / n_cand tokens that followed it (cut at the end of the
+ * context); a guess equal to one already taken is skipped; at most n_cand
+ * guesses. Guess c fills verify rows 1 + c*g .. c*g + g. sf_verify then runs
+ * the rows of each guess at the positions after the pending token, each
+ * seeing the committed sequence and its own guess only, and
+ * sf_accept_rollback takes the guess with the longest accepted prefix (the
+ * lowest c on ties), commits as for one guess and moves that guess's
+ * target-cache entries down to the committed slots. Optional device outputs:
+ * d_prop [batch][n_cand][g] (unused 0), d_len [batch][n_cand] (0: no guess).
+ * 1 <= n_cand <= K; 1 <= min_n <= max_n <= 64.
+ */
+SF_API sf_status sf_tree_draft(sf_handle h, int32_t n_cand, int32_t min_n, int32_t max_n, int32_t* d_prop,
+                               int32_t* d_len);
+
+/*
  * Target verify ("Speculative Decoding: The Idea": the target checks all
  * guesses in one forward pass; the Sangama page: the model's own choice at
  * every position): one causal pass over [pending, d_1..d_K] per sequence,
@@ -228,8 +249,15 @@ SF_API sf_status sf_generate(sf_handle h, int32_t n_new, int32_t* h_out, int32_t
 SF_API sf_status sf_reset(sf_handle h);
 
 /* Select the drafter used by sf_step / sf_generate (SF_DRAFT_*; min_n and
- * max_n apply to SF_DRAFT_NGRAM only). */
+ * max_n apply to SF_DRAFT_NGRAM and SF_DRAFT_TREE only). */
 SF_API sf_status sf_set_drafter(sf_handle h, int32_t mode, int32_t min_n, int32_t max_n);
+
+/* Guesses per round of SF_DRAFT_TREE in sf_step / sf_generate (1..K; the
+ * default is 2, or 1 when K = 1). */
+SF_API sf_status sf_set_tree_candidates(sf_handle h, int32_t n_cand);
+
+/* The guess each sequence's last multi-candidate round took (host [batch]). */
+SF_API sf_status sf_tree_winner(sf_handle h, int32_t* h_c);
 
 /* Current cache lengths per sequence (host [batch] each, may be NULL): the
  * positions the in-place rewind left ("Why It Kept Breaking", fixes 3-4:

@@ -60,3 +60,44 @@ def planted_prompt(model, vocab, j, K=4, seed=0, a_len=20, tol=3e-2, tries=64):
             continue
         return P, gr
     raise RuntimeError(f"no planted prompt for j={j}")
+
+
+def planted_tree_prompt(model, vocab, ns, g, seed=0, a_len=20, tol=3e-2, tries=64):
+    """(prompt, greedy continuation) such that multi-candidate prompt lookup
+    (oracle ngram_candidates with len(ns) candidates of g tokens) proposes
+    len(ns) guesses of which guess c starts with exactly ns[c] of the
+    target's choices. The prompt is A + (s + Y_c + B_c for c from last to
+    first) + s: the most recent occurrence of s is followed by Y_0, the one
+    before it by Y_1, and so on; each Y_c is planted by the same fixed point
+    as planted_prompt."""
+    n_cand = len(ns)
+    for attempt in range(tries):
+        gen = torch.Generator().manual_seed(seed * 1000 + attempt)
+        rnd = lambda n: torch.randint(0, vocab, (n,), generator=gen).tolist()
+        A, s = rnd(a_len), rnd(4)
+        Bs = [rnd(5) for _ in ns]
+        Ys = [rnd(g + 1) for _ in ns]
+        for _ in range(8):
+            P = list(A)
+            for c in reversed(range(n_cand)):
+                P += s + Ys[c] + Bs[c]
+            P += s
+            gr, mg = _greedy_margins(model, P, max(ns) + 1)
+            new = []
+            for c, n in enumerate(ns):
+                head = gr[:n]
+                if n < g:
+                    head = head + [Ys[c][n] if Ys[c][n] != gr[n] else (gr[n] + 1) % vocab]
+                new.append(head + Ys[c][len(head):])
+            if new == Ys:
+                break
+            Ys = new
+        else:
+            continue
+        if od.ngram_candidates(P, n_cand, g, 2, 4) != [y[:g] for y in Ys] or min(mg) <= tol:
+            continue
+        pad = gr + [-1] * (g + 1 - len(gr))
+        if [od.accept_length(y[:g], pad, g) for y in Ys] != list(ns):
+            continue
+        return P, gr
+    raise RuntimeError(f"no planted prompt for accept lengths {ns}")
