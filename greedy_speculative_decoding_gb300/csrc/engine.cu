@@ -90,7 +90,6 @@ struct Model {
   CUtensorMap kvmap;       // the whole cache as [rows][head_dim] for the attention kernel's TMA
   CUtensorMap kvmap8;      // the same with 8-slot boxes
   int attn_R = 1;          // cache chunks per attention work item
-  int attn_TG = 1;         // query tiles per attention work item
   int attn_stages = 1;     // key/value chunks in flight per attention CTA
   float2* rope = nullptr;
   Plan p_qkv, p_o, p_gu, p_d, p_lm;
@@ -347,12 +346,9 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     // small; up to 8 for a large batch of long caches, so the items fill the
     // GPU a few times over and the merge reads a few partials per row. Fixed
     // per model and engine: a row's arithmetic never depends on other rows.
-    // The same load decides whether an item carries every query tile of its
-    // KV head (each chunk read once, two chunks in flight) or one tile (more
-    // items for a small batch: the same work spread over more CTAs).
+    // The same load decides how many chunks a CTA keeps in flight.
     const long load = (long)e->B * c->n_kv_heads * (e->s_max / kKvChunk) / 2048;
     md.attn_R = load >= 8 ? 8 : (load >= 4 ? 4 : (load >= 2 ? 2 : 1));
-    md.attn_TG = load >= 2 ? 4 : 1;
     md.attn_stages = load >= 2 ? 2 : 1;
   }
   const int H = c->hidden;
@@ -572,7 +568,13 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     t.kv_vrows = e->B * t.kv_brows;
     t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
     t.R = md.attn_R;
-    t.TG = md.attn_TG;
+    // Query tiles per work item, from this launch's rows (a row's result
+    // does not depend on it): every tile of a KV head's queries together, up
+    // to four, one team of warps each.
+    {
+      const int ntiles = (rs.rps * (c.n_heads / c.n_kv_heads) + 15) / 16;
+      t.TG = ntiles >= 3 ? 4 : ntiles;
+    }
     t.stages = md.attn_stages;
     t.q = e->q;
     t.part = e->apart;

@@ -70,48 +70,60 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uin
 }
 
 // One work item = (sequence b, KV head, range r of R consecutive 64-slot
-// chunks, group of up to four 16-query tiles); the queries are all rows of the
+// chunks, group of up to kTG 16-query tiles); the queries are all rows of the
 // sequence times the query heads that read this KV head. The chunks' keys and
 // values arrive by 2-D TMA (box 64 dims x 64 slots, 128-byte swizzle) into a
 // two-stage ring that runs across the CTA's items, so the next chunk is in
 // flight while this one is computed; every query tile of the group is
-// computed from one copy. Per tile, all eight warps work on each chunk:
-//   S = Q K^T   warp w computes the 8 keys 8w..8w+7 over the whole head
+// computed from one copy. The eight warps split into kTG teams of
+// W = 8 / kTG, one per query tile, all tiles at once:
+//   S = Q K^T   a team's warp computes 64 / W keys over the whole head
 //               dimension (mma.sync m16n8k16, Q as an fp32-accurate bf16
-//               hi+lo pair);
+//               hi+lo pair), 8 keys per MMA tile;
 //   softmax     online over the range: row max and row sum combined across
-//               the warps through shared memory (sums in warp order), the
-//               running max and sum rescaled per chunk;
-//   O = P V     P (hi+lo) through shared memory, warp w producing output
-//               dimensions w*HD/8 .. (w+1)*HD/8 - 1 from all 64 keys, the
-//               running output rescaled per chunk.
-// The range's unnormalised output, running max and sum go to scratch; the
-// merge kernel combines the ranges of every (row, head) in order. R is fixed
-// per model and engine and the ranges start at fixed multiples of R chunks,
-// so a row's result does not depend on how many other rows the launch carries.
+//               the team through shared memory (the sums of every 8 keys
+//               added in key order), the running max and sum rescaled per
+//               chunk;
+//   O = P V     P (hi+lo) through shared memory, a team's warp producing
+//               HD / W output dimensions from all 64 keys, the running
+//               output rescaled per chunk.
+// Every score, sum and output element is the same sequence of operations
+// whatever W is (W only decides which warp performs it), so kTG can follow
+// the row count of each launch. The range's unnormalised output, running max
+// and sum go to scratch; the merge kernel combines the ranges of every
+// (row, head) in order. R is fixed per model and engine and the ranges start
+// at fixed multiples of R chunks, so a row's result does not depend on how
+// many other rows the launch carries.
 template <int HD, int kTG>
-__global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, kTG == 4 ? 1 : 2) k_attn_chunks(const __grid_constant__ AttnArgs a) {
   constexpr int kBox = kKvChunk * 128;          // one TMA box: 64 slots x 64 dims (8 KB)
   constexpr int kHalf = HD / 64;                // boxes per chunk of keys (or values)
   constexpr int kKV = kHalf * kBox;             // one chunk's keys (or values)
   constexpr int kStage = 2 * kKV;
   constexpr int KS = HD / 16;                   // k-steps over the head dimension
-  constexpr int NTW = HD / 64;                  // output n-tiles (8 dimensions each) per warp
+  constexpr int WPT = 8 / kTG;                  // warps per query tile
+  constexpr int KPW = kKvChunk / WPT;           // keys per warp in S = Q K^T
+  constexpr int NKT = KPW / 8;                  // key n-tiles (8 keys each) per warp
+  constexpr int NTW = HD / 8 / WPT;             // output n-tiles (8 dimensions each) per warp
   constexpr int HP = HD + 16;                   // query hi / lo row pitch (bf16): 8-bank shift per row
   constexpr int PP = kKvChunk + 8;              // probability tile row pitch (bf16)
-  static_assert(kAttnThreads == 256 && kKvChunk == 64, "eight warps of eight keys");
+  static_assert(kAttnThreads == 256 && kKvChunk == 64 && 8 % kTG == 0, "eight warps over kTG tiles");
   extern __shared__ unsigned char attn_smem_raw[];
   unsigned char* base = attn_smem_raw + ((1024 - (smem_u32(attn_smem_raw) & 1023)) & 1023);
-  bf16* sph = reinterpret_cast<bf16*>(base + a.stages * kStage); // [16][PP] P hi
-  bf16* spl = sph + 16 * PP;                                     // [16][PP] P lo
-  bf16* sq = spl + 16 * PP;                                      // [TG][2][16][HP] queries hi / lo
-  __shared__ float red_mx[8][16], red_l[8][16];
+  bf16* sph = reinterpret_cast<bf16*>(base + a.stages * kStage); // [TG][16][PP] P hi
+  bf16* spl = sph + kTG * 16 * PP;                               // [TG][16][PP] P lo
+  bf16* sq = spl + kTG * 16 * PP;                                // [TG][2][16][HP] queries hi / lo
+  __shared__ float red_mx[8][16];                                // per warp: row max of its keys
+  __shared__ float red_l[kTG][8][16];                            // per tile and 8 keys: row sums
   __shared__ float m_run[kTG][16], l_run[kTG][16];
   __shared__ __align__(8) uint64_t full[2];
 
   trace_mark(a.rs, 0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c4 = lane & 3;
+  const int ti = warp / WPT, wq = warp % WPT;   // this warp's query tile within the item, its rank there
+  // The warps of one query tile meet at a named barrier of their own.
+  auto tile_sync = [](int t) { asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "r"(WPT * 32) : "memory"); };
   const int group = a.nq / a.nkv;
   const int rps = a.rs.rps;
   const int Mq = rps * group;
@@ -217,9 +229,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
     {
       const int n4 = nt * 16 * (HD / 4);
       for (int i = tid; i < n4; i += kAttnThreads) {
-        const int ti = i / (16 * (HD / 4)), rem = i - ti * (16 * (HD / 4));
+        const int qt = i / (16 * (HD / 4)), rem = i - qt * (16 * (HD / 4));
         const int qr = rem / (HD / 4), u = rem - qr * (HD / 4);
-        const int qi = (t0 + ti) * 16 + qr;
+        const int qi = (t0 + qt) * 16 + qr;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (qi < Mq) {
           const int j = qi / group, hh = qi - j * group;
@@ -228,19 +240,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
         uint2 h, l;
         split_bf16x2(v.x, v.y, h.x, l.x);
         split_bf16x2(v.z, v.w, h.y, l.y);
-        *reinterpret_cast<uint2*>(sq + ((2 * ti) * 16 + qr) * HP + 4 * u) = h;
-        *reinterpret_cast<uint2*>(sq + ((2 * ti + 1) * 16 + qr) * HP + 4 * u) = l;
+        *reinterpret_cast<uint2*>(sq + ((2 * qt) * 16 + qr) * HP + 4 * u) = h;
+        *reinterpret_cast<uint2*>(sq + ((2 * qt + 1) * 16 + qr) * HP + 4 * u) = l;
       }
       if (tid < kTG * 16) {
         m_run[tid >> 4][tid & 15] = -INFINITY;
         l_run[tid >> 4][tid & 15] = 0.f;
       }
     }
-    float oacc[kTG][NTW][4];
+    float oacc[NTW][4];
 #pragma unroll
-    for (int ti = 0; ti < kTG; ++ti)
-#pragma unroll
-      for (int t2 = 0; t2 < NTW; ++t2) oacc[ti][t2][0] = oacc[ti][t2][1] = oacc[ti][t2][2] = oacc[ti][t2][3] = 0.f;
+    for (int t2 = 0; t2 < NTW; ++t2) oacc[t2][0] = oacc[t2][1] = oacc[t2][2] = oacc[t2][3] = 0.f;
     __syncthreads();
 
     for (int c = it.c0; c < it.c1; ++c, ++step) {
@@ -263,14 +273,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
           const int r = nvalid + i / (8 * kHalf), rem = i % (8 * kHalf);
           *reinterpret_cast<uint4*>(vs + (rem >> 3) * kBox + r * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
-        fence_proxy_async();   // ordered before the next copy into this stage; the first
-                               // tile's barrier orders it before the P V reads
+        fence_proxy_async();   // ordered before the next copy into this stage
+        __syncthreads();       // and before every tile's P V reads
       }
-#pragma unroll
-      for (int ti = 0; ti < kTG; ++ti) {
-        if (ti >= nt) break;
+      if (ti < nt) {
         const bf16* qht = sq + (2 * ti) * 16 * HP;
         const bf16* qlt = sq + (2 * ti + 1) * 16 * HP;
+        bf16* tph = sph + ti * 16 * PP;
+        bf16* tpl = spl + ti * 16 * PP;
         // Row j sees the chunk's keys below nk, except [gl, gh): in a
         // multi-candidate verify, the slots of the candidates before its own.
         int nk[2], gl[2], gh[2];
@@ -282,13 +292,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
           gl[r] = it.p0 + 1 - c * kKvChunk;
           gh[r] = gl[r] + tree_gap(a.rs, j);
         }
-        // S for keys 8w .. 8w+7: four independent chains (hi / lo part of Q
-        // x even / odd k-step), added in a fixed order at the end. Key row
-        // `key` of the swizzled tile: dims 8q .. 8q+7 at 16-byte piece q ^ (key & 7).
-        float sa[4][4];
+        // S for this warp's keys, 8 at a time (n8 tile t: keys
+        // wq*KPW + 8t .. +7): per tile four independent chains (hi / lo part
+        // of Q x even / odd k-step), added in a fixed order at the end. Key
+        // row `key` of the swizzled tile: dims 8q .. 8q+7 at 16-byte piece
+        // q ^ (key & 7).
+        float sa[NKT][4][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sa[i][0] = sa[i][1] = sa[i][2] = sa[i][3] = 0.f;
-        const int key = 8 * warp + g;
+        for (int t = 0; t < NKT; ++t)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sa[t][i][0] = sa[t][i][1] = sa[t][i][2] = sa[t][i][3] = 0.f;
 #pragma unroll
         for (int k = 0; k < KS; ++k) {
           const uint2 h0 = *reinterpret_cast<const uint2*>(qht + g * HP + 16 * k + 4 * c4);
@@ -296,55 +309,66 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
           const uint2 l0 = *reinterpret_cast<const uint2*>(qlt + g * HP + 16 * k + 4 * c4);
           const uint2 l1 = *reinterpret_cast<const uint2*>(qlt + (g + 8) * HP + 16 * k + 4 * c4);
           const int q16 = 2 * (k & 3) + (c4 >> 1);
-          const uint2 kb = *reinterpret_cast<const uint2*>(ks + (k >> 2) * kBox + key * 128 +
-                                                           ((q16 ^ (key & 7)) << 4) + 8 * (c4 & 1));
-          mma_bf16_16816(sa[k & 1], h0.x, h1.x, h0.y, h1.y, kb.x, kb.y);
-          mma_bf16_16816(sa[2 + (k & 1)], l0.x, l1.x, l0.y, l1.y, kb.x, kb.y);
-        }
-        float sacc[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
-          const float v = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
-          sacc[e] = (kk < nk[r] && (kk < gl[r] || kk >= gh[r])) ? v * a.scale : -INFINITY;
+          for (int t = 0; t < NKT; ++t) {
+            const int key = wq * KPW + 8 * t + g;
+            const uint2 kb = *reinterpret_cast<const uint2*>(ks + (k >> 2) * kBox + key * 128 +
+                                                             ((q16 ^ (key & 7)) << 4) + 8 * (c4 & 1));
+            mma_bf16_16816(sa[t][k & 1], h0.x, h1.x, h0.y, h1.y, kb.x, kb.y);
+            mma_bf16_16816(sa[t][2 + (k & 1)], l0.x, l1.x, l0.y, l1.y, kb.x, kb.y);
+          }
         }
-        float mx[2];
+        float sacc[NKT][4];
+#pragma unroll
+        for (int t = 0; t < NKT; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = e >> 1, kk = wq * KPW + 8 * t + 2 * c4 + (e & 1);
+            const float v = (sa[t][0][e] + sa[t][1][e]) + (sa[t][2][e] + sa[t][3][e]);
+            sacc[t][e] = (kk < nk[r] && (kk < gl[r] || kk >= gh[r])) ? v * a.scale : -INFINITY;
+          }
+        // Row maxima (exact, so the order of combination does not matter).
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          mx[r] = fmaxf(sacc[2 * r], sacc[2 * r + 1]);
-          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-          if (c4 == 0) red_mx[warp][g + 8 * r] = mx[r];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < NKT; ++t) mx = fmaxf(mx, fmaxf(sacc[t][2 * r], sacc[t][2 * r + 1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          if (c4 == 0) red_mx[warp][g + 8 * r] = mx;
         }
-        __syncthreads();   // red_mx complete
+        tile_sync(ti);   // the tile's red_mx complete
         float m_new[2], alpha[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          float m8 = red_mx[0][g + 8 * r];
+          float m8 = red_mx[ti * WPT][g + 8 * r];
 #pragma unroll
-          for (int w = 1; w < 8; ++w) m8 = fmaxf(m8, red_mx[w][g + 8 * r]);
+          for (int w = 1; w < WPT; ++w) m8 = fmaxf(m8, red_mx[ti * WPT + w][g + 8 * r]);
           const float m_old = m_run[ti][g + 8 * r];
           m_new[r] = fmaxf(m_old, m8);
           alpha[r] = m_new[r] == -INFINITY ? 1.f : expf(m_old - m_new[r]);
         }
-        float pe[4];
+        // Probabilities; the row sum of every 8 keys (summed over the 64 in
+        // key order below); P as bf16 hi + lo through shared memory.
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
-          pe[e] = sacc[e] != -INFINITY ? expf(sacc[e] - m_new[r]) : 0.f;
-        }
+        for (int t = 0; t < NKT; ++t) {
+          float pe[4];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float l = pe[2 * r] + pe[2 * r + 1];
-          l += __shfl_xor_sync(0xffffffffu, l, 1);
-          l += __shfl_xor_sync(0xffffffffu, l, 2);
-          if (c4 == 0) red_l[warp][g + 8 * r] = l;
-          uint32_t h, lo;
-          split_bf16x2(pe[2 * r], pe[2 * r + 1], h, lo);
-          *reinterpret_cast<uint32_t*>(sph + (g + 8 * r) * PP + 8 * warp + 2 * c4) = h;
-          *reinterpret_cast<uint32_t*>(spl + (g + 8 * r) * PP + 8 * warp + 2 * c4) = lo;
+          for (int e = 0; e < 4; ++e) pe[e] = sacc[t][e] != -INFINITY ? expf(sacc[t][e] - m_new[e >> 1]) : 0.f;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float l = pe[2 * r] + pe[2 * r + 1];
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (c4 == 0) red_l[ti][wq * NKT + t][g + 8 * r] = l;
+            uint32_t h, lo;
+            split_bf16x2(pe[2 * r], pe[2 * r + 1], h, lo);
+            const int col = wq * KPW + 8 * t + 2 * c4;
+            *reinterpret_cast<uint32_t*>(tph + (g + 8 * r) * PP + col) = h;
+            *reinterpret_cast<uint32_t*>(tpl + (g + 8 * r) * PP + col) = lo;
+          }
         }
-        __syncthreads();   // P and red_l complete
+        tile_sync(ti);   // the tile's P and red_l complete
 
         // O = O * alpha + P V for this warp's output dimensions (P hi and P lo
         // in two chains, added at the end). Value row `slot`, dims 8n .. 8n+7:
@@ -358,18 +382,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
         for (int kk = 0; kk < kKvChunk / 16; ++kk) {
           uint32_t ph[4], pl[4];
           const int k0 = 16 * kk + 2 * c4;
-          ph[0] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0);
-          ph[1] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0);
-          ph[2] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0 + 8);
-          ph[3] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0 + 8);
-          pl[0] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0);
-          pl[1] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0);
-          pl[2] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0 + 8);
-          pl[3] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0 + 8);
+          ph[0] = *reinterpret_cast<const uint32_t*>(tph + g * PP + k0);
+          ph[1] = *reinterpret_cast<const uint32_t*>(tph + (g + 8) * PP + k0);
+          ph[2] = *reinterpret_cast<const uint32_t*>(tph + g * PP + k0 + 8);
+          ph[3] = *reinterpret_cast<const uint32_t*>(tph + (g + 8) * PP + k0 + 8);
+          pl[0] = *reinterpret_cast<const uint32_t*>(tpl + g * PP + k0);
+          pl[1] = *reinterpret_cast<const uint32_t*>(tpl + (g + 8) * PP + k0);
+          pl[2] = *reinterpret_cast<const uint32_t*>(tpl + g * PP + k0 + 8);
+          pl[3] = *reinterpret_cast<const uint32_t*>(tpl + (g + 8) * PP + k0 + 8);
           const int slot = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
           for (int t2 = 0; t2 < NTW; ++t2) {
-            const int n = warp * NTW + t2;
+            const int n = wq * NTW + t2;
             uint32_t b0, b1;
             ldsm_x2_trans(b0, b1, vs + (n >> 3) * kBox + slot * 128 + (((n & 7) ^ (slot & 7)) << 4));
             mma_bf16_16816(oh[t2], ph[0], ph[1], ph[2], ph[3], b0, b1);
@@ -379,26 +403,24 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
 #pragma unroll
         for (int t2 = 0; t2 < NTW; ++t2)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) oacc[ti][t2][e] = oacc[ti][t2][e] * alpha[e >> 1] + (oh[t2][e] + ol[t2][e]);
-        if (warp == 0 && c4 == 0) {
+          for (int e = 0; e < 4; ++e) oacc[t2][e] = oacc[t2][e] * alpha[e >> 1] + (oh[t2][e] + ol[t2][e]);
+        if (wq == 0 && c4 == 0) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            float l = red_l[0][g + 8 * r];
+            float l = red_l[ti][0][g + 8 * r];
 #pragma unroll
-            for (int w = 1; w < 8; ++w) l += red_l[w][g + 8 * r];
+            for (int w = 1; w < 8; ++w) l += red_l[ti][w][g + 8 * r];
             l_run[ti][g + 8 * r] = l_run[ti][g + 8 * r] * alpha[r] + l;
             m_run[ti][g + 8 * r] = m_new[r];
           }
         }
-        __syncthreads();   // P, red_* and the stage free; running max / sum updated
       }
+      __syncthreads();   // the stage, P, red_* free; running max / sum updated
       if (tid == 0 && NS == 1) issue_next();
     }
 
-    // The range's partial result of every row that sees a slot of it.
-#pragma unroll
-    for (int ti = 0; ti < kTG; ++ti) {
-      if (ti >= nt) break;
+    // The range's partial result of every row of this warp's tile that sees a slot of it.
+    if (ti < nt) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int qi = (t0 + ti) * 16 + g + 8 * r;
@@ -409,9 +431,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunks(const __grid_co
         float* dst = a.part + (((size_t)m * a.nq + h) * a.n_kv_chunks + it.r) * (HD + 2);
 #pragma unroll
         for (int t2 = 0; t2 < NTW; ++t2)
-          *reinterpret_cast<float2*>(dst + 8 * (warp * NTW + t2) + 2 * c4) =
-              make_float2(oacc[ti][t2][2 * r], oacc[ti][t2][2 * r + 1]);
-        if (warp == 0 && c4 == 0) {
+          *reinterpret_cast<float2*>(dst + 8 * (wq * NTW + t2) + 2 * c4) =
+              make_float2(oacc[t2][2 * r], oacc[t2][2 * r + 1]);
+        if (wq == 0 && c4 == 0) {
           dst[HD] = m_run[ti][g + 8 * r];
           dst[HD + 1] = l_run[ti][g + 8 * r];
         }
@@ -441,28 +463,30 @@ __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_const
 // (1024-byte aligned for the swizzled TMA boxes), P hi + lo, and TG query
 // tiles (hi + lo).
 static int attn_smem_bytes(int hd, int stages, int tg) {
-  return 1024 + stages * 2 * kKvChunk * hd * 2 + 2 * 16 * (kKvChunk + 8) * 2 + tg * 2 * 16 * (hd + 16) * 2;
+  return 1024 + stages * 2 * kKvChunk * hd * 2 + tg * 2 * 16 * (kKvChunk + 8) * 2 + tg * 2 * 16 * (hd + 16) * 2;
 }
 
 // Dynamic shared-memory limits of the chunk kernels and the largest
 // shared-memory carve-out for every kernel of the chain.
 cudaError_t attn_init() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_attn_chunks<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                attn_smem_bytes(128, 2, 4))) ||
-      (e = cudaFuncSetAttribute(k_attn_chunks<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                attn_smem_bytes(128, 2, 1))) ||
-      (e = cudaFuncSetAttribute(k_attn_chunks<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                attn_smem_bytes(64, 2, 4))) ||
-      (e = cudaFuncSetAttribute(k_attn_chunks<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                attn_smem_bytes(64, 2, 1))))
-    return e;
+  const void* chunk_fns[] = {reinterpret_cast<const void*>(k_attn_chunks<128, 1>),
+                             reinterpret_cast<const void*>(k_attn_chunks<128, 2>),
+                             reinterpret_cast<const void*>(k_attn_chunks<128, 4>),
+                             reinterpret_cast<const void*>(k_attn_chunks<64, 1>),
+                             reinterpret_cast<const void*>(k_attn_chunks<64, 2>),
+                             reinterpret_cast<const void*>(k_attn_chunks<64, 4>)};
+  const int hd_of[] = {128, 128, 128, 64, 64, 64}, tg_of[] = {1, 2, 4, 1, 2, 4};
+  for (int i = 0; i < 6; ++i)
+    if ((e = cudaFuncSetAttribute(chunk_fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  attn_smem_bytes(hd_of[i], 2, tg_of[i]))) != cudaSuccess)
+      return e;
   // Largest shared-memory carve-out for every kernel of the chain (see gemm_init).
-  const void* fns[] = {reinterpret_cast<const void*>(k_attn_chunks<128, 4>),
-                       reinterpret_cast<const void*>(k_attn_chunks<128, 1>),
-                       reinterpret_cast<const void*>(k_attn_chunks<64, 4>),
-                       reinterpret_cast<const void*>(k_attn_chunks<64, 1>),
-                       reinterpret_cast<const void*>(k_attn_merge), reinterpret_cast<const void*>(k_embed)};
+  for (const void* f : chunk_fns)
+    if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+  const void* fns[] = {reinterpret_cast<const void*>(k_attn_merge), reinterpret_cast<const void*>(k_embed)};
   for (const void* f : fns)
     if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
@@ -487,10 +511,17 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bo
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
   cfg.dynamicSmemBytes = attn_smem_bytes(a.hd, a.stages, a.TG);
-  if (a.TG != 1 && a.TG != 4) return cudaErrorInvalidValue;
-  if (a.hd == 128) e = a.TG == 4 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 4>, a) : cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 1>, a);
-  else if (a.hd == 64) e = a.TG == 4 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 4>, a) : cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 1>, a);
-  else return cudaErrorInvalidValue;
+  if (a.TG != 1 && a.TG != 2 && a.TG != 4) return cudaErrorInvalidValue;
+  if (a.hd == 128)
+    e = a.TG == 4   ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 4>, a)
+        : a.TG == 2 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 2>, a)
+                    : cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 1>, a);
+  else if (a.hd == 64)
+    e = a.TG == 4   ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 4>, a)
+        : a.TG == 2 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 2>, a)
+                    : cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 1>, a);
+  else
+    return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.rs.M * a.nq);
