@@ -396,11 +396,17 @@ def nf4_batch_workload(pkg, peak, tq, d_shape, dw, lin):
 
 def _kernel_bytes(shape, label, ctx):
     """Algorithmic bytes one launch of a forward kernel moves (weights it
-    streams; for attention the keys and values it reads at context ctx)."""
+    streams; for attention the keys and values it reads at context ctx). A
+    phase of the persistent decode kernel ("d_" + kernel) moves what the
+    kernel of that name does."""
+    if label.startswith("d_"):
+        label = label[2:]
     h, f = shape.hidden, shape.ffn
     w = {"qkv": (shape.q_dim + 2 * shape.kv_dim) * h * 2, "o_proj": h * shape.q_dim * 2,
          "gate_up": 2 * f * h * 2, "down": h * f * 2, "lm_head": shape.vocab * h * 2,
          "attention": 2 * shape.n_kv_heads * shape.head_dim * 2 * ctx}
+    # The persistent decode kernel: every layer's projections and cache.
+    w["decode"] = shape.layers * (w["qkv"] + w["o_proj"] + w["gate_up"] + w["down"] + w["attention"])
     return w.get(label)
 
 

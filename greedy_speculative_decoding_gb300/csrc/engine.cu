@@ -91,6 +91,8 @@ struct Model {
   CUtensorMap kvmap8;      // the same with 8-slot boxes
   int attn_R = 1;          // cache chunks per attention work item
   int attn_stages = 1;     // key/value chunks in flight per attention CTA
+  int dec_rows = 0;        // forwards of at most this many rows (<= 4) run as one persistent kernel (k_decode)
+  DecLayer* dlay = nullptr;   // its device table of layer pointers
   float2* rope = nullptr;
   Plan p_qkv, p_o, p_gu, p_d, p_lm;
   Plan u_qkv, u_o, u_gu, u_d, u_lm;   // tcgen05 GEMM plans (forwards of more than 16 rows)
@@ -132,7 +134,8 @@ bool cfg_ok(const sf_model_cfg* c, std::string* why) {
 }
 
 struct Layout {
-  size_t x, ssq, q, apart, upart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, total;
+  size_t x, ssq, q, apart, upart, counters, keys, done, zeros, fx, fh, fo, fa, rope_t, rope_d, state, trace, dh, dbar,
+      dlay_t, dlay_d, total;
   int n_kv_chunks, max_blocks;
 };
 
@@ -233,6 +236,12 @@ Layout make_layout(const sf_model_cfg* t, const sf_model_cfg* d, int B, int K, i
   L.rope_d = d ? take((size_t)s_max * (d->head_dim / 2) * 8) : p;
   L.state = take(state_offsets(B, K, s_max).n_ints * 4);
   L.trace = take((size_t)2 * 8192 * 8);
+  // The persistent decode forward: SwiGLU output of up to 4 rows, its grid
+  // barrier words, and each model's table of layer pointers.
+  L.dh = take((size_t)4 * F * 4);
+  L.dbar = take(16 + (size_t)4 * 64 * 4);   // barrier words + per-(sequence, KV head) counters
+  L.dlay_t = take((size_t)t->layers * sizeof(DecLayer));
+  L.dlay_d = d ? take((size_t)d->layers * sizeof(DecLayer)) : p;
   L.total = p;
   return L;
 }
@@ -253,6 +262,9 @@ struct sf_engine {
   Model tgt, dft;
   bool has_dft = false;
   bool pdl = true;      // programmatic dependent launch between the round's kernels
+  bool dec_on = false;  // SF_PERSISTENT=1: forwards of at most 4 rows run as one persistent kernel
+  float* dh = nullptr;       // persistent decode: SwiGLU output
+  unsigned* dbar = nullptr;  // persistent decode: grid barrier words
   bool expire_waits = false;   // SF_TEST_WAIT_EXPIRE=1: every GEMM reports an expired wait (error-path test)
   unsigned long long* trace = nullptr;     // launch timeline (SF_TRACE=1), kTraceSlots entries
   int trace_next = 0;
@@ -449,7 +461,6 @@ GemmArgs base_args(sf_engine* e, const Model& md, const Plan& p, const RowSet& r
   return a;
 }
 
-constexpr int kTraceSlots = 8192;
 
 // Give the next launch a timeline slot (when tracing) and remember its name.
 RowSet traced(sf_engine* e, RowSet rs, const char* what) {
@@ -499,6 +510,48 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
     a.cluster = p.cluster;
     a.part = e->upart;
   };
+  // At most four rows (a decode step): one persistent kernel for the whole
+  // forward up to the LM head's input.
+  const bool use_dec = e->dec_on && rs.M <= md.dec_rows && rs.rps <= 2 && rs.tree_g == 0 && seq < 0;
+  if (use_dec) {
+    DecArgs d{};
+    d.layers = md.dlay;
+    d.L = c.layers;
+    d.H = H;
+    d.nq = c.n_heads;
+    d.nkv = c.n_kv_heads;
+    d.hd = c.head_dim;
+    d.F = c.ffn;
+    d.vocab = c.vocab;
+    d.embed = static_cast<const bf16*>(md.embed);
+    d.embed_ld = md.embed_ld;
+    d.norm = static_cast<const bf16*>(md.norm);
+    d.eps = c.rms_eps;
+    d.scale = 1.0f / sqrtf((float)c.head_dim);
+    d.rope = md.rope;
+    d.kv = md.kv;
+    d.B = e->B;
+    d.s_max = e->s_max;
+    d.R = 1;
+    d.n_ranges = e->lay.n_kv_chunks;
+    d.x = e->x;
+    d.q = e->q;
+    d.part = e->apart;
+    d.h = e->dh;
+    d.frag = e->fx;
+    d.ssq = e->ssq;
+    d.bar = e->dbar;
+    d.cnt = e->dbar + 4;
+    d.err = e->st.err;
+    d.expire_first_wait = e->expire_waits ? 1 : 0;
+    d.rs = traced(e, rs, "decode");
+    // Timeline slots of the kernel's phases, right after its own (which the
+    // embedding phase stamps).
+    if (e->trace)
+      for (int l = 0; l < c.layers; ++l)
+        for (const char* ph : {"d_qkv", "d_attention", "d_o_proj", "d_gate_up", "d_down"}) traced(e, rs, ph);
+    CK(launch_decode(d, e->num_sms, s));
+  }
   EmbedArgs ea{};
   ea.E = md.embed;
   ea.ld = md.embed_ld;
@@ -511,149 +564,151 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   ea.gain = md.L[0].ln1;
   ea.f32 = f32;
   ea.umma = tc;
-  ea.rs = traced(e, rs, "embed");
-  CK(launch_embed(ea, s, e->pdl));
-  const size_t seq_elems = (size_t)c.n_kv_heads * e->s_max * c.head_dim;   // one sequence's keys of a layer
-  const size_t layer_elems = 2 * e->B * seq_elems;
-  for (int l = 0; l < c.layers; ++l) {
-    const LayerW& lw = md.L[l];
-    bf16* kc = md.kv + (size_t)l * layer_elems;
-    bf16* vc = kc + layer_elems / 2;
-    if (seq >= 0) {
-      kc += seq * seq_elems;
-      vc += seq * seq_elems;
+  if (!use_dec) {
+    ea.rs = traced(e, rs, "embed");
+    CK(launch_embed(ea, s, e->pdl));
+    const size_t seq_elems = (size_t)c.n_kv_heads * e->s_max * c.head_dim;   // one sequence's keys of a layer
+    const size_t layer_elems = 2 * e->B * seq_elems;
+    for (int l = 0; l < c.layers; ++l) {
+      const LayerW& lw = md.L[l];
+      bf16* kc = md.kv + (size_t)l * layer_elems;
+      bf16* vc = kc + layer_elems / 2;
+      if (seq >= 0) {
+        kc += seq * seq_elems;
+        vc += seq * seq_elems;
+      }
+      // q, k, v (+ bias, RoPE, cache append)
+      GemmArgs a = base_args(e, md, tc ? md.u_qkv : md.p_qkv, rs);
+      a.w[0] = lw.w[W_Q];
+      a.w[1] = lw.w[W_K];
+      a.w[2] = lw.w[W_V];
+      maps(a, lw, 0, W_Q);
+      maps(a, lw, 1, W_K);
+      maps(a, lw, 2, W_V);
+      a.nf4 = nf4;
+      a.stages = stages(a);
+      uplan_args(a, tc ? md.u_qkv : md.p_qkv);
+      a.bias[0] = lw.bq;
+      a.bias[1] = lw.bk;
+      a.bias[2] = lw.bv;
+      a.seg_end[0] = QD;
+      a.seg_end[1] = QD + KVD;
+      a.seg_end[2] = QD + 2 * KVD;
+      a.ld[0] = a.ld[1] = a.ld[2] = H;
+      a.nseg = 3;
+      a.N = QD + 2 * KVD;
+      a.K = H;
+      a.in = reinterpret_cast<const uint4*>(e->fx);
+      a.ssq = e->ssq;
+      a.nssq = H / 128;
+      a.inv_k = 1.0f / H;
+      a.out = e->q;
+      a.out_ld = QD;
+      a.q_dim = QD;
+      a.kv_dim = KVD;
+      a.hd = c.head_dim;
+      a.nkv = c.n_kv_heads;
+      a.s_max = e->s_max;
+      a.kc = kc;
+      a.vc = vc;
+      a.rope = md.rope;
+      a.rs = traced(e, rs, "qkv");
+      CK(gemm(a, EPI_QKV));
+      // attention
+      AttnArgs t{};
+      t.kvmap = md.kvmap;
+      t.kvmap8 = md.kvmap8;
+      t.kv_brows = c.n_kv_heads * e->s_max;
+      t.kv_vrows = e->B * t.kv_brows;
+      t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
+      t.R = md.attn_R;
+      // Query tiles per work item, from this launch's rows (a row's result
+      // does not depend on it): every tile of a KV head's queries together, up
+      // to four, one team of warps each.
+      {
+        const int ntiles = (rs.rps * (c.n_heads / c.n_kv_heads) + 15) / 16;
+        t.TG = ntiles >= 3 ? 4 : ntiles;
+      }
+      t.stages = md.attn_stages;
+      t.q = e->q;
+      t.part = e->apart;
+      t.out = e->fo;
+      t.nq = c.n_heads;
+      t.nkv = c.n_kv_heads;
+      t.hd = c.head_dim;
+      t.s_max = e->s_max;
+      t.B = seq >= 0 ? 1 : e->B;
+      t.n_kv_chunks = e->lay.n_kv_chunks;
+      t.scale = 1.0f / sqrtf((float)c.head_dim);
+      t.err = e->st.err;
+      t.umma = tc;
+      t.rs = traced(e, rs, "attention");
+      t.merge_trace_id = traced(e, rs, "merge").trace_id;
+      CK(launch_attention(t, e->num_sms, s, e->pdl));
+      // o-projection + residual
+      a = base_args(e, md, tc ? md.u_o : md.p_o, rs);
+      a.w[0] = lw.w[W_O];
+      maps(a, lw, 0, W_O);
+      a.nf4 = nf4;
+      a.stages = stages(a);
+      uplan_args(a, tc ? md.u_o : md.p_o);
+      a.seg_end[0] = H;
+      a.ld[0] = QD;
+      a.nseg = 1;
+      a.N = H;
+      a.K = QD;
+      a.in = reinterpret_cast<const uint4*>(e->fo);
+      a.out = e->x;
+      a.out_ld = H;
+      a.ssq_out = e->ssq;
+      a.frag_out = e->fh;
+      a.frag_gain = lw.ln2;
+      a.frag_umma = tc;
+      a.rs = traced(e, rs, "o_proj");
+      CK(gemm(a, EPI_RESID));
+      // gate/up + SwiGLU
+      a = base_args(e, md, tc ? md.u_gu : md.p_gu, rs);
+      a.w[0] = lw.w[W_G];
+      a.w[1] = lw.w[W_U];
+      maps(a, lw, 0, W_G);
+      maps(a, lw, 1, W_U);
+      a.nf4 = nf4;
+      a.stages = stages(a);
+      uplan_args(a, tc ? md.u_gu : md.p_gu);
+      a.ld[0] = a.ld[1] = H;
+      a.nseg = 2;
+      a.N = c.ffn;
+      a.K = H;
+      a.in = reinterpret_cast<const uint4*>(e->fh);
+      a.ssq = e->ssq;
+      a.nssq = H / 128;
+      a.inv_k = 1.0f / H;
+      a.frag_out = e->fa;
+      a.frag_umma = tc;
+      a.rs = traced(e, rs, "gate_up");
+      CK(gemm(a, EPI_SWIGLU));
+      // down + residual
+      a = base_args(e, md, tc ? md.u_d : md.p_d, rs);
+      a.w[0] = lw.w[W_D];
+      maps(a, lw, 0, W_D);
+      a.nf4 = nf4;
+      a.stages = stages(a);
+      uplan_args(a, tc ? md.u_d : md.p_d);
+      a.seg_end[0] = H;
+      a.ld[0] = c.ffn;
+      a.nseg = 1;
+      a.N = H;
+      a.K = c.ffn;
+      a.in = reinterpret_cast<const uint4*>(e->fa);
+      a.out = e->x;
+      a.out_ld = H;
+      a.ssq_out = e->ssq;
+      a.frag_out = e->fx;   // the next layer's QKV input, or the LM head's
+      a.frag_gain = l + 1 < c.layers ? md.L[l + 1].ln1 : md.norm;
+      a.frag_umma = tc;   // the next layer's QKV or the LM head, same kernel family
+      a.rs = traced(e, rs, "down");
+      CK(gemm(a, EPI_RESID));
     }
-    // q, k, v (+ bias, RoPE, cache append)
-    GemmArgs a = base_args(e, md, tc ? md.u_qkv : md.p_qkv, rs);
-    a.w[0] = lw.w[W_Q];
-    a.w[1] = lw.w[W_K];
-    a.w[2] = lw.w[W_V];
-    maps(a, lw, 0, W_Q);
-    maps(a, lw, 1, W_K);
-    maps(a, lw, 2, W_V);
-    a.nf4 = nf4;
-    a.stages = stages(a);
-    uplan_args(a, tc ? md.u_qkv : md.p_qkv);
-    a.bias[0] = lw.bq;
-    a.bias[1] = lw.bk;
-    a.bias[2] = lw.bv;
-    a.seg_end[0] = QD;
-    a.seg_end[1] = QD + KVD;
-    a.seg_end[2] = QD + 2 * KVD;
-    a.ld[0] = a.ld[1] = a.ld[2] = H;
-    a.nseg = 3;
-    a.N = QD + 2 * KVD;
-    a.K = H;
-    a.in = reinterpret_cast<const uint4*>(e->fx);
-    a.ssq = e->ssq;
-    a.nssq = H / 128;
-    a.inv_k = 1.0f / H;
-    a.out = e->q;
-    a.out_ld = QD;
-    a.q_dim = QD;
-    a.kv_dim = KVD;
-    a.hd = c.head_dim;
-    a.nkv = c.n_kv_heads;
-    a.s_max = e->s_max;
-    a.kc = kc;
-    a.vc = vc;
-    a.rope = md.rope;
-    a.rs = traced(e, rs, "qkv");
-    CK(gemm(a, EPI_QKV));
-    // attention
-    AttnArgs t{};
-    t.kvmap = md.kvmap;
-    t.kvmap8 = md.kvmap8;
-    t.kv_brows = c.n_kv_heads * e->s_max;
-    t.kv_vrows = e->B * t.kv_brows;
-    t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
-    t.R = md.attn_R;
-    // Query tiles per work item, from this launch's rows (a row's result
-    // does not depend on it): every tile of a KV head's queries together, up
-    // to four, one team of warps each.
-    {
-      const int ntiles = (rs.rps * (c.n_heads / c.n_kv_heads) + 15) / 16;
-      t.TG = ntiles >= 3 ? 4 : ntiles;
-    }
-    t.stages = md.attn_stages;
-    t.q = e->q;
-    t.part = e->apart;
-    t.out = e->fo;
-    t.nq = c.n_heads;
-    t.nkv = c.n_kv_heads;
-    t.hd = c.head_dim;
-    t.s_max = e->s_max;
-    t.B = seq >= 0 ? 1 : e->B;
-    t.n_kv_chunks = e->lay.n_kv_chunks;
-    t.scale = 1.0f / sqrtf((float)c.head_dim);
-    t.err = e->st.err;
-    t.umma = tc;
-    t.rs = traced(e, rs, "attention");
-    t.merge_trace_id = traced(e, rs, "merge").trace_id;
-    CK(launch_attention(t, e->num_sms, s, e->pdl));
-    // o-projection + residual
-    a = base_args(e, md, tc ? md.u_o : md.p_o, rs);
-    a.w[0] = lw.w[W_O];
-    maps(a, lw, 0, W_O);
-    a.nf4 = nf4;
-    a.stages = stages(a);
-    uplan_args(a, tc ? md.u_o : md.p_o);
-    a.seg_end[0] = H;
-    a.ld[0] = QD;
-    a.nseg = 1;
-    a.N = H;
-    a.K = QD;
-    a.in = reinterpret_cast<const uint4*>(e->fo);
-    a.out = e->x;
-    a.out_ld = H;
-    a.ssq_out = e->ssq;
-    a.frag_out = e->fh;
-    a.frag_gain = lw.ln2;
-    a.frag_umma = tc;
-    a.rs = traced(e, rs, "o_proj");
-    CK(gemm(a, EPI_RESID));
-    // gate/up + SwiGLU
-    a = base_args(e, md, tc ? md.u_gu : md.p_gu, rs);
-    a.w[0] = lw.w[W_G];
-    a.w[1] = lw.w[W_U];
-    maps(a, lw, 0, W_G);
-    maps(a, lw, 1, W_U);
-    a.nf4 = nf4;
-    a.stages = stages(a);
-    uplan_args(a, tc ? md.u_gu : md.p_gu);
-    a.ld[0] = a.ld[1] = H;
-    a.nseg = 2;
-    a.N = c.ffn;
-    a.K = H;
-    a.in = reinterpret_cast<const uint4*>(e->fh);
-    a.ssq = e->ssq;
-    a.nssq = H / 128;
-    a.inv_k = 1.0f / H;
-    a.frag_out = e->fa;
-    a.frag_umma = tc;
-    a.rs = traced(e, rs, "gate_up");
-    CK(gemm(a, EPI_SWIGLU));
-    // down + residual
-    a = base_args(e, md, tc ? md.u_d : md.p_d, rs);
-    a.w[0] = lw.w[W_D];
-    maps(a, lw, 0, W_D);
-    a.nf4 = nf4;
-    a.stages = stages(a);
-    uplan_args(a, tc ? md.u_d : md.p_d);
-    a.seg_end[0] = H;
-    a.ld[0] = c.ffn;
-    a.nseg = 1;
-    a.N = H;
-    a.K = c.ffn;
-    a.in = reinterpret_cast<const uint4*>(e->fa);
-    a.out = e->x;
-    a.out_ld = H;
-    a.ssq_out = e->ssq;
-    a.frag_out = e->fx;   // the next layer's QKV input, or the LM head's
-    a.frag_gain = l + 1 < c.layers ? md.L[l + 1].ln1 : md.norm;
-    a.frag_umma = tc;   // the next layer's QKV or the LM head, same kernel family
-    a.rs = traced(e, rs, "down");
-    CK(gemm(a, EPI_RESID));
   }
   if (!lm) return SF_OK;
   GemmArgs a = base_args(e, md, tc ? md.u_lm : md.p_lm, rs);
@@ -869,6 +924,43 @@ sf_status build_loop_graph(sf_engine* e, int mode) {
   return fail(SF_ERR_CUDA, "device loop graph: %s", cudaGetErrorString(last));
 }
 
+// The persistent decode forward for model `md`: shapes it handles (bf16
+// weights; H a multiple of 128 for the LM head's sums of squares; every row
+// of 16-byte pieces; at most 16 query rows of a KV head over two token rows
+// and 2048 (row, dimension) outputs per attention item), the most rows whose
+// shared memory fits in kDecSmemMax, and the device table of its layer pointers.
+constexpr int kDecSmemMax = 200 * 1024;
+
+int decode_smem(const sf_engine* e, const Model& md, int rows) {
+  const sf_model_cfg& c = md.c;
+  return decode_smem_bytes(rows, c.hidden, c.n_heads * c.head_dim, c.ffn, c.head_dim, c.n_heads / c.n_kv_heads, 2,
+                           e->lay.n_kv_chunks);
+}
+
+sf_status setup_decode(sf_engine* e, Model& md, DecLayer* dev, int* smem_need) {
+  const sf_model_cfg& c = md.c;
+  const int group = c.n_heads / c.n_kv_heads;
+  int rows = 4;
+  while (rows > 0 && decode_smem(e, md, rows) > kDecSmemMax) --rows;
+  if (!e->dec_on || rows == 0 || c.wdtype != SF_WDTYPE_BF16 || c.hidden % 128 || c.ffn % 8 || c.head_dim % 8 ||
+      md.embed_ld % 8 || 2 * group > 16 || 2 * group * c.head_dim > 2048 || c.n_kv_heads > 64)
+    return SF_OK;
+  const int smem = decode_smem(e, md, rows);
+  std::vector<DecLayer> t(c.layers);
+  for (int l = 0; l < c.layers; ++l) {
+    const LayerW& lw = md.L[l];
+    auto b = [](const void* p) { return static_cast<const bf16*>(p); };
+    t[l] = DecLayer{b(lw.ln1), b(lw.w[W_Q]), b(lw.w[W_K]), b(lw.w[W_V]), b(lw.bq), b(lw.bk), b(lw.bv),
+                    b(lw.w[W_O]), b(lw.ln2), b(lw.w[W_G]), b(lw.w[W_U]), b(lw.w[W_D])};
+  }
+  CK(cudaMemcpyAsync(dev, t.data(), t.size() * sizeof(DecLayer), cudaMemcpyHostToDevice, e->user));
+  CK(cudaStreamSynchronize(e->user));
+  md.dlay = dev;
+  md.dec_rows = rows;
+  *smem_need = std::max(*smem_need, smem);
+  return SF_OK;
+}
+
 // Copy the report block to pinned memory, wait, and turn device error bits
 // into a status (clearing them).
 sf_status sync_report(sf_engine* e) {
@@ -877,6 +969,9 @@ sf_status sync_report(sf_engine* e) {
   const int err = e->pin[e->so.err - e->so.report];
   if (err) {
     CK(cudaMemsetAsync(e->st.err, 0, sizeof(int), e->user));
+    // A barrier wait that gave up leaves the persistent kernel's barrier
+    // words inconsistent: start them afresh (no kernel is running now).
+    if (err & kErrWait) CK(cudaMemsetAsync(e->dbar, 0, 16 + 4 * 64 * 4, e->user));
     CK(cudaStreamSynchronize(e->user));
     if (err & kErrWait) return fail(SF_ERR_DEVICE, "a kernel's bounded wait expired (device flag %d)", err);
     if (err & kErrNonfinite) return fail(SF_ERR_NONFINITE, "non-finite logits (device flag %d)", err);
@@ -967,6 +1062,10 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   // SF_PDL=0 in the environment launches the kernels without programmatic
   // dependent launch (for comparing the two; results are identical).
   if (const char* v = getenv("SF_PDL")) e->pdl = v[0] != '0';
+  // SF_PERSISTENT=1: forwards of at most four rows run as the persistent
+  // decode kernel instead of the per-projection kernels (measured slower on
+  // GB300 for the draft step: it is kept as an alternative, not the default).
+  if (const char* v = getenv("SF_PERSISTENT")) e->dec_on = v[0] == '1';
   // SF_TEST_WAIT_EXPIRE=1: the first weight-tile wait of every projection
   // gives up at once and reports it (the wait then completes normally), so
   // tests can drive the device error path without stalling a kernel.
@@ -1012,6 +1111,8 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   e->done = reinterpret_cast<int*>(ws + e->lay.done);
   e->zeros = reinterpret_cast<int*>(ws + e->lay.zeros);
   e->tgt.rope = reinterpret_cast<float2*>(ws + e->lay.rope_t);
+  e->dh = reinterpret_cast<float*>(ws + e->lay.dh);
+  e->dbar = reinterpret_cast<unsigned*>(ws + e->lay.dbar);
   if (trace_on) e->trace = reinterpret_cast<unsigned long long*>(ws + e->lay.trace);
   if (dft) e->dft.rope = reinterpret_cast<float2*>(ws + e->lay.rope_d);
   int* S = reinterpret_cast<int*>(ws + e->lay.state);
@@ -1057,8 +1158,17 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
       (ce = cudaStreamCreateWithFlags(&e->cap, cudaStreamNonBlocking)) ||
       (ce = cudaHostAlloc(reinterpret_cast<void**>(&e->pin), e->so.report_ints * sizeof(int) + 64,
                           cudaHostAllocDefault)) ||
+      (ce = cudaMemsetAsync(e->dbar, 0, 16 + 4 * 64 * 4, e->user)) ||
       (ce = cudaStreamSynchronize(e->user)))
     return bail(fail(SF_ERR_CUDA, "sf_create set-up: %s", cudaGetErrorString(ce)));
+  {
+    int smem = 0;
+    sf_status dr = setup_decode(e, e->tgt, reinterpret_cast<DecLayer*>(ws + e->lay.dlay_t), &smem);
+    if (dr == SF_OK && dft) dr = setup_decode(e, e->dft, reinterpret_cast<DecLayer*>(ws + e->lay.dlay_d), &smem);
+    if (dr != SF_OK) return bail(dr);
+    if (smem > 0 && (ce = decode_init(smem)) != cudaSuccess)
+      return bail(fail(SF_ERR_CUDA, "decode_init: %s", cudaGetErrorString(ce)));
+  }
   *out = e;
   return SF_OK;
 }

@@ -51,6 +51,8 @@ struct RowSet {
   int tree_g;          // guesses per candidate of a multi-candidate verify pass; 0: one chain
 };
 
+constexpr int kTraceSlots = 8192;   // launch timeline slots (ring)
+
 // Launch timeline for profiling: CTA 0 stamps the global timer when the
 // kernel starts and when its wait on the preceding kernel returns (that is,
 // when the preceding kernel has finished).

@@ -199,6 +199,38 @@ struct SpecState {
   int B, K, s_max;
 };
 
+// The persistent decode forward (k_decode.cu): bf16 weights of one layer.
+struct DecLayer {
+  const bf16 *ln1, *wq, *wk, *wv, *bq, *bk, *bv, *wo, *ln2, *wg, *wu, *wd;
+};
+struct DecArgs {
+  const DecLayer* layers;   // device array [L]
+  int L, H, nq, nkv, hd, F, vocab;
+  const bf16* embed;
+  int embed_ld;
+  const bf16* norm;         // final RMSNorm gain
+  float eps, scale;
+  const float2* rope;       // [s_max][hd / 2]
+  bf16* kv;                 // the model's cache [L][2][B][nkv][s_max][hd]
+  int B, s_max;
+  RowSet rs;                // M <= 4 rows
+  int R;                    // cache chunks per attention range
+  int n_ranges;             // range stride of `part` (>= ranges of the longest row)
+  float* x;                 // [M][H] residual stream
+  float* q;                 // [M][nq * hd]
+  float* part;              // [M][nq][n_ranges][hd + 2] attention partials
+  float* h;                 // [M][F] SwiGLU output
+  bf16* frag;               // LM-head input, fragment order
+  float* ssq;               // [H / 128][kRows] sums of squares for the LM head
+  unsigned* bar;            // grid barrier {count, generation}
+  unsigned* cnt;            // [B][nkv] attention items finished (zero between launches)
+  int* err;
+  int expire_first_wait;    // test hook: the first barrier reports an expired wait
+};
+int decode_smem_bytes(int MR, int H, int QD, int F, int hd, int group, int rps, int n_ranges);
+cudaError_t decode_init(int max_smem);
+cudaError_t launch_decode(const DecArgs& a, int num_sms, cudaStream_t st);
+
 // Record a message for sf_last_error() and return `s`.
 sf_status set_error(sf_status s, const char* fmt, ...);
 

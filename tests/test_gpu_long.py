@@ -163,9 +163,14 @@ def test_batch8_ragged_long_contexts(pkg):
     assert worst < LOGIT_TOL_BF16
 
 
-def test_05b_shape_stream_over_rounds(pkg):
-    """The 0.5B shape drafting for itself (every guess accepted), four
-    replayed rounds = 36 tokens, scored by the oracle at every position."""
+@pytest.mark.parametrize("persistent", [False, True])
+def test_05b_shape_stream_over_rounds(pkg, monkeypatch, persistent):
+    """The 0.5B shape drafting for itself, scored by the oracle at every
+    position. On the per-projection kernels draft and verify rows agree bit
+    for bit (every guess accepted: four replayed rounds = 36 tokens); with
+    the persistent decode kernel the draft steps agree within rounding, so
+    the round count is printed, not asserted."""
+    monkeypatch.setenv("SF_PERSISTENT", "1" if persistent else "0")
     w = make_weights(QWEN05B, seed=0, device="cuda")
     eng = pkg.SpecEngine(QWEN05B, w, QWEN05B, w, batch=1, K=8, s_max=4096)
     _poison(eng)
@@ -173,7 +178,8 @@ def test_05b_shape_stream_over_rounds(pkg):
     eng.prefill([prompt])
     out, rounds = eng.generate(36)
     eng.close()
-    assert rounds == 4
+    if not persistent:
+        assert rounds == 4
     m = om.Model(QWEN05B, to_cpu(w), memoize=True, rowwise=False)
     n, flips, near = stream_report(m, prompt, out[0].tolist())
     print(f"0.5B shape, {n} tokens over {rounds} rounds: {flips} flips, {near} near-tie positions")

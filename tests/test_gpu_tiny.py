@@ -98,11 +98,12 @@ def test_draft_and_verify_logits_match_oracle(pkg, tiny):
     eng.close()
 
 
-def test_batch_invariance_target_as_its_own_draft(pkg, tiny):
+def test_batch_invariance_target_as_its_own_draft(pkg, tiny, monkeypatch):
     """Draft = the target itself: decode rows (1-2 per launch) and verify rows
     (K+1 per launch) must agree bit for bit, so every guess is accepted. (The
     16-token prompt is prefilled in one 15-row forward, on the same mma.sync
     GEMM as the rounds, so both caches hold the same bits.)"""
+    monkeypatch.setenv("SF_PERSISTENT", "0")   # the per-projection kernels' invariant (the persistent decode kernel has its own arithmetic)
     _, _, gt, _ = tiny
     K = 4
     V = TINY_TARGET.vocab
@@ -120,7 +121,7 @@ def test_batch_invariance_target_as_its_own_draft(pkg, tiny):
     eng.close()
 
 
-def test_batch8_ragged_rows_match_single_sequences(pkg, tiny):
+def test_batch8_ragged_rows_match_single_sequences(pkg, tiny, monkeypatch):
     """Eight sequences whose prompts differ in length, K=8: every verify
     forward has 72 token rows (the tcgen05 GEMM) and the first draft step 16
     (the mma.sync GEMM). Per sequence, the draft logits equal those of the
@@ -131,6 +132,7 @@ def test_batch8_ragged_rows_match_single_sequences(pkg, tiny):
     lengths, committed tokens and cache lengths agree with the batch's own
     guesses and target choices (a brute-force prefix compare); the generated
     streams are the oracle's greedy streams (near ties allowed)."""
+    monkeypatch.setenv("SF_PERSISTENT", "0")   # the per-projection kernels' invariant (the persistent decode kernel has its own arithmetic)
     tw = tiny[0]
     K, B, V = 8, 8, TINY_TARGET.vocab
     lens = [20, 33, 47, 12, 60, 25, 8, 41]
@@ -191,9 +193,10 @@ def test_generate_matches_oracle_greedy(pkg, tiny, K):
     assert int((hist[0] * (np.arange(K + 1) + 1)).sum()) >= 64
 
 
-def test_spec_streams_identical_across_drafters(pkg, tiny):
+def test_spec_streams_identical_across_drafters(pkg, tiny, monkeypatch):
     """Speculation never changes the output: neural K=1, K=4, K=7 and n-gram
     drafting all give the same tokens bit for bit on the GPU."""
+    monkeypatch.setenv("SF_PERSISTENT", "0")   # the per-projection kernels' invariant (the persistent decode kernel has its own arithmetic)
     prompt = uniform_prompt(32, 1024, seed=101).tolist()
     streams = []
     for K in (1, 4, 7):
@@ -252,12 +255,13 @@ def test_rounds_integer_state_and_rollback(pkg, tiny):
     eng.close()
 
 
-def test_rollback_bit_exact_short(pkg, tiny):
+def test_rollback_bit_exact_short(pkg, tiny, monkeypatch):
     """Two rounds from a 6-token prompt keep every forward (prefill, draft
     steps, verify, and the fresh prefill of the committed prefix) at 16 rows
     or fewer, so all run on the same GEMM kernel: after the in-place
     rollback both caches below their lengths equal a fresh prefill of the
     committed prefix bit for bit."""
+    monkeypatch.setenv("SF_PERSISTENT", "0")   # the per-projection kernels' invariant (the persistent decode kernel has its own arithmetic)
     K = 4
     prompt = uniform_prompt(6, 1024, seed=104).tolist()
     eng = make_engine(pkg, tiny, K=K)
@@ -437,18 +441,23 @@ def test_head_shapes_with_poisoned_caches(pkg, name):
     eng.close()
 
 
-def test_round_graph_kernel_count(pkg, tiny):
-    """One replay of the round graph launches: per forward an embedding, six
-    kernels per layer (QKV, attention chunks, merge, O, gate/up, down) and the
-    LM head; K draft forwards, one verify forward and the acceptance kernel
-    (the n-gram round: the lookup kernel instead of the draft forwards)."""
+@pytest.mark.parametrize("persistent", [False, True])
+def test_round_graph_kernel_count(pkg, tiny, monkeypatch, persistent):
+    """One replay of the round graph launches: per forward of more than four
+    rows (the verify) an embedding, six kernels per layer (QKV, attention
+    chunks, merge, O, gate/up, down) and the LM head; per draft step the
+    same, or with the persistent decode kernel two launches (the forward and
+    the LM head); K draft steps, one verify forward and the acceptance kernel
+    (the n-gram round: the lookup kernel instead of the draft steps)."""
+    monkeypatch.setenv("SF_PERSISTENT", "1" if persistent else "0")
     K = 4
     eng = make_engine(pkg, tiny, K=K)
     assert eng.round_launches() == 0          # no round graph yet
     eng.prefill([uniform_prompt(32, 1024, seed=100).tolist()])
     eng.step()
     per_fwd = lambda s: 2 + 6 * s.layers
-    assert eng.round_launches() == K * per_fwd(TINY_DRAFT) + per_fwd(TINY_TARGET) + 1
+    per_draft = 2 if persistent else per_fwd(TINY_DRAFT)
+    assert eng.round_launches() == K * per_draft + per_fwd(TINY_TARGET) + 1
     eng.set_drafter(pkg.SF_DRAFT_NGRAM)
     eng.step()
     assert eng.round_launches() == 1 + per_fwd(TINY_TARGET) + 1
