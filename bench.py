@@ -867,6 +867,7 @@ def main():
     ap.add_argument("--gemm-rows", type=int, default=K_GUESS + 1, help="token rows of --gemm-only")
     ap.add_argument("--nf4-b8-small", action="store_true", help="small case: 2-layer 14B-shape NF4 batch-8 rounds")
     ap.add_argument("--trace", action="store_true", help="launch timeline of a round (needs SF_TRACE=1)")
+    ap.add_argument("--nf4-only", action="store_true", help="only the 14B-shape NF4 workloads (batch 1 and 8)")
     args = ap.parse_args()
     globals()["N_NEW"] = args.tokens
     if args.gemm_only:
@@ -874,6 +875,15 @@ def main():
         return
     if args.nf4_b8_small:
         run_nf4_b8_small(args)
+        return
+    if args.nf4_only:
+        import torch
+        torch.cuda.set_device(0)
+        import __graft_entry__ as g
+        g.build()
+        import greedy_speculative_decoding_gb300 as pkg
+        b1, b8 = nf4_workload(pkg, _peaks()[0])
+        print(json.dumps({"nf4_14b_b1": b1, "nf4_14b_b8": b8}))
         return
     if args.trace:
         run_trace(args)

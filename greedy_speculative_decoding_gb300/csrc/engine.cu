@@ -263,6 +263,7 @@ struct sf_engine {
   bool has_dft = false;
   bool pdl = true;      // programmatic dependent launch between the round's kernels
   bool dec_on = false;  // SF_PERSISTENT=1: forwards of at most 4 rows run as one persistent kernel
+  bool box8 = true;     // SF_KV_BOX8=0: attention loads a partly filled chunk whole
   float* dh = nullptr;       // persistent decode: SwiGLU output
   unsigned* dbar = nullptr;  // persistent decode: grid barrier words
   bool expire_waits = false;   // SF_TEST_WAIT_EXPIRE=1: every GEMM reports an expired wait (error-path test)
@@ -494,7 +495,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
   // inputs the producers write in the tensor-core operand order (the LM head
   // keeps reading fragment order).
   const bool f32 = c.wdtype == SF_WDTYPE_F32;   // fp32 weights: the plain fp32 kernel, fragment order
-  const bool tc = !f32 && rs.M >= umma_min_rows();
+  const bool tc = !f32 && rs.M >= (nf4 ? umma_min_rows_nf4() : umma_min_rows());
   auto gemm = [&](const GemmArgs& a, int epi) {
     if (f32) return launch_gemm_f32(a, epi, s, e->pdl);
     return tc ? launch_umma(a, epi, s, e->pdl) : launch_gemm(a, epi, s, e->pdl);
@@ -618,6 +619,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
       AttnArgs t{};
       t.kvmap = md.kvmap;
       t.kvmap8 = md.kvmap8;
+    t.box8 = e->box8 ? 1 : 0;
       t.kv_brows = c.n_kv_heads * e->s_max;
       t.kv_vrows = e->B * t.kv_brows;
       t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
@@ -1066,6 +1068,10 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   // decode kernel instead of the per-projection kernels (measured slower on
   // GB300 for the draft step: it is kept as an alternative, not the default).
   if (const char* v = getenv("SF_PERSISTENT")) e->dec_on = v[0] == '1';
+  // SF_KV_BOX8=0: the attention kernel loads a sequence's partly filled last
+  // cache chunk whole instead of in 8-slot boxes (for comparing the two;
+  // results are identical).
+  if (const char* v = getenv("SF_KV_BOX8")) e->box8 = v[0] != '0';
   // SF_TEST_WAIT_EXPIRE=1: the first weight-tile wait of every projection
   // gives up at once and reports it (the wait then completes normally), so
   // tests can drive the device error path without stalling a kernel.

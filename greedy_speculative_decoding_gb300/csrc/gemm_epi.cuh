@@ -18,6 +18,11 @@ struct EpiPre {
   float2 cs[kE];
 };
 
+// The epilogues' barrier: the first kGemmThreads threads of the CTA (all of
+// them in the 256-thread kernels; the tcgen05 kernel's NF4 form has four more
+// warps, which do not take part in the epilogue).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kGemmThreads) : "memory"); }
+
 // Rows m < M of the CTA are token rows m0 + m of the forward; pos[m] is the
 // cache slot of row m0 + m (its RoPE position differs for the rows of a
 // multi-candidate verify).
@@ -74,7 +79,7 @@ __device__ void epi_resid(const GemmArgs& a, float* ys, int rb, int m0, int M, i
     }
     ys[i] = v;
   }
-  __syncthreads();
+  epi_sync();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int m = warp; m < M; m += kGemmThreads / 32) {
     float s = 0.f;
@@ -183,9 +188,9 @@ __device__ void epi_argmax(const GemmArgs& a, const float* ys, int rb, int m0, i
     if (lane == 0) atomicMax(a.keys + m0 + m, best);
   }
   __threadfence();
-  __syncthreads();
+  epi_sync();
   if (threadIdx.x == 0) *s_flag = (atomicAdd(a.done, 1) == finishers - 1);
-  __syncthreads();
+  epi_sync();
   if (!*s_flag) return;
   __threadfence();
   if (threadIdx.x < a.rs.M) {

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kAttnThreads, kTG == 4 ? 1 : 2) k_attn_chunks(
     // Slots past the sequence's last row hold nothing of this pass: a partly
     // filled last chunk loads only the 8-slot boxes that hold valid slots.
     const int nvalid = min(kKvChunk, is_it.p_last - is_c * kKvChunk + 1);
-    if (nvalid < kKvChunk) {
+    if (nvalid < kKvChunk && a.box8) {
       const int nb = (nvalid + 7) / 8;
       mbar_expect_tx(&full[s], 2 * kHalf * nb * 8 * 128);
       for (int h = 0; h < kHalf; ++h)
@@ -274,7 +274,9 @@ __global__ void __launch_bounds__(kAttnThreads, kTG == 4 ? 1 : 2) k_attn_chunks(
           *reinterpret_cast<uint4*>(vs + (rem >> 3) * kBox + r * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async();   // ordered before the next copy into this stage
-        __syncthreads();       // and before every tile's P V reads
+        // Ordered before every team's P V reads: by the team's first barrier
+        // when one team is the whole block, else by a block barrier.
+        if (kTG > 1) __syncthreads();
       }
       if (ti < nt) {
         const bf16* qht = sq + (2 * ti) * 16 * HP;

@@ -1,7 +1,8 @@
 // The weight-streaming GEMM on the tcgen05 tensor cores, for forwards of more
 // than 16 token rows (the verify pass of a batch of sequences, prefill
-// chunks): y[m][n] = sum_k x[m][k] W[n][k] for every token row m (up to
-// SF_MAX_ROWS) in one CTA per (128 weight rows, K slice).
+// chunks) and for every forward with NF4 weights: y[m][n] = sum_k x[m][k]
+// W[n][k] for every token row m (up to SF_MAX_ROWS) in one CTA per (128
+// weight rows, K slice).
 //
 // The mma.sync kernel (k_gemm.cu) covers at most 16 token rows per CTA, so a
 // 72-row verify ran as five row groups that each streamed (from L2) and, for
@@ -10,7 +11,7 @@
 // token (bf16 activations; rounded up to a multiple of 16), accumulated in
 // tensor memory, so every weight tile is read and dequantised once.
 //
-// Warp roles, 256 threads:
+// Warp roles, 256 threads (bf16 weights) or 384 (NF4):
 //   thread 0      producer: weight tiles by TMA (two 64-row boxes, 128-byte
 //                 swizzle) or NF4 code tiles + block scales, and the token
 //                 operand of each 64-k chunk by one bulk copy (the producers
@@ -18,18 +19,21 @@
 //                 the MMA reads: umma_index in sf_common.cuh);
 //   thread 32     MMA issuer: four tcgen05.mma (K = 16 each) per chunk,
 //                 tcgen05.commit to the stage's "empty" barrier;
-//   warps 4-7     NF4 only: dequantise each chunk's codes (thread r = weight
-//                 row r: one lookup of a per-lane table of bf16 level pairs
-//                 and one bf16x2 multiply by the block scale per two codes)
-//                 and write the bf16 tile straight into tensor memory
-//                 (tcgen05.st), four chunks deep; the MMA reads A from there;
-//   warps 4-7     afterwards: read the accumulator (tcgen05.ld, one weight row
-//                 per thread, one column per token) and write the CTA's tile
+//   warps 4-11    NF4 only: dequantise each chunk's codes (thread r of warps
+//                 4-7 and of warps 8-11 = weight row r, the first group the
+//                 chunk's elements 0-31, the second 32-63: one lookup of a
+//                 per-lane table of bf16 level pairs and one bf16x2 multiply
+//                 by the block scale per two codes) and write the bf16 tile
+//                 straight into tensor memory (tcgen05.st), four chunks deep;
+//                 the MMA reads A from there;
+//   warps 4-7(11) afterwards: read the accumulator (tcgen05.ld, one weight
+//                 row per thread, one column per token; NF4: the two groups
+//                 take alternate 16-column blocks) and write the CTA's tile
 //                 ys[m][128] in shared memory.
-// Then all 256 threads sum the K slices (thread-block cluster, rank 0 reads
-// the other ranks' tiles; or global partial tiles and an arrival counter),
-// apply the RMSNorm row factor and run the same epilogues as k_gemm, one
-// 16-row group at a time.
+// Then all threads sum the K slices (thread-block cluster, rank 0 reads the
+// other ranks' tiles; or global partial tiles and an arrival counter) and
+// apply the RMSNorm row factor; the first 256 run the same epilogues as
+// k_gemm, one 16-row group at a time.
 #include <algorithm>
 #include <cstdlib>
 #include <mutex>
@@ -42,7 +46,9 @@ namespace sf {
 namespace {
 
 constexpr uint32_t kUWaitIters = 1u << 24;
-constexpr int kUThreads = 256;
+constexpr int kUThreads = 256;              // bf16 weights
+constexpr int kUThreadsNf4 = 384;           // NF4: eight dequantising warps
+template <bool NF4> __host__ __device__ constexpr int uthreads() { return NF4 ? kUThreadsNf4 : kUThreads; }
 constexpr int kUMaxStages = 6;
 constexpr int kATileBytes = 128 * 128;      // 128 weight rows x 64 k bf16 (also 128 rows x 256 k of NF4 codes)
 constexpr int kUScaleBytes = 128 * 16;      // NF4: 128 rows x 8 fp16 block scales
@@ -90,7 +96,8 @@ __device__ __forceinline__ void block_rows(const GemmArgs& a, int rb, int* seg_l
 }  // namespace
 
 template <int EPI, bool NF4>
-__global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ GemmArgs a) {
+__global__ void __launch_bounds__(uthreads<NF4>(), 2) k_umma(const __grid_constant__ GemmArgs a) {
+  constexpr int kThr = uthreads<NF4>();
   extern __shared__ unsigned char usmem_raw[];
   unsigned char* base = usmem_raw + ((1024 - (smem_u32(usmem_raw) & 1023)) & 1023);
   __shared__ USmem sm;
@@ -136,10 +143,10 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     }
     for (int s = 0; s < kCodeStages; ++s) {
       mbar_init(&sm.cfull[s], 1);
-      mbar_init(&sm.cempty[s], 4);   // one arrival per dequantising warp
+      mbar_init(&sm.cempty[s], 8);   // one arrival per dequantising warp
     }
     for (int s = 0; s < kDeqStages; ++s) {
-      mbar_init(&sm.afull[s], 4);
+      mbar_init(&sm.afull[s], 8);
       mbar_init(&sm.aempty[s], 1);
     }
     mbar_init(&sm.acc, 1);
@@ -148,7 +155,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
   // An odd tile count leaves the last tile of every token stage unwritten by
   // the copies: it reads as zero columns.
   if (Tp > T)
-    for (int i = tid; i < S * 64; i += kUThreads)
+    for (int i = tid; i < S * 64; i += kThr)
       reinterpret_cast<uint4*>(btile_p(i / 64) + (size_t)T * 1024)[i % 64] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async();
   // Token positions (QKV epilogue), read before the wait: lengths are never
@@ -156,7 +163,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
   if (EPI == EPI_QKV && tid < M) sm.pos[tid] = row_slot(a.rs, tid);
   if (NF4) {
     // Entry b of lane l at 32 b + l: every lookup of a warp hits its own bank.
-    for (int i = tid; i < 256 * 32; i += kUThreads) {
+    for (int i = tid; i < 256 * 32; i += kThr) {
       const int b = i >> 5;
       lut[i] = pack_bf16x2(__float2bfloat16_rn(c_levels[b & 15]), __float2bfloat16_rn(c_levels[b >> 4]));
     }
@@ -253,34 +260,32 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     }
     umma_commit(&sm.acc);
   } else if (NF4 && warp >= 4) {
-    // ---- dequantisers: thread r owns weight row r = tensor-memory lane r
-    const int r = tid - 128;
+    // ---- dequantisers: warps 4-7 and 8-11; thread r of a group owns weight
+    // row r = tensor-memory lane r, the first group columns 0-15 of every
+    // chunk (elements 0-31), the second columns 16-31 (elements 32-63).
+    const int quarter = warp & 3, h = (warp - 4) >> 2;
+    const int r = 32 * quarter + lane;
     const int sw = r & 7;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     for (int st = 0; st < nch; ++st) {
       const int q = st >> 2, sub = st & 3, cs = q % kCodeStages, ds = st % kDeqStages;
       if (sub == 0 && !mbar_wait(&sm.cfull[cs], (q / kCodeStages) & 1, kUWaitIters)) timed_out = true;
       if (!mbar_wait(&sm.aempty[ds], ((st / kDeqStages) + 1) & 1, kUWaitIters)) timed_out = true;
       tc_fence_after();
       const unsigned char* crow = ctile(cs) + (r >> 3) * 1024 + sw * 128;
-      const uint4 b0 = *reinterpret_cast<const uint4*>(crow + (((2 * sub) ^ sw) << 4));
-      const uint4 b1 = *reinterpret_cast<const uint4*>(crow + (((2 * sub + 1) ^ sw) << 4));
+      const uint4 bw = *reinterpret_cast<const uint4*>(crow + (((2 * sub + h) ^ sw) << 4));
       const __half* sc = reinterpret_cast<const __half*>(ctile(cs) + kATileBytes) + r * 8;
       const bf16 sb = __float2bfloat16_rn(__half2float(sc[(c0 + st) & 7]));
       const uint32_t scale2 = pack_bf16x2(sb, sb);
-      // Column j of the chunk: elements 2j (low nibble of code byte j) and
-      // 2j + 1; written in two halves of 16 columns.
+      // Column j of the chunk: elements 2j (low nibble of code byte j) and 2j + 1.
+      const uint32_t cw[4] = {bw.x, bw.y, bw.z, bw.w};
+      const uint32_t* lut_l = lut + lane;
+      uint32_t av[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 bw = h ? b1 : b0;
-        const uint32_t cw[4] = {bw.x, bw.y, bw.z, bw.w};
-        uint32_t a[16];
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) a[4 * c + e] = bf16x2_mul(lut[(((cw[c] >> (8 * e)) & 255u) << 5) + lane], scale2);
-        tmem_st16(lane_addr + kAccCols + 32 * ds + 16 * h, a);
-      }
+        for (int e = 0; e < 4; ++e) av[4 * c + e] = bf16x2_mul(lut_l[((cw[c] >> (8 * e)) & 255u) << 5], scale2);
+      tmem_st16(lane_addr + kAccCols + 32 * ds + 16 * h, av);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -291,16 +296,18 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     }
   }
 
-  // ---- accumulator -> ys[m][128] (warps 4-7: lane 32 * (warp - 4) + lane = weight row)
+  // ---- accumulator -> ys[m][128] (warps 4-7, and 8-11 with NF4 taking every
+  // other 16 columns: lane 32 * (warp % 4) + lane = weight row)
   if (warp >= 4) {
     if (!mbar_wait(&sm.acc, 0, kUWaitIters)) {
       timed_out = true;
       mbar_wait(&sm.acc, 0, kUWaitIters);
     }
     tc_fence_after();
-    const int row = 32 * (warp - 4) + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
-    for (int c16 = 0; c16 < N / 16; ++c16) {
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int ngroups = kThr / 128 - 1;   // drain groups of four warps: 1 (bf16) or 2 (NF4)
+    for (int c16 = (warp - 4) >> 2; c16 < N / 16; c16 += ngroups) {
       uint32_t v[16];
       tmem_ld16(taddr + 16 * c16, v);
       tmem_ld_wait();
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
 
   // ---- RMSNorm row factors 1 / rms(x_m)
   if (a.ssq)
-    for (int m = warp; m < M; m += kUThreads / 32) {
+    for (int m = warp; m < M; m += kThr / 32) {
       float sq = (lane < a.nssq ? a.ssq[lane * kRows + m] : 0.f) + (lane + 32 < a.nssq ? a.ssq[(lane + 32) * kRows + m] : 0.f);
       sq = warp_sum(sq);
       if (lane == 0) sm.rinv[m] = 1.0f / sqrtf(sq * a.inv_k + a.eps);
@@ -354,7 +361,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     const uint32_t ys_s = smem_u32(ys);
     for (int g = (int)rank; g < G; g += a.nsplit) {
       const int m0 = g * kGroupRows, Mg = min(kGroupRows, M - m0);
-      for (int i = tid; i < Mg * (kBlockRows / 4); i += kUThreads) {
+      for (int i = tid; i < Mg * (kBlockRows / 4); i += kThr) {
         const int e = m0 * (kBlockRows / 4) + i;   // float4 index in the tile
         float4 v[8];
 #pragma unroll
@@ -380,12 +387,13 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
       }
     }
     __syncthreads();
-    for (int g = (int)rank; g < G; g += a.nsplit) epilogue(g * kGroupRows);
+    if (tid < kGemmThreads)   // the epilogues' own barriers count kGemmThreads threads
+      for (int g = (int)rank; g < G; g += a.nsplit) epilogue(g * kGroupRows);
     cluster_sync();
     return;
   }
   if (a.nsplit > 1) {
-    for (int i = tid; i < nel; i += kUThreads) {
+    for (int i = tid; i < nel; i += kThr) {
       const int m = i / kBlockRows, g = m / kGroupRows;
       __stcg(a.part + (((size_t)(rb * G + g) * a.nsplit + sp) * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
                  (i - m * kBlockRows),
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     // The last CTA of the row block adds the slices in order, 16-byte loads
     // of up to eight slices in flight at once.
     const int n4 = nel / 4;
-    for (int i = tid; i < n4; i += kUThreads) {
+    for (int i = tid; i < n4; i += kThr) {
       const int m = (4 * i) / kBlockRows, g = m / kGroupRows;
       const float4* src = reinterpret_cast<const float4*>(
           a.part + ((size_t)(rb * G + g) * a.nsplit * kGroupRows + (m - g * kGroupRows)) * kBlockRows +
@@ -425,10 +433,11 @@ __global__ void __launch_bounds__(kUThreads, 2) k_umma(const __grid_constant__ G
     }
     if (tid == 0) a.counter[rb * G] = 0;
   } else if (a.ssq) {
-    for (int i = tid; i < nel; i += kUThreads) ys[i] *= sm.rinv[i / kBlockRows];
+    for (int i = tid; i < nel; i += kThr) ys[i] *= sm.rinv[i / kBlockRows];
   }
   __syncthreads();
-  for (int m0 = 0; m0 < M; m0 += kGroupRows) epilogue(m0);
+  if (tid < kGemmThreads)   // the epilogues' own barriers count kGemmThreads threads
+    for (int m0 = 0; m0 < M; m0 += kGroupRows) epilogue(m0);
 }
 
 // Dynamic shared memory of a launch (plus 1 KB for the 1024-byte alignment).
@@ -454,7 +463,7 @@ template <int EPI, bool NF4>
 static cudaError_t launch_ut(const GemmArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nblocks * a.nsplit);
-  cfg.blockDim = dim3(kUThreads);
+  cfg.blockDim = dim3(uthreads<NF4>());
   cfg.dynamicSmemBytes = umma_smem_bytes(a.rs.M, a.stages, NF4);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -495,6 +504,19 @@ int umma_min_rows() {
   static const int v = [] {
     const char* e = getenv("SF_UMMA_MIN_ROWS");
     const int n = e ? atoi(e) : kGroupRows + 1;
+    return n < 1 ? 1 : (n > kRows + 1 ? kRows + 1 : n);
+  }();
+  return v;
+}
+
+// The same threshold for forwards with NF4 weights (SF_UMMA_MIN_ROWS_NF4).
+// Default 1: every NF4 forward dequantises each weight tile once into tensor
+// memory (the batch-1 14B-shape NF4 verify: 7.2 ms against 8.6 ms on the
+// mma.sync kernel on GB300).
+int umma_min_rows_nf4() {
+  static const int v = [] {
+    const char* e = getenv("SF_UMMA_MIN_ROWS_NF4");
+    const int n = e ? atoi(e) : 1;
     return n < 1 ? 1 : (n > kRows + 1 ? kRows + 1 : n);
   }();
   return v;
@@ -541,7 +563,7 @@ cudaError_t umma_init() {
 int umma_max_clusters(int csize, int M, int stages, bool nf4) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize * 512);
-  cfg.blockDim = dim3(kUThreads);
+  cfg.blockDim = dim3(nf4 ? kUThreadsNf4 : kUThreads);
   cfg.dynamicSmemBytes = umma_smem_bytes(M, stages, nf4);
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;

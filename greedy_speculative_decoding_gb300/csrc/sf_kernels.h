@@ -119,6 +119,7 @@ cudaError_t launch_gemm(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
 // block are one cluster (at most 8) or use `part` / `counter`.
 cudaError_t launch_umma(const GemmArgs& a, int epi, cudaStream_t st, bool pdl);
 int umma_min_rows();
+int umma_min_rows_nf4();
 cudaError_t umma_init();
 int umma_smem_bytes(int M, int stages, bool nf4);
 int umma_stages(int M, bool nf4);
@@ -154,6 +155,7 @@ struct AttnArgs {
   // values kv_vrows rows further.
   CUtensorMap kvmap;
   CUtensorMap kvmap8;      // the same with 8-slot boxes: a sequence's partly filled last chunk
+  int box8;                // 1: load a partly filled last chunk in 8-slot boxes
   int kv_row0, kv_brows, kv_vrows;
   int R;                   // cache chunks per work item (one partial result per R chunks)
   int TG;                  // 16-query tiles per work item (1..4)
