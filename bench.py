@@ -528,6 +528,32 @@ def run_nf4_b8_small(args):
     print(json.dumps({"nf4_b8_small": True, "contexts": [int(n) for n in ctx]}))
 
 
+def run_verify_small(args):
+    """Small case for kernel profiling of the batch-1 verify: the 7B shape
+    with 2 layers (about 2.6 GB on the device), the cache prefilled to 2048
+    tokens, prompt-lookup rounds of 9 verify rows; the last two rounds run
+    inside the NVTX range "round"."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__ as g
+    g.build()
+    import greedy_speculative_decoding_gb300 as pkg
+    from synth import QWEN7B, make_weights, uniform_prompt
+    shape = QWEN7B.with_(layers=2)
+    w = make_weights(shape, seed=0, device="cuda")
+    eng = pkg.SpecEngine(shape, w, batch=1, K=K_GUESS, s_max=S_MAX)
+    eng.prefill([uniform_prompt(VERIFY_CTX, shape.vocab, seed=103).numpy()])
+    eng.step()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        torch.cuda.nvtx.range_push("round")
+        eng.step()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    eng.close()
+    print(json.dumps({"verify_small": True, "ctx": VERIFY_CTX}))
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -868,6 +894,7 @@ def main():
     ap.add_argument("--nf4-b8-small", action="store_true", help="small case: 2-layer 14B-shape NF4 batch-8 rounds")
     ap.add_argument("--trace", action="store_true", help="launch timeline of a round (needs SF_TRACE=1)")
     ap.add_argument("--nf4-only", action="store_true", help="only the 14B-shape NF4 workloads (batch 1 and 8)")
+    ap.add_argument("--verify-small", action="store_true", help="small case: 2-layer 7B-shape verify rounds at 2048")
     args = ap.parse_args()
     globals()["N_NEW"] = args.tokens
     if args.gemm_only:
@@ -875,6 +902,9 @@ def main():
         return
     if args.nf4_b8_small:
         run_nf4_b8_small(args)
+        return
+    if args.verify_small:
+        run_verify_small(args)
         return
     if args.nf4_only:
         import torch

@@ -91,6 +91,7 @@ struct Model {
   CUtensorMap kvmap8;      // the same with 8-slot boxes
   int attn_R = 1;          // cache chunks per attention work item
   int attn_stages = 1;     // key/value chunks in flight per attention CTA
+  bool attn_group = false; // attention items carry up to four query tiles (else one)
   int dec_rows = 0;        // forwards of at most this many rows (<= 4) run as one persistent kernel (k_decode)
   DecLayer* dlay = nullptr;   // its device table of layer pointers
   float2* rope = nullptr;
@@ -263,7 +264,7 @@ struct sf_engine {
   bool has_dft = false;
   bool pdl = true;      // programmatic dependent launch between the round's kernels
   bool dec_on = false;  // SF_PERSISTENT=1: forwards of at most 4 rows run as one persistent kernel
-  bool box8 = true;     // SF_KV_BOX8=0: attention loads a partly filled chunk whole
+  bool box8 = false;    // SF_KV_BOX8=1: attention loads a partly filled chunk in 8-slot boxes
   float* dh = nullptr;       // persistent decode: SwiGLU output
   unsigned* dbar = nullptr;  // persistent decode: grid barrier words
   bool expire_waits = false;   // SF_TEST_WAIT_EXPIRE=1: every GEMM reports an expired wait (error-path test)
@@ -359,10 +360,14 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     // small; up to 8 for a large batch of long caches, so the items fill the
     // GPU a few times over and the merge reads a few partials per row. Fixed
     // per model and engine: a row's arithmetic never depends on other rows.
-    // The same load decides how many chunks a CTA keeps in flight.
+    // The same load decides how many chunks a CTA keeps in flight, and
+    // whether an item carries every query tile of its KV head (each chunk
+    // read once) or one tile (more items for a small batch: the same work
+    // spread over more CTAs; measured faster for the batch-1 verify).
     const long load = (long)e->B * c->n_kv_heads * (e->s_max / kKvChunk) / 2048;
     md.attn_R = load >= 8 ? 8 : (load >= 4 ? 4 : (load >= 2 ? 2 : 1));
     md.attn_stages = load >= 2 ? 2 : 1;
+    md.attn_group = load >= 2;
   }
   const int H = c->hidden;
   const int QD = c->n_heads * c->head_dim, KVD = c->n_kv_heads * c->head_dim, F = c->ffn;
@@ -624,12 +629,12 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
       t.kv_vrows = e->B * t.kv_brows;
       t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
       t.R = md.attn_R;
-      // Query tiles per work item, from this launch's rows (a row's result
-      // does not depend on it): every tile of a KV head's queries together, up
-      // to four, one team of warps each.
+      // Query tiles per work item (a row's result does not depend on it):
+      // one, or every tile of a KV head's queries together, up to four, one
+      // team of warps each.
       {
         const int ntiles = (rs.rps * (c.n_heads / c.n_kv_heads) + 15) / 16;
-        t.TG = ntiles >= 3 ? 4 : ntiles;
+        t.TG = !md.attn_group ? 1 : (ntiles >= 3 ? 4 : ntiles);
       }
       t.stages = md.attn_stages;
       t.q = e->q;
@@ -1068,10 +1073,10 @@ sf_status sf_create(const sf_model_cfg* tgt, const void* const* tgt_w, const sf_
   // decode kernel instead of the per-projection kernels (measured slower on
   // GB300 for the draft step: it is kept as an alternative, not the default).
   if (const char* v = getenv("SF_PERSISTENT")) e->dec_on = v[0] == '1';
-  // SF_KV_BOX8=0: the attention kernel loads a sequence's partly filled last
-  // cache chunk whole instead of in 8-slot boxes (for comparing the two;
-  // results are identical).
-  if (const char* v = getenv("SF_KV_BOX8")) e->box8 = v[0] != '0';
+  // SF_KV_BOX8=1: the attention kernel loads a sequence's partly filled last
+  // cache chunk in 8-slot boxes instead of whole (results are identical;
+  // measured slightly slower on GB300, so off by default).
+  if (const char* v = getenv("SF_KV_BOX8")) e->box8 = v[0] == '1';
   // SF_TEST_WAIT_EXPIRE=1: the first weight-tile wait of every projection
   // gives up at once and reports it (the wait then completes normally), so
   // tests can drive the device error path without stalling a kernel.

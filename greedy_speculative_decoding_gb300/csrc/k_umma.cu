@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(uthreads<NF4>(), 2) k_umma(const __grid_consta
     const int r = 32 * quarter + lane;
     const int sw = r & 7;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    const uint32_t lut_lane = smem_u32(lut) + 4 * lane;
     for (int st = 0; st < nch; ++st) {
       const int q = st >> 2, sub = st & 3, cs = q % kCodeStages, ds = st % kDeqStages;
       if (sub == 0 && !mbar_wait(&sm.cfull[cs], (q / kCodeStages) & 1, kUWaitIters)) timed_out = true;
@@ -277,14 +278,19 @@ __global__ void __launch_bounds__(uthreads<NF4>(), 2) k_umma(const __grid_consta
       const __half* sc = reinterpret_cast<const __half*>(ctile(cs) + kATileBytes) + r * 8;
       const bf16 sb = __float2bfloat16_rn(__half2float(sc[(c0 + st) & 7]));
       const uint32_t scale2 = pack_bf16x2(sb, sb);
-      // Column j of the chunk: elements 2j (low nibble of code byte j) and 2j + 1.
+      // Column j of the chunk: elements 2j (low nibble of code byte j) and
+      // 2j + 1. Table entry b of this lane at shared address lut_lane + 128 b.
       const uint32_t cw[4] = {bw.x, bw.y, bw.z, bw.w};
-      const uint32_t* lut_l = lut + lane;
       uint32_t av[16];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) av[4 * c + e] = bf16x2_mul(lut_l[((cw[c] >> (8 * e)) & 255u) << 5], scale2);
+        for (int e = 0; e < 4; ++e) {
+          uint32_t idx, v;
+          asm("bfe.u32 %0, %1, %2, 8;" : "=r"(idx) : "r"(cw[c]), "r"(8 * e));
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(lut_lane + (idx << 7)));
+          av[4 * c + e] = bf16x2_mul(v, scale2);
+        }
       tmem_st16(lane_addr + kAccCols + 32 * ds + 16 * h, av);
       tmem_st_wait();
       tc_fence_before();
