@@ -368,6 +368,10 @@ sf_status bind_model(sf_engine* e, Model& md, const sf_model_cfg* c, const void*
     md.attn_R = load >= 8 ? 8 : (load >= 4 ? 4 : (load >= 2 ? 2 : 1));
     md.attn_stages = load >= 2 ? 2 : 1;
     md.attn_group = load >= 2;
+    // SF_ATTN_R (chunks per range, 1..16) and SF_ATTN_STAGES (1 or 2)
+    // override the choice, for tuning; results depend on R only.
+    if (const char* v = getenv("SF_ATTN_R")) md.attn_R = std::min(16, std::max(1, atoi(v)));
+    if (const char* v = getenv("SF_ATTN_STAGES")) md.attn_stages = atoi(v) == 2 ? 2 : 1;
   }
   const int H = c->hidden;
   const int QD = c->n_heads * c->head_dim, KVD = c->n_kv_heads * c->head_dim, F = c->ffn;
