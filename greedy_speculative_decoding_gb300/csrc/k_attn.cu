@@ -183,8 +183,9 @@ __global__ void __launch_bounds__(kAttnThreads, kTG == 4 ? 1 : 2) k_attn_chunks(
     unsigned char* st = base + s * kStage;
     fence_proxy_async();
     const int row = kv_row(is_it, is_c);
-    // Slots past the sequence's last row hold nothing of this pass: a partly
-    // filled last chunk loads only the 8-slot boxes that hold valid slots.
+    // Slots past the sequence's last row hold nothing of this pass: with
+    // box8 a partly filled last chunk loads only the 8-slot boxes that hold
+    // valid slots.
     const int nvalid = min(kKvChunk, is_it.p_last - is_c * kKvChunk + 1);
     if (nvalid < kKvChunk && a.box8) {
       const int nb = (nvalid + 7) / 8;
@@ -227,19 +228,34 @@ __global__ void __launch_bounds__(kAttnThreads, kTG == 4 ? 1 : 2) k_attn_chunks(
     // The item's query tiles -> shared memory as bf16 hi + lo pairs (rows
     // past Mq are zero); the running max and sum start empty.
     {
+      // All of a thread's query loads in flight at once, then the splits.
+      constexpr int kQB = (kTG * 16 * (HD / 4) + kAttnThreads - 1) / kAttnThreads;
       const int n4 = nt * 16 * (HD / 4);
-      for (int i = tid; i < n4; i += kAttnThreads) {
+      float4 qv[kQB];
+#pragma unroll
+      for (int e = 0; e < kQB; ++e) {
+        const int i = tid + e * kAttnThreads;
+        qv[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n4) {
+          const int qt = i / (16 * (HD / 4)), rem = i - qt * (16 * (HD / 4));
+          const int qr = rem / (HD / 4), u = rem - qr * (HD / 4);
+          const int qi = (t0 + qt) * 16 + qr;
+          if (qi < Mq) {
+            const int j = qi / group, hh = qi - j * group;
+            qv[e] = *reinterpret_cast<const float4*>(a.q + ((size_t)(it.b * rps + j) * a.nq + it.kvh * group + hh) * HD +
+                                                     4 * u);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kQB; ++e) {
+        const int i = tid + e * kAttnThreads;
+        if (i >= n4) break;
         const int qt = i / (16 * (HD / 4)), rem = i - qt * (16 * (HD / 4));
         const int qr = rem / (HD / 4), u = rem - qr * (HD / 4);
-        const int qi = (t0 + qt) * 16 + qr;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qi < Mq) {
-          const int j = qi / group, hh = qi - j * group;
-          v = *reinterpret_cast<const float4*>(a.q + ((size_t)(it.b * rps + j) * a.nq + it.kvh * group + hh) * HD + 4 * u);
-        }
         uint2 h, l;
-        split_bf16x2(v.x, v.y, h.x, l.x);
-        split_bf16x2(v.z, v.w, h.y, l.y);
+        split_bf16x2(qv[e].x, qv[e].y, h.x, l.x);
+        split_bf16x2(qv[e].z, qv[e].w, h.y, l.y);
         *reinterpret_cast<uint2*>(sq + ((2 * qt) * 16 + qr) * HP + 4 * u) = h;
         *reinterpret_cast<uint2*>(sq + ((2 * qt + 1) * 16 + qr) * HP + 4 * u) = l;
       }
@@ -445,6 +461,246 @@ __global__ void __launch_bounds__(kAttnThreads, kTG == 4 ? 1 : 2) k_attn_chunks(
   }
 }
 
+// One-chunk, one-tile items (a small cache load: R = 1, TG = 1) without the
+// TMA ring: work item = (sequence b, KV head, 64-slot chunk c, 16-query tile
+// qt); the chunk's keys and values come into padded shared-memory rows with
+// 16-byte asynchronous copies issued by every thread (slots past the last
+// row's position are zero-filled instead: a zero probability times a stale
+// NaN would still be NaN), the first item's before the wait on the
+// producing kernel when the chunk holds no slot of this pass. Per tile, the
+// same arithmetic as k_attn_chunks with one team of eight warps and an empty
+// running state: S by eight keys per warp (Q as bf16 hi + lo, four
+// accumulation chains), the chunk's row max and the 8-key sums combined in
+// warp order, P (hi + lo) through shared memory, warp w producing output
+// dimensions w*HD/8 .. from all 64 keys. Measured faster than the ring
+// kernel for these launches (the draft step's and the batch-1 verify's).
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk1(const __grid_constant__ AttnArgs a) {
+  constexpr int KP = HD * 2 + 32;   // key row pitch (bytes): 8-bank shift per row for the 8-byte fragment loads
+  constexpr int VP = HD * 2 + 16;   // value row pitch: 4-bank shift per row for ldmatrix
+  constexpr int KS = HD / 16;       // k-steps over the head dimension
+  constexpr int NTW = HD / 64;      // output n-tiles (8 dimensions each) per warp
+  constexpr int HP = HD + 16;       // query hi / lo row pitch (bf16)
+  constexpr int PP = kKvChunk + 8;  // probability tile row pitch (bf16)
+  constexpr int kPieces = kKvChunk * HD / 8;   // 16-byte pieces of a chunk's keys (and of its values)
+  static_assert(kAttnThreads == 256 && kKvChunk == 64, "eight warps of eight keys");
+  extern __shared__ __align__(128) unsigned char attn1_smem[];
+  unsigned char* ks = attn1_smem;                                  // [64][KP]
+  unsigned char* vs = ks + kKvChunk * KP;                          // [64][VP]
+  bf16* sph = reinterpret_cast<bf16*>(vs + kKvChunk * VP);         // [16][PP] P hi
+  bf16* spl = sph + 16 * PP;                                       // [16][PP] P lo
+  bf16* sqh = spl + 16 * PP;                                       // [16][HP] queries of the tile, hi
+  bf16* sql = sqh + 16 * HP;                                       // [16][HP] queries of the tile, lo
+  __shared__ float red_mx[8][16], red_l[8][16];
+
+  trace_mark(a.rs, 0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c4 = lane & 3;
+  const int group = a.nq / a.nkv;
+  const int rps = a.rs.rps;
+  const int Mq = rps * group;
+  const int ntiles = (Mq + 15) / 16;
+  // Lengths and the cache slots below this pass's first position may be
+  // read before the wait (see k_attn_chunks).
+  int total = 0;
+  for (int b = 0; b < a.B; ++b) {
+    const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
+    total += a.nkv * (p_last / kKvChunk + 1) * ntiles;
+  }
+  auto locate = [&](int item, int& b, int& kvh, int& c, int& qt) {
+    int rest = item, nch = 0;
+    for (b = 0; b < a.B; ++b) {
+      const int p_last = a.rs.pos_base[b] + a.rs.pos_off + rps - 1;
+      nch = p_last / kKvChunk + 1;
+      if (rest < a.nkv * nch * ntiles) break;
+      rest -= a.nkv * nch * ntiles;
+    }
+    kvh = rest / (nch * ntiles);
+    rest -= kvh * nch * ntiles;
+    c = rest / ntiles;
+    qt = rest - c * ntiles;
+  };
+  // Copy slots [0, nvalid) of the chunk; zero the rest of the tile.
+  auto issue = [&](int b, int kvh, int c, int nvalid) {
+    const size_t off = (((size_t)b * a.nkv + kvh) * a.s_max + (size_t)c * kKvChunk) * HD;
+    for (int i = tid; i < kPieces; i += kAttnThreads) {
+      const int r = i / (HD / 8), u = i - r * (HD / 8);
+      if (r < nvalid) {
+        cp_async16(ks + r * KP + 16 * u, a.kc + off + (size_t)r * HD + 8 * u);
+        cp_async16(vs + r * VP + 16 * u, a.vc + off + (size_t)r * HD + 8 * u);
+      } else {
+        *reinterpret_cast<uint4*>(ks + r * KP + 16 * u) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vs + r * VP + 16 * u) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_async_commit();
+  };
+  bool issued = false;
+  if ((int)blockIdx.x < total) {
+    int b, kvh, c, qt;
+    locate(blockIdx.x, b, kvh, c, qt);
+    if ((c + 1) * kKvChunk <= a.rs.pos_base[b] + a.rs.pos_off) {   // no slot of this pass in the chunk
+      issue(b, kvh, c, kKvChunk);
+      issued = true;
+    }
+  }
+  pdl_wait();
+  trace_mark(a.rs, 1);
+  pdl_launch_next();
+
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    int b, kvh, c, qt;
+    locate(item, b, kvh, c, qt);
+    const int p0 = a.rs.pos_base[b] + a.rs.pos_off;
+    if (!issued) issue(b, kvh, c, min(kKvChunk, p0 + rps - c * kKvChunk));
+    issued = false;
+    // The tile's 16 query rows -> bf16 hi + lo (rows past Mq are zero), all
+    // of a thread's loads in flight at once.
+    {
+      constexpr int kQB = 16 * (HD / 4) / kAttnThreads;
+      float4 qv[kQB];
+#pragma unroll
+      for (int e = 0; e < kQB; ++e) {
+        const int i = tid + e * kAttnThreads;
+        const int qi = qt * 16 + i / (HD / 4), u = i % (HD / 4);
+        qv[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qi < Mq) {
+          const int j = qi / group, hh = qi - j * group;
+          qv[e] = *reinterpret_cast<const float4*>(a.q + ((size_t)(b * rps + j) * a.nq + kvh * group + hh) * HD +
+                                                   4 * u);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kQB; ++e) {
+        const int i = tid + e * kAttnThreads;
+        const int qr = i / (HD / 4), u = i - qr * (HD / 4);
+        uint2 h, l;
+        split_bf16x2(qv[e].x, qv[e].y, h.x, l.x);
+        split_bf16x2(qv[e].z, qv[e].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(sqh + qr * HP + 4 * u) = h;
+        *reinterpret_cast<uint2*>(sql + qr * HP + 4 * u) = l;
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // Row j sees the chunk's keys below nk, except [gl, gh): in a
+    // multi-candidate verify, the slots of the candidates before its own.
+    int nk[2], gl[2], gh[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int qi = qt * 16 + g + 8 * r;
+      const int j = qi / group;
+      nk[r] = qi < Mq ? min(kKvChunk, p0 + j - c * kKvChunk + 1) : 0;
+      gl[r] = p0 + 1 - c * kKvChunk;
+      gh[r] = gl[r] + tree_gap(a.rs, j);
+    }
+    float sa[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sa[i][0] = sa[i][1] = sa[i][2] = sa[i][3] = 0.f;
+    const unsigned char* krow = ks + (8 * warp + g) * KP + 8 * c4;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const uint2 h0 = *reinterpret_cast<const uint2*>(sqh + g * HP + 16 * k + 4 * c4);
+      const uint2 h1 = *reinterpret_cast<const uint2*>(sqh + (g + 8) * HP + 16 * k + 4 * c4);
+      const uint2 l0 = *reinterpret_cast<const uint2*>(sql + g * HP + 16 * k + 4 * c4);
+      const uint2 l1 = *reinterpret_cast<const uint2*>(sql + (g + 8) * HP + 16 * k + 4 * c4);
+      const uint2 kb = *reinterpret_cast<const uint2*>(krow + 32 * k);
+      mma_bf16_16816(sa[k & 1], h0.x, h1.x, h0.y, h1.y, kb.x, kb.y);
+      mma_bf16_16816(sa[2 + (k & 1)], l0.x, l1.x, l0.y, l1.y, kb.x, kb.y);
+    }
+    float sacc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = e >> 1, kk = 8 * warp + 2 * c4 + (e & 1);
+      const float v = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+      sacc[e] = (kk < nk[r] && (kk < gl[r] || kk >= gh[r])) ? v * a.scale : -INFINITY;
+    }
+    float mx[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(sacc[2 * r], sacc[2 * r + 1]);
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      if (c4 == 0) red_mx[warp][g + 8 * r] = mx[r];
+    }
+    __syncthreads();   // red_mx complete
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float m8 = red_mx[0][g + 8 * r];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) m8 = fmaxf(m8, red_mx[w][g + 8 * r]);
+      mx[r] = m8;
+    }
+    float pe[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pe[e] = sacc[e] != -INFINITY ? expf(sacc[e] - mx[e >> 1]) : 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float l = pe[2 * r] + pe[2 * r + 1];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (c4 == 0) red_l[warp][g + 8 * r] = l;
+      uint32_t h, lo;
+      split_bf16x2(pe[2 * r], pe[2 * r + 1], h, lo);
+      *reinterpret_cast<uint32_t*>(sph + (g + 8 * r) * PP + 8 * warp + 2 * c4) = h;
+      *reinterpret_cast<uint32_t*>(spl + (g + 8 * r) * PP + 8 * warp + 2 * c4) = lo;
+    }
+    __syncthreads();
+
+    float oh[NTW][4], ol[NTW][4];
+#pragma unroll
+    for (int t = 0; t < NTW; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oh[t][e] = ol[t][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kKvChunk / 16; ++kk) {
+      uint32_t ph[4], pl[4];
+      const int k0 = 16 * kk + 2 * c4;
+      ph[0] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0);
+      ph[1] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0);
+      ph[2] = *reinterpret_cast<const uint32_t*>(sph + g * PP + k0 + 8);
+      ph[3] = *reinterpret_cast<const uint32_t*>(sph + (g + 8) * PP + k0 + 8);
+      pl[0] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0);
+      pl[1] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0);
+      pl[2] = *reinterpret_cast<const uint32_t*>(spl + g * PP + k0 + 8);
+      pl[3] = *reinterpret_cast<const uint32_t*>(spl + (g + 8) * PP + k0 + 8);
+      const unsigned char* vrow = vs + (16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1)) * VP;
+#pragma unroll
+      for (int t = 0; t < NTW; ++t) {
+        uint32_t b0, b1;
+        ldsm_x2_trans(b0, b1, vrow + 16 * (warp * NTW + t));
+        mma_bf16_16816(oh[t], ph[0], ph[1], ph[2], ph[3], b0, b1);
+        mma_bf16_16816(ol[t], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (nk[r] <= 0) continue;   // the row sees no slot of this chunk
+      const int qi = qt * 16 + g + 8 * r;
+      const int j = qi / group, hh = qi - j * group;
+      const int m = b * rps + j, h = kvh * group + hh;
+      float* dst = a.part + (((size_t)m * a.nq + h) * a.n_kv_chunks + c) * (HD + 2);
+#pragma unroll
+      for (int t = 0; t < NTW; ++t)
+        *reinterpret_cast<float2*>(dst + 8 * (warp * NTW + t) + 2 * c4) =
+            make_float2(oh[t][2 * r] + ol[t][2 * r], oh[t][2 * r + 1] + ol[t][2 * r + 1]);
+      if (warp == 0 && c4 == 0) {
+        float l = red_l[0][g + 8 * r];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) l += red_l[w][g + 8 * r];
+        dst[HD] = mx[r];
+        dst[HD + 1] = l;
+      }
+    }
+    __syncthreads();   // keys, values, P and red_* are free again
+  }
+}
+
+static int attn1_smem_bytes(int hd) {
+  return kKvChunk * (hd * 2 + 32) + kKvChunk * (hd * 2 + 16) + 2 * 16 * (kKvChunk + 8) * 2 + 2 * 16 * (hd + 16) * 2;
+}
+
 // The merge kernel: one CTA of kMergeThreads per (row, head); writes the
 // output projection's input in fragment order.
 __global__ void __launch_bounds__(kMergeThreads) k_attn_merge(const __grid_constant__ AttnArgs a) {
@@ -488,7 +744,14 @@ cudaError_t attn_init() {
     if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
       return e;
-  const void* fns[] = {reinterpret_cast<const void*>(k_attn_merge), reinterpret_cast<const void*>(k_embed)};
+  if ((e = cudaFuncSetAttribute(k_attn_chunk1<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn1_smem_bytes(128))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_attn_chunk1<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn1_smem_bytes(64))) != cudaSuccess)
+    return e;
+  const void* fns[] = {reinterpret_cast<const void*>(k_attn_chunk1<128>),
+                       reinterpret_cast<const void*>(k_attn_chunk1<64>),
+                       reinterpret_cast<const void*>(k_attn_merge), reinterpret_cast<const void*>(k_embed)};
   for (const void* f : fns)
     if ((e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
@@ -512,18 +775,26 @@ cudaError_t launch_attention(const AttnArgs& a, int num_sms, cudaStream_t st, bo
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  cfg.dynamicSmemBytes = attn_smem_bytes(a.hd, a.stages, a.TG);
   if (a.TG != 1 && a.TG != 2 && a.TG != 4) return cudaErrorInvalidValue;
-  if (a.hd == 128)
-    e = a.TG == 4   ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 4>, a)
-        : a.TG == 2 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 2>, a)
-                    : cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 1>, a);
-  else if (a.hd == 64)
-    e = a.TG == 4   ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 4>, a)
-        : a.TG == 2 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 2>, a)
-                    : cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 1>, a);
-  else
-    return cudaErrorInvalidValue;
+  if (a.R == 1 && a.TG == 1 && a.kc && a.vc) {
+    // One chunk, one tile per item: the copy kernel (same arithmetic).
+    cfg.dynamicSmemBytes = attn1_smem_bytes(a.hd);
+    if (a.hd == 128) e = cudaLaunchKernelEx(&cfg, k_attn_chunk1<128>, a);
+    else if (a.hd == 64) e = cudaLaunchKernelEx(&cfg, k_attn_chunk1<64>, a);
+    else return cudaErrorInvalidValue;
+  } else {
+    cfg.dynamicSmemBytes = attn_smem_bytes(a.hd, a.stages, a.TG);
+    if (a.hd == 128)
+      e = a.TG == 4   ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 4>, a)
+          : a.TG == 2 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 2>, a)
+                      : cudaLaunchKernelEx(&cfg, k_attn_chunks<128, 1>, a);
+    else if (a.hd == 64)
+      e = a.TG == 4   ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 4>, a)
+          : a.TG == 2 ? cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 2>, a)
+                      : cudaLaunchKernelEx(&cfg, k_attn_chunks<64, 1>, a);
+    else
+      return cudaErrorInvalidValue;
+  }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(a.rs.M * a.nq);

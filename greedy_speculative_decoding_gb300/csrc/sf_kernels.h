@@ -155,6 +155,8 @@ struct AttnArgs {
   // values kv_vrows rows further.
   CUtensorMap kvmap;
   CUtensorMap kvmap8;      // the same with 8-slot boxes: a sequence's partly filled last chunk
+  const bf16* kc;          // this layer's keys [B][nkv][s_max][hd] (the one-chunk copy kernel)
+  const bf16* vc;          // and values
   int box8;                // 1: load a partly filled last chunk in 8-slot boxes
   int kv_row0, kv_brows, kv_vrows;
   int R;                   // cache chunks per work item (one partial result per R chunks)
