@@ -26,7 +26,8 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // Rows m < M of the CTA are token rows m0 + m of the forward; pos[m] is the
 // cache slot of row m0 + m (its RoPE position differs for the rows of a
 // multi-candidate verify).
-template <int T, int EPI>
+// F32: the fp32-weight kernel (biases and gains in fp32); the others read bf16.
+template <int T, int EPI, bool F32 = false>
 __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, int M, EpiPre<T>& pre,
                                              const int* pos) {
   constexpr int kE = EpiPre<T>::kE;
@@ -36,7 +37,7 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, 
       const int i = threadIdx.x + e * kGemmThreads;
       const int m = i / kBlockRows, n = rb * kBlockRows + (i - m * kBlockRows);
       pre.v0[e] = (m < M && n < a.N) ? a.out[(size_t)(m0 + m) * a.out_ld + n] : 0.f;
-      pre.v1[e] = (a.frag_gain && n < a.N) ? ldw(a.frag_gain, n, a.wf32) : 0.f;
+      pre.v1[e] = (a.frag_gain && n < a.N) ? ldw(a.frag_gain, n, F32) : 0.f;
     }
   } else if (EPI == EPI_QKV) {
     const int half = a.hd >> 1;
@@ -53,10 +54,11 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, int rb, int m0, 
       pre.v0[e] = pre.v1[e] = 0.f;
       pre.cs[e] = make_float2(1.f, 0.f);
       if (m < M && n0 + r < a.N) {
-        if (bias) pre.v0[e] = ldw(bias, local, a.wf32);
+        if (bias) pre.v0[e] = ldw(bias, local, F32);
         if (s < 2 && d < half) {
-          if (bias) pre.v1[e] = ldw(bias, local + half, a.wf32);
-          pre.cs[e] = a.rope[(size_t)(pos[m] - tree_gap(a.rs, (m0 + m) % a.rs.rps)) * half + d];
+          if (bias) pre.v1[e] = ldw(bias, local + half, F32);
+          const int gap = a.rs.tree_g > 0 ? tree_gap(a.rs, (m0 + m) % a.rs.rps) : 0;
+          pre.cs[e] = a.rope[(size_t)(pos[m] - gap) * half + d];
         }
       }
     }

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kGemmThreads) k_gemm_f32(const __grid_constant
     const int Mg = min(kGroupRows, M - m0);
     float* yg = ys + m0 * kBlockRows;
     EpiPre<4> pre;
-    epi_prefetch<4, EPI>(a, rb, m0, Mg, pre, s_pos + m0);
+    epi_prefetch<4, EPI, true>(a, rb, m0, Mg, pre, s_pos + m0);
     if (EPI == EPI_RESID) epi_resid<4>(a, yg, rb, m0, Mg, T4, pre);
     else if (EPI == EPI_QKV) epi_qkv<4>(a, yg, rb, m0, Mg, pre, s_pos + m0);
     else if (EPI == EPI_SWIGLU) epi_swiglu(a, yg, rb, m0, Mg, T4);
