@@ -630,7 +630,7 @@ sf_status forward(sf_engine* e, Model& md, const RowSet& rs, bool lm, const TokO
       t.kvmap8 = md.kvmap8;
       t.kc = kc;
       t.vc = vc;
-    t.box8 = e->box8 ? 1 : 0;
+      t.box8 = e->box8 ? 1 : 0;
       t.kv_brows = c.n_kv_heads * e->s_max;
       t.kv_vrows = e->B * t.kv_brows;
       t.kv_row0 = (2 * l * e->B + (seq >= 0 ? seq : 0)) * t.kv_brows;
