@@ -42,10 +42,11 @@
  *     calling thread's last failure.
  *   - Batch: sequences are independent; per-sequence lengths and accept
  *     lengths are kept on the device.
- *   - Rows per forward (batch * (K + 1)) are limited to SF_MAX_ROWS. Up to 16
- *     rows run in one pass over the weights per CTA; a forward with more
- *     rows runs one CTA per 16-row group side by side (weights from HBM once,
- *     then from L2).
+ *   - Rows per forward (batch * (K + 1)) are limited to SF_MAX_ROWS. Every
+ *     forward reads each weight from HBM once: up to 16 bf16 rows on the
+ *     weight-streaming mma.sync GEMM (all rows in one pass per CTA), more
+ *     rows and every NF4 forward on the tcgen05 GEMM (tensor-memory
+ *     accumulators, all token rows as the MMA's N side).
  */
 #ifndef SF_H_
 #define SF_H_
